@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these re-types the oracle's own formula: each compares it with a hand
+worked value, a brute-force search, a library routine, a closed form or an
+invariant that a plausible slip (dropped term, wrong sign or index,
+transposed operand, wrong rounding) would break.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import qattn_oracle as O
+from quantized_attention_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# e4m3
+# --------------------------------------------------------------------------
+
+def _golden_e4m3():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3_worked_cases.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            x, v, byte = line.split()[:3]
+            rows.append((float(x), float(v), int(byte, 16)))
+    return rows
+
+
+def _decode_e4m3_byte(b: int) -> float:
+    """Value of an e4m3 byte from the bit layout (sign | 4 exponent | 3 mantissa)."""
+    s = -1.0 if b & 0x80 else 1.0
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * m * 2.0 ** -9
+    return s * (1 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def test_e4m3_worked_cases():
+    for x, v, byte in _golden_e4m3():
+        got = float(O.e4m3_round(np.float32(x)))
+        assert got == v, (x, got, v)
+        assert _decode_e4m3_byte(byte) == v, (x, byte)
+
+
+def test_e4m3_against_brute_force_grid():
+    """Nearest grid value by exhaustive search over all 254 finite codes, ties
+    to the code with an even mantissa, saturating above 448."""
+    grid = []
+    for b in range(256):
+        v = _decode_e4m3_byte(b)
+        if not math.isnan(v):
+            grid.append((v, b))
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([
+        rng.uniform(-470, 470, 3000),
+        np.exp2(rng.uniform(-14, 9, 3000)) * rng.choice([-1, 1], 3000),
+        # exact midpoints between neighbours: the tie rule decides these
+        [(a + b) / 2 for (a, _), (b, _) in zip(sorted(grid)[:-1], sorted(grid)[1:])],
+    ]).astype(np.float32)
+    got = O.e4m3_round(xs)
+    for x, g in zip(xs.astype(np.float64), got):
+        if abs(x) >= 448:
+            assert g == math.copysign(448.0, x)
+            continue
+        best = min(abs(v - x) for v, _ in grid)
+        cands = [(v, b) for v, b in grid if abs(v - x) == best]
+        if len(cands) > 1:
+            cands = [(v, b) for v, b in cands if (b & 1) == 0 and (v != 0 or b == 0)] or cands
+        want = cands[0][0]
+        assert g == want or (g == 0 and want == 0), (x, g, want)
+
+
+def test_e4m3_against_torch_cast():
+    """Library routine: torch's float8_e4m3fn cast rounds to nearest even
+    (it does not saturate, so only |x| < 464 is compared)."""
+    import torch
+
+    rng = np.random.default_rng(1)
+    xs = np.concatenate([rng.uniform(-463, 463, 20000),
+                         np.exp2(rng.uniform(-16, 8.8, 20000))]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(xs), ref)
+
+
+def test_e4m3_reaches_about_4e6():
+    """ZINC-ATTN: with the static scale 448 e4m3 holds probabilities down to
+    about 4e-6; int8 at 127 has step 0.0079 and flushes below 0.0039."""
+    smallest = 2.0 ** -9 / 448
+    assert 4e-6 < smallest < 5e-6
+    assert O.e4m3_round(np.float32(smallest * 448)) > 0
+    assert O.e4m3_round(np.float32(0.4 * smallest * 448)) == 0
+    assert round(1 / 127, 4) == 0.0079 and round(0.5 / 127, 4) == 0.0039
+
+
+# --------------------------------------------------------------------------
+# int8 quantizer (QFLASH eq. (1)-(2))
+# --------------------------------------------------------------------------
+
+def test_quantizer_hand_cases():
+    x = np.zeros((1, 1, 4, 4), np.float32)
+    x[0, 0, 0] = [2.0, -2.0, 1.0, 0.0]
+    codes, scale = O.quantize_sym(x, O.GRAN_TENSOR)
+    assert scale[0] == np.float32(2.0) / np.float32(127)
+    assert list(codes[0, 0, 0]) == [127, -127, 64, 0]       # 63.5 -> 64 (even)
+    # half-way cases with amax = 127: x * 1 = x exactly
+    y = np.zeros((1, 1, 1, 5), np.float32)
+    y[0, 0, 0] = [127.0, 0.5, 1.5, 2.5, -0.5]
+    c, s = O.quantize_sym(y, O.GRAN_TENSOR)
+    assert list(c[0, 0, 0]) == [127, 0, 2, 2, 0]
+    assert s[0] == 1.0
+    z, sz = O.quantize_sym(np.zeros((1, 1, 3, 2), np.float32), O.GRAN_TENSOR)
+    assert (z == 0).all() and sz[0] == 0
+
+
+def test_quantizer_brute_force():
+    """code = the integer in [-127, 127] nearest to x * fp32(127/amax), ties to
+    even, by exhaustive search."""
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal((2, 3, 300, 8)) * 3).astype(np.float32)
+    for gran in (O.GRAN_TENSOR, O.GRAN_HEAD, O.GRAN_BLOCK):
+        codes, scale = O.quantize_sym(x, gran)
+        zs = np.arange(-127, 128)
+        for b in range(2):
+            for h in range(3):
+                for n in (0, 127, 128, 299):
+                    if gran == O.GRAN_TENSOR:
+                        amax = np.abs(x).max()
+                    elif gran == O.GRAN_HEAD:
+                        amax = np.abs(x[b, h]).max()
+                    else:
+                        amax = np.abs(x[b, h, (n // 128) * 128:(n // 128 + 1) * 128]).max()
+                    inv = np.float32(127) / np.float32(amax)
+                    for cidx in range(8):
+                        v = float(np.float32(x[b, h, n, cidx] * inv))
+                        dist = np.abs(zs - v)
+                        best = zs[dist == dist.min()]
+                        want = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+                        assert codes[b, h, n, cidx] == want
+                    gi = {O.GRAN_TENSOR: (0,), O.GRAN_HEAD: (b, h), O.GRAN_BLOCK: (b, h, n // 128)}[gran]
+                    assert scale[gi] == np.float32(amax) / np.float32(127)
+
+
+def test_dequantized_error_within_half_step():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((1, 2, 256, 16)).astype(np.float32)
+    codes, scale = O.quantize_sym(x, O.GRAN_BLOCK)
+    s = O.expand_per_token(scale, O.GRAN_BLOCK, 1, 2, 256)[..., None]
+    assert np.all(np.abs(codes * s - x) <= 0.5 * s * (1 + 1e-6))
+    assert codes.min() >= -127  # -128 is never produced
+
+
+# --------------------------------------------------------------------------
+# K channel mean
+# --------------------------------------------------------------------------
+
+def test_mean_exact_on_dyadic_values():
+    """Values on a 2^-8 grid are exact in the 2^-24 fixed point; with Nk a
+    power of two the exact mean is a dyadic number representable in fp32."""
+    rng = np.random.default_rng(4)
+    K = (rng.integers(-4096, 4096, size=(1, 2, 64, 8)) / 256.0).astype(np.float32)
+    mu = O.smooth_k(K)
+    for h in range(2):
+        for c in range(8):
+            exact = sum(Fraction(float(v)) for v in K[0, h, :, c]) / 64
+            assert Fraction(float(mu[0, h, c])) == exact
+
+
+def test_mean_order_free():
+    rng = np.random.default_rng(5)
+    K = I.to_bf16(rng.standard_normal((1, 2, 300, 16)).astype(np.float32) * 7)
+    perm = rng.permutation(300)
+    a = O.smooth_k(K)
+    b = O.smooth_k(K[:, :, perm])
+    assert a.tobytes() == b.tobytes()
+    np.testing.assert_allclose(a, K.astype(np.float64).mean(axis=2), rtol=0, atol=1e-6)
+
+
+def test_mean_subtraction_is_exact_for_softmax():
+    """ZINC-ATTN 'K's outliers': subtracting a per-channel vector from K shifts
+    each row's scores by a constant, so fp64 attention is unchanged."""
+    rng = np.random.default_rng(6)
+    Q = rng.standard_normal((1, 2, 40, 16))
+    K = rng.standard_normal((1, 2, 70, 16)) + rng.standard_normal(16) * 10
+    V = rng.standard_normal((1, 2, 70, 16))
+    mu = K.mean(axis=2, keepdims=True)
+    for causal in (False, True):
+        a = O.attn_fp64(Q, K, V, causal=causal)
+        b = O.attn_fp64(Q, K - mu, V, causal=causal)
+        assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))
+
+
+def test_smoothing_shrinks_outlier_channels():
+    """ZINC-ATTN K-outlier figure: raw K's worst channel is ~44x the median
+    channel amax; after the mean subtraction every channel is <= 4.1x, and the
+    typical channel's share of the int8 grid goes from ~3 to ~31 levels."""
+    wl = I.small("llm8k", Hq=4, Hkv=1, Nq=128, Nk=8192)
+    inp = I.make_inputs(wl)
+    amax_raw = np.abs(inp.K[0, 0]).max(axis=0)
+    mu = O.smooth_k(inp.K)
+    amax_s = np.abs(inp.K[0, 0] - mu[0, 0]).max(axis=0)
+    r_raw = amax_raw.max() / np.median(amax_raw)
+    r_s = amax_s.max() / np.median(amax_s)
+    assert 40 < r_raw < 50
+    assert r_s <= 4.1
+    assert round(127 / 44) == 3 and round(127 / 4.1) == 31
+
+
+# --------------------------------------------------------------------------
+# integer scores
+# --------------------------------------------------------------------------
+
+def test_scores_match_python_loops():
+    rng = np.random.default_rng(7)
+    q = rng.integers(-127, 128, size=(1, 4, 5, 32)).astype(np.int8)
+    k = rng.integers(-127, 128, size=(1, 2, 6, 32)).astype(np.int8)
+    S = O.qk_scores(q, k)
+    for h in range(4):
+        for i in range(5):
+            for j in range(6):
+                want = 0
+                for c in range(32):
+                    want += int(q[0, h, i, c]) * int(k[0, h // 2, j, c])
+                assert S[0, h, i, j] == want
+
+
+def test_scores_extreme_values():
+    q = np.full((1, 1, 2, 128), 127, np.int8)
+    q[0, 0, 1] = -127
+    k = np.full((1, 1, 3, 128), -127, np.int8)
+    S = O.qk_scores(q, k)
+    assert S[0, 0, 0, 0] == -128 * 127 * 127 and S[0, 0, 1, 2] == 128 * 127 * 127
+
+
+# --------------------------------------------------------------------------
+# online softmax loop
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [
+    dict(B=1, Hq=2, Hkv=2, Nq=50, Nk=300, d=16, causal=False, bias=False, pos0=None),
+    dict(B=2, Hq=4, Hkv=2, Nq=130, Nk=130, d=8, causal=True, bias=False, pos0=None),
+    dict(B=1, Hq=2, Hkv=1, Nq=64, Nk=512, d=8, causal=True, bias=False, pos0=448),
+    dict(B=1, Hq=1, Hkv=1, Nq=49, Nk=49, d=32, causal=False, bias=True, pos0=None),
+    dict(B=1, Hq=1, Hkv=1, Nq=300, Nk=200, d=8, causal=True, bias=False, pos0=-100),
+])
+def test_blockwise_loop_equals_dense_softmax(case):
+    """With quantization off (real scores, P unquantized, fp64), the blockwise
+    online softmax equals dense softmax attention (QFLASH section 2.1)."""
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, Nq, Nk, d = (case[k] for k in ("B", "Hq", "Hkv", "Nq", "Nk", "d"))
+    Q = rng.standard_normal((B, Hq, Nq, d)) * 2
+    K = rng.standard_normal((B, Hkv, Nk, d))
+    V = rng.standard_normal((B, Hkv, Nk, d))
+    bias = rng.standard_normal((Nq, Nk)) if case["bias"] else None
+    kw = dict(causal=case["causal"], q_pos0=case["pos0"], bias=bias)
+    dense = O.attn_fp64(Q, K, V, **kw).reshape(B, Hq, Nq, d)
+    blk = O.attn_blockwise_real(Q, K, V, ftype=np.float64, **kw)
+    assert np.max(np.abs(dense - blk)) <= 1e-12 * max(1.0, np.max(np.abs(dense)))
+    blk32 = O.attn_blockwise_real(Q, K, V, ftype=np.float32, **kw)
+    assert np.max(np.abs(dense - blk32)) <= 2e-5 * max(1.0, np.max(np.abs(dense)))
+
+
+def test_fully_masked_rows_give_zero():
+    rng = np.random.default_rng(9)
+    Q = rng.standard_normal((1, 1, 20, 8))
+    K = rng.standard_normal((1, 1, 10, 8))
+    V = rng.standard_normal((1, 1, 10, 8))
+    out = O.attn_blockwise_real(Q, K, V, causal=True, q_pos0=-5)
+    assert np.all(out[0, 0, :5] == 0) and np.all(np.abs(out[0, 0, 5:]).sum(axis=1) > 0)
+
+
+def _tiny_prep(seed=11, **kw):
+    wl = I.small("tiny", seed=seed, **kw)
+    inp = I.make_inputs(wl)
+    return wl, inp, O.prepare(inp)
+
+
+def test_p_bounded_by_one_and_p8_by_448():
+    """ZINC-ATTN: every P = exp(s - m) <= 1 by construction, so P * 448 fits e4m3."""
+    wl, inp, prep = _tiny_prep()
+    S = O.qk_scores(prep["q_codes"], prep["k_codes"])[0, 0].astype(np.float64)
+    c = O.block_factor(prep["q_scales"][0, 0][:, None].repeat(128, 0)[:256],
+                       prep["k_scales"][0, 0][None, :], O.default_sm_scale(64))
+    r = O.online_softmax_pv(S, c, prep["v8"][0, 0], prep["s_v"][0, 0],
+                            visible=np.ones((256, 256), bool))
+    assert 0.99 < r["p_max"] <= 1.0
+    assert np.abs(prep["v8"]).max() <= 448
+
+
+def test_recipe_close_to_fp64():
+    """The quantized recipe stays near unquantized attention on Tiny (reported
+    error, sanity bound only): e4m3 has 3 mantissa bits."""
+    wl, inp, prep = _tiny_prep()
+    out = O.run_workload(inp, prep)["O"].reshape(1, 1, 256, 64)
+    ref = O.attn_fp64(inp.Q, inp.K, inp.V, causal=False).reshape(1, 1, 256, 64)
+    err = np.abs(out - ref).max() / np.abs(ref).max()
+    assert err < 0.05, err
+
+
+def test_gqa_equals_repeated_heads():
+    wl = I.small("llm8k", Hq=4, Hkv=2, Nq=160, Nk=160, d=32, seed=12)
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    out = O.run_workload(inp, prep)["O"]
+    rep = dict(prep)
+    rep["k_codes"] = np.repeat(prep["k_codes"], 2, axis=1)
+    rep["k_scales"] = np.repeat(prep["k_scales"], 2, axis=1)
+    rep["v8"] = np.repeat(prep["v8"], 2, axis=1)
+    rep["s_v"] = np.repeat(prep["s_v"], 2, axis=1)
+    inp2 = I.Inputs(wl.replace(Hkv=4), inp.Q, K=None, V=None)
+    out2 = O.run_workload(inp2, rep)["O"]
+    assert np.array_equal(out, out2)
+
+
+def test_causal_chunk_is_slice_of_full():
+    """Chunked prefill: queries at positions Nk-64..Nk-1 against all Nk keys
+    equal the last 64 rows of full causal attention over Nk."""
+    wl = I.small("llm8k", Hq=2, Hkv=1, Nq=512, Nk=512, d=32, seed=13)
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    full = O.run_workload(inp, prep)["O"]
+    part = O.attn_fwd(prep["q_codes"][:, :, 448:], prep["q_scales"][:, :, 3:],
+                      prep["k_codes"], prep["k_scales"], prep["v8"], prep["s_v"],
+                      q_gran=wl.q_gran, k_gran=wl.k_gran, causal=True, q_pos0=448)["O"]
+    assert np.array_equal(full[:, 448:], part)
+
+
+def test_row_subset_equals_full():
+    wl, inp, prep = _tiny_prep(seed=14)
+    full = O.run_workload(inp, prep)["O"]
+    rows = np.array([0, 5, 127, 128, 255])
+    sub = O.run_workload(inp, prep, rows=rows)["O"]
+    assert np.array_equal(full[:, rows], sub)
+
+
+def test_flip_bound_is_small_and_nonnegative():
+    wl, inp, prep = _tiny_prep(seed=15)
+    r = O.run_workload(inp, prep, want_bound=True)
+    assert (r["bound"] >= 0).all()
+    assert r["bound"].max() < 1e-2 * np.abs(r["O"]).max()
+
+
+def test_cache_inputs_fold_channel_scale_into_q():
+    """int8 K codes with per-channel scales: S * sq equals Q . K_real up to the
+    Q quantization error, i.e. the fold puts the K scale on the Q side."""
+    wl = I.small("chunk32k", Nq=128, Nk=384, q_pos0=256, Hq=2, Hkv=1)
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    assert (prep["k_scales"] == 1).all()
+    S = O.qk_scores(prep["q_codes"], prep["k_codes"])[0, 0].astype(np.float64)
+    Kreal = inp.K_codes[0, 0].astype(np.float64) * inp.K_scale[0, 0].astype(np.float64)
+    exact = inp.Q[0, 0].astype(np.float64) @ Kreal.T
+    sq = prep["q_scales"][0, 0, 0]
+    err = np.abs(S * sq - exact).max() / np.abs(exact).max()
+    assert err < 0.05
+
+
+def test_v_codes_path():
+    rng = np.random.default_rng(16)
+    Vc = rng.integers(-127, 128, size=(1, 1, 50, 4)).astype(np.int8)
+    Vc[0, 0, :, 3] = 0
+    sc = np.array([[[0.5, 2.0, 1.0, 3.0]]], np.float32)
+    v8, s_v = O.quantize_v_codes(Vc, sc)
+    amax = np.abs(Vc[0, 0].astype(int)).max(axis=0)
+    assert s_v[0, 0, 3] == 0 and (v8[0, 0, :, 3] == 0).all()
+    for c in range(3):
+        want_s = np.float32(np.float32(sc[0, 0, c] * np.float32(amax[c])) / np.float32(448))
+        assert s_v[0, 0, c] == want_s
+        real = Vc[0, 0, :, c] * float(sc[0, 0, c])
+        # e4m3 keeps 3 mantissa bits: relative error <= 2^-4
+        got = v8[0, 0, :, c] * float(s_v[0, 0, c])
+        assert np.all(np.abs(got - real) <= 2 ** -4 * np.abs(real) + 1e-9)
+
+
+def test_v_bf16_path():
+    """Per-channel e4m3 V: the channel's largest |v| lands exactly on +-448,
+    an all-zero channel stays zero, and the dequantized value keeps 3
+    mantissa bits (relative error <= 2^-4 above the subnormal range)."""
+    rng = np.random.default_rng(17)
+    V = I.to_bf16(rng.standard_normal((1, 2, 300, 8)).astype(np.float32) * 3)
+    V[0, 1, :, 5] = 0
+    v8, s_v = O.quantize_v(V)
+    for h in range(2):
+        for c in range(8):
+            col = V[0, h, :, c].astype(np.float64)
+            if not col.any():
+                assert s_v[0, h, c] == 0 and not v8[0, h, :, c].any()
+                continue
+            k = np.argmax(np.abs(col))
+            assert abs(v8[0, h, k, c]) == 448 and np.sign(v8[0, h, k, c]) == np.sign(col[k])
+            assert s_v[0, h, c] == np.float32(np.abs(col).max()) / np.float32(448)
+            got = v8[0, h, :, c] * float(s_v[0, h, c])
+            normal = np.abs(v8[0, h, :, c]) >= 2 ** -6
+            assert np.all(np.abs(got - col)[normal] <= 2 ** -4 * np.abs(col)[normal] * (1 + 1e-6))
