@@ -1,0 +1,373 @@
+"""Benchmark of the quantized attention prefill path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+K channel mean, Q/K int8 quantization, V e4m3 quantization and the fused
+attention kernel (qattn_smooth_k, qattn_quantize_qk, qattn_quantize_v,
+qattn_fwd).  Default workload: LLM prefill, B=1, 32 query heads / 8 KV heads,
+8192 tokens, d=128, causal (the 8K causal prefill shape the throughput target
+is stated on).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention effective TOPS and % of measured GB300 dense int8/fp8 tensor peak"
+UNIT = "TOPS"
+
+
+def _peaks():
+    """Measured GB300 peaks (generated file), else the documented fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def mixed_peak(peaks, sustained=True):
+    """Peak of the attention contraction: half the algorithmic ops (QK^T) run
+    at the fp16 rate (= the measured bf16 rate), half (PV) at the e4m3 rate
+    (= the fp16 rate times the nominal 4.5/2.25 ratio); harmonic combination."""
+    p16 = peaks["bf16_sustained"] if sustained else peaks["bf16"]
+    p8 = 2.0 * p16
+    return 1.0 / (0.5 / p16 + 0.5 / p8)
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline): bounded sample, all host cores
+# ----------------------------------------------------------------------------
+
+_SAMPLE = None
+
+
+def _init_worker(sample):
+    global _SAMPLE
+    _SAMPLE = sample
+
+
+def _oracle_sample_worker(args):
+    head, rows_lo, rows_hi = args
+    from oracle import qattn_oracle as O
+    wl, inp, prep = _SAMPLE
+    rows = np.arange(rows_lo, rows_hi)
+    O.run_workload(inp, prep, heads=[(0, head)], rows=rows)
+    return 4 * wl.d * int(O.visible_mask(rows, wl.Nk, wl.causal, wl.pos0).sum())
+
+
+def sample_problem(wl_name):
+    """The bounded sample: batch 0, the first KV head and the query heads that
+    read it, with every token (the quantization sees the same data as in the
+    full workload, so the codes are identical)."""
+    from oracle import qattn_oracle as O
+    from quantized_attention_gb300 import inputs as I
+    wl = I.WORKLOADS[wl_name]
+    full = I.make_inputs(wl)
+    g = wl.Hq // wl.Hkv
+    sub = wl.replace(B=1, Hq=g, Hkv=1)
+    kw = {"Q": full.Q[:1, :g].copy(), "bias": full.bias}
+    if wl.kv_codes:
+        kw.update(K_codes=full.K_codes[:1, :1].copy(), K_scale=full.K_scale[:1, :1].copy(),
+                  V_codes=full.V_codes[:1, :1].copy(), V_scale=full.V_scale[:1, :1].copy())
+    else:
+        kw.update(K=full.K[:1, :1].copy(), V=full.V[:1, :1].copy())
+    inp = I.Inputs(sub, **kw)
+    return sub, inp, O.prepare(inp)
+
+
+def run_oracle_sample(sample, pool, n_tiles):
+    """Times the oracle on n_tiles (query head, 128-row tile) items of the
+    sample, heaviest causal tiles first; returns (ops, seconds)."""
+    wl = sample[0]
+    nqt = (wl.Nq + 127) // 128
+    items = []
+    for t in range(n_tiles):
+        h = t % wl.Hq
+        qt = nqt - 1 - (t // wl.Hq) % nqt
+        items.append((h, qt * 128, min(wl.Nq, qt * 128 + 128)))
+    t0 = time.perf_counter()
+    ops = sum(pool.map(_oracle_sample_worker, items))
+    return ops, time.perf_counter() - t0
+
+
+def make_pool(sample):
+    """A spawn-started pool over every host core, each worker holding the sample."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    return mp.get_context("spawn").Pool(cores, initializer=_init_worker, initargs=(sample,)), cores
+
+
+def time_cpu_baseline(wl_name, warmup=1, steps=1):
+    sample = sample_problem(wl_name)
+    pool, cores = make_pool(sample)
+    try:
+        n_tiles = 2 * cores
+        for _ in range(warmup):
+            run_oracle_sample(sample, pool, cores)
+        ops, secs = 0, 0.0
+        for _ in range(steps):
+            o, s = run_oracle_sample(sample, pool, n_tiles)
+            ops += o
+            secs += s
+    finally:
+        pool.close()
+    desc = (f"{n_tiles} (query head, 128-row tile) items per step of {wl_name} "
+            f"(batch 0, KV head 0), heaviest tiles first")
+    return ops, secs, cores, desc
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    ops, secs, cores, desc = time_cpu_baseline(args.workload, args.warmup, args.steps)
+    value = ops / secs / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3",
+            "data": "synthetic", "config": _config(args.workload),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl_name):
+    from quantized_attention_gb300 import inputs as I
+    wl = I.WORKLOADS[wl_name]
+    return {"workload": f"{wl_name}: B={wl.B} Hq={wl.Hq} Hkv={wl.Hkv} Nq={wl.Nq} Nk={wl.Nk} "
+                        f"d={wl.d} causal={int(wl.causal)} q_pos0={wl.pos0}",
+            "granularity": {0: "tensor", 1: "head", 2: "block128"}[wl.q_gran],
+            "kv_input": "int8 codes" if wl.kv_codes else "bf16",
+            "output": "bf16", "l2": "flushed (256 MB write) before every timed step"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+
+    from quantized_attention_gb300 import binding as qb
+    from quantized_attention_gb300 import inputs as I
+    from quantized_attention_gb300.pipeline import device_inputs, problem_for
+
+    wl = I.WORKLOADS[args.workload]
+    inp = I.make_inputs(wl)
+    dev = device_inputs(inp)
+    bias = dev.pop("bias", None)
+    P = problem_for(wl, out_dtype=qb.DT_BF16)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
+
+    ops = 4 * wl.d * wl.unmasked_pairs()
+
+    def step():
+        P.quantize(**dev, stream=stream)
+        ev_a.record(stream)
+        P.attend(bias, stream)
+        ev_b.record(stream)
+
+    for _ in range(args.warmup):
+        ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        step()
+    torch.cuda.synchronize()
+    if qb.get_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    attn_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    attn_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # evict L2 (outside the timed interval)
+            starts[i].record(stream)
+            ev_a, ev_b = attn_a[i], attn_b[i]
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if qb.get_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [a.elapsed_time(b) for a, b in zip(attn_a, attn_b)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = world * ops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers, copies timed
+    host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+    out_host = torch.empty(P.O.shape, dtype=P.O.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        P.run(**dev, bias=bias, stream=stream)
+        out_host.copy_(P.O, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e_ms = 0.0
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e_s.record(stream)
+        e2e_step()
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e_ms += e_s.elapsed_time(e_e)
+    if world > 1:
+        t = torch.tensor([e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = world * ops / (e_ms / args.steps * 1e-3) / 1e12
+
+    if rank != 0:
+        return 0
+    peaks = _peaks()
+    pmix = mixed_peak(peaks, sustained=True)
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = ops / (attn_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "qattn_fwd (fused attention)",
+                "achieved": achieved, "peak": pmix, "unit": "TFLOP/s", "frac": achieved / pmix,
+                "peak_basis": (f"{peaks['source']}: QK^T at the sustained bf16 rate "
+                               f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
+                "traffic": None}
+    cpu = None
+    if not args.no_cpu_baseline:
+        c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
+        cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}; {c_s:.1f} s"}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3", "data": "synthetic",
+            "config": _config(args.workload),
+            "frac_of_mixed_peak": value / pmix,
+            "attn_kernel_ms": attn_avg_ms,
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": P.kernel_launches() * args.steps,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="llm8k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

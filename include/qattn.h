@@ -1,0 +1,204 @@
+/*
+ * qattn -- quantized flash-attention prefill for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libqattn.so.  The recipe it implements:
+ *
+ *   - K's per-channel mean is subtracted first.  Every score of a query row
+ *     then moves by the same q.mu, which softmax ignores, so the result is
+ *     unchanged while K's outlier channels shrink ("int8 Flash Attention on
+ *     RDNA4: QK Wants Integers, PV Wants FP8", section "K's outliers, and the
+ *     subtraction softmax does not notice").
+ *   - Q and K become symmetric int8 codes with fp32 scales s = amax / 127
+ *     ("QFlash: Bridging Quantization and Memory Efficiency in Vision
+ *     Transformer Attention", section 4, eq. (1)-(2)); the score tile is the
+ *     exact integer dot product of the codes (same page, eq. (3)).
+ *   - The online softmax runs in fp32 with a running row maximum, so every
+ *     P = exp(s - m) is <= 1 (ZINC post, section "The scale P needs is
+ *     already sitting in a register").
+ *   - P is scaled by the static 448 and rounded to fp8 e4m3; V is e4m3 with
+ *     one fp32 scale per channel; PV accumulates in fp32 (ZINC post, section
+ *     "fp8 is not faster, it is shaped correctly").
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers owned by the caller, unless stated.  The
+ *     library allocates no device memory of its own except one error word per
+ *     device.  Scratch memory is the caller's `workspace` of at least
+ *     qattn_workspace_size() bytes; its contents need not be initialised.
+ *   - Tensors are dense and row-major.  Q-like tensors are [B][Hq][Nq][d],
+ *     K/V-like tensors [B][Hkv][Nk][d].  bf16 tensors are passed as uint16_t
+ *     bit patterns.  Every tensor pointer must be 16-byte aligned.
+ *   - Supported head dims: d in {32, 64, 128}.  Hq must be a multiple of Hkv;
+ *     query head h reads KV head h / (Hq / Hkv).  Limits (else
+ *     QATTN_ERR_UNSUPPORTED): Nq, Nk <= 65535 * 128 and B * Hq <= 65535.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Arguments are validated on the host first: an
+ *     invalid call returns a status and launches nothing.  A launch failure
+ *     returns QATTN_ERR_CUDA.  No call aborts or throws.
+ *   - Empty problems (B, Hq or Nq equal to 0) return QATTN_OK and launch
+ *     nothing.
+ *   - Kernels never wait forever: a pipeline wait that exceeds its time limit
+ *     makes the kernel record QATTN_ERR_TIMEOUT in the device error word and
+ *     return early; qattn_get_error() reports it.
+ */
+#ifndef QATTN_H_
+#define QATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qattn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  QATTN_OK = 0,
+  QATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, bad enum */
+  QATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d = 96)      */
+  QATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed            */
+  QATTN_ERR_TIMEOUT = 4,      /* a kernel's pipeline wait ran out (device)    */
+  QATTN_ERR_WORKSPACE = 5     /* workspace missing or smaller than required   */
+} qattn_status;
+
+/* Scale granularity of Q and K codes ("QFlash", section 3.3: per tensor,
+ * per head or per token; finer is allowed here because the softmax is fp32). */
+typedef enum {
+  QATTN_GRAN_TENSOR = 0, /* one scale for the whole tensor                   */
+  QATTN_GRAN_HEAD = 1,   /* one scale per (batch, head): [B][H]              */
+  QATTN_GRAN_BLOCK = 2   /* one per (batch, head, 128 tokens): [B][H][ceil(N/128)] */
+} qattn_gran;
+
+typedef enum { QATTN_BF16 = 0, QATTN_F32 = 1, QATTN_I8 = 2, QATTN_E4M3 = 3 } qattn_dtype;
+
+/* Tokens per scale block and keys per softmax block. */
+#define QATTN_BLOCK 128
+/* q_pos0 value meaning "Nk - Nq" (the last query sits on the last key). */
+#define QATTN_POS0_BOTTOM_RIGHT INT64_MIN
+
+typedef struct {
+  int64_t B, Hq, Hkv, Nq, Nk, d;
+} qattn_shape;
+
+typedef struct {
+  int32_t causal;           /* 1: key k is visible to query i iff k <= q_pos0 + i   */
+  int32_t q_gran;           /* qattn_gran of the Q codes                           */
+  int32_t k_gran;           /* qattn_gran of the K codes                           */
+  int32_t out_dtype;        /* QATTN_F32 or QATTN_BF16                             */
+  int64_t q_pos0;           /* key position of query row 0, or QATTN_POS0_BOTTOM_RIGHT */
+  float sm_scale;           /* softmax scale; 0 -> fp32(1/sqrt(d))                 */
+  int32_t reserved;         /* must be 0                                           */
+  int64_t bias_head_stride; /* elements between heads' bias matrices; 0 = shared   */
+} qattn_params;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int qattn_version(void);
+
+/* Human-readable text of a status.  Never NULL; the string is static. */
+const char* qattn_status_string(qattn_status s);
+
+/* Bytes of workspace that every entry point below accepts for this shape and
+ * parameters (the maximum over them).  0 for an empty problem. */
+size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params);
+
+/* Row stride, in bytes, of the transposed e4m3 V written by qattn_quantize_v:
+ * Nk rounded up to a multiple of 16 (a TMA stride must be 16-byte aligned). */
+int64_t qattn_v_ld(int64_t Nk);
+
+/* a1 -- K channel mean ("int8 Flash Attention on RDNA4", section "K's outliers,
+ * and the subtraction softmax does not notice": one reduction over the K
+ * block, reused by every query tile).
+ *   K       bf16 [B][Hkv][Nk][d]
+ *   k_mean  fp32 [B][Hkv][d] (out):
+ *           mu = fp32( fp64( sum_t round_half_even(K * 2^24) ) * 2^-24 / Nk )
+ *           The int64 fixed-point sum makes the result independent of the
+ *           summation order.  Valid while |K| < 2^20; Nk = 0 gives mu = 0.
+ */
+qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* k_mean,
+                            void* workspace, size_t workspace_bytes, qattn_stream_t stream);
+
+/* a2 -- Q/K to int8 codes ("QFlash", section 4, eq. (1)-(2)).
+ * For each scale granule:  amax = max |x|;  inv = fp32(127 / amax) (0 if amax
+ * is 0);  code = clamp(round_half_even(fp32(x * inv)), -127, 127);
+ * scale = fp32(amax / 127).
+ *   Q            bf16 [B][Hq][Nq][d]                          x = fp32(Q)
+ *   K, k_dtype   QATTN_BF16: bf16 [B][Hkv][Nk][d];             x = fp32(fp32(K) - k_mean)
+ *                QATTN_I8:   int8 codes of an int8 KV cache, used as they are.
+ *   k_mean       fp32 [B][Hkv][d] (BF16 K; NULL = no mean subtraction)
+ *   k_chan_scale fp32 [B][Hkv][d] per-channel scale of int8 K codes (I8 K only).
+ *                It is folded into Q before Q is quantized,
+ *                x = fp32(fp32(Q) * k_chan_scale[b][h / (Hq/Hkv)][c]), so the
+ *                integer dot product with the stored codes stays exact, and
+ *                every K scale written is 1.
+ *   q_codes      int8 [B][Hq][Nq][d] (out)
+ *   q_scales     fp32, params->q_gran layout (out)
+ *   k_codes      int8 [B][Hkv][Nk][d] (out; BF16 K only, ignored for I8 K)
+ *   k_scales     fp32, params->k_gran layout (out)
+ */
+qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
+                               const float* k_mean, const float* k_chan_scale,
+                               const qattn_shape* shape, const qattn_params* params,
+                               int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                               float* k_scales, void* workspace, size_t workspace_bytes,
+                               qattn_stream_t stream);
+
+/* a3 -- V to e4m3 with one fp32 scale per (batch, KV head, channel) (ZINC
+ * post, "fp8 is not faster": e4m3 PV; the per-channel scale factors out of the
+ * PV sum onto the output channel).
+ *   V, v_dtype   QATTN_BF16: bf16 [B][Hkv][Nk][d];  x = fp32(V)
+ *                QATTN_I8:   int8 codes [B][Hkv][Nk][d] with v_chan_scale
+ *                            fp32 [B][Hkv][d];       x = fp32(code)
+ *   amax_c = max_t |x|;  v8 = e4m3_rn_satfinite(fp32(x * fp32(448 / amax_c)))
+ *   v_scales (out) fp32 [B][Hkv][d]: amax_c / 448 (BF16), or
+ *                  fp32(fp32(v_chan_scale * amax_c) / 448) (I8)
+ *   v8t (out)      e4m3 bytes [B][Hkv][d][ldv], TRANSPOSED (key index
+ *                  fastest); bytes for keys Nk..ldv-1 are written as 0.
+ *   ldv            row stride in bytes, >= qattn_v_ld(Nk), multiple of 16.
+ */
+qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,
+                              const qattn_shape* shape, uint8_t* v8t, int64_t ldv,
+                              float* v_scales, void* workspace, size_t workspace_bytes,
+                              qattn_stream_t stream);
+
+/* a4-a10 -- fused attention forward (prefill).
+ *   q_codes/q_scales, k_codes/k_scales   as written by qattn_quantize_qk
+ *   v8t, ldv, v_scales                    as written by qattn_quantize_v
+ *   bias   NULL, or fp32 [Nq][Nk] in natural-log units added to the scaled
+ *          scores (one matrix per head if params->bias_head_stride != 0).
+ *   O      (out) [B][Hq][Nq][d], fp32 or bf16 per params->out_dtype.
+ *   lse    (out, nullable) fp32 [B][Hq][Nq]: natural log of the softmax
+ *          denominator of the scaled scores (-inf for a fully masked row).
+ * Per query row, over key blocks of 128 in ascending order:
+ *   t = S * c_j (+ bias * log2 e), S the exact int32 score of the codes and
+ *       c_j = fp32(fp32(fp32(sq * sk_j) * sm_scale) * log2 e);  masked -> -inf
+ *   m' = max(m, max t);  alpha = 2^(m - m');  P = 2^(t - m') <= 1
+ *   l = alpha * l + sum P;  O = alpha * O + e4m3(448 P) . V8
+ *   out = O * v_scale / (448 l)   (0 for a row with no visible key)
+ * ("QFlash", section 2.1 and Algorithm 1 for the blockwise loop; ZINC post for
+ * P <= 1, the static 448 and e4m3.)  The QK^T product runs on the tensor cores
+ * as exact small integers held in fp16 (kind::f16, fp32 accumulation: every
+ * partial sum is an integer below 2^21, so no rounding occurs); PV runs as
+ * kind::f8f6f4 e4m3 x e4m3 with fp32 accumulation.
+ */
+qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
+                       const float* k_scales, const uint8_t* v8t, int64_t ldv,
+                       const float* v_scales, const float* bias, const qattn_shape* shape,
+                       const qattn_params* params, void* O, float* lse, void* workspace,
+                       size_t workspace_bytes, qattn_stream_t stream);
+
+/* a4 alone (debug) -- the int32 score tiles S = q_codes . k_codes^T
+ * ("QFlash", eq. (3)), through the same tensor-core path as qattn_fwd.
+ *   S (out) int32 [B][Hq][Nq][Nk]
+ */
+qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
+                                   const qattn_shape* shape, int32_t* S, void* workspace,
+                                   size_t workspace_bytes, qattn_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of
+ * the current device (QATTN_ERR_TIMEOUT if a kernel gave up on a wait). */
+qattn_status qattn_get_error(qattn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QATTN_H_ */

@@ -346,7 +346,10 @@ def online_softmax_pv(S, c, V8, s_v, *, visible, bias2=None, p_quant="e4m3",
     with np.errstate(divide="ignore", invalid="ignore"):
         inv_l = np.where(l > 0, 1.0 / l, 0.0)
     out = O * np.asarray(s_v, dtype=F64)[None, :] * inv_l[:, None]
-    res = {"O": out, "l": l, "m": m, "p_max": p_max}
+    with np.errstate(divide="ignore"):
+        lse = np.where(l > 0, (m.astype(F64) + np.log2(np.where(l > 0, l, 1.0))) * math.log(2.0),
+                       -np.inf)
+    res = {"O": out, "l": l, "m": m, "lse": lse, "p_max": p_max}
     if want_bound:
         res["bound"] = Bacc * np.asarray(s_v, dtype=F64)[None, :] * inv_l[:, None]
         res["n_ambiguous"] = n_amb
@@ -389,7 +392,7 @@ def attn_fwd(q_codes, q_scales, k_codes, k_scales, v8, s_v, *, q_gran, k_gran,
     bias2 = None
     if bias is not None:
         bias2 = (np.asarray(bias, F32)[rows] * LOG2E_F32).astype(F32)
-    outs, bounds = [], []
+    outs, bounds, lses = [], [], []
     for (b, h) in heads:
         g = kh[h]
         S = np.matmul(q_codes[b, h, rows].astype(F64), k_codes[b, g].astype(F64).T)
@@ -397,9 +400,10 @@ def attn_fwd(q_codes, q_scales, k_codes, k_scales, v8, s_v, *, q_gran, k_gran,
         r = online_softmax_pv(S, c, v8[b, g], s_v[b, g], visible=vis, bias2=bias2,
                               p_quant=p_quant, want_bound=want_bound)
         outs.append(r["O"])
+        lses.append(r["lse"])
         if want_bound:
             bounds.append(r["bound"])
-    res = {"O": np.stack(outs)}
+    res = {"O": np.stack(outs), "lse": np.stack(lses)}
     if want_bound:
         res["bound"] = np.stack(bounds)
     return res

@@ -1,0 +1,185 @@
+"""ctypes binding of libqattn.so (the C ABI in include/qattn.h).
+
+Argument marshalling only: every step of the recipe runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  The
+functions raise if the library is missing -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqattn.so")
+_lib = None
+
+OK = 0
+GRAN_TENSOR, GRAN_HEAD, GRAN_BLOCK = 0, 1, 2
+DT_BF16, DT_F32, DT_I8, DT_E4M3 = 0, 1, 2, 3
+POS0_BOTTOM_RIGHT = -(2 ** 63)
+
+EXPORTED = (
+    "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
+    "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
+    "qattn_debug_qk_scores", "qattn_get_error",
+)
+
+
+class QattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64),
+                ("Nq", ctypes.c_int64), ("Nk", ctypes.c_int64), ("d", ctypes.c_int64)]
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("causal", ctypes.c_int32), ("q_gran", ctypes.c_int32),
+                ("k_gran", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("q_pos0", ctypes.c_int64), ("sm_scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libqattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with quantized_attention_gb300.build.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    PS, PP = ctypes.POINTER(Shape), ctypes.POINTER(Params)
+    L.qattn_version.restype = ctypes.c_int
+    L.qattn_status_string.restype = ctypes.c_char_p
+    L.qattn_status_string.argtypes = [ctypes.c_int]
+    L.qattn_workspace_size.restype = sz
+    L.qattn_workspace_size.argtypes = [PS, PP]
+    L.qattn_v_ld.restype = i64
+    L.qattn_v_ld.argtypes = [i64]
+    L.qattn_smooth_k.argtypes = [vp, PS, vp, vp, sz, vp]
+    L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, sz, vp]
+    L.qattn_quantize_v.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
+    L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
+    L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
+    L.qattn_get_error.argtypes = [vp]
+    for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
+                 "qattn_debug_qk_scores", "qattn_get_error"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(st: int) -> str:
+    return lib().qattn_status_string(st).decode()
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise QattnError(st, where)
+
+
+def _dense(t: torch.Tensor, dtype, name: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def make_shape(B, Hq, Hkv, Nq, Nk, d) -> Shape:
+    return Shape(B, Hq, Hkv, Nq, Nk, d)
+
+
+def make_params(causal=False, q_gran=GRAN_BLOCK, k_gran=GRAN_BLOCK, out_dtype=DT_F32,
+                q_pos0=None, sm_scale=0.0, bias_head_stride=0) -> Params:
+    return Params(int(bool(causal)), q_gran, k_gran, out_dtype,
+                  POS0_BOTTOM_RIGHT if q_pos0 is None else int(q_pos0), float(sm_scale), 0,
+                  int(bias_head_stride))
+
+
+def version() -> int:
+    return lib().qattn_version()
+
+
+def workspace_size(shape: Shape, params: Params) -> int:
+    return lib().qattn_workspace_size(ctypes.byref(shape), ctypes.byref(params))
+
+
+def v_ld(Nk: int) -> int:
+    return lib().qattn_v_ld(Nk)
+
+
+def n_scales(gran: int, B: int, H: int, N: int) -> int:
+    return {GRAN_TENSOR: 1, GRAN_HEAD: B * H}.get(gran, B * H * ((N + 127) // 128))
+
+
+def smooth_k(K, shape, k_mean, workspace, stream=None):
+    _dense(K, torch.bfloat16, "K")
+    _dense(k_mean, torch.float32, "k_mean")
+    _check(lib().qattn_smooth_k(_p(K), ctypes.byref(shape), _p(k_mean), _p(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_smooth_k")
+
+
+def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_scales,
+                k_codes, k_scales, workspace, stream=None):
+    _dense(Q, torch.bfloat16, "Q")
+    _dense(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")
+    _check(lib().qattn_quantize_qk(_p(Q), _p(K), k_dtype, _p(k_mean), _p(k_chan_scale),
+                                   ctypes.byref(shape), ctypes.byref(params), _p(q_codes),
+                                   _p(q_scales), _p(k_codes), _p(k_scales), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_quantize_qk")
+
+
+def quantize_v(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, workspace, stream=None):
+    _dense(V, torch.int8 if v_dtype == DT_I8 else torch.bfloat16, "V")
+    _check(lib().qattn_quantize_v(_p(V), v_dtype, _p(v_chan_scale), ctypes.byref(shape), _p(v8t),
+                                  ldv, _p(v_scales), _p(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_quantize_v")
+
+
+def fwd(q_codes, q_scales, k_codes, k_scales, v8t, ldv, v_scales, bias, shape, params, O, lse,
+        workspace, stream=None):
+    _check(lib().qattn_fwd(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales), _p(v8t), ldv,
+                           _p(v_scales), _p(bias), ctypes.byref(shape), ctypes.byref(params),
+                           _p(O), _p(lse), _p(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_fwd")
+
+
+def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):
+    _dense(q_codes, torch.int8, "q_codes")
+    _dense(k_codes, torch.int8, "k_codes")
+    _dense(S, torch.int32, "S")
+    _check(lib().qattn_debug_qk_scores(_p(q_codes), _p(k_codes), ctypes.byref(shape), _p(S),
+                                       _p(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)),
+           "qattn_debug_qk_scores")
+
+
+def get_error(stream=None) -> int:
+    return lib().qattn_get_error(_stream(stream))

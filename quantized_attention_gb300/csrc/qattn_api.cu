@@ -1,0 +1,350 @@
+// The C ABI of libqattn.so (declared in include/qattn.h): host-side argument
+// validation, workspace carving, TMA descriptor encoding and kernel launches.
+// No entry point allocates device memory; every failure becomes a status.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qattn.h"
+#include "qattn_internal.h"
+
+namespace {
+
+using qattn::AttnArgs;
+
+// One error word per device; kernels OR error bits into it.
+__device__ unsigned int g_qattn_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+unsigned int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qattn_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool valid_d(int64_t d) { return d == 32 || d == 64 || d == 128; }
+
+// Shape checks shared by all entry points.  Returns QATTN_OK, or an error.
+qattn_status check_shape(const qattn_shape* s) {
+  if (!s) return QATTN_ERR_INVALID_ARG;
+  if (s->B < 0 || s->Hq < 0 || s->Hkv < 0 || s->Nq < 0 || s->Nk < 0 || s->d <= 0)
+    return QATTN_ERR_INVALID_ARG;
+  if (s->Hkv == 0 || (s->Hq % s->Hkv) != 0) return QATTN_ERR_INVALID_ARG;
+  if (!valid_d(s->d)) return QATTN_ERR_UNSUPPORTED;
+  // Grid limits: 128-token tiles index gridDim.y/z (<= 65535), and (batch,
+  // head) pairs index gridDim.y of the quantizers.
+  const int64_t lim = int64_t{65535} * 128;
+  if (s->Nq > lim || s->Nk > lim || s->B * s->Hq > 65535 || s->B > 65535)
+    return QATTN_ERR_UNSUPPORTED;
+  return QATTN_OK;
+}
+
+qattn_status check_params(const qattn_params* p) {
+  if (!p) return QATTN_ERR_INVALID_ARG;
+  if (p->q_gran < 0 || p->q_gran > 2 || p->k_gran < 0 || p->k_gran > 2) return QATTN_ERR_INVALID_ARG;
+  if (p->out_dtype != QATTN_F32 && p->out_dtype != QATTN_BF16) return QATTN_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return QATTN_ERR_INVALID_ARG;
+  if (p->reserved != 0 || p->bias_head_stride < 0) return QATTN_ERR_INVALID_ARG;
+  if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return QATTN_ERR_INVALID_ARG;
+  return QATTN_OK;
+}
+
+int64_t pos0_of(const qattn_shape* s, const qattn_params* p) {
+  return p->q_pos0 == QATTN_POS0_BOTTOM_RIGHT ? s->Nk - s->Nq : p->q_pos0;
+}
+
+qattn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QATTN_OK : QATTN_ERR_CUDA; }
+
+bool empty_problem(const qattn_shape* s) { return s->B == 0 || s->Hq == 0 || s->Nq == 0; }
+
+// Workspace regions of each entry point.
+size_t ws_smooth(const qattn_shape* s) { return align256(qattn::smooth_k_ws_bytes(s->B * s->Hkv, s->Nk, s->d)); }
+size_t ws_quant_qk(const qattn_shape* s, const qattn_params* p) {
+  return align256(qattn::quantize_rows_ws_bytes(s->B, s->Hq, s->Nq, p ? p->q_gran : 0)) +
+         align256(qattn::quantize_rows_ws_bytes(s->B, s->Hkv, s->Nk, p ? p->k_gran : 0));
+}
+size_t ws_quant_v(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hkv * s->d) * 4); }
+size_t ws_carriers_q(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hq * s->Nq * s->d) * 2); }
+size_t ws_carriers_k(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hkv * s->Nk * s->d) * 2); }
+size_t ws_fwd(const qattn_shape* s) { return ws_carriers_q(s) + ws_carriers_k(s); }
+
+// 3-D tiled map over a dense [planes][rows][inner] tensor.
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const void* ptr,
+               uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride_bytes,
+               uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, planes};
+  const cuuint64_t strides[2] = {row_stride_bytes, row_stride_bytes * rows};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  (void)esize;
+  return fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Maps over the fp16 carriers of Q [B*Hq][Nq][d] or K [B*Hkv][Nk][d].
+bool encode_carrier(CUtensorMap* map, const void* ptr, int64_t planes, int64_t rows, int64_t d) {
+  const uint32_t colblock = d >= 64 ? 64 : static_cast<uint32_t>(d);
+  const CUtensorMapSwizzle swz = (colblock * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, d, rows, planes, d * 2, colblock,
+                   128, swz);
+}
+
+}  // namespace
+
+extern "C" {
+
+int qattn_version(void) { return 100; }
+
+const char* qattn_status_string(qattn_status s) {
+  switch (s) {
+    case QATTN_OK: return "ok";
+    case QATTN_ERR_INVALID_ARG: return "invalid argument";
+    case QATTN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case QATTN_ERR_CUDA: return "CUDA error";
+    case QATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case QATTN_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int64_t qattn_v_ld(int64_t Nk) { return Nk <= 0 ? 16 : ((Nk + 15) / 16) * 16; }
+
+size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params) {
+  if (check_shape(shape) != QATTN_OK || empty_problem(shape)) return 0;
+  size_t m = ws_smooth(shape);
+  const size_t q = ws_quant_qk(shape, params);
+  if (q > m) m = q;
+  if (ws_quant_v(shape) > m) m = ws_quant_v(shape);
+  if (ws_fwd(shape) > m) m = ws_fwd(shape);
+  return m;
+}
+
+qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* k_mean,
+                            void* workspace, size_t workspace_bytes, qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if (shape->B == 0 || shape->Hkv == 0) return QATTN_OK;
+  if (!k_mean || !aligned16(k_mean) || (shape->Nk > 0 && (!K || !aligned16(K)))) return QATTN_ERR_INVALID_ARG;
+  const size_t need = ws_smooth(shape);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
+  return from_cuda(qattn::launch_smooth_k(K, static_cast<int>(shape->B * shape->Hkv),
+                                          static_cast<int>(shape->Nk), static_cast<int>(shape->d),
+                                          static_cast<long long*>(workspace), k_mean,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
+                               const float* k_mean, const float* k_chan_scale,
+                               const qattn_shape* shape, const qattn_params* params,
+                               int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                               float* k_scales, void* workspace, size_t workspace_bytes,
+                               qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (k_dtype != QATTN_BF16 && k_dtype != QATTN_I8) return QATTN_ERR_INVALID_ARG;
+  if (empty_problem(shape)) return QATTN_OK;
+  const bool i8 = (k_dtype == QATTN_I8);
+  if (!Q || !aligned16(Q) || !q_codes || !aligned16(q_codes) || !q_scales || !k_scales) return QATTN_ERR_INVALID_ARG;
+  if (i8 && (!k_chan_scale || !aligned16(k_chan_scale))) return QATTN_ERR_INVALID_ARG;
+  if (!i8 && shape->Nk > 0 && (!K || !aligned16(K) || !k_codes || !aligned16(k_codes))) return QATTN_ERR_INVALID_ARG;
+  if (k_mean && (i8 || !aligned16(k_mean))) return QATTN_ERR_INVALID_ARG;
+  const size_t wq = align256(qattn::quantize_rows_ws_bytes(shape->B, shape->Hq, shape->Nq, params->q_gran));
+  const size_t need = ws_quant_qk(shape, params);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* ws_q = static_cast<float*>(workspace);
+  float* ws_k = reinterpret_cast<float*>(static_cast<char*>(workspace) + wq);
+  const int B = static_cast<int>(shape->B), Hq = static_cast<int>(shape->Hq);
+  const int Hkv = static_cast<int>(shape->Hkv), d = static_cast<int>(shape->d);
+  cudaError_t e;
+  if (i8) {
+    e = qattn::launch_quantize_rows(Q, B, Hq, static_cast<int>(shape->Nq), d, 2, k_chan_scale, Hkv,
+                                    params->q_gran, q_codes, q_scales, ws_q, s);
+    if (e != cudaSuccess) return QATTN_ERR_CUDA;
+    const int64_t nkb = (shape->Nk + 127) / 128;
+    const int64_t n = params->k_gran == QATTN_GRAN_TENSOR ? 1
+                      : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
+                                                          : shape->B * shape->Hkv * nkb;
+    return from_cuda(qattn::launch_fill_ones(k_scales, n, s));
+  }
+  e = qattn::launch_quantize_rows(Q, B, Hq, static_cast<int>(shape->Nq), d, 0, nullptr, 1,
+                                  params->q_gran, q_codes, q_scales, ws_q, s);
+  if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  if (shape->Nk == 0) return QATTN_OK;
+  e = qattn::launch_quantize_rows(static_cast<const uint16_t*>(K), B, Hkv,
+                                  static_cast<int>(shape->Nk), d, k_mean ? 1 : 0, k_mean, Hkv,
+                                  params->k_gran, k_codes, k_scales, ws_k, s);
+  return from_cuda(e);
+}
+
+qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,
+                              const qattn_shape* shape, uint8_t* v8t, int64_t ldv,
+                              float* v_scales, void* workspace, size_t workspace_bytes,
+                              qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if (v_dtype != QATTN_BF16 && v_dtype != QATTN_I8) return QATTN_ERR_INVALID_ARG;
+  if (shape->B == 0 || shape->Hkv == 0) return QATTN_OK;
+  const bool i8 = (v_dtype == QATTN_I8);
+  if (!v_scales || !aligned16(v_scales)) return QATTN_ERR_INVALID_ARG;
+  if (shape->Nk > 0 && (!V || !aligned16(V) || !v8t || !aligned16(v8t))) return QATTN_ERR_INVALID_ARG;
+  if (i8 && (!v_chan_scale || !aligned16(v_chan_scale))) return QATTN_ERR_INVALID_ARG;
+  if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
+  const size_t need = ws_quant_v(shape);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  return from_cuda(qattn::launch_quantize_v(V, i8 ? 1 : 0, v_chan_scale,
+                                            static_cast<int>(shape->B * shape->Hkv),
+                                            static_cast<int>(shape->Nk), static_cast<int>(shape->d),
+                                            v8t, ldv, v_scales, static_cast<unsigned int*>(workspace),
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
+                       const float* k_scales, const uint8_t* v8t, int64_t ldv,
+                       const float* v_scales, const float* bias, const qattn_shape* shape,
+                       const qattn_params* params, void* O, float* lse, void* workspace,
+                       size_t workspace_bytes, qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (empty_problem(shape)) return QATTN_OK;
+  if (!q_codes || !aligned16(q_codes) || !q_scales || !O || !aligned16(O)) return QATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return QATTN_ERR_INVALID_ARG;
+  const int64_t pos0 = pos0_of(shape, params);
+  if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
+  if (shape->Nk > 0) {
+    if (!k_codes || !aligned16(k_codes) || !k_scales || !v8t || !aligned16(v8t) || !v_scales) return QATTN_ERR_INVALID_ARG;
+    if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return QATTN_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* err = error_word();
+  if (!err) return QATTN_ERR_CUDA;
+  AttnArgs a{};
+  a.B = static_cast<int>(shape->B);
+  a.Hq = static_cast<int>(shape->Hq);
+  a.Hkv = static_cast<int>(shape->Hkv);
+  a.Nq = static_cast<int>(shape->Nq);
+  a.Nk = static_cast<int>(shape->Nk);
+  a.d = static_cast<int>(shape->d);
+  a.causal = params->causal;
+  a.pos0 = params->causal ? static_cast<int>(pos0) : 0;
+  a.sm_scale = params->sm_scale > 0.f ? params->sm_scale
+                                      : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
+  a.q_gran = params->q_gran;
+  a.k_gran = params->k_gran;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.bias = bias;
+  a.bias_head_stride = params->bias_head_stride;
+  a.out = O;
+  a.out_bf16 = params->out_dtype == QATTN_BF16;
+  a.lse = lse;
+  a.err = err;
+  if (shape->Nk == 0) {
+    // No keys: every row is fully masked.  The kernel's empty-tile path
+    // writes the zeros; give it valid (unused) maps.
+    a.Nk = 0;
+  }
+  const size_t need = ws_fwd(shape);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  uint16_t* qc16 = static_cast<uint16_t*>(workspace);
+  uint16_t* kc16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + ws_carriers_q(shape));
+  cudaError_t e = qattn::launch_codes_to_f16(q_codes, qc16, static_cast<size_t>(shape->B * shape->Hq * shape->Nq * shape->d), s);
+  if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  if (shape->Nk > 0) {
+    e = qattn::launch_codes_to_f16(k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+    if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  }
+  CUtensorMap tq, tk, tv;
+  const int64_t nk_map = shape->Nk > 0 ? shape->Nk : 1;
+  if (!encode_carrier(&tq, qc16, shape->B * shape->Hq, shape->Nq, shape->d) ||
+      !encode_carrier(&tk, kc16, shape->B * shape->Hkv, nk_map, shape->d) ||
+      !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, shape->Nk > 0 ? static_cast<const void*>(v8t) : workspace,
+                 static_cast<uint64_t>(nk_map), static_cast<uint64_t>(shape->d),
+                 static_cast<uint64_t>(shape->B * shape->Hkv), static_cast<uint64_t>(shape->Nk > 0 ? ldv : 16), 128,
+                 static_cast<uint32_t>(shape->d), CU_TENSOR_MAP_SWIZZLE_128B))
+    return QATTN_ERR_CUDA;
+  return from_cuda(qattn::launch_attn_fwd(tq, tk, tv, a, s));
+}
+
+qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
+                                   const qattn_shape* shape, int32_t* S, void* workspace,
+                                   size_t workspace_bytes, qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if (empty_problem(shape) || shape->Nk == 0) return QATTN_OK;
+  if (!q_codes || !aligned16(q_codes) || !k_codes || !aligned16(k_codes) || !S || (reinterpret_cast<uintptr_t>(S) & 3u))
+    return QATTN_ERR_INVALID_ARG;
+  const size_t need = ws_fwd(shape);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* err = error_word();
+  if (!err) return QATTN_ERR_CUDA;
+  uint16_t* qc16 = static_cast<uint16_t*>(workspace);
+  uint16_t* kc16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + ws_carriers_q(shape));
+  cudaError_t e = qattn::launch_codes_to_f16(q_codes, qc16, static_cast<size_t>(shape->B * shape->Hq * shape->Nq * shape->d), s);
+  if (e == cudaSuccess)
+    e = qattn::launch_codes_to_f16(k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+  if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  CUtensorMap tq, tk;
+  if (!encode_carrier(&tq, qc16, shape->B * shape->Hq, shape->Nq, shape->d) ||
+      !encode_carrier(&tk, kc16, shape->B * shape->Hkv, shape->Nk, shape->d))
+    return QATTN_ERR_CUDA;
+  return from_cuda(qattn::launch_qk_debug(tq, tk, static_cast<int>(shape->B), static_cast<int>(shape->Hq),
+                                          static_cast<int>(shape->Hkv), static_cast<int>(shape->Nq),
+                                          static_cast<int>(shape->Nk), static_cast<int>(shape->d), S, err, s));
+}
+
+qattn_status qattn_get_error(qattn_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QATTN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qattn_error_word, sizeof(v)) != cudaSuccess) return QATTN_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_qattn_error_word, &zero, sizeof(zero)) != cudaSuccess) return QATTN_ERR_CUDA;
+  }
+  return (v & qattn::kErrTimeout) ? QATTN_ERR_TIMEOUT : QATTN_OK;
+}
+
+}  // extern "C"

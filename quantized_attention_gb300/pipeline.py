@@ -1,0 +1,110 @@
+"""The whole prefill path for one problem shape, with its device buffers.
+
+``Problem.run`` issues, on the current stream, the library calls of the
+recipe in order: K channel mean, Q/K int8 codes, per-channel e4m3 V, fused
+attention.  Buffers are allocated once (PyTorch supplies the memory) and
+reused across calls.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as qb
+
+
+class Problem:
+    def __init__(self, B, Hq, Hkv, Nq, Nk, d, *, causal=False, q_gran=qb.GRAN_BLOCK,
+                 k_gran=qb.GRAN_BLOCK, q_pos0=None, kv_codes=False, out_dtype=qb.DT_F32,
+                 bias_head_stride=0, want_lse=False, device="cuda"):
+        self.B, self.Hq, self.Hkv, self.Nq, self.Nk, self.d = B, Hq, Hkv, Nq, Nk, d
+        self.kv_codes = kv_codes
+        self.shape = qb.make_shape(B, Hq, Hkv, Nq, Nk, d)
+        self.params = qb.make_params(causal=causal, q_gran=q_gran, k_gran=k_gran,
+                                     out_dtype=out_dtype, q_pos0=q_pos0,
+                                     bias_head_stride=bias_head_stride)
+        self.ldv = qb.v_ld(Nk)
+        dev = torch.device(device)
+        i8, f32 = torch.int8, torch.float32
+        self.q_codes = torch.empty((B, Hq, Nq, d), dtype=i8, device=dev)
+        self.q_scales = torch.empty((qb.n_scales(q_gran, B, Hq, Nq),), dtype=f32, device=dev)
+        self.k_codes = None if kv_codes else torch.empty((B, Hkv, Nk, d), dtype=i8, device=dev)
+        self.k_scales = torch.empty((qb.n_scales(k_gran, B, Hkv, Nk),), dtype=f32, device=dev)
+        self.k_mean = None if kv_codes else torch.empty((B, Hkv, d), dtype=f32, device=dev)
+        self.v8t = torch.empty((B, Hkv, d, self.ldv), dtype=torch.uint8, device=dev)
+        self.v_scales = torch.empty((B, Hkv, d), dtype=f32, device=dev)
+        odt = torch.bfloat16 if out_dtype == qb.DT_BF16 else f32
+        self.O = torch.empty((B, Hq, Nq, d), dtype=odt, device=dev)
+        self.lse = torch.empty((B, Hq, Nq), dtype=f32, device=dev) if want_lse else None
+        ws = max(qb.workspace_size(self.shape, self.params), 256)
+        self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
+
+    def quantize(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
+                 V_scale=None, stream=None):
+        """a1-a3: codes and scales for Q, K and V."""
+        if self.kv_codes:
+            qb.quantize_qk(Q, K_codes, qb.DT_I8, None, K_scale, self.shape, self.params,
+                           self.q_codes, self.q_scales, None, self.k_scales, self.workspace, stream)
+            qb.quantize_v(V_codes, qb.DT_I8, V_scale, self.shape, self.v8t, self.ldv,
+                          self.v_scales, self.workspace, stream)
+            self._k_codes = K_codes
+        else:
+            qb.smooth_k(K, self.shape, self.k_mean, self.workspace, stream)
+            qb.quantize_qk(Q, K, qb.DT_BF16, self.k_mean, None, self.shape, self.params,
+                           self.q_codes, self.q_scales, self.k_codes, self.k_scales,
+                           self.workspace, stream)
+            qb.quantize_v(V, qb.DT_BF16, None, self.shape, self.v8t, self.ldv, self.v_scales,
+                          self.workspace, stream)
+            self._k_codes = self.k_codes
+
+    def attend(self, bias: Optional[torch.Tensor] = None, stream=None):
+        """a4-a10: the fused attention kernel on the quantized operands."""
+        qb.fwd(self.q_codes, self.q_scales, self._k_codes, self.k_scales, self.v8t, self.ldv,
+               self.v_scales, bias, self.shape, self.params, self.O, self.lse, self.workspace,
+               stream)
+        return self.O
+
+    def kernel_launches(self) -> int:
+        """Kernels of this library that one ``run`` launches (memsets excluded)."""
+        two_pass_q = self.params.q_gran != qb.GRAN_BLOCK
+        two_pass_k = self.params.k_gran != qb.GRAN_BLOCK
+        n = 1 + int(two_pass_q)                      # Q codes
+        if self.kv_codes:
+            n += 1                                   # K scales set to 1
+        else:
+            n += 2 + 1 + int(two_pass_k)             # channel mean (2), K codes
+        n += 2                                       # V amax, V e4m3 transpose
+        n += 3                                       # Q/K fp16 carriers, fused attention
+        return n
+
+    def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
+            V_scale=None, bias=None, stream=None):
+        self.quantize(Q, K, V, K_codes=K_codes, K_scale=K_scale, V_codes=V_codes,
+                      V_scale=V_scale, stream=stream)
+        return self.attend(bias, stream)
+
+
+def problem_for(wl, **kw) -> Problem:
+    """A Problem sized for a workload from quantized_attention_gb300.inputs."""
+    return Problem(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d, causal=wl.causal, q_gran=wl.q_gran,
+                   k_gran=wl.k_gran, q_pos0=wl.q_pos0, kv_codes=wl.kv_codes, **kw)
+
+
+def device_inputs(inp, device="cuda") -> dict:
+    """Host inputs (numpy) -> device tensors with the library's dtypes."""
+    def bf16(x):
+        return torch.from_numpy(x).to(device=device, dtype=torch.bfloat16)
+
+    d = {"Q": bf16(inp.Q)}
+    if inp.wl.kv_codes:
+        d["K_codes"] = torch.from_numpy(inp.K_codes).to(device)
+        d["K_scale"] = torch.from_numpy(inp.K_scale).to(device)
+        d["V_codes"] = torch.from_numpy(inp.V_codes).to(device)
+        d["V_scale"] = torch.from_numpy(inp.V_scale).to(device)
+    else:
+        d["K"] = bf16(inp.K)
+        d["V"] = bf16(inp.V)
+    if inp.bias is not None:
+        d["bias"] = torch.from_numpy(inp.bias).to(device)
+    return d

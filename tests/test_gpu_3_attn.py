@@ -1,0 +1,81 @@
+"""Fused attention output on the GPU against the oracle, element by element,
+at sizes the oracle finishes in seconds: several tiles, ragged tails, GQA,
+causal alignment, bias, every head dim, and the degenerate cases."""
+import numpy as np
+import pytest
+
+from oracle import qattn_oracle as O
+from quantized_attention_gb300 import binding as qb
+from quantized_attention_gb300 import inputs as I
+from tests.gpu_common import ensure_library, gpu_lse_rows, gpu_out_rows, run_gpu
+from tests.parity import check_output, rel_err_vs_fp64
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    I.WORKLOADS["tiny"],
+    I.small("vit", B=3),
+    I.small("vit", B=2, q_gran=I.GRAN_HEAD, k_gran=I.GRAN_HEAD),
+    I.small("swin", B=6),
+    I.small("llm8k", Hq=4, Hkv=2, Nq=640, Nk=640),
+    I.small("llm8k", Hq=2, Hkv=1, Nq=333, Nk=333, d=64),
+    I.small("llm8k", Hq=2, Hkv=2, Nq=300, Nk=300, d=32),
+    I.small("llm8k", Hq=2, Hkv=1, Nq=200, Nk=400, q_pos0=100),      # pos0 not on a block edge
+    I.small("llm8k", Hq=2, Hkv=1, Nq=300, Nk=100),                  # Nq > Nk: early rows see nothing
+    I.small("llm8k", Hq=1, Hkv=1, Nq=1, Nk=1, d=64),                # single token
+    I.small("llm8k", Hq=2, Hkv=1, Nq=1, Nk=777),                    # one query (decode-shaped row)
+    I.small("tiny", causal=False, Nq=3, Nk=1000),                   # few rows, many keys
+    I.small("chunk32k", Hq=4, Hkv=2, Nq=256, Nk=1024, q_pos0=768),
+    I.small("chunk32k", Hq=2, Hkv=2, Nq=100, Nk=301, q_pos0=201, d=32),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def _ids(w):
+    return f"{w.name}-B{w.B}-H{w.Hq}/{w.Hkv}-{w.Nq}x{w.Nk}-d{w.d}-c{int(w.causal)}"
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
+def test_output_matches_oracle(wl):
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P = run_gpu(wl, inp)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)][:16]
+    rows = np.arange(wl.Nq)
+    ref = O.run_workload(inp, prep, heads=heads, rows=rows, want_bound=True)
+    gpu = gpu_out_rows(P, heads, rows)
+    stats = check_output(gpu, ref["O"], ref["bound"], _ids(wl))
+    lse = gpu_lse_rows(P, heads, rows)
+    fin = np.isfinite(ref["lse"])
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref["lse"][fin], rtol=0, atol=1e-4)
+    K, V = O.real_kv(inp)
+    ref64 = O.attn_fp64(inp.Q, K, V, causal=wl.causal, q_pos0=wl.q_pos0, bias=inp.bias,
+                        heads=heads, rows=rows)
+    print(f"{_ids(wl)}: {stats}; rel err vs fp64 {rel_err_vs_fp64(gpu, ref64):.3e}")
+
+
+def test_bf16_output():
+    wl = I.small("llm8k", Hq=2, Hkv=1, Nq=384, Nk=384)
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P32 = run_gpu(wl, inp)
+    P16 = run_gpu(wl, inp, out_dtype=qb.DT_BF16)
+    heads = [(0, 0), (0, 1)]
+    rows = np.arange(wl.Nq)
+    o32 = gpu_out_rows(P32, heads, rows)
+    o16 = gpu_out_rows(P16, heads, rows)
+    # bf16 is the fp32 result rounded to nearest: within half a bf16 ulp
+    assert np.all(np.abs(o16 - o32) <= 2.0 ** -9 * np.abs(o32) + 1e-30)
+
+
+def test_repeat_calls_identical():
+    wl = I.small("llm8k", Hq=2, Hkv=1, Nq=256, Nk=256)
+    inp = I.make_inputs(wl)
+    a = run_gpu(wl, inp).O.cpu().numpy()
+    b = run_gpu(wl, inp).O.cpu().numpy()
+    assert np.array_equal(a, b)

@@ -402,3 +402,17 @@ def test_v_bf16_path():
             got = v8[0, h, :, c] * float(s_v[0, h, c])
             normal = np.abs(v8[0, h, :, c]) >= 2 ** -6
             assert np.all(np.abs(got - col)[normal] <= 2 ** -4 * np.abs(col)[normal] * (1 + 1e-6))
+
+
+def test_lse_matches_dense_log_sum_exp():
+    """The recipe's log-sum-exp equals ln sum_k exp(scaled score) of the
+    integer scores, computed densely in float64 (quantized P plays no part)."""
+    wl, inp, prep = _tiny_prep(seed=18)
+    r = O.run_workload(inp, prep)
+    S = O.qk_scores(prep["q_codes"], prep["k_codes"])[0, 0].astype(np.float64)
+    sq = O.expand_per_token(prep["q_scales"], wl.q_gran, 1, 1, 256)[0, 0]
+    sk = O.expand_per_token(prep["k_scales"], wl.k_gran, 1, 1, 256)[0, 0]
+    z = S * sq[:, None] * sk[None, :] / np.sqrt(64)
+    mx = z.max(axis=1, keepdims=True)
+    want = (mx + np.log(np.exp(z - mx).sum(axis=1, keepdims=True)))[:, 0]
+    np.testing.assert_allclose(r["lse"][0], want, rtol=0, atol=1e-5)

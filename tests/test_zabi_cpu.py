@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads without a GPU, exports every function
+include/qattn.h declares, and rejects bad arguments on the host (no kernel
+launch, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_attention_gb300 import binding, build
+    if not os.path.exists(binding.library_path()):
+        build.build()
+    return binding.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qattn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported(L):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    from quantized_attention_gb300 import binding
+    assert sorted(binding.EXPORTED) == names
+
+
+def test_host_only_queries(L):
+    from quantized_attention_gb300 import binding as qb
+    assert qb.version() == 100
+    assert qb.status_string(0) == "ok" and "workspace" in qb.status_string(5)
+    assert qb.v_ld(49) == 64 and qb.v_ld(128) == 128 and qb.v_ld(1) == 16
+    s = qb.make_shape(1, 32, 8, 8192, 8192, 128)
+    p = qb.make_params(causal=True)
+    assert qb.workspace_size(s, p) >= 2 * (32 + 8) * 8192 * 128
+    assert qb.workspace_size(qb.make_shape(0, 32, 8, 8192, 8192, 128), p) == 0
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    from quantized_attention_gb300 import binding as qb
+    vp = ctypes.c_void_p
+    s = qb.make_shape(1, 4, 2, 256, 256, 64)
+    p = qb.make_params()
+    fake = vp(1 << 20)  # aligned, never dereferenced: validation fails first
+    # null outputs
+    assert L.qattn_fwd(None, fake, fake, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
+    # misaligned pointer
+    assert L.qattn_fwd(vp((1 << 20) + 4), fake, fake, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
+    # unsupported head dim
+    s96 = qb.make_shape(1, 4, 2, 256, 256, 96)
+    assert L.qattn_smooth_k(fake, ctypes.byref(s96), fake, fake, 1 << 30, None) == 2
+    # Hq not a multiple of Hkv
+    s_bad = qb.make_shape(1, 5, 2, 256, 256, 64)
+    assert L.qattn_smooth_k(fake, ctypes.byref(s_bad), fake, fake, 1 << 30, None) == 1
+    # ldv too small
+    assert L.qattn_quantize_v(fake, 0, None, ctypes.byref(s), fake, 128, fake, fake, 1 << 30,
+                              None) == 1
+    # bad enum
+    p_bad = qb.make_params(q_gran=7)
+    assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p_bad),
+                               fake, fake, fake, fake, fake, 1 << 30, None) == 1
+    # workspace too small
+    assert L.qattn_smooth_k(fake, ctypes.byref(s), fake, fake, 16, None) == 5
+    # empty problem: ok, nothing launched
+    s0 = qb.make_shape(0, 4, 2, 256, 256, 64)
+    assert L.qattn_fwd(None, None, None, None, None, 0, None, None, ctypes.byref(s0),
+                       ctypes.byref(p), None, None, None, 0, None) == 0
