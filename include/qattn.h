@@ -160,6 +160,29 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
                               float* v_scales, void* workspace, size_t workspace_bytes,
                               qattn_stream_t stream);
 
+/* qattn_quantize_v without a workspace, for callers that cannot allocate
+ * device memory where they quantize V (an engine plugin handed only its
+ * tensors, a serving loop that bans cudaMalloc because it can synchronise the
+ * device, code running under an allocator it does not own).  The pages have no
+ * counterpart to this entry point; it computes exactly what qattn_quantize_v
+ * computes, with the same arguments minus the workspace.
+ *   Scratch: one library-owned device array of 2^19 32-bit slots (2 MiB),
+ *            held by every GPU that loads the library until the process exits.
+ *   Limit:   B * Hkv * d <= 524288, else QATTN_ERR_UNSUPPORTED.
+ *   Set-up:  the first call on a device looks up that array's device address
+ *            (cudaGetSymbolAddress) with the device current; make that first
+ *            call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *            contents; each call zeroes the slots it uses first.  Calls that
+ *            overlap on the GPU (e.g. on two streams at once) race on the
+ *            array: order them on one stream or with events.
+ *   No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+qattn_status qattn_quantize_v_noalloc(const void* V, qattn_dtype v_dtype,
+                                      const float* v_chan_scale, const qattn_shape* shape,
+                                      uint8_t* v8t, int64_t ldv, float* v_scales,
+                                      qattn_stream_t stream);
+
 /* a4-a10 -- fused attention forward (prefill).
  *   q_codes/q_scales, k_codes/k_scales   as written by qattn_quantize_qk
  *   v8t, ldv, v_scales                    as written by qattn_quantize_v

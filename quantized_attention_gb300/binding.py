@@ -23,7 +23,7 @@ POS0_BOTTOM_RIGHT = -(2 ** 63)
 EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-    "qattn_debug_qk_scores", "qattn_get_error",
+    "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
 )
 
 
@@ -69,11 +69,12 @@ def lib() -> ctypes.CDLL:
     L.qattn_smooth_k.argtypes = [vp, PS, vp, vp, sz, vp]
     L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, sz, vp]
     L.qattn_quantize_v.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
+    L.qattn_quantize_v_noalloc.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp]
     L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-                 "qattn_debug_qk_scores", "qattn_get_error"):
+                 "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -160,6 +161,15 @@ def quantize_v(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, workspace, s
                                   ldv, _p(v_scales), _p(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "qattn_quantize_v")
+
+
+def quantize_v_noalloc(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, stream=None):
+    """qattn_quantize_v for callers that cannot allocate: the library keeps the
+    scratch in its own static device array (see include/qattn.h)."""
+    _dense(V, torch.int8 if v_dtype == DT_I8 else torch.bfloat16, "V")
+    _check(lib().qattn_quantize_v_noalloc(_p(V), v_dtype, _p(v_chan_scale), ctypes.byref(shape),
+                                          _p(v8t), ldv, _p(v_scales), _stream(stream)),
+           "qattn_quantize_v_noalloc")
 
 
 def fwd(q_codes, q_scales, k_codes, k_scales, v8t, ldv, v_scales, bias, shape, params, O, lse,
