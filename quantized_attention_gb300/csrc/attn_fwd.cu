@@ -1,23 +1,26 @@
 // Fused quantized attention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
-// One CTA owns one 128-row query tile of one (batch, head).  Warp roles:
-//   warps 0-3 (128 threads, one query row each, TMEM lanes 0-127): read the
-//     score tile from TMEM, scale and mask it, keep the running row max and
-//     row sum in fp32, write P * 448 as e4m3 to shared memory, rescale the
-//     TMEM output accumulator when the max grows, and run the epilogue.
-//   warp 4: allocates TMEM; its lane 0 issues every TMA load and every MMA.
+// Persistent kernel, one CTA per SM.  A work item is one (batch, head) and two
+// consecutive 128-row query tiles (t0, t1); items are handed out heaviest
+// first (causal) in a snake order over the CTAs.  Warp roles (12 warps):
+//   warp 0      lane 0 issues every TMA load: the item's two Q tiles and a
+//               ring of K / V^T stages;
+//   warp 1      owns the 512 TMEM columns; lane 0 issues every MMA;
+//   warps 2-3   idle;
+//   warps 4-7   softmax of tile t0, warps 8-11 softmax of tile t1 (one query
+//               row per thread, row r = TMEM lane r).
+// TMEM: S_t at columns [128 t, 128 t + 128), O_t at [256 + 128 t, ...).  The
+// softmax writes e4m3 P_t over the first 32 columns of S_t; the PV MMA reads
+// it from TMEM as its A operand.
 //
-// Per key block j (128 keys):
-//   S  = Q . K_j^T     tcgen05.mma kind::f16  (int8 codes held exactly in fp16,
-//                      fp32 accumulation: every partial sum is an integer of
-//                      magnitude <= d * 127^2 < 2^21, so the result is exact)
-//   P8 = e4m3(448 * 2^(t - m))                 (softmax warps)
-//   O += P8 . V8_j     tcgen05.mma kind::f8f6f4 (e4m3 x e4m3 -> fp32 in TMEM)
-// The MMA thread issues PV_{j-1} before QK_j, so the commit that signals
-// "S_j ready" also certifies that PV_{j-1} has finished with O and with the
-// P buffer: the softmax warps may rescale O and overwrite P without another
-// barrier.  Two CTAs share an SM, so one CTA's softmax overlaps the other's
-// MMAs.
+// Per key block j the MMA thread issues, for t = t0 then t1:
+//   PV(t, j):   O_t (+)= P_t . V8_j      kind::f8f6f4, A from TMEM
+//   QK(t, j+1): S_t = Q_t . K_{j+1}^T    kind::f16 on exact fp16 carriers of
+//               the int8 codes (every partial sum is an integer below 2^21, so
+//               the fp32 accumulator holds it exactly)
+// so the tensor core works on one tile while the other tile's softmax runs.
+// The commit that publishes S_t(j+1) also certifies that PV(t, j) is done, so
+// the softmax may rescale O_t and overwrite P_t without another barrier.
 #include <cuda_bf16.h>
 
 #include "qattn_internal.h"
@@ -28,16 +31,16 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (MMA M)
 constexpr int kBN = 128;  // keys per block
-constexpr int kThreads = 160;
-constexpr float kLog2e = 1.44269502162933349609375f;   // fp32(log2 e)
-constexpr float kLog2_448 = 8.8073549220576041f;       // log2(448)
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.44269502162933349609375f;  // fp32(log2 e)
+constexpr float kLog2_448 = 8.8073549220576041f;      // log2(448)
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kNegInf = -__builtin_huge_valf();
 
-// Shared-memory plan for head dim D.  Q/K are fp16 carriers stored as
+// Shared-memory plan for head dim D.  Q and K are fp16 carriers stored as
 // column blocks of [128 rows][row_bytes] in the TMA/UMMA swizzled K-major
-// layout (128-byte rows with the 128B swizzle, 64-byte rows with the 64B
-// swizzle for D = 32).  V is e4m3 transposed, [D rows][128 keys]; P is e4m3
-// [128 rows][128 keys]; both use 128-byte rows with the 128B swizzle.
+// layout (128-byte rows and the 128B swizzle; 64-byte rows and the 64B
+// swizzle for D = 32).  V is e4m3 transposed, [D rows][128 keys], 128B swizzle.
 template <int D>
 struct Cfg {
   static constexpr int kColBlock = (D >= 64) ? 64 : D;  // fp16 elements per row of a block
@@ -46,18 +49,28 @@ struct Cfg {
   static constexpr int kColBlockBytes = kBM * kRowBytes;
   static constexpr uint32_t kSwz = (kRowBytes == 128) ? kSwizzle128B : kSwizzle64B;
   static constexpr uint32_t kSBO = 8 * kRowBytes;  // bytes between 8-row groups
-  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQS = (D == 128) ? 1 : 2;   // Q stages (each holds both tiles)
+  static constexpr int kNS = (D == 128) ? 3 : 4;   // K/V ring stages
+  static constexpr int kQTileBytes = kBM * D * 2;
   static constexpr int kKBytes = kBN * D * 2;
   static constexpr int kVBytes = D * kBN;
-  static constexpr int kPBytes = kBM * kBN;
+  static constexpr int kStageBytes = kKBytes + kVBytes;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kKBytes;
-  static constexpr int kOffP = kOffV + kVBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-  static constexpr uint32_t kTmemCols = 256;               // S: [0,128)  O: [128, 128+D)
-  static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "tile alignment");
+  static constexpr int kOffKV = kQS * 2 * kQTileBytes;
+  static constexpr int kOffBar = kOffKV + kNS * kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
+  static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kStageBytes % 1024 == 0,
+                "tile alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// Debug-kernel plan: one Q tile and one K tile.
+template <int D>
+struct DbgCfg {
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = Cfg<D>::kQTileBytes;
+  static constexpr int kOffBar = kOffK + Cfg<D>::kKBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
 };
 
 // S = Q . K^T for one 128 x 128 tile: D/16 MMAs of K = 16, fp32 into TMEM.
@@ -74,14 +87,15 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t sq, uint32_t 
   }
 }
 
-// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3.
+// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3, P read from TMEM
+// (8 columns of 4 e4m3 per MMA).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t sp, uint32_t sv, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t sv, bool acc) {
   constexpr uint32_t idesc = make_idesc(kBM, D, 0, 0);  // E4M3 x E4M3 -> F32
 #pragma unroll
   for (int s = 0; s < kBN / 32; ++s) {
-    mma_f8(tmem_o, smem_desc(sp + s * 32, 1024, kSwizzle128B),
-           smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc, (acc || s > 0) ? 1u : 0u);
+    mma_f8_tmem_a(tmem_o, tmem_p + s * 8, smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc,
+                  (acc || s > 0) ? 1u : 0u);
   }
 }
 
@@ -100,240 +114,385 @@ __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int 
   return __ldg(s + static_cast<size_t>(bh) * nblk + blk);
 }
 
-enum Bar { kQFull = 0, kKFull, kVFull, kSFull, kPFull, kKEmpty, kVEmpty, kOFull, kDrain, kNumBars };
+// Barrier slots.
+enum {
+  kBarQFull = 0,     // [2]   Q stage loaded
+  kBarQEmpty = 2,    // [2]   Q stage free
+  kBarKFull = 4,     // [4]   K stage loaded
+  kBarVFull = 8,     // [4]   V stage loaded
+  kBarKVEmpty = 12,  // [4]   K/V stage free
+  kBarSFull = 16,    // [2]   S_t ready (MMA commit)
+  kBarPFull = 18,    // [2]   P_t written, O_t rescaled (128 softmax threads)
+  kBarOFull = 20,    // [2]   last PV of the item done for tile t
+  kBarDrain = 22,    //       every MMA done (teardown)
+  kNumBars = 23
+};
+
+// One work item: (batch, head) x a pair of query tiles.
+struct Item {
+  int bq, bkv, h, q0;  // q0: first row of tile t0
+  int nb[2];           // key blocks each tile visits (0: no visible key, or no row)
+};
+
+__device__ __forceinline__ Item decode_item(int w, const AttnArgs& a, int n_pairs) {
+  const int BHq = a.B * a.Hq;
+  Item it;
+  const int pair = n_pairs - 1 - w / BHq;
+  const int bq = w % BHq;
+  const int b = bq / a.Hq;
+  it.h = bq % a.Hq;
+  it.bq = bq;
+  it.bkv = b * a.Hkv + it.h / (a.Hq / a.Hkv);
+  it.q0 = pair * 2 * kBM;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qs = it.q0 + t * kBM;
+    int kend = 0;
+    if (qs < a.Nq) {
+      kend = a.Nk;
+      if (a.causal) {
+        const long long last = static_cast<long long>(a.pos0) + min(qs + kBM - 1, a.Nq - 1);
+        kend = static_cast<int>(max(0LL, min(static_cast<long long>(a.Nk), last + 1)));
+      }
+    }
+    it.nb[t] = (kend + kBN - 1) / kBN;
+  }
+  return it;
+}
+
+// k-th item of CTA c (snake order over rounds of G items); -1 if none.
+__device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
+  const int w = (k & 1) ? (k + 1) * G - 1 - c : k * G + c;
+  return w < n_items ? w : -1;
+}
+
+// One softmax step for one query row and one key block.
+//   s      the row's 128 scores (fp32 bit patterns of integers; with BIAS they
+//          are overwritten by t = S c + bias log2e)
+//   nvis   keys 0 .. nvis-1 of the block are visible (MASKED only)
+// Updates the running max m and sum l (l in units of 448 P), returns alpha
+// and the e4m3 codes of 448 P packed four per word (key 4q + e in byte e).
+template <bool BIAS, bool MASKED>
+__device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int nvis,
+                                              const float* brow, float& m, float& l,
+                                              uint32_t (&pw)[kBN / 4]) {
+  float mx;
+  {
+    if (BIAS) {
+#pragma unroll
+      for (int k = 0; k < kBN; ++k) {
+        float t = fmaf(__uint_as_float(s[k]), c, __fmul_rn(__ldg(brow + k), kLog2e));
+        if (MASKED && k >= nvis) t = kNegInf;
+        s[k] = __float_as_uint(t);
+      }
+    }
+    float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
+#pragma unroll
+    for (int k = 0; k < kBN; k += 8) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[e] = __uint_as_float(s[k + e]);
+        if (MASKED && !BIAS && k + e >= nvis) v[e] = kNegInf;
+      }
+      mx0 = fmax3(mx0, v[0], v[1]);
+      mx1 = fmax3(mx1, v[2], v[3]);
+      mx2 = fmax3(mx2, v[4], v[5]);
+      mx3 = fmax3(mx3, v[6], v[7]);
+    }
+    mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+  }
+  float m_blk;
+  if (BIAS) m_blk = mx;
+  else m_blk = (mx == kNegInf) ? kNegInf : __fmul_rn(mx, c);
+  const float m_new = fmaxf(m, m_blk);
+  const bool dead = (m_new == kNegInf);
+  const float alpha = dead ? 1.f : ex2_approx(m - m_new);
+  const float kneg = dead ? 0.f : (kLog2_448 - m_new);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int k = 0; k < kBN; k += 4) {
+    uint32_t half[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int kk = k + 2 * e;
+      float2 x;
+      if (BIAS) {
+        x = fadd2(make_float2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])),
+                  make_float2(kneg, kneg));
+      } else {
+        x = ffma2(make_float2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])),
+                  make_float2(c, c), make_float2(kneg, kneg));
+      }
+      if (MASKED) {
+        if (kk >= nvis) x.x = kNegInf;
+        if (kk + 1 >= nvis) x.y = kNegInf;
+      }
+      const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      acc[(k / 2 + e) & 3] = fadd2(acc[(k / 2 + e) & 3], p);
+      half[e] = cvt_e4m3x2(p.x, p.y);
+    }
+    pw[k / 4] = half[0] | (half[1] << 16);
+  }
+  const float2 a01 = fadd2(acc[0], acc[1]);
+  const float2 a23 = fadd2(acc[2], acc[3]);
+  const float2 tot = fadd2(a01, a23);
+  l = fmaf(alpha, l, tot.x + tot.y);
+  m = m_new;
+  return alpha;
+}
 
 template <int D, bool BIAS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a, int n_items) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::kOffQ, sK = base + C::kOffK, sV = base + C::kOffV;
-  const uint32_t sP = base + C::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 8 * kNumBars + 4);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto sQ = [&](int qs, int t) { return base + C::kOffQ + (qs * 2 + t) * C::kQTileBytes; };
+  auto sK = [&](int st) { return base + C::kOffKV + st * C::kStageBytes; };
+  auto sV = [&](int st) { return base + C::kOffKV + st * C::kStageBytes + C::kKBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int G = gridDim.x, cta = blockIdx.x;
   const int n_qt = (a.Nq + kBM - 1) / kBM;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.z);  // heaviest causal tiles first
-  const int q0 = qt * kBM;
-  const int hkv = h / (a.Hq / a.Hkv);
-  const int bq = b * a.Hq + h, bkv = b * a.Hkv + hkv;
-
-  int kend = a.Nk;  // one past the last key any row of this tile can see
-  if (a.causal) {
-    const long long last = static_cast<long long>(a.pos0) + min(q0 + kBM - 1, a.Nq - 1);
-    kend = static_cast<int>(max(0LL, min(static_cast<long long>(a.Nk), last + 1)));
-  }
-  const int nb = (kend + kBN - 1) / kBN;
-
-  if (nb == 0) {  // every row of the tile sees no key: output 0, lse -inf
-    if (threadIdx.x < kBM) {
-      const int qi = q0 + threadIdx.x;
-      if (qi < a.Nq) {
-        const size_t row = static_cast<size_t>(bq) * a.Nq + qi;
-        for (int c = 0; c < D; ++c) {
-          if (a.out_bf16) reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + c] = __float2bfloat16(0.f);
-          else reinterpret_cast<float*>(a.out)[row * D + c] = 0.f;
-        }
-        if (a.lse) a.lse[row] = -INFINITY;
-      }
-    }
-    return;
-  }
+  const int n_pairs = (n_qt + 1) / 2;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, kBM, 1, 1, 1, 1};
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), counts[i]);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? kBM : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
 
-  if (warp == 4) {
+  if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA + MMA issue
+      // ------------------------------------------------------------ TMA
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int pend_k = -1, pend_v = -1;  // loads issued but not yet observed complete
-      mbar_arrive_expect_tx(bar(kQFull), C::kQBytes);
-      tma_tile<D>(&tmQ, sQ, bar(kQFull), q0, bq);
-      mbar_arrive_expect_tx(bar(kKFull), C::kKBytes);
-      tma_tile<D>(&tmK, sK, bar(kKFull), 0, bkv);
-      pend_k = 0;
-      mbar_arrive_expect_tx(bar(kVFull), C::kVBytes);
-      tma_load_3d(sV, &tmV, bar(kVFull), 0, 0, bkv);
-      pend_v = 0;
-      bool ok = mbar_wait(bar(kQFull), 0, abort_flag, a.err, kErrTimeout);
-      for (int j = 0; ok && j < nb; ++j) {
-        if (!(ok = mbar_wait(bar(kKFull), j & 1, abort_flag, a.err, kErrTimeout))) break;
-        pend_k = -1;
-        if (j > 0) {
-          if (!(ok = mbar_wait(bar(kPFull), (j - 1) & 1, abort_flag, a.err, kErrTimeout))) break;
-          if (!(ok = mbar_wait(bar(kVFull), (j - 1) & 1, abort_flag, a.err, kErrTimeout))) break;
-          pend_v = -1;
-          tc_fence_after();
-          issue_pv<D>(tO, sP, sV, j - 1 > 0);
-          mma_commit(bar(kVEmpty));
+      int last_q[2] = {-1, -1}, last_kv[4] = {-1, -1, -1, -1};
+      uint32_t kv = 0;
+      int i = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * G < n_items; ++k) {
+        const int w = item_index(k, cta, G, n_items);
+        if (w < 0) continue;
+        const Item it = decode_item(w, a, n_pairs);
+        const int qs = i % C::kQS;
+        if (i >= C::kQS &&
+            !(ok = mbar_wait(bar(kBarQEmpty + qs), ((i / C::kQS) - 1) & 1, abort_flag, a.err,
+                             kErrTimeout)))
+          break;
+        mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * C::kQTileBytes);
+        tma_tile<D>(&tmQ, sQ(qs, 0), bar(kBarQFull + qs), it.q0, it.bq);
+        tma_tile<D>(&tmQ, sQ(qs, 1), bar(kBarQFull + qs), it.q0 + kBM, it.bq);
+        last_q[qs] = i;
+        const int nb = max(it.nb[0], it.nb[1]);
+        for (int j = 0; j < nb; ++j, ++kv) {
+          const int st = kv % C::kNS;
+          if (kv >= static_cast<uint32_t>(C::kNS) &&
+              !(ok = mbar_wait(bar(kBarKVEmpty + st), ((kv / C::kNS) - 1) & 1, abort_flag, a.err,
+                               kErrTimeout)))
+            break;
+          mbar_arrive_expect_tx(bar(kBarKFull + st), C::kKBytes);
+          tma_tile<D>(&tmK, sK(st), bar(kBarKFull + st), j * kBN, it.bkv);
+          mbar_arrive_expect_tx(bar(kBarVFull + st), C::kVBytes);
+          tma_load_3d(sV(st), &tmV, bar(kBarVFull + st), j * kBN, 0, it.bkv);
+          last_kv[st] = static_cast<int>(kv);
         }
-        tc_fence_after();
-        issue_qk<D>(tS, sQ, sK);
-        mma_commit(bar(kSFull));
-        mma_commit(bar(kKEmpty));
-        if (j + 1 < nb) {
-          if (!(ok = mbar_wait(bar(kKEmpty), j & 1, abort_flag, a.err, kErrTimeout))) break;
-          mbar_arrive_expect_tx(bar(kKFull), C::kKBytes);
-          tma_tile<D>(&tmK, sK, bar(kKFull), (j + 1) * kBN, bkv);
-          pend_k = (j + 1) & 1;
-        }
-        if (j > 0) {
-          if (!(ok = mbar_wait(bar(kVEmpty), (j - 1) & 1, abort_flag, a.err, kErrTimeout))) break;
-          mbar_arrive_expect_tx(bar(kVFull), C::kVBytes);
-          tma_load_3d(sV, &tmV, bar(kVFull), j * kBN, 0, bkv);
-          pend_v = j & 1;
-        }
+        ++i;
       }
-      if (ok) {
-        ok = mbar_wait(bar(kPFull), (nb - 1) & 1, abort_flag, a.err, kErrTimeout) &&
-             mbar_wait(bar(kVFull), (nb - 1) & 1, abort_flag, a.err, kErrTimeout);
-        if (ok) {
-          pend_v = -1;
-          tc_fence_after();
-          issue_pv<D>(tO, sP, sV, nb - 1 > 0);
-          mma_commit(bar(kOFull));
-        }
-      }
-      // Let every MMA this thread issued finish before TMEM can be freed, and
-      // let any TMA load still in flight land, each with a bounded wait.
-      mma_commit(bar(kDrain));
+      // Every load this thread issued lands before the CTA may exit.
       volatile int never = 0;
-      mbar_wait(bar(kDrain), 0, &never, a.err, kErrTimeout);
-      if (pend_k >= 0) mbar_wait(bar(kKFull), pend_k, &never, a.err, kErrTimeout);
-      if (pend_v >= 0) mbar_wait(bar(kVFull), pend_v, &never, a.err, kErrTimeout);
+      for (int qs = 0; qs < C::kQS; ++qs)
+        if (last_q[qs] >= 0)
+          mbar_wait(bar(kBarQFull + qs), (last_q[qs] / C::kQS) & 1, &never, a.err, kErrTimeout);
+      for (int st = 0; st < C::kNS; ++st)
+        if (last_kv[st] >= 0) {
+          mbar_wait(bar(kBarKFull + st), (last_kv[st] / C::kNS) & 1, &never, a.err, kErrTimeout);
+          mbar_wait(bar(kBarVFull + st), (last_kv[st] / C::kNS) & 1, &never, a.err, kErrTimeout);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA
+      uint32_t kv = 0, pc[2] = {0, 0};
+      int i = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * G < n_items; ++k) {
+        const int w = item_index(k, cta, G, n_items);
+        if (w < 0) continue;
+        const Item it = decode_item(w, a, n_pairs);
+        const int qs = i % C::kQS;
+        if (!(ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
+          break;
+        const int nb = max(it.nb[0], it.nb[1]);
+        if (nb > 0) {
+          const int st0 = kv % C::kNS;
+          if (!(ok = mbar_wait(bar(kBarKFull + st0), (kv / C::kNS) & 1, abort_flag, a.err, kErrTimeout)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (it.nb[t] > 0) {
+              issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st0));
+              mma_commit(bar(kBarSFull + t));
+            }
+          for (int j = 0; ok && j < nb; ++j) {
+            const uint32_t cur = kv + j, nxt = kv + j + 1;
+            const int st = cur % C::kNS, stn = nxt % C::kNS;
+            bool v_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || j >= it.nb[t]) continue;
+              if (!(ok = mbar_wait(bar(kBarPFull + t), pc[t] & 1, abort_flag, a.err, kErrTimeout)))
+                continue;
+              ++pc[t];
+              if (!v_ready) {
+                if (!(ok = mbar_wait(bar(kBarVFull + st), (cur / C::kNS) & 1, abort_flag, a.err,
+                                     kErrTimeout)))
+                  continue;
+                v_ready = true;
+              }
+              tc_fence_after();
+              issue_pv<D>(tmem + 256 + 128 * t, tmem + 128 * t, sV(st), j > 0);
+              if (j + 1 < it.nb[t]) {
+                if (!(ok = mbar_wait(bar(kBarKFull + stn), (nxt / C::kNS) & 1, abort_flag, a.err,
+                                     kErrTimeout)))
+                  continue;
+                tc_fence_after();
+                issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(stn));
+                mma_commit(bar(kBarSFull + t));
+              } else {
+                mma_commit(bar(kBarOFull + t));
+              }
+            }
+            if (ok) mma_commit(bar(kBarKVEmpty + st));
+          }
+          kv += nb;
+        }
+        if (ok) mma_commit(bar(kBarQEmpty + qs));
+        ++i;
+      }
+      // Every MMA this thread issued finishes before TMEM is freed.
+      mma_commit(bar(kBarDrain));
+      volatile int never = 0;
+      mbar_wait(bar(kBarDrain), 0, &never, a.err, kErrTimeout);
       if (!ok) *abort_flag = 1;
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------ softmax warpgroup
-    const int r = threadIdx.x;  // row within the tile == TMEM lane
-    const int qi = q0 + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) / 4;  // tile of this warpgroup
+    const int wq = warp & 3;       // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;  // row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
     const int nqb = (a.Nq + kBM - 1) / kBM, nkb = (a.Nk + kBN - 1) / kBN;
-    const float sq = scale_of(a.q_scales, a.q_gran, bq, nqb, qt);
-    const long long lim = static_cast<long long>(a.pos0) + qi;  // last visible key (causal)
-    const float* brow = nullptr;
-    if (BIAS) brow = a.bias + static_cast<size_t>(h) * a.bias_head_stride + static_cast<size_t>(min(qi, a.Nq - 1)) * a.Nk;
-    const uint32_t prow = sP + r * 128;
-    const uint32_t sw = r & 7;
-    float m = -INFINITY, l = 0.f;
+    uint32_t sc = 0, oc = 0;
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      ok = mbar_wait(bar(kSFull), j & 1, abort_flag, a.err, kErrTimeout);
-      if (!__all_sync(0xffffffffu, ok)) {  // keep the warp converged for tcgen05.ld
+    for (int k = 0; ok && k * G < n_items; ++k) {
+      const int w = item_index(k, cta, G, n_items);
+      if (w < 0) continue;
+      const Item it = decode_item(w, a, n_pairs);
+      const int q0t = it.q0 + t * kBM;
+      const int qi = q0t + r;
+      const int nbt = it.nb[t];
+      const size_t row = static_cast<size_t>(it.bq) * a.Nq + qi;
+      if (nbt == 0) {  // no visible key for any row of this tile: output 0
+        if (qi < a.Nq) {
+          for (int cidx = 0; cidx < D; ++cidx) {
+            if (a.out_bf16)
+              reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + cidx] = __float2bfloat16(0.f);
+            else
+              reinterpret_cast<float*>(a.out)[row * D + cidx] = 0.f;
+          }
+          if (a.lse) a.lse[row] = kNegInf;
+        }
+        continue;
+      }
+      const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
+      const long long lim = static_cast<long long>(a.pos0) + qi;  // last visible key (causal)
+      const float* brow = nullptr;
+      if (BIAS)
+        brow = a.bias + static_cast<size_t>(it.h) * a.bias_head_stride +
+               static_cast<size_t>(min(qi, a.Nq - 1)) * a.Nk;
+      float m = kNegInf, l = 0.f;
+      for (int j = 0; j < nbt; ++j) {
+        ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag, a.err, kErrTimeout);
+        ++sc;
+        if (!__all_sync(0xffffffffu, ok)) {  // keep the warp converged for tcgen05.ld
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[kBN];
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i)
+          tmem_ld32(tS + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[i * 32]));
+        tmem_wait_ld();
+        const float sk = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j);
+        const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
+        const int kbase = j * kBN;
+        const bool need_mask =
+            (kbase + kBN > a.Nk) ||
+            (a.causal && static_cast<long long>(kbase) + kBN - 1 > static_cast<long long>(a.pos0) + q0t);
+        long long lastk = static_cast<long long>(a.Nk) - 1;
+        if (a.causal && lim < lastk) lastk = lim;
+        const int nvis =
+            static_cast<int>(max(0LL, min(static_cast<long long>(kBN), lastk - kbase + 1)));
+        uint32_t pw[kBN / 4];
+        const float* bk = BIAS ? brow + kbase : nullptr;
+        const float alpha = need_mask ? softmax_step<BIAS, true>(s, c, nvis, bk, m, l, pw)
+                                      : softmax_step<BIAS, false>(s, c, kBN, bk, m, l, pw);
+        tmem_st32(tS + lane_base, pw);  // P over the first 32 columns of S_t
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_base + cc * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const float2 v = fmul2(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])),
+                                     make_float2(alpha, alpha));
+              o[q] = __float_as_uint(v.x);
+              o[q + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + lane_base + cc * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + t));
+      }
+      if (!ok) break;
+      ok = mbar_wait(bar(kBarOFull + t), oc & 1, abort_flag, a.err, kErrTimeout);
+      ++oc;
+      if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t s[kBN];
-#pragma unroll
-      for (int i = 0; i < kBN / 32; ++i)
-        tmem_ld32(tS + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[i * 32]));
-      tmem_wait_ld();
-      const float sk = scale_of(a.k_scales, a.k_gran, bkv, nkb, j);
-      const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
-      const int kbase = j * kBN;
-      long long lastk = static_cast<long long>(a.Nk) - 1;
-      if (a.causal && lim < lastk) lastk = lim;
-      const int nvis = static_cast<int>(max(0LL, min(static_cast<long long>(kBN), lastk - kbase + 1)));
-      float m_blk = -INFINITY;
-      if (!BIAS) {
-        float mx = -INFINITY;
-        if (nvis == kBN) {
-#pragma unroll
-          for (int k = 0; k < kBN; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < kBN; ++k)
-            if (k < nvis) mx = fmaxf(mx, __uint_as_float(s[k]));
-        }
-        m_blk = (mx == -INFINITY) ? -INFINITY : __fmul_rn(mx, c);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBN; ++k) {
-          float t = -INFINITY;
-          if (k < nvis) t = fmaf(__uint_as_float(s[k]), c, __fmul_rn(__ldg(brow + kbase + k), kLog2e));
-          s[k] = __float_as_uint(t);
-          m_blk = fmaxf(m_blk, t);
-        }
-      }
-      const float m_new = fmaxf(m, m_blk);
-      const bool dead = (m_new == -INFINITY);
-      const float alpha = dead ? 1.f : ex2_approx(m - m_new);
-      const float kneg = dead ? 0.f : (kLog2_448 - m_new);
-      float sum = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < kBN / 16; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = ch * 16 + q * 4 + e;
-            float x;
-            if (!BIAS) x = fmaf(__uint_as_float(s[k]), c, kneg);
-            else x = __uint_as_float(s[k]) + kneg;
-            if (k >= nvis) x = -INFINITY;
-            p[e] = ex2_approx(x);
-            sum += p[e];
-          }
-          w[q] = cvt_e4m3x2(p[0], p[1]) | (cvt_e4m3x2(p[2], p[3]) << 16);
-        }
-        const uint32_t addr = prow + ((static_cast<uint32_t>(ch) ^ sw) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                     "r"(w[2]), "r"(w[3])
-                     : "memory");
-      }
-      l = fmaf(alpha, l, sum);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + lane_base + cc * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + lane_base + cc * 32, o);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kPFull));
-      m = m_new;
-    }
-    if (ok) ok = mbar_wait(bar(kOFull), 0, abort_flag, a.err, kErrTimeout);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const float* sv = a.v_scales + static_cast<size_t>(bkv) * D;
-      const size_t row = static_cast<size_t>(bq) * a.Nq + qi;
+      const float* sv = a.v_scales + static_cast<size_t>(it.bkv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -342,44 +501,44 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (qi < a.Nq) {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * (__ldg(sv + cc * 32 + i) * inv_l);
+          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(o[q]) * (__ldg(sv + cc * 32 + q) * inv_l);
           if (a.out_bf16) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t w[4];
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wv[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
-                w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                wv[e] = *reinterpret_cast<const uint32_t*>(&pr);
               }
-              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           } else {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + row * D + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
       }
-      if (a.lse && qi < a.Nq)
-        a.lse[row] = (l > 0.f) ? (m + __log2f(l) - kLog2_448) * kLn2 : -INFINITY;
+      if (a.lse && qi < a.Nq) a.lse[row] = (l > 0.f) ? (m + __log2f(l) - kLog2_448) * kLn2 : kNegInf;
     }
+    if (!ok) *abort_flag = 1;
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 // Debug: the int32 score tile of one (q tile, k tile) through issue_qk.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(160, 1)
     qk_debug_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     int Hq, int Hkv, int Nq, int Nk, int32_t* __restrict__ S, unsigned int* err) {
-  using C = Cfg<D>;
+  using C = DbgCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -410,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     if (lane == 0) {
       const uint32_t full = smem_u32(&bars[0]);
-      mbar_arrive_expect_tx(full, C::kQBytes + C::kKBytes);
+      mbar_arrive_expect_tx(full, Cfg<D>::kQTileBytes + Cfg<D>::kKBytes);
       tma_tile<D>(&tmQ, sQ, full, qt * kBM, bq);
       tma_tile<D>(&tmK, sK, full, kt * kBN, bkv);
       volatile int never = 0;
@@ -454,6 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
 template <int D, bool BIAS>
 cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnArgs& a, cudaStream_t s) {
@@ -461,20 +627,23 @@ cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BIAS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.Hq, a.B, (a.Nq + kBM - 1) / kBM);
-  attn_fwd_kernel<D, BIAS><<<grid, kThreads, smem, s>>>(tq, tk, tv, a);
+  const int n_qt = (a.Nq + kBM - 1) / kBM;
+  const long long n_items = static_cast<long long>(a.B) * a.Hq * ((n_qt + 1) / 2);
+  if (n_items <= 0) return cudaSuccess;
+  const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
+  attn_fwd_kernel<D, BIAS><<<grid, kThreads, smem, s>>>(tq, tk, tv, a, static_cast<int>(n_items));
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dbg_t(const CUtensorMap& tq, const CUtensorMap& tk, int B, int Hq, int Hkv,
                          int Nq, int Nk, int32_t* S, unsigned int* err, cudaStream_t s) {
-  const int smem = Cfg<D>::kSmemBytes;
+  const int smem = DbgCfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(qk_debug_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((Nk + kBN - 1) / kBN, (Nq + kBM - 1) / kBM, B * Hq);
-  qk_debug_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, Hq, Hkv, Nq, Nk, S, err);
+  qk_debug_kernel<D><<<grid, 160, smem, s>>>(tq, tk, Hq, Hkv, Nq, Nk, S, err);
   return cudaGetLastError();
 }
 
