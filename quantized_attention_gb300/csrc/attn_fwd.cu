@@ -3,24 +3,27 @@
 // Persistent kernel, one CTA per SM.  A work item is one (batch, head) and two
 // consecutive 128-row query tiles (t0, t1); items are handed out heaviest
 // first (causal) in a snake order over the CTAs.  Warp roles (12 warps):
-//   warp 0      lane 0 issues every TMA load: the item's two Q tiles and a
-//               ring of K / V^T stages;
-//   warp 1      owns the 512 TMEM columns; lane 0 issues every MMA;
-//   warps 2-3   idle;
+//   warp 0      lane 0 issues every TMA load: the item's two Q tiles, a ring
+//               of K stages and a ring of V^T stages;
+//   warp 1      owns the 512 TMEM columns; lane 0 issues the QK^T MMAs;
+//   warp 2      lane 0 issues the PV MMAs;
+//   warp 3      idle;
 //   warps 4-7   softmax of tile t0, warps 8-11 softmax of tile t1 (one query
 //               row per thread, row r = TMEM lane r).
-// TMEM: S_t at columns [128 t, 128 t + 128), O_t at [256 + 128 t, ...).  The
-// softmax writes e4m3 P_t over the first 32 columns of S_t; the PV MMA reads
-// it from TMEM as its A operand.
+// TMEM: S_t at columns [128 t, 128 t + 128), O_t at [256 + 128 t, ...).
+// Shared memory holds the e4m3 P_t tiles the PV MMAs read.
 //
-// Per key block j the MMA thread issues, for t = t0 then t1:
-//   PV(t, j):   O_t (+)= P_t . V8_j      kind::f8f6f4, A from TMEM
-//   QK(t, j+1): S_t = Q_t . K_{j+1}^T    kind::f16 on exact fp16 carriers of
-//               the int8 codes (every partial sum is an integer below 2^21, so
-//               the fp32 accumulator holds it exactly)
-// so the tensor core works on one tile while the other tile's softmax runs.
-// The commit that publishes S_t(j+1) also certifies that PV(t, j) is done, so
-// the softmax may rescale O_t and overwrite P_t without another barrier.
+// Per tile t and key block j:
+//   softmax(t, j) loads S_t(j) from TMEM and at once releases it (s_free), so
+//   the MMA thread issues QK(t, j+1) -- S_t = Q_t . K_{j+1}^T, kind::f16 on
+//   exact fp16 carriers of the int8 codes (every partial sum is an integer
+//   below 2^21, so the fp32 accumulator holds it exactly) -- while the
+//   softmax computes P; when P_t(j) is in shared memory and O_t rescaled
+//   (p_full) the MMA thread issues PV(t, j): O_t (+)= P_t . V8_j, kind::f8f6f4.
+//   softmax(t, j+1) waits for PV(t, j) (pv_done) before it overwrites P_t or
+//   rescales O_t.
+// The two tiles' softmaxes run on different warps, so the tensor core works on
+// one tile while the other's softmax runs, and QK(t, j+1) overlaps softmax(t, j).
 #include <cuda_bf16.h>
 
 #include "qattn_internal.h"
@@ -40,7 +43,8 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // Shared-memory plan for head dim D.  Q and K are fp16 carriers stored as
 // column blocks of [128 rows][row_bytes] in the TMA/UMMA swizzled K-major
 // layout (128-byte rows and the 128B swizzle; 64-byte rows and the 64B
-// swizzle for D = 32).  V is e4m3 transposed, [D rows][128 keys], 128B swizzle.
+// swizzle for D = 32).  V is e4m3 transposed, [D rows][128 keys]; P is e4m3
+// [128 rows][128 keys]; both 128-byte rows with the 128B swizzle.
 template <int D>
 struct Cfg {
   static constexpr int kColBlock = (D >= 64) ? 64 : D;  // fp16 elements per row of a block
@@ -50,16 +54,19 @@ struct Cfg {
   static constexpr uint32_t kSwz = (kRowBytes == 128) ? kSwizzle128B : kSwizzle64B;
   static constexpr uint32_t kSBO = 8 * kRowBytes;  // bytes between 8-row groups
   static constexpr int kQS = (D == 128) ? 1 : 2;   // Q stages (each holds both tiles)
-  static constexpr int kNS = (D == 128) ? 3 : 4;   // K/V ring stages
+  static constexpr int kNK = (D == 128) ? 3 : 4;   // K ring stages
+  static constexpr int kNV = (D == 128) ? 2 : 4;   // V ring stages
   static constexpr int kQTileBytes = kBM * D * 2;
   static constexpr int kKBytes = kBN * D * 2;
   static constexpr int kVBytes = D * kBN;
-  static constexpr int kStageBytes = kKBytes + kVBytes;
+  static constexpr int kPBytes = kBM * kBN;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kQS * 2 * kQTileBytes;
-  static constexpr int kOffBar = kOffKV + kNS * kStageBytes;
-  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
-  static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kStageBytes % 1024 == 0,
+  static constexpr int kOffK = kQS * 2 * kQTileBytes;
+  static constexpr int kOffV = kOffK + kNK * kKBytes;
+  static constexpr int kOffP = kOffV + kNV * kVBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kVBytes % 1024 == 0,
                 "tile alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -87,15 +94,14 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t sq, uint32_t 
   }
 }
 
-// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3, P read from TMEM
-// (8 columns of 4 e4m3 per MMA).
+// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t sv, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t sp, uint32_t sv, bool acc) {
   constexpr uint32_t idesc = make_idesc(kBM, D, 0, 0);  // E4M3 x E4M3 -> F32
 #pragma unroll
   for (int s = 0; s < kBN / 32; ++s) {
-    mma_f8_tmem_a(tmem_o, tmem_p + s * 8, smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc,
-                  (acc || s > 0) ? 1u : 0u);
+    mma_f8(tmem_o, smem_desc(sp + s * 32, 1024, kSwizzle128B),
+           smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc, (acc || s > 0) ? 1u : 0u);
   }
 }
 
@@ -116,16 +122,18 @@ __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int 
 
 // Barrier slots.
 enum {
-  kBarQFull = 0,     // [2]   Q stage loaded
-  kBarQEmpty = 2,    // [2]   Q stage free
-  kBarKFull = 4,     // [4]   K stage loaded
-  kBarVFull = 8,     // [4]   V stage loaded
-  kBarKVEmpty = 12,  // [4]   K/V stage free
-  kBarSFull = 16,    // [2]   S_t ready (MMA commit)
-  kBarPFull = 18,    // [2]   P_t written, O_t rescaled (128 softmax threads)
-  kBarOFull = 20,    // [2]   last PV of the item done for tile t
-  kBarDrain = 22,    //       every MMA done (teardown)
-  kNumBars = 23
+  kBarQFull = 0,    // [2]  Q stage loaded
+  kBarQEmpty = 2,   // [2]  Q stage free
+  kBarKFull = 4,    // [4]  K stage loaded
+  kBarKEmpty = 8,   // [4]  K stage free
+  kBarVFull = 12,   // [4]  V stage loaded
+  kBarVEmpty = 16,  // [4]  V stage free
+  kBarSFull = 20,   // [2]  S_t ready (MMA commit)
+  kBarSFree = 22,   // [2]  S_t loaded by the softmax (128 threads)
+  kBarPFull = 24,   // [2]  P_t written, O_t rescaled (128 threads)
+  kBarPVDone = 26,  // [2]  PV(t, j) finished (MMA commit)
+  kBarDrain = 28,   // [2]  every MMA of the QK / PV issuer done (teardown)
+  kNumBars = 30
 };
 
 // One work item: (batch, head) x a pair of query tiles.
@@ -257,8 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 8 * kNumBars + 4);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto sQ = [&](int qs, int t) { return base + C::kOffQ + (qs * 2 + t) * C::kQTileBytes; };
-  auto sK = [&](int st) { return base + C::kOffKV + st * C::kStageBytes; };
-  auto sV = [&](int st) { return base + C::kOffKV + st * C::kStageBytes + C::kKBytes; };
+  auto sK = [&](int st) { return base + C::kOffK + st * C::kKBytes; };
+  auto sV = [&](int st) { return base + C::kOffV + st * C::kVBytes; };
+  auto sP = [&](int t) { return base + C::kOffP + t * C::kPBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -266,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_pairs = (n_qt + 1) / 2;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i)
-      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? kBM : 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool softmax_side = (i >= kBarSFree && i < kBarSFree + 2) || (i >= kBarPFull && i < kBarPFull + 2);
+      mbar_init(bar(i), softmax_side ? kBM : 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -283,13 +294,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA
+      // Order per item: Q; then K runs one block ahead of V:
+      // K0, K1, V0, K2, V1, ..., K(nb-1), V(nb-2), V(nb-1).
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int last_q[2] = {-1, -1}, last_kv[4] = {-1, -1, -1, -1};
-      uint32_t kv = 0;
+      int last_q[2] = {-1, -1}, last_k[4] = {-1, -1, -1, -1}, last_v[4] = {-1, -1, -1, -1};
+      uint32_t kc = 0, vc = 0;
       int i = 0;
       bool ok = true;
+      auto load_k = [&](int j, int bkv) -> bool {
+        const int st = kc % C::kNK;
+        if (kc >= static_cast<uint32_t>(C::kNK) &&
+            !mbar_wait(bar(kBarKEmpty + st), ((kc / C::kNK) - 1) & 1, abort_flag, a.err, kErrTimeout))
+          return false;
+        mbar_arrive_expect_tx(bar(kBarKFull + st), C::kKBytes);
+        tma_tile<D>(&tmK, sK(st), bar(kBarKFull + st), j * kBN, bkv);
+        last_k[st] = static_cast<int>(kc++);
+        return true;
+      };
+      auto load_v = [&](int j, int bkv) -> bool {
+        const int st = vc % C::kNV;
+        if (vc >= static_cast<uint32_t>(C::kNV) &&
+            !mbar_wait(bar(kBarVEmpty + st), ((vc / C::kNV) - 1) & 1, abort_flag, a.err, kErrTimeout))
+          return false;
+        mbar_arrive_expect_tx(bar(kBarVFull + st), C::kVBytes);
+        tma_load_3d(sV(st), &tmV, bar(kBarVFull + st), j * kBN, 0, bkv);
+        last_v[st] = static_cast<int>(vc++);
+        return true;
+      };
       for (int k = 0; ok && k * G < n_items; ++k) {
         const int w = item_index(k, cta, G, n_items);
         if (w < 0) continue;
@@ -304,36 +337,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_tile<D>(&tmQ, sQ(qs, 1), bar(kBarQFull + qs), it.q0 + kBM, it.bq);
         last_q[qs] = i;
         const int nb = max(it.nb[0], it.nb[1]);
-        for (int j = 0; j < nb; ++j, ++kv) {
-          const int st = kv % C::kNS;
-          if (kv >= static_cast<uint32_t>(C::kNS) &&
-              !(ok = mbar_wait(bar(kBarKVEmpty + st), ((kv / C::kNS) - 1) & 1, abort_flag, a.err,
-                               kErrTimeout)))
-            break;
-          mbar_arrive_expect_tx(bar(kBarKFull + st), C::kKBytes);
-          tma_tile<D>(&tmK, sK(st), bar(kBarKFull + st), j * kBN, it.bkv);
-          mbar_arrive_expect_tx(bar(kBarVFull + st), C::kVBytes);
-          tma_load_3d(sV(st), &tmV, bar(kBarVFull + st), j * kBN, 0, it.bkv);
-          last_kv[st] = static_cast<int>(kv);
+        if (nb > 0) ok = load_k(0, it.bkv);
+        for (int j = 0; ok && j < nb; ++j) {
+          if (j + 1 < nb && !(ok = load_k(j + 1, it.bkv))) break;
+          ok = load_v(j, it.bkv);
         }
         ++i;
       }
       // Every load this thread issued lands before the CTA may exit.
       volatile int never = 0;
-      for (int qs = 0; qs < C::kQS; ++qs)
-        if (last_q[qs] >= 0)
-          mbar_wait(bar(kBarQFull + qs), (last_q[qs] / C::kQS) & 1, &never, a.err, kErrTimeout);
-      for (int st = 0; st < C::kNS; ++st)
-        if (last_kv[st] >= 0) {
-          mbar_wait(bar(kBarKFull + st), (last_kv[st] / C::kNS) & 1, &never, a.err, kErrTimeout);
-          mbar_wait(bar(kBarVFull + st), (last_kv[st] / C::kNS) & 1, &never, a.err, kErrTimeout);
-        }
+      for (int q = 0; q < C::kQS; ++q)
+        if (last_q[q] >= 0)
+          mbar_wait(bar(kBarQFull + q), (last_q[q] / C::kQS) & 1, &never, a.err, kErrTimeout);
+      for (int st = 0; st < C::kNK; ++st)
+        if (last_k[st] >= 0)
+          mbar_wait(bar(kBarKFull + st), (last_k[st] / C::kNK) & 1, &never, a.err, kErrTimeout);
+      for (int st = 0; st < C::kNV; ++st)
+        if (last_v[st] >= 0)
+          mbar_wait(bar(kBarVFull + st), (last_v[st] / C::kNV) & 1, &never, a.err, kErrTimeout);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
-      uint32_t kv = 0, pc[2] = {0, 0};
+      // Two issuing threads in separate warps, so that one thread's barrier
+      // waits and commits overlap the other's MMAs (the tensor core accepts
+      // only a short queue of MMAs, so a single issuer would leave it idle
+      // whenever it waits):
+      //   warp 1: QK(t, b) = S_t <- Q_t . K_b^T once K_b is loaded and
+      //           softmax(t, b-1) has released S_t; commits s_full[t], then
+      //           frees the K stage, and the Q stage after the item's last QK;
+      //   warp 2: PV(t, b) = O_t (+)= P_t . V8_b once V_b is loaded and P_t(b)
+      //           is written; commits pv_done[t], then frees the V stage.
+      const bool qk_issuer = (warp == 1);
+      uint32_t kvc = 0;                   // K (or V) blocks consumed so far
+      uint32_t nev[2] = {0, 0};           // QKs (or PVs) issued per tile
       int i = 0;
       bool ok = true;
       for (int k = 0; ok && k * G < n_items; ++k) {
@@ -341,60 +379,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w < 0) continue;
         const Item it = decode_item(w, a, n_pairs);
         const int qs = i % C::kQS;
-        if (!(ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
-          break;
         const int nb = max(it.nb[0], it.nb[1]);
-        if (nb > 0) {
-          const int st0 = kv % C::kNS;
-          if (!(ok = mbar_wait(bar(kBarKFull + st0), (kv / C::kNS) & 1, abort_flag, a.err, kErrTimeout)))
+        if (qk_issuer) {
+          if (!(ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
             break;
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (it.nb[t] > 0) {
-              issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st0));
-              mma_commit(bar(kBarSFull + t));
-            }
-          for (int j = 0; ok && j < nb; ++j) {
-            const uint32_t cur = kv + j, nxt = kv + j + 1;
-            const int st = cur % C::kNS, stn = nxt % C::kNS;
-            bool v_ready = false;
+          for (int b = 0; ok && b < nb; ++b) {
+            const uint32_t kk = kvc + b;
+            const int st = kk % C::kNK;
+            if (!(ok = mbar_wait(bar(kBarKFull + st), (kk / C::kNK) & 1, abort_flag, a.err, kErrTimeout)))
+              break;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              if (!ok || j >= it.nb[t]) continue;
-              if (!(ok = mbar_wait(bar(kBarPFull + t), pc[t] & 1, abort_flag, a.err, kErrTimeout)))
+              if (!ok || b >= it.nb[t]) continue;
+              if (nev[t] > 0 &&
+                  !(ok = mbar_wait(bar(kBarSFree + t), (nev[t] - 1) & 1, abort_flag, a.err, kErrTimeout)))
                 continue;
-              ++pc[t];
-              if (!v_ready) {
-                if (!(ok = mbar_wait(bar(kBarVFull + st), (cur / C::kNS) & 1, abort_flag, a.err,
-                                     kErrTimeout)))
-                  continue;
-                v_ready = true;
-              }
               tc_fence_after();
-              issue_pv<D>(tmem + 256 + 128 * t, tmem + 128 * t, sV(st), j > 0);
-              if (j + 1 < it.nb[t]) {
-                if (!(ok = mbar_wait(bar(kBarKFull + stn), (nxt / C::kNS) & 1, abort_flag, a.err,
-                                     kErrTimeout)))
-                  continue;
-                tc_fence_after();
-                issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(stn));
-                mma_commit(bar(kBarSFull + t));
-              } else {
-                mma_commit(bar(kBarOFull + t));
-              }
+              issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st));
+              mma_commit(bar(kBarSFull + t));
+              ++nev[t];
             }
-            if (ok) mma_commit(bar(kBarKVEmpty + st));
+            if (ok) mma_commit(bar(kBarKEmpty + st));
           }
-          kv += nb;
+          if (ok) mma_commit(bar(kBarQEmpty + qs));
+        } else {
+          for (int b = 0; ok && b < nb; ++b) {
+            const uint32_t vv = kvc + b;
+            const int st = vv % C::kNV;
+            if (!(ok = mbar_wait(bar(kBarVFull + st), (vv / C::kNV) & 1, abort_flag, a.err, kErrTimeout)))
+              break;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || b >= it.nb[t]) continue;
+              if (!(ok = mbar_wait(bar(kBarPFull + t), nev[t] & 1, abort_flag, a.err, kErrTimeout)))
+                continue;
+              tc_fence_after();
+              issue_pv<D>(tmem + 256 + 128 * t, sP(t), sV(st), b > 0);
+              mma_commit(bar(kBarPVDone + t));
+              ++nev[t];
+            }
+            if (ok) mma_commit(bar(kBarVEmpty + st));
+          }
         }
-        if (ok) mma_commit(bar(kBarQEmpty + qs));
+        kvc += nb;
         ++i;
       }
       // Every MMA this thread issued finishes before TMEM is freed.
-      mma_commit(bar(kBarDrain));
+      const int drain = kBarDrain + (qk_issuer ? 0 : 1);
+      mma_commit(bar(drain));
       volatile int never = 0;
-      mbar_wait(bar(kBarDrain), 0, &never, a.err, kErrTimeout);
+      mbar_wait(bar(drain), 0, &never, a.err, kErrTimeout);
       if (!ok) *abort_flag = 1;
     }
     __syncwarp();
@@ -405,8 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;  // row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
+    const uint32_t prow = sP(t) + r * 128;
+    const uint32_t sw = r & 7;
     const int nqb = (a.Nq + kBM - 1) / kBM, nkb = (a.Nk + kBN - 1) / kBN;
-    uint32_t sc = 0, oc = 0;
+    uint32_t sc = 0, pvc = 0;
     bool ok = true;
     for (int k = 0; ok && k * G < n_items; ++k) {
       const int w = item_index(k, cta, G, n_items);
@@ -429,13 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
-      const long long lim = static_cast<long long>(a.pos0) + qi;  // last visible key (causal)
+      const int lim = a.causal ? min(a.Nk - 1, a.pos0 + qi) : a.Nk - 1;  // last visible key
+      const int tile_lim = a.causal ? a.pos0 + q0t : a.Nk;  // blocks ending <= this need no causal mask
       const float* brow = nullptr;
       if (BIAS)
         brow = a.bias + static_cast<size_t>(it.h) * a.bias_head_stride +
                static_cast<size_t>(min(qi, a.Nq - 1)) * a.Nk;
       float m = kNegInf, l = 0.f;
+      float sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, 0);
       for (int j = 0; j < nbt; ++j) {
+        const float sk = sk_next;
+        if (j + 1 < nbt) sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j + 1);
         ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag, a.err, kErrTimeout);
         ++sc;
         if (!__all_sync(0xffffffffu, ok)) {  // keep the warp converged for tcgen05.ld
@@ -445,47 +485,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t s[kBN];
 #pragma unroll
-        for (int i = 0; i < kBN / 32; ++i)
-          tmem_ld32(tS + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[i * 32]));
+        for (int q = 0; q < kBN / 32; ++q)
+          tmem_ld32(tS + lane_base + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[q * 32]));
         tmem_wait_ld();
-        const float sk = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j);
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten by the next QK
         const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
         const int kbase = j * kBN;
-        const bool need_mask =
-            (kbase + kBN > a.Nk) ||
-            (a.causal && static_cast<long long>(kbase) + kBN - 1 > static_cast<long long>(a.pos0) + q0t);
-        long long lastk = static_cast<long long>(a.Nk) - 1;
-        if (a.causal && lim < lastk) lastk = lim;
-        const int nvis =
-            static_cast<int>(max(0LL, min(static_cast<long long>(kBN), lastk - kbase + 1)));
+        const bool need_mask = (kbase + kBN > a.Nk) || (kbase + kBN - 1 > tile_lim);
+        const int nvis = max(0, min(kBN, lim - kbase + 1));
         uint32_t pw[kBN / 4];
         const float* bk = BIAS ? brow + kbase : nullptr;
         const float alpha = need_mask ? softmax_step<BIAS, true>(s, c, nvis, bk, m, l, pw)
                                       : softmax_step<BIAS, false>(s, c, kBN, bk, m, l, pw);
-        tmem_st32(tS + lane_base, pw);  // P over the first 32 columns of S_t
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_base + cc * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const float2 v = fmul2(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])),
-                                     make_float2(alpha, alpha));
-              o[q] = __float_as_uint(v.x);
-              o[q + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(tO + lane_base + cc * 32, o);
+        if (j > 0) {  // PV(t, j-1) must be done with P_t and O_t
+          ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);
+          ++pvc;
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
         }
-        tmem_wait_st();
+#pragma unroll
+        for (int ch = 0; ch < kBN / 16; ++ch) {
+          const uint32_t addr = prow + ((static_cast<uint32_t>(ch) ^ sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pw[4 * ch]),
+                       "r"(pw[4 * ch + 1]), "r"(pw[4 * ch + 2]), "r"(pw[4 * ch + 3])
+                       : "memory");
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // Rescale the O_t row: one TMEM round trip for all D columns.
+          uint32_t o[D];
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+            tmem_ld32(tO + lane_base + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[cc * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < D; q += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])),
+                                   make_float2(alpha, alpha));
+            o[q] = __float_as_uint(v.x);
+            o[q + 1] = __float_as_uint(v.y);
+          }
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+            tmem_st32(tO + lane_base + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[cc * 32]));
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + t));
       }
       if (!ok) break;
-      ok = mbar_wait(bar(kBarOFull + t), oc & 1, abort_flag, a.err, kErrTimeout);
-      ++oc;
+      ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);  // last PV
+      ++pvc;
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;

@@ -9,7 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/qattn.h"
+#include "qattn.h"
 #include "qattn_internal.h"
 
 namespace {

@@ -11,7 +11,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/qattn.h"
+#include "qattn.h"
 #include "qattn_internal.h"
 
 namespace {

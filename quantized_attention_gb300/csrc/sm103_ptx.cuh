@@ -7,18 +7,18 @@
 
 namespace qattn {
 
-// A wait that has not completed after this long gives up, records an error
-// and lets the kernel unwind instead of hanging the device.
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+// A wait that has not completed after this many SM clock cycles (about 2 s at
+// the GB300 boost clock) gives up, records an error and lets the kernel unwind
+// instead of hanging the device.  Cycles (clock64) rather than %globaltimer:
+// the cycle counter is cheap to read on the polling path.
+constexpr unsigned long long kWaitTimeoutCycles = 4000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+__device__ __forceinline__ unsigned long long cycles() {
+  return static_cast<unsigned long long>(clock64());
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -48,18 +48,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if
-// the CTA-wide abort flag is raised or the wait exceeds kWaitTimeoutNs; in the
-// timeout case the abort flag is raised and the device error word is set.
+// the CTA-wide abort flag is raised or the wait exceeds kWaitTimeoutCycles; in
+// the timeout case the abort flag is raised and the device error word is set.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* err, unsigned int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = cycles();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (cycles() - t0 > kWaitTimeoutCycles) {
         *abort_flag = 1;
         atomicOr(err, code);
         return false;
