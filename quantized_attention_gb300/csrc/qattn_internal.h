@@ -29,8 +29,8 @@ struct AttnArgs {
 };
 
 // ---- quant_kernels.cu
-cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* partials,
-                            float* mu, cudaStream_t s);
+cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
+                            cudaStream_t s);
 size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d);
 
 cudaError_t launch_quantize_rows(const uint16_t* X, int B, int H, int N, int d, int mode,

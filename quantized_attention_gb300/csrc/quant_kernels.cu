@@ -16,7 +16,7 @@ namespace qattn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTokPerChunk = 256;  // tokens per CTA in the reduction passes
+constexpr int kTokPerChunk = 64;  // tokens per CTA in the reduction passes
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -51,43 +51,97 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 }
 
 // ------------------------------------------------------------------ a1
-// Partial channel sums of round(K * 2^24) over one chunk of tokens.
-__global__ void __launch_bounds__(kThreads) k_mean_partial_kernel(
-    const uint16_t* __restrict__ K, int Nk, int d, int nchunks, long long* __restrict__ part) {
-  extern __shared__ long long red64[];  // [rows per iteration][d]
-  const int bh = blockIdx.y, chunk = blockIdx.x;
-  const int vpr = d / 8;
-  const int rpi = kThreads / vpr;
-  const int v = threadIdx.x % vpr, r0 = threadIdx.x / vpr;
-  long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * d;
-  const int t_end = min(Nk, (chunk + 1) * kTokPerChunk);
-  for (int t = chunk * kTokPerChunk + r0; t < t_end; t += rpi) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * d) + v);
-    float f[8];
-    unpack_bf16x8(raw, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += __float2ll_rn(__fmul_rn(f[e], 16777216.0f));
+// round_half_even(x * 2^24) for a bf16 bit pattern, with integer operations
+// only (exact: x = M * 2^(e - 134) with the 8-bit significand M, so
+// x * 2^24 = M * 2^(e - 110)).  Valid for finite |x| < 2^39.
+__device__ __forceinline__ long long bf16_fix24(uint32_t b) {
+  const int e = (b >> 7) & 0xFF;
+  uint32_t M = b & 0x7Fu;
+  int ee = e;
+  if (e == 0) ee = 1;  // subnormal: no implicit bit
+  else M |= 0x80u;
+  const int sh = ee - 110;
+  long long v;
+  if (sh >= 0) {
+    v = static_cast<long long>(M) << sh;
+  } else {
+    const int r = -sh;
+    if (r > 9) {
+      v = 0;  // M < 2^8, so M / 2^r < 1/2
+    } else {
+      uint32_t q = M >> r;
+      const uint32_t rem = M & ((1u << r) - 1u), half = 1u << (r - 1);
+      if (rem > half || (rem == half && (q & 1u))) ++q;
+      v = q;
+    }
   }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) red64[r0 * d + v * 8 + e] = acc[e];
-  __syncthreads();
-  for (int c = threadIdx.x; c < d; c += kThreads) {
-    long long s = 0;
-    for (int r = 0; r < rpi; ++r) s += red64[r * d + c];
-    part[(static_cast<size_t>(bh) * nchunks + chunk) * d + c] = s;
-  }
+  return (b & 0x8000u) ? -v : v;
 }
 
-__global__ void k_mean_finish_kernel(const long long* __restrict__ part, int nchunks, int d,
-                                     int Nk, float* __restrict__ mu) {
-  const int bh = blockIdx.x;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    long long s = 0;
-    for (int k = 0; k < nchunks; ++k) s += part[(static_cast<size_t>(bh) * nchunks + k) * d + c];
-    double m = 0.0;
-    if (Nk > 0) m = (__ll2double_rn(s) * 0x1p-24) / static_cast<double>(Nk);
-    mu[static_cast<size_t>(bh) * d + c] = __double2float_rn(m);
+// Channel sums of round(K * 2^24) over one chunk of kTokPerChunk tokens,
+// added into acc[bh][c] with 64-bit atomics (integer, so the order does not
+// matter).  The last CTA of each (batch, head) to finish turns the sums into
+// mu = fp32(fp64(sum) * 2^-24 / Nk).  acc and done must start at zero.
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
+                                                         int nchunks,
+                                                         unsigned long long* __restrict__ acc,
+                                                         unsigned int* __restrict__ done,
+                                                         float* __restrict__ mu) {
+  constexpr int VPR = D / 8;               // 16-byte vectors per token row
+  constexpr int RPI = kThreads / VPR;      // rows per pass over the CTA
+  constexpr int NIT = kTokPerChunk / RPI;  // passes per chunk
+  __shared__ long long red64[RPI / 2][D];
+  __shared__ unsigned int last;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
+  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
+  uint4 raw[NIT];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int t = chunk * kTokPerChunk + r0 + it * RPI;
+    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * D) + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+  long long a8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a8[2 * e] += bf16_fix24(w[e] & 0xFFFFu);
+      a8[2 * e + 1] += bf16_fix24(w[e] >> 16);
+    }
+  }
+  // Fold the CTA's rows: the upper half into the lower half, then a column sum.
+  if (r0 >= RPI / 2) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red64[r0 - RPI / 2][v * 8 + e] = a8[e];
+  }
+  __syncthreads();
+  if (r0 < RPI / 2) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red64[r0][v * 8 + e] += a8[e];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += kThreads) {
+    long long sum = 0;
+#pragma unroll
+    for (int r = 0; r < RPI / 2; ++r) sum += red64[r][c];
+    atomicAdd(acc + static_cast<size_t>(bh) * D + c, static_cast<unsigned long long>(sum));
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(done + bh, 1u) == static_cast<unsigned int>(nchunks - 1));
+  __syncthreads();
+  if (last) {
+    __threadfence();
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+      const long long tot =
+          static_cast<long long>(atomicAdd(acc + static_cast<size_t>(bh) * D + c, 0ull));
+      const double m = (__ll2double_rn(tot) * 0x1p-24) / static_cast<double>(Nk);
+      mu[static_cast<size_t>(bh) * D + c] = __double2float_rn(m);
+    }
   }
 }
 
@@ -95,6 +149,20 @@ __global__ void k_mean_finish_kernel(const long long* __restrict__ part, int nch
 // One CTA per (batch*head, 128-token block).  MODE 0: x = X; 1: x = X - chan
 // (K minus its channel mean); 2: x = X * chan (Q times K's channel scale).
 // pass 0 writes the block's amax (tensor/head granules); pass 1 quantizes.
+// The raw bf16 vectors stay in registers and x is recomputed when quantizing,
+// which halves the registers and doubles the CTAs per SM.
+template <int D, int MODE>
+__device__ __forceinline__ void load_x8(const uint4& raw, const float* crow, int cv, float (&x)[8]) {
+  unpack_bf16x8(raw, x);
+  if (MODE != 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float cc = __ldg(crow + cv * 8 + e);
+      x[e] = (MODE == 1) ? __fsub_rn(x[e], cc) : __fmul_rn(x[e], cc);
+    }
+  }
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const uint16_t* __restrict__ X, int H, int N, const float* __restrict__ chan, int Hchan,
@@ -111,27 +179,23 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   const float* crow = nullptr;
   if (MODE != 0) crow = chan + (static_cast<size_t>(b) * Hchan + h / group) * D;
 
-  float x[NV][8];
-  float amax = 0.f;
+  uint4 raw[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int v = threadIdx.x + i * kThreads;
     const int r = v / VPR, cv = v % VPR;
-    if (r < rows) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + cv);
-      float f[8];
-      unpack_bf16x8(raw, f);
+    raw[i] = (r < rows) ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + cv)
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float amax = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float y = f[e];
-        if (MODE == 1) y = __fsub_rn(y, __ldg(crow + cv * 8 + e));
-        if (MODE == 2) y = __fmul_rn(y, __ldg(crow + cv * 8 + e));
-        x[i][e] = y;
-        amax = fmaxf(amax, fabsf(y));
-      }
-    } else {
+  for (int i = 0; i < NV; ++i) {
+    const int v = threadIdx.x + i * kThreads;
+    if (v / VPR < rows) {
+      float x[8];
+      load_x8<D, MODE>(raw[i], crow, v % VPR, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[i][e] = 0.f;
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
     }
   }
   const float blk_amax = block_max(amax, red);
@@ -153,10 +217,12 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const int v = threadIdx.x + i * kThreads;
     const int r = v / VPR, cv = v % VPR;
     if (r < rows) {
+      float x[8];
+      load_x8<D, MODE>(raw[i], crow, cv, x);
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(__fmul_rn(x[i][e], inv));
+        int q = __float2int_rn(__fmul_rn(x[e], inv));
         q = max(-127, min(127, q));
         w[e / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e % 4));
       }
@@ -179,33 +245,41 @@ __global__ void fill_ones_kernel(float* p, long long n) {
 }
 
 // ------------------------------------------------------------------ a3
-// Per-channel amax of V over one chunk of tokens, merged with atomicMax on
-// the (non-negative) float bit patterns.
+// Per-channel amax of V over one chunk of tokens (every load issued before any
+// is used), merged with atomicMax on the (non-negative) float bit patterns.
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
                                                          unsigned int* __restrict__ amax_bits) {
   constexpr int EPV = I8 ? 16 : 8;
   constexpr int VPR = D / EPV;
   constexpr int RPI = kThreads / VPR;
+  constexpr int NIT = (kTokPerChunk + RPI - 1) / RPI;
   __shared__ float red[RPI * D];
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
+  const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
+  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
+  uint4 raw[NIT];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int r = r0 + it * RPI;
+    const int t = chunk * kTokPerChunk + r;
+    raw[it] = (r < kTokPerChunk && t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + t * row_bytes) + v)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+  }
   float mx[EPV];
 #pragma unroll
   for (int e = 0; e < EPV; ++e) mx[e] = 0.f;
-  const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
-  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
-  const int t_end = min(Nk, (chunk + 1) * kTokPerChunk);
-  for (int t = chunk * kTokPerChunk + r0; t < t_end; t += RPI) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + t * row_bytes) + v);
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
     if constexpr (I8) {
       float f[16];
-      unpack_i8x16(raw, f);
+      unpack_i8x16(raw[it], f);
 #pragma unroll
       for (int e = 0; e < 16; ++e) mx[e] = fmaxf(mx[e], fabsf(f[e]));
     } else {
       float f[8];
-      unpack_bf16x8(raw, f);
+      unpack_bf16x8(raw[it], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], fabsf(f[e]));
     }
@@ -221,7 +295,9 @@ __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict
 }
 
 // Quantize a 128-key slice of one (batch, KV head) to e4m3 and write it
-// transposed: v8t[bh][c][t0 .. t0+127].  Keys >= Nk are written as 0; the
+// transposed: v8t[bh][c][t0 .. t0+127].  Each thread converts the channels of
+// one 16-byte input vector and scatters the e4m3 bytes into a [D][128] byte
+// tile; the tile leaves as 16-byte rows.  Keys >= Nk are written as 0; the
 // write stops at the row stride ldv.
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_convert_kernel(
@@ -230,34 +306,22 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     float* __restrict__ v_scales) {
   constexpr int EPV = I8 ? 16 : 8;
   constexpr int VPR = D / EPV;
-  constexpr int PITCH = D + 1;  // floats per tile row (odd: fewer bank conflicts)
-  extern __shared__ float tile[];  // [128][PITCH]
+  constexpr int PITCH = 128 + 16;  // bytes per tile row (16-byte aligned, staggered banks)
+  constexpr int NV = (128 * VPR + kThreads - 1) / kThreads;
+  __shared__ __align__(16) uint8_t tile[D * PITCH];
   __shared__ float inv_s[D];
   const int bh = blockIdx.y;
   const int t0 = blockIdx.x * 128;
   const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
   const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
-  for (int v = threadIdx.x; v < 128 * VPR; v += kThreads) {
+  uint4 raw[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int v = threadIdx.x + i * kThreads;
     const int r = v / VPR, cv = v % VPR;
     const int t = t0 + r;
-    float* dst = tile + r * PITCH + cv * EPV;
-    if (t < Nk) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + t * row_bytes) + cv);
-      if constexpr (I8) {
-        float f[16];
-        unpack_i8x16(raw, f);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) dst[e] = f[e];
-      } else {
-        float f[8];
-        unpack_bf16x8(raw, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = f[e];
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) dst[e] = 0.f;
-    }
+    raw[i] = (v < 128 * VPR && t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + t * row_bytes) + cv)
+                                       : make_uint4(0u, 0u, 0u, 0u);
   }
   for (int c = threadIdx.x; c < D; c += kThreads) {
     const float a = __uint_as_float(amax_bits[static_cast<size_t>(bh) * D + c]);
@@ -268,21 +332,32 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     }
   }
   __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int v = threadIdx.x + i * kThreads;
+    if (v >= 128 * VPR) continue;
+    const int r = v / VPR, cv = v % VPR;
+    float f[EPV];
+    if constexpr (I8) {
+      unpack_i8x16(raw[i], f);
+    } else {
+      unpack_bf16x8(raw[i], f);
+    }
+#pragma unroll
+    for (int e = 0; e < EPV; e += 2) {
+      const int c = cv * EPV + e;
+      const uint32_t two = cvt_e4m3x2(__fmul_rn(f[e], inv_s[c]), __fmul_rn(f[e + 1], inv_s[c + 1]));
+      tile[c * PITCH + r] = static_cast<uint8_t>(two & 0xFFu);
+      tile[(c + 1) * PITCH + r] = static_cast<uint8_t>(two >> 8);
+    }
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < D * 8; idx += kThreads) {
     const int c = idx / 8, k = idx % 8;
     const long long pos = t0 + 16 * k;
     if (pos >= ldv) continue;
-    const float inv = inv_s[c];
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float* col = tile + (16 * k + 4 * q) * PITCH + c;
-      const uint32_t lo = cvt_e4m3x2(__fmul_rn(col[0], inv), __fmul_rn(col[PITCH], inv));
-      const uint32_t hi = cvt_e4m3x2(__fmul_rn(col[2 * PITCH], inv), __fmul_rn(col[3 * PITCH], inv));
-      w[q] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(v8t + (static_cast<size_t>(bh) * D + c) * ldv + pos) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + c * PITCH + 16 * k);
+    *reinterpret_cast<uint4*>(v8t + (static_cast<size_t>(bh) * D + c) * ldv + pos) = w;
   }
 }
 
@@ -321,18 +396,23 @@ int grid_for(size_t n, int threads) {
 }  // namespace
 
 size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d) {
-  const long long nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  return static_cast<size_t>(BH * nchunks * d) * sizeof(long long);
+  (void)Nk;
+  // 64-bit channel sums, then one completion counter per (batch, head)
+  return static_cast<size_t>(BH * d) * sizeof(unsigned long long) + static_cast<size_t>(BH) * 4;
 }
 
-cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* partials,
-                            float* mu, cudaStream_t s) {
+cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
+                            cudaStream_t s) {
+  if (Nk == 0) return cudaMemsetAsync(mu, 0, static_cast<size_t>(BH) * d * sizeof(float), s);
+  unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws);
+  unsigned int* done = reinterpret_cast<unsigned int*>(acc + static_cast<size_t>(BH) * d);
+  cudaError_t e = cudaMemsetAsync(ws, 0, smooth_k_ws_bytes(BH, Nk, d), s);
+  if (e != cudaSuccess) return e;
   const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  if (nchunks > 0) {
-    const size_t smem = static_cast<size_t>(kThreads / (d / 8)) * d * sizeof(long long);
-    k_mean_partial_kernel<<<dim3(nchunks, BH), kThreads, smem, s>>>(K, Nk, d, nchunks, partials);
-  }
-  k_mean_finish_kernel<<<BH, 128, 0, s>>>(partials, nchunks, d, Nk, mu);
+  const dim3 grid(nchunks, BH);
+  if (d == 32) k_mean_kernel<32><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
+  else if (d == 64) k_mean_kernel<64><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
+  else k_mean_kernel<128><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
   return cudaGetLastError();
 }
 
@@ -393,10 +473,7 @@ static void quantize_v_impl(const void* V, const float* chan, int BH, int Nk, ui
   const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
   v_amax_kernel<D, I8><<<dim3(nchunks, BH), kThreads, 0, s>>>(V, Nk, ws);
   const int nt = static_cast<int>((ldv + 127) / 128);
-  const size_t smem = static_cast<size_t>(128) * (D + 1) * sizeof(float);
-  cudaFuncSetAttribute(v_convert_kernel<D, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
-  v_convert_kernel<D, I8><<<dim3(nt, BH), kThreads, smem, s>>>(V, Nk, ws, chan, v8t, ldv, v_scales);
+  v_convert_kernel<D, I8><<<dim3(nt, BH), kThreads, 0, s>>>(V, Nk, ws, chan, v8t, ldv, v_scales);
 }
 
 cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,

@@ -47,3 +47,29 @@ def test_prepasses_bit_exact(wl):
     assert np.array_equal(vals[..., : wl.Nk].transpose(0, 1, 3, 2), prep["v8"])
     assert not v8t[..., wl.Nk:].any(), "V padding must be zero"
     assert np.array_equal(P.v_scales.cpu().numpy().view(np.uint32), prep["s_v"].view(np.uint32))
+
+
+def test_channel_mean_edge_values():
+    """Channel mean on bf16 patterns that exercise the fixed-point rounding:
+    values below 2^-17 (rounded to the 2^-24 grid, ties to even), subnormals,
+    zeros of both signs, and magnitudes up to 2^18."""
+    from quantized_attention_gb300 import binding as qb
+
+    rng = np.random.default_rng(21)
+    B, H, N, d = 1, 2, 300, 32
+    sign = rng.integers(0, 2, size=(B, H, N, d)).astype(np.uint32) << 15
+    exp = rng.integers(0, 146, size=(B, H, N, d)).astype(np.uint32)
+    exp[..., :4] = rng.integers(95, 112, size=(B, H, N, 4))  # the rounding region
+    mant = rng.integers(0, 128, size=(B, H, N, d)).astype(np.uint32)
+    bits = (sign | (exp << 7) | mant).astype(np.uint32)
+    K = (bits << 16).view(np.float32).reshape(B, H, N, d)
+    mu_ref = O.smooth_k(K)
+    shape = qb.make_shape(B, H, H, 8, N, d)
+    ws = torch.empty(max(qb.workspace_size(shape, qb.make_params()), 256), dtype=torch.uint8,
+                     device="cuda")
+    Kd = torch.from_numpy(K.copy()).to("cuda").to(torch.bfloat16)
+    mu = torch.empty((B, H, d), dtype=torch.float32, device="cuda")
+    for _ in range(2):  # the workspace accumulators must be cleared on every call
+        qb.smooth_k(Kd, shape, mu, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(mu.cpu().numpy().view(np.uint32), mu_ref.view(np.uint32))
