@@ -3,8 +3,8 @@
 // Persistent kernel, one CTA per SM.  A work item is one (batch, head) and two
 // consecutive 128-row query tiles (t0, t1); items are handed out heaviest
 // first (causal) in a snake order over the CTAs.  Warp roles (12 warps):
-//   warp 0      lane 0 issues every TMA load: the item's two Q tiles, a ring
-//               of K stages and a ring of V^T stages;
+//   warp 0      lane 0 issues every TMA load: the item's two int8 Q tiles, a
+//               ring of K stages and a ring of V^T stages;
 //   warp 1      owns the 512 TMEM columns; lane 0 issues the QK^T MMAs;
 //   warp 2      lane 0 issues the PV MMAs;
 //   warp 3      idle;
@@ -13,6 +13,8 @@
 // TMEM: S_t at columns [128 t, 128 t + 128), O_t at [256 + 128 t, ...).
 // Shared memory holds the e4m3 P_t tiles the PV MMAs read.
 //
+// Per item, each softmax warpgroup first widens its tile's int8 Q codes to
+// exact fp16 in shared memory (q_conv); K arrives as fp16 carriers.
 // Per tile t and key block j:
 //   softmax(t, j) loads S_t(j) from TMEM and at once releases it (s_free), so
 //   the MMA thread issues QK(t, j+1) -- S_t = Q_t . K_{j+1}^T, kind::f16 on
@@ -64,11 +66,18 @@ struct Cfg {
   static constexpr int kOffK = kQS * 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kNK * kKBytes;
   static constexpr int kOffP = kOffV + kNV * kVBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  // int8 Q codes as loaded: in the upper half of each fp16 Q tile for D = 128
+  // (see convert_q_tile), in a region of their own for smaller D.
+  static constexpr bool kQ8InPlace = (D == 128);
+  static constexpr int kQ8Bytes = kBM * D;
+  static constexpr int kOffQ8 = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffQ8 + (kQ8InPlace ? 0 : kQS * 2 * kQ8Bytes);
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
   static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kVBytes % 1024 == 0,
                 "tile alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(!kQ8InPlace || (kColBlockBytes == kQTileBytes / 2 && kRowBytes == D),
+                "in-place Q widening needs row r of the codes = row r of column block 1");
 };
 
 // Debug-kernel plan: one Q tile and one K tile.
@@ -76,8 +85,9 @@ template <int D>
 struct DbgCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = Cfg<D>::kQTileBytes;
-  static constexpr int kOffBar = kOffK + Cfg<D>::kKBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kOffQ8 = kOffK + Cfg<D>::kKBytes;
+  static constexpr int kOffBar = kOffQ8 + Cfg<D>::kQ8Bytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
 };
 
 // S = Q . K^T for one 128 x 128 tile: D/16 MMAs of K = 16, fp32 into TMEM.
@@ -114,6 +124,39 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* map, uint32_t dst, u
     tma_load_3d(dst + cb * C::kColBlockBytes, map, bar, cb * C::kColBlock, row, plane);
 }
 
+// int8 Q codes -> exact fp16 carriers.  The 128 calling threads each widen
+// one row: thread r reads row r of the codes ([128 rows][D] bytes at `codes`)
+// into registers, then writes it to the fp16 tile in the swizzled K-major
+// layout the MMA descriptors expect.  With D = 128 the codes sit in the upper
+// half of the fp16 tile itself: row r's codes then occupy exactly the bytes of
+// row r of the second column block, which only thread r writes, after reading
+// them -- so no thread needs to wait for another.  Chunks are visited starting
+// at chunk r, so eight consecutive rows touch eight different bank groups.
+template <int D>
+__device__ __forceinline__ void convert_q_tile(uint32_t tile, uint32_t codes, int r) {
+  using C = Cfg<D>;
+  constexpr int kChunks = D / 16;  // 16-byte chunks of codes per row
+  uint4 raw[kChunks];
+  const uint32_t src = codes + r * D;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) raw[c] = lds128(src + ((c + r) & (kChunks - 1)) * 16);
+  const uint32_t sw = (C::kRowBytes == 128) ? (r & 7) : ((r >> 1) & 3);
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int cc = (c + r) & (kChunks - 1);
+    uint32_t h[8];
+    codes4_to_f16x2(raw[c].x, h[0], h[1]);
+    codes4_to_f16x2(raw[c].y, h[2], h[3]);
+    codes4_to_f16x2(raw[c].z, h[4], h[5]);
+    codes4_to_f16x2(raw[c].w, h[6], h[7]);
+    const int ch = cc * 16;                       // first channel of the chunk
+    const uint32_t k0 = (ch % C::kColBlock) / 8;  // its 16-byte slot in the row
+    const uint32_t row = tile + (ch / C::kColBlock) * C::kColBlockBytes + r * C::kRowBytes;
+    sts128(row + ((k0 ^ sw) << 4), h[0], h[1], h[2], h[3]);
+    sts128(row + (((k0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
+
 __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int nblk, int blk) {
   if (gran == 0) return __ldg(s);
   if (gran == 1) return __ldg(s + bh);
@@ -133,7 +176,8 @@ enum {
   kBarPFull = 24,   // [2]  P_t written, O_t rescaled (128 threads)
   kBarPVDone = 26,  // [2]  PV(t, j) finished (MMA commit)
   kBarDrain = 28,   // [2]  every MMA of the QK / PV issuer done (teardown)
-  kNumBars = 30
+  kBarQConv = 30,   // [2]  Q_t widened to fp16 (128 threads)
+  kNumBars = 32
 };
 
 // One work item: (batch, head) x a pair of query tiles.
@@ -268,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sK = [&](int st) { return base + C::kOffK + st * C::kKBytes; };
   auto sV = [&](int st) { return base + C::kOffV + st * C::kVBytes; };
   auto sP = [&](int t) { return base + C::kOffP + t * C::kPBytes; };
+  auto sQ8 = [&](int qs, int t) {
+    return C::kQ8InPlace ? sQ(qs, t) + C::kQTileBytes / 2
+                         : base + C::kOffQ8 + (qs * 2 + t) * C::kQ8Bytes;
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -276,7 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool softmax_side = (i >= kBarSFree && i < kBarSFree + 2) || (i >= kBarPFull && i < kBarPFull + 2);
+      const bool softmax_side = (i >= kBarSFree && i < kBarSFree + 2) ||
+                                (i >= kBarPFull && i < kBarPFull + 2) ||
+                                (i >= kBarQConv && i < kBarQConv + 2);
       mbar_init(bar(i), softmax_side ? kBM : 1);
     }
     *abort_flag = 0;
@@ -332,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             !(ok = mbar_wait(bar(kBarQEmpty + qs), ((i / C::kQS) - 1) & 1, abort_flag, a.err,
                              kErrTimeout)))
           break;
-        mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * C::kQTileBytes);
-        tma_tile<D>(&tmQ, sQ(qs, 0), bar(kBarQFull + qs), it.q0, it.bq);
-        tma_tile<D>(&tmQ, sQ(qs, 1), bar(kBarQFull + qs), it.q0 + kBM, it.bq);
+        mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * C::kQ8Bytes);  // int8 codes
+        tma_load_3d(sQ8(qs, 0), &tmQ, bar(kBarQFull + qs), 0, it.q0, it.bq);
+        tma_load_3d(sQ8(qs, 1), &tmQ, bar(kBarQFull + qs), 0, it.q0 + kBM, it.bq);
         last_q[qs] = i;
         const int nb = max(it.nb[0], it.nb[1]);
         if (nb > 0) ok = load_k(0, it.bkv);
@@ -372,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool qk_issuer = (warp == 1);
       uint32_t kvc = 0;                   // K (or V) blocks consumed so far
       uint32_t nev[2] = {0, 0};           // QKs (or PVs) issued per tile
+      uint32_t nqc[2] = {0, 0};           // Q tiles widened per tile
       int i = 0;
       bool ok = true;
       for (int k = 0; ok && k * G < n_items; ++k) {
@@ -381,8 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qs = i % C::kQS;
         const int nb = max(it.nb[0], it.nb[1]);
         if (qk_issuer) {
-          if (!(ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
-            break;
           for (int b = 0; ok && b < nb; ++b) {
             const uint32_t kk = kvc + b;
             const int st = kk % C::kNK;
@@ -394,6 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (nev[t] > 0 &&
                   !(ok = mbar_wait(bar(kBarSFree + t), (nev[t] - 1) & 1, abort_flag, a.err, kErrTimeout)))
                 continue;
+              if (b == 0) {  // the item's Q_t, widened by the tile's softmax warps
+                if (!(ok = mbar_wait(bar(kBarQConv + t), nqc[t] & 1, abort_flag, a.err, kErrTimeout)))
+                  continue;
+                ++nqc[t];
+              }
               tc_fence_after();
               issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st));
               mma_commit(bar(kBarSFull + t));
@@ -444,9 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nqb = (a.Nq + kBM - 1) / kBM, nkb = (a.Nk + kBN - 1) / kBN;
     uint32_t sc = 0, pvc = 0;
     bool ok = true;
+    int i = -1;  // items of this CTA so far
     for (int k = 0; ok && k * G < n_items; ++k) {
       const int w = item_index(k, cta, G, n_items);
       if (w < 0) continue;
+      ++i;
       const Item it = decode_item(w, a, n_pairs);
       const int q0t = it.q0 + t * kBM;
       const int qi = q0t + r;
@@ -463,6 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.lse) a.lse[row] = kNegInf;
         }
         continue;
+      }
+      {  // widen this tile's Q codes for the item's QK MMAs
+        const int qs = i % C::kQS;
+        ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        convert_q_tile<D>(sQ(qs, t), sQ8(qs, t), r);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarQConv + t));
       }
       const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
       const int lim = a.causal ? min(a.Nk - 1, a.pos0 + qi) : a.Nk - 1;  // last visible key
@@ -597,7 +664,7 @@ __global__ void __launch_bounds__(160, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::kOffQ, sK = base + C::kOffK;
+  const uint32_t sQ = base + C::kOffQ, sK = base + C::kOffK, sQ8 = base + C::kOffQ8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 36);
@@ -606,9 +673,10 @@ __global__ void __launch_bounds__(160, 1)
   const int b = bq / Hq, h = bq % Hq;
   const int bkv = b * Hkv + h / (Hq / Hkv);
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
-    mbar_init(smem_u32(&bars[2]), 1);
+    mbar_init(smem_u32(&bars[0]), 1);    // Q codes and K loaded
+    mbar_init(smem_u32(&bars[1]), 1);    // S ready
+    mbar_init(smem_u32(&bars[2]), 1);    // MMA drained
+    mbar_init(smem_u32(&bars[3]), kBM);  // Q widened
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -623,11 +691,12 @@ __global__ void __launch_bounds__(160, 1)
   if (warp == 4) {
     if (lane == 0) {
       const uint32_t full = smem_u32(&bars[0]);
-      mbar_arrive_expect_tx(full, Cfg<D>::kQTileBytes + Cfg<D>::kKBytes);
-      tma_tile<D>(&tmQ, sQ, full, qt * kBM, bq);
+      mbar_arrive_expect_tx(full, Cfg<D>::kQ8Bytes + Cfg<D>::kKBytes);
+      tma_load_3d(sQ8, &tmQ, full, 0, qt * kBM, bq);
       tma_tile<D>(&tmK, sK, full, kt * kBN, bkv);
       volatile int never = 0;
-      if (mbar_wait(full, 0, &never, err, kErrTimeout)) {
+      if (mbar_wait(full, 0, &never, err, kErrTimeout) &&
+          mbar_wait(smem_u32(&bars[3]), 0, abort_flag, err, kErrTimeout)) {
         tc_fence_after();
         issue_qk<D>(tmem, sQ, sK);
         mma_commit(smem_u32(&bars[1]));
@@ -640,7 +709,13 @@ __global__ void __launch_bounds__(160, 1)
     __syncwarp();
   } else {
     const int r = threadIdx.x;
-    const bool ok = mbar_wait(smem_u32(&bars[1]), 0, abort_flag, err, kErrTimeout);
+    bool ok = mbar_wait(smem_u32(&bars[0]), 0, abort_flag, err, kErrTimeout);
+    if (__all_sync(0xffffffffu, ok)) {
+      convert_q_tile<D>(sQ, sQ8, r);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars[3]));
+      ok = mbar_wait(smem_u32(&bars[1]), 0, abort_flag, err, kErrTimeout);
+    }
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       uint32_t s[kBN];

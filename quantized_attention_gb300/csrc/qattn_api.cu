@@ -99,9 +99,9 @@ size_t ws_quant_qk(const qattn_shape* s, const qattn_params* p) {
          align256(qattn::quantize_rows_ws_bytes(s->B, s->Hkv, s->Nk, p ? p->k_gran : 0));
 }
 size_t ws_quant_v(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hkv * s->d) * 4); }
-size_t ws_carriers_q(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hq * s->Nq * s->d) * 2); }
+// fp16 carriers of the K codes (Q codes are widened inside the kernels).
 size_t ws_carriers_k(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hkv * s->Nk * s->d) * 2); }
-size_t ws_fwd(const qattn_shape* s) { return ws_carriers_q(s) + ws_carriers_k(s); }
+size_t ws_fwd(const qattn_shape* s) { return ws_carriers_k(s); }
 
 // 3-D tiled map over a dense [planes][rows][inner] tensor.
 bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const void* ptr,
@@ -119,7 +119,14 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const voi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Maps over the fp16 carriers of Q [B*Hq][Nq][d] or K [B*Hkv][Nk][d].
+// Map over the int8 Q codes [B*Hq][Nq][d]: one 128-row tile per load,
+// unswizzled (the kernels widen it to fp16 themselves).
+bool encode_q_codes(CUtensorMap* map, const void* ptr, int64_t planes, int64_t rows, int64_t d) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, d, rows, planes, d,
+                   static_cast<uint32_t>(d), 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Map over the fp16 carriers of K [B*Hkv][Nk][d].
 bool encode_carrier(CUtensorMap* map, const void* ptr, int64_t planes, int64_t rows, int64_t d) {
   const uint32_t colblock = d >= 64 ? 64 : static_cast<uint32_t>(d);
   const CUtensorMapSwizzle swz = (colblock * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -195,25 +202,44 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   float* ws_k = reinterpret_cast<float*>(static_cast<char*>(workspace) + wq);
   const int B = static_cast<int>(shape->B), Hq = static_cast<int>(shape->Hq);
   const int Hkv = static_cast<int>(shape->Hkv), d = static_cast<int>(shape->d);
-  cudaError_t e;
+  const int64_t nqb = (shape->Nq + 127) / 128, nkb = (shape->Nk + 127) / 128;
+  qattn::RowsJob jq{};
+  jq.X = Q;
+  jq.H = Hq;
+  jq.N = static_cast<int>(shape->Nq);
+  jq.chan = i8 ? k_chan_scale : nullptr;
+  jq.Hchan = i8 ? Hkv : 1;
+  jq.group = i8 ? Hq / Hkv : 1;
+  jq.gran = params->q_gran;
+  jq.codes = q_codes;
+  jq.scales = q_scales;
+  jq.ws_amax = ws_q;
+  jq.nblk = static_cast<int>(nqb);
+  jq.BH = B * Hq;
+  qattn::RowsJob jk{};
   if (i8) {
-    e = qattn::launch_quantize_rows(Q, B, Hq, static_cast<int>(shape->Nq), d, 2, k_chan_scale, Hkv,
-                                    params->q_gran, q_codes, q_scales, ws_q, s);
+    cudaError_t e = qattn::launch_quantize_rows(jq, 2, jk, 0, d, s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
-    const int64_t nkb = (shape->Nk + 127) / 128;
     const int64_t n = params->k_gran == QATTN_GRAN_TENSOR ? 1
                       : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
                                                           : shape->B * shape->Hkv * nkb;
     return from_cuda(qattn::launch_fill_ones(k_scales, n, s));
   }
-  e = qattn::launch_quantize_rows(Q, B, Hq, static_cast<int>(shape->Nq), d, 0, nullptr, 1,
-                                  params->q_gran, q_codes, q_scales, ws_q, s);
-  if (e != cudaSuccess) return QATTN_ERR_CUDA;
-  if (shape->Nk == 0) return QATTN_OK;
-  e = qattn::launch_quantize_rows(static_cast<const uint16_t*>(K), B, Hkv,
-                                  static_cast<int>(shape->Nk), d, k_mean ? 1 : 0, k_mean, Hkv,
-                                  params->k_gran, k_codes, k_scales, ws_k, s);
-  return from_cuda(e);
+  if (shape->Nk > 0) {
+    jk.X = static_cast<const uint16_t*>(K);
+    jk.H = Hkv;
+    jk.N = static_cast<int>(shape->Nk);
+    jk.chan = k_mean;
+    jk.Hchan = Hkv;
+    jk.group = 1;
+    jk.gran = params->k_gran;
+    jk.codes = k_codes;
+    jk.scales = k_scales;
+    jk.ws_amax = ws_k;
+    jk.nblk = static_cast<int>(nkb);
+    jk.BH = B * Hkv;
+  }
+  return from_cuda(qattn::launch_quantize_rows(jq, 0, jk, k_mean ? 1 : 0, d, s));
 }
 
 qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,
@@ -288,17 +314,15 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   }
   const size_t need = ws_fwd(shape);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
-  uint16_t* qc16 = static_cast<uint16_t*>(workspace);
-  uint16_t* kc16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + ws_carriers_q(shape));
-  cudaError_t e = qattn::launch_codes_to_f16(q_codes, qc16, static_cast<size_t>(shape->B * shape->Hq * shape->Nq * shape->d), s);
-  if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  uint16_t* kc16 = static_cast<uint16_t*>(workspace);
   if (shape->Nk > 0) {
-    e = qattn::launch_codes_to_f16(k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+    const cudaError_t e = qattn::launch_codes_to_f16(
+        k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
   }
   CUtensorMap tq, tk, tv;
   const int64_t nk_map = shape->Nk > 0 ? shape->Nk : 1;
-  if (!encode_carrier(&tq, qc16, shape->B * shape->Hq, shape->Nq, shape->d) ||
+  if (!encode_q_codes(&tq, q_codes, shape->B * shape->Hq, shape->Nq, shape->d) ||
       !encode_carrier(&tk, kc16, shape->B * shape->Hkv, nk_map, shape->d) ||
       !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, shape->Nk > 0 ? static_cast<const void*>(v8t) : workspace,
                  static_cast<uint64_t>(nk_map), static_cast<uint64_t>(shape->d),
@@ -321,14 +345,12 @@ qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned int* err = error_word();
   if (!err) return QATTN_ERR_CUDA;
-  uint16_t* qc16 = static_cast<uint16_t*>(workspace);
-  uint16_t* kc16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + ws_carriers_q(shape));
-  cudaError_t e = qattn::launch_codes_to_f16(q_codes, qc16, static_cast<size_t>(shape->B * shape->Hq * shape->Nq * shape->d), s);
-  if (e == cudaSuccess)
-    e = qattn::launch_codes_to_f16(k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+  uint16_t* kc16 = static_cast<uint16_t*>(workspace);
+  const cudaError_t e = qattn::launch_codes_to_f16(
+      k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
   if (e != cudaSuccess) return QATTN_ERR_CUDA;
   CUtensorMap tq, tk;
-  if (!encode_carrier(&tq, qc16, shape->B * shape->Hq, shape->Nq, shape->d) ||
+  if (!encode_q_codes(&tq, q_codes, shape->B * shape->Hq, shape->Nq, shape->d) ||
       !encode_carrier(&tk, kc16, shape->B * shape->Hkv, shape->Nk, shape->d))
     return QATTN_ERR_CUDA;
   return from_cuda(qattn::launch_qk_debug(tq, tk, static_cast<int>(shape->B), static_cast<int>(shape->Hq),

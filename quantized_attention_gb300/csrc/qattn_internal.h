@@ -33,9 +33,23 @@ cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long*
                             cudaStream_t s);
 size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d);
 
-cudaError_t launch_quantize_rows(const uint16_t* X, int B, int H, int N, int d, int mode,
-                                 const float* chan, int Hchan, int gran, int8_t* codes,
-                                 float* scales, float* ws_amax, cudaStream_t s);
+// One tensor to quantize per 128-token block rows (a2): X [B*H][N][d] bf16.
+//   mode 0: x = X;  1: x = X - chan[b][h][:] (Hchan = H);
+//   2: x = X * chan[b][h / group][:] (chan has Hchan heads, group = H / Hchan)
+struct RowsJob {
+  const uint16_t* X;
+  int H, N;
+  const float* chan;
+  int Hchan, group, gran;
+  int8_t* codes;
+  float* scales;
+  float* ws_amax;  // B*H*nblk block maxima (tensor / head granules only)
+  int nblk, BH;    // 128-token blocks per head; B*H (0: no job)
+};
+// Quantizes j0 (mode m0) and j1 (mode m1) in the same launches.  Supported:
+// (m0, m1) = (0, 0), (0, 1), or (2, -) with j1.BH = 0.
+cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, int m1, int d,
+                                 cudaStream_t s);
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
 cudaError_t launch_fill_ones(float* p, long long n, cudaStream_t s);
 

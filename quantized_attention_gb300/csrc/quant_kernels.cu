@@ -146,11 +146,12 @@ __global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __rest
 }
 
 // ------------------------------------------------------------------ a2
-// One CTA per (batch*head, 128-token block).  MODE 0: x = X; 1: x = X - chan
-// (K minus its channel mean); 2: x = X * chan (Q times K's channel scale).
-// pass 0 writes the block's amax (tensor/head granules); pass 1 quantizes.
-// The raw bf16 vectors stay in registers and x is recomputed when quantizing,
-// which halves the registers and doubles the CTAs per SM.
+// One CTA per (batch*head, 128-token block) of a job.  MODE 0: x = X;
+// 1: x = X - chan (K minus its channel mean); 2: x = X * chan (Q times K's
+// channel scale).  pass 0 writes the block's amax (tensor/head granules);
+// pass 1 quantizes.  The raw bf16 vectors stay in registers and x is
+// recomputed when quantizing, which halves the registers and doubles the
+// CTAs per SM.
 template <int D, int MODE>
 __device__ __forceinline__ void load_x8(const uint4& raw, const float* crow, int cv, float (&x)[8]) {
   unpack_bf16x8(raw, x);
@@ -164,20 +165,17 @@ __device__ __forceinline__ void load_x8(const uint4& raw, const float* crow, int
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads) quant_rows_kernel(
-    const uint16_t* __restrict__ X, int H, int N, const float* __restrict__ chan, int Hchan,
-    int group, int gran, int pass, int8_t* __restrict__ codes, float* __restrict__ scales,
-    float* __restrict__ ws_amax, int nblk, int BH) {
+__device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int blk, int pass,
+                                                float* red) {
   constexpr int VPR = D / 8;
   constexpr int NV = 128 * VPR / kThreads;
-  __shared__ float red[kThreads / 32];
-  const int bh = blockIdx.y, blk = blockIdx.x;
-  const int b = bh / H, h = bh % H;
+  if (pass == 0 && j.gran == 2) return;  // block granules need no pre-pass
+  const int b = bh / j.H, h = bh % j.H;
   const int t0 = blk * 128;
-  const int rows = min(128, N - t0);
-  const uint16_t* src = X + (static_cast<size_t>(bh) * N + t0) * D;
+  const int rows = min(128, j.N - t0);
+  const uint16_t* src = j.X + (static_cast<size_t>(bh) * j.N + t0) * D;
   const float* crow = nullptr;
-  if (MODE != 0) crow = chan + (static_cast<size_t>(b) * Hchan + h / group) * D;
+  if (MODE != 0) crow = j.chan + (static_cast<size_t>(b) * j.Hchan + h / j.group) * D;
 
   uint4 raw[NV];
 #pragma unroll
@@ -200,15 +198,15 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   }
   const float blk_amax = block_max(amax, red);
   if (pass == 0) {
-    if (threadIdx.x == 0) ws_amax[static_cast<size_t>(bh) * nblk + blk] = blk_amax;
+    if (threadIdx.x == 0) j.ws_amax[static_cast<size_t>(bh) * j.nblk + blk] = blk_amax;
     return;
   }
   float g = blk_amax;
-  if (gran != 2) {  // tensor (0) or head (1): reduce the granule's block maxima
-    const int lo = (gran == 0) ? 0 : bh * nblk;
-    const int hi = (gran == 0) ? BH * nblk : (bh + 1) * nblk;
+  if (j.gran != 2) {  // tensor (0) or head (1): reduce the granule's block maxima
+    const int lo = (j.gran == 0) ? 0 : bh * j.nblk;
+    const int hi = (j.gran == 0) ? j.BH * j.nblk : (bh + 1) * j.nblk;
     float m = 0.f;
-    for (int i = lo + threadIdx.x; i < hi; i += kThreads) m = fmaxf(m, ws_amax[i]);
+    for (int i = lo + threadIdx.x; i < hi; i += kThreads) m = fmaxf(m, j.ws_amax[i]);
     g = block_max(m, red);
   }
   const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
@@ -226,15 +224,29 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
         q = max(-127, min(127, q));
         w[e / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e % 4));
       }
-      *reinterpret_cast<uint2*>(codes + (static_cast<size_t>(bh) * N + t0 + r) * D + cv * 8) =
+      *reinterpret_cast<uint2*>(j.codes + (static_cast<size_t>(bh) * j.N + t0 + r) * D + cv * 8) =
           make_uint2(w[0], w[1]);
     }
   }
   if (threadIdx.x == 0) {
     const float sc = __fdiv_rn(g, 127.0f);
-    if (gran == 2) scales[static_cast<size_t>(bh) * nblk + blk] = sc;
-    else if (gran == 1 && blk == 0) scales[bh] = sc;
-    else if (gran == 0 && blk == 0 && bh == 0) scales[0] = sc;
+    if (j.gran == 2) j.scales[static_cast<size_t>(bh) * j.nblk + blk] = sc;
+    else if (j.gran == 1 && blk == 0) j.scales[bh] = sc;
+    else if (j.gran == 0 && blk == 0 && bh == 0) j.scales[0] = sc;
+  }
+}
+
+// Q and K in one launch: blockIdx.x < j0.BH are (batch, head)s of job 0, the
+// rest of job 1; blockIdx.y is the 128-token block.
+template <int D, int M0, int M1>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsJob j0, const RowsJob j1,
+                                                             int pass) {
+  __shared__ float red[kThreads / 32];
+  const int x = blockIdx.x, blk = blockIdx.y;
+  if (x < j0.BH) {
+    if (blk < j0.nblk) quant_rows_body<D, M0>(j0, x, blk, pass, red);
+  } else if (blk < j1.nblk) {
+    quant_rows_body<D, M1>(j1, x - j0.BH, blk, pass, red);
   }
 }
 
@@ -295,33 +307,41 @@ __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict
 }
 
 // Quantize a 128-key slice of one (batch, KV head) to e4m3 and write it
-// transposed: v8t[bh][c][t0 .. t0+127].  Each thread converts the channels of
-// one 16-byte input vector and scatters the e4m3 bytes into a [D][128] byte
-// tile; the tile leaves as 16-byte rows.  Keys >= Nk are written as 0; the
-// write stops at the row stride ldv.
+// transposed: v8t[bh][c][t0 .. t0+127].  Lane l of a warp owns keys
+// 4l .. 4l+3 and reads, for each, 32 contiguous bytes of the row (two 16-byte
+// vectors: a whole sector); each warp takes its own channel slices.  The four
+// keys' e4m3 bytes of one channel form one word, stored at [c][4l] of a
+// [D][128]-byte tile: the 32 lanes write 32 consecutive words (no bank
+// conflict).  The tile leaves as 16-byte rows.  Keys >= Nk are written as 0;
+// the write stops at the row stride ldv.
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     const void* __restrict__ V, int Nk, const unsigned int* __restrict__ amax_bits,
     const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
     float* __restrict__ v_scales) {
-  constexpr int EPV = I8 ? 16 : 8;
-  constexpr int VPR = D / EPV;
-  constexpr int PITCH = 128 + 16;  // bytes per tile row (16-byte aligned, staggered banks)
-  constexpr int NV = (128 * VPR + kThreads - 1) / kThreads;
-  __shared__ __align__(16) uint8_t tile[D * PITCH];
+  constexpr int EPV = I8 ? 16 : 8;        // channels per 16-byte vector
+  constexpr int kSlices = D / (2 * EPV);  // 32-byte channel slices per key row
+  constexpr int kWarps = kThreads / 32;
+  constexpr int NS = (kSlices + kWarps - 1) / kWarps;  // slices per warp
+  __shared__ __align__(16) uint8_t tile[D * 128];
   __shared__ float inv_s[D];
   const int bh = blockIdx.y;
   const int t0 = blockIdx.x * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
   const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
-  uint4 raw[NV];
+  uint4 raw[NS][4][2];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int v = threadIdx.x + i * kThreads;
-    const int r = v / VPR, cv = v % VPR;
-    const int t = t0 + r;
-    raw[i] = (v < 128 * VPR && t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + t * row_bytes) + cv)
-                                       : make_uint4(0u, 0u, 0u, 0u);
+  for (int u = 0; u < NS; ++u) {
+    const int sl = warp + u * kWarps;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int t = t0 + 4 * lane + q;
+      const bool in = (sl < kSlices) && (t < Nk);
+      const uint4* src = reinterpret_cast<const uint4*>(base + t * row_bytes) + 2 * sl;
+      raw[u][q][0] = in ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
+      raw[u][q][1] = in ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   for (int c = threadIdx.x; c < D; c += kThreads) {
     const float a = __uint_as_float(amax_bits[static_cast<size_t>(bh) * D + c]);
@@ -333,22 +353,31 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
   }
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int v = threadIdx.x + i * kThreads;
-    if (v >= 128 * VPR) continue;
-    const int r = v / VPR, cv = v % VPR;
-    float f[EPV];
-    if constexpr (I8) {
-      unpack_i8x16(raw[i], f);
-    } else {
-      unpack_bf16x8(raw[i], f);
-    }
+  for (int u = 0; u < NS; ++u) {
+    const int sl = warp + u * kWarps;
+    if (sl >= kSlices) continue;
 #pragma unroll
-    for (int e = 0; e < EPV; e += 2) {
-      const int c = cv * EPV + e;
-      const uint32_t two = cvt_e4m3x2(__fmul_rn(f[e], inv_s[c]), __fmul_rn(f[e + 1], inv_s[c + 1]));
-      tile[c * PITCH + r] = static_cast<uint8_t>(two & 0xFFu);
-      tile[(c + 1) * PITCH + r] = static_cast<uint8_t>(two >> 8);
+    for (int v = 0; v < 2; ++v) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const int c = (2 * sl + v) * EPV + e;
+        const float sc = inv_s[c];
+        float x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 r4 = raw[u][q][v];
+          if constexpr (I8) {
+            const uint32_t w = (e < 4) ? r4.x : (e < 8) ? r4.y : (e < 12) ? r4.z : r4.w;
+            x[q] = static_cast<float>(static_cast<int8_t>((w >> (8 * (e % 4))) & 0xFFu));
+          } else {
+            const uint32_t w = (e < 2) ? r4.x : (e < 4) ? r4.y : (e < 6) ? r4.z : r4.w;
+            x[q] = __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+          }
+        }
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[0], sc), __fmul_rn(x[1], sc));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[2], sc), __fmul_rn(x[3], sc));
+        *reinterpret_cast<uint32_t*>(tile + c * 128 + 4 * lane) = lo | (hi << 16);
+      }
     }
   }
   __syncthreads();
@@ -356,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     const int c = idx / 8, k = idx % 8;
     const long long pos = t0 + 16 * k;
     if (pos >= ldv) continue;
-    const uint4 w = *reinterpret_cast<const uint4*>(tile + c * PITCH + 16 * k);
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + c * 128 + 16 * k);
     *reinterpret_cast<uint4*>(v8t + (static_cast<size_t>(bh) * D + c) * ldv + pos) = w;
   }
 }
@@ -422,41 +451,26 @@ size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran) {
 }
 
 template <int D>
-static void quant_rows_dispatch(dim3 grid, cudaStream_t s, const uint16_t* X, int H, int N,
-                                int mode, const float* chan, int Hchan, int group, int gran,
-                                int pass, int8_t* codes, float* scales, float* ws, int nblk,
-                                int BH) {
-  if (mode == 0)
-    quant_rows_kernel<D, 0><<<grid, kThreads, 0, s>>>(X, H, N, chan, Hchan, group, gran, pass,
-                                                      codes, scales, ws, nblk, BH);
-  else if (mode == 1)
-    quant_rows_kernel<D, 1><<<grid, kThreads, 0, s>>>(X, H, N, chan, Hchan, group, gran, pass,
-                                                      codes, scales, ws, nblk, BH);
-  else
-    quant_rows_kernel<D, 2><<<grid, kThreads, 0, s>>>(X, H, N, chan, Hchan, group, gran, pass,
-                                                      codes, scales, ws, nblk, BH);
+static void quant_rows_dispatch(dim3 grid, cudaStream_t s, const RowsJob& j0, int m0,
+                                const RowsJob& j1, int m1, int pass) {
+  if (m0 == 0 && m1 == 1) quant_rows_kernel<D, 0, 1><<<grid, kThreads, 0, s>>>(j0, j1, pass);
+  else if (m0 == 0) quant_rows_kernel<D, 0, 0><<<grid, kThreads, 0, s>>>(j0, j1, pass);
+  else quant_rows_kernel<D, 2, 0><<<grid, kThreads, 0, s>>>(j0, j1, pass);
 }
 
-cudaError_t launch_quantize_rows(const uint16_t* X, int B, int H, int N, int d, int mode,
-                                 const float* chan, int Hchan, int gran, int8_t* codes,
-                                 float* scales, float* ws_amax, cudaStream_t s) {
-  const int nblk = (N + 127) / 128;
-  const int BH = B * H;
-  const int group = (mode == 2) ? H / Hchan : 1;
-  const dim3 grid(nblk, BH);
-  for (int pass = (gran == 2 ? 1 : 0); pass < 2; ++pass) {
+cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, int m1, int d,
+                                 cudaStream_t s) {
+  if (!((m0 == 0 && (m1 == 0 || m1 == 1)) || (m0 == 2 && j1.BH == 0))) return cudaErrorInvalidValue;
+  const int nblk = max(j0.nblk, j1.BH > 0 ? j1.nblk : 0);
+  const int nx = j0.BH + j1.BH;
+  if (nblk <= 0 || nx <= 0) return cudaSuccess;
+  const dim3 grid(nx, nblk);
+  const bool two_pass = (j0.BH > 0 && j0.gran != 2) || (j1.BH > 0 && j1.gran != 2);
+  for (int pass = two_pass ? 0 : 1; pass < 2; ++pass) {
     switch (d) {
-      case 32:
-        quant_rows_dispatch<32>(grid, s, X, H, N, mode, chan, Hchan, group, gran, pass, codes,
-                                scales, ws_amax, nblk, BH);
-        break;
-      case 64:
-        quant_rows_dispatch<64>(grid, s, X, H, N, mode, chan, Hchan, group, gran, pass, codes,
-                                scales, ws_amax, nblk, BH);
-        break;
-      default:
-        quant_rows_dispatch<128>(grid, s, X, H, N, mode, chan, Hchan, group, gran, pass, codes,
-                                 scales, ws_amax, nblk, BH);
+      case 32: quant_rows_dispatch<32>(grid, s, j0, m0, j1, m1, pass); break;
+      case 64: quant_rows_dispatch<64>(grid, s, j0, m0, j1, m1, pass); break;
+      default: quant_rows_dispatch<128>(grid, s, j0, m0, j1, m1, pass);
     }
   }
   return cudaGetLastError();

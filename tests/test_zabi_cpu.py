@@ -40,7 +40,8 @@ def test_host_only_queries(L):
     assert qb.v_ld(49) == 64 and qb.v_ld(128) == 128 and qb.v_ld(1) == 16
     s = qb.make_shape(1, 32, 8, 8192, 8192, 128)
     p = qb.make_params(causal=True)
-    assert qb.workspace_size(s, p) >= 2 * (32 + 8) * 8192 * 128
+    # at least the fp16 carriers of the K codes (Q codes are widened in-kernel)
+    assert qb.workspace_size(s, p) >= 2 * 8 * 8192 * 128
     assert qb.workspace_size(qb.make_shape(0, 32, 8, 8192, 8192, 128), p) == 0
 
 
