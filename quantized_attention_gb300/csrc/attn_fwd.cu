@@ -5,8 +5,8 @@
 // first (causal) in a snake order over the CTAs.  Warp roles (12 warps):
 //   warp 0      lane 0 issues every TMA load: the item's two int8 Q tiles, a
 //               ring of K stages and a ring of V^T stages;
-//   warp 1      owns the 512 TMEM columns; lane 0 issues the QK^T MMAs;
-//   warp 2      lane 0 issues the PV MMAs;
+//   warp 1      owns the 512 TMEM columns; lane 0 issues the MMAs of tile t0;
+//   warp 2      lane 0 issues the MMAs of tile t1;
 //   warp 3      idle;
 //   warps 4-7   softmax of tile t0, warps 8-11 softmax of tile t1 (one query
 //               row per thread, row r = TMEM lane r).
@@ -17,15 +17,16 @@
 // exact fp16 in shared memory (q_conv); K arrives as fp16 carriers.
 // Per tile t and key block j:
 //   softmax(t, j) loads S_t(j) from TMEM and at once releases it (s_free), so
-//   the MMA thread issues QK(t, j+1) -- S_t = Q_t . K_{j+1}^T, kind::f16 on
-//   exact fp16 carriers of the int8 codes (every partial sum is an integer
-//   below 2^21, so the fp32 accumulator holds it exactly) -- while the
-//   softmax computes P; when P_t(j) is in shared memory and O_t rescaled
-//   (p_full) the MMA thread issues PV(t, j): O_t (+)= P_t . V8_j, kind::f8f6f4.
+//   the tile's MMA thread issues QK(t, j+1) -- S_t = Q_t . K_{j+1}^T,
+//   kind::f16 on exact fp16 carriers of the int8 codes (every partial sum is
+//   an integer below 2^21, so the fp32 accumulator holds it exactly) -- while
+//   the softmax computes P; when P_t(j) is in shared memory and O_t rescaled
+//   (p_full) it issues PV(t, j): O_t (+)= P_t . V8_j, kind::f8f6f4.
 //   softmax(t, j+1) waits for PV(t, j) (pv_done) before it overwrites P_t or
 //   rescales O_t.
-// The two tiles' softmaxes run on different warps, so the tensor core works on
-// one tile while the other's softmax runs, and QK(t, j+1) overlaps softmax(t, j).
+// The two tiles run independently (their own softmax warps and MMA thread),
+// sharing only the K / V stages, so the tensor core works on one tile while
+// the other's softmax runs, and QK(t, j+1) overlaps softmax(t, j).
 #include <cuda_bf16.h>
 
 #include "qattn_internal.h"
@@ -219,12 +220,15 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
 }
 
 // One softmax step for one query row and one key block.
-//   s      the row's 128 scores (fp32 bit patterns of integers; with BIAS they
-//          are overwritten by t = S c + bias log2e)
-//   nvis   keys 0 .. nvis-1 of the block are visible (MASKED only)
+//   s      the row's 128 scores: fp32 bit patterns of the integer scores, with
+//          -inf for masked keys (without BIAS); with BIAS they are
+//          overwritten by t = S c + bias log2e, and keys >= nvis are masked
+//   c      the block's score scale (> 0 without BIAS, so -inf * c = -inf)
 // Updates the running max m and sum l (l in units of 448 P), returns alpha
 // and the e4m3 codes of 448 P packed four per word (key 4q + e in byte e).
-template <bool BIAS, bool MASKED>
+// One body serves masked and unmasked blocks: a second, masked copy of this
+// fully unrolled code would double the loop's instruction footprint.
+template <bool BIAS>
 __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int nvis,
                                               const float* brow, float& m, float& l,
                                               uint32_t (&pw)[kBN / 4]) {
@@ -234,23 +238,17 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
 #pragma unroll
       for (int k = 0; k < kBN; ++k) {
         float t = fmaf(__uint_as_float(s[k]), c, __fmul_rn(__ldg(brow + k), kLog2e));
-        if (MASKED && k >= nvis) t = kNegInf;
+        if (k >= nvis) t = kNegInf;
         s[k] = __float_as_uint(t);
       }
     }
     float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
 #pragma unroll
     for (int k = 0; k < kBN; k += 8) {
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[e] = __uint_as_float(s[k + e]);
-        if (MASKED && !BIAS && k + e >= nvis) v[e] = kNegInf;
-      }
-      mx0 = fmax3(mx0, v[0], v[1]);
-      mx1 = fmax3(mx1, v[2], v[3]);
-      mx2 = fmax3(mx2, v[4], v[5]);
-      mx3 = fmax3(mx3, v[6], v[7]);
+      mx0 = fmax3(mx0, __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
+      mx1 = fmax3(mx1, __uint_as_float(s[k + 2]), __uint_as_float(s[k + 3]));
+      mx2 = fmax3(mx2, __uint_as_float(s[k + 4]), __uint_as_float(s[k + 5]));
+      mx3 = fmax3(mx3, __uint_as_float(s[k + 6]), __uint_as_float(s[k + 7]));
     }
     mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
   }
@@ -276,10 +274,6 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
       } else {
         x = ffma2(make_float2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])),
                   make_float2(c, c), make_float2(kneg, kneg));
-      }
-      if (MASKED) {
-        if (kk >= nvis) x.x = kNegInf;
-        if (kk + 1 >= nvis) x.y = kNegInf;
       }
       const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
       acc[(k / 2 + e) & 3] = fadd2(acc[(k / 2 + e) & 3], p);
@@ -327,7 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool softmax_side = (i >= kBarSFree && i < kBarSFree + 2) ||
                                 (i >= kBarPFull && i < kBarPFull + 2) ||
                                 (i >= kBarQConv && i < kBarQConv + 2);
-      mbar_init(bar(i), softmax_side ? kBM : 1);
+      // Q, K and V stages are freed by both tiles' issuers.
+      const bool shared_stage = (i >= kBarQEmpty && i < kBarQEmpty + 2) ||
+                                (i >= kBarKEmpty && i < kBarKEmpty + 4) ||
+                                (i >= kBarVEmpty && i < kBarVEmpty + 4);
+      mbar_init(bar(i), softmax_side ? kBM : shared_stage ? 2 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -410,19 +408,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
-      // Two issuing threads in separate warps, so that one thread's barrier
-      // waits and commits overlap the other's MMAs (the tensor core accepts
-      // only a short queue of MMAs, so a single issuer would leave it idle
-      // whenever it waits):
-      //   warp 1: QK(t, b) = S_t <- Q_t . K_b^T once K_b is loaded and
-      //           softmax(t, b-1) has released S_t; commits s_full[t], then
-      //           frees the K stage, and the Q stage after the item's last QK;
-      //   warp 2: PV(t, b) = O_t (+)= P_t . V8_b once V_b is loaded and P_t(b)
-      //           is written; commits pv_done[t], then frees the V stage.
-      const bool qk_issuer = (warp == 1);
-      uint32_t kvc = 0;                   // K (or V) blocks consumed so far
-      uint32_t nev[2] = {0, 0};           // QKs (or PVs) issued per tile
-      uint32_t nqc[2] = {0, 0};           // Q tiles widened per tile
+      // One issuing thread per query tile (warp 1: t0, warp 2: t1), so a tile
+      // whose softmax runs ahead is never held back by the other.  Per item
+      // it issues, in the order its softmax frees the inputs,
+      //   QK(0), QK(1), PV(0), QK(2), PV(1), ..., PV(nb_t - 1)
+      // where QK(b): S_t <- Q_t . K_b^T once K_b is loaded and softmax(t,
+      // b-1) has loaded S_t (s_free), plus, for b = 0, once Q_t is widened;
+      // PV(b): O_t (+)= P_t . V8_b once V_b is loaded and P_t(b) written
+      // (p_full).  Each Q / K / V stage is freed by a commit from both issuers
+      // (barrier count 2); a tile with fewer key blocks than its partner
+      // still waits for and frees each remaining stage, in order, so neither
+      // issuer can free a stage the other is still reading.
+      const int t = warp - 1;
+      uint32_t kvc = 0;          // K (and V) blocks of earlier items
+      uint32_t nqk = 0, npv = 0;  // QKs / PVs issued for this tile
+      uint32_t nqc = 0;          // Q tiles widened for this tile
       int i = 0;
       bool ok = true;
       for (int k = 0; ok && k * G < n_items; ++k) {
@@ -431,55 +431,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode_item(w, a, n_pairs);
         const int qs = i % C::kQS;
         const int nb = max(it.nb[0], it.nb[1]);
-        if (qk_issuer) {
-          for (int b = 0; ok && b < nb; ++b) {
+        const int nbt = it.nb[t];
+        if (nbt == 0) {  // nothing for this tile: free the item's Q stage
+          if ((ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
+            mma_commit(bar(kBarQEmpty + qs));
+        }
+        for (int b = 0; ok && b <= nb; ++b) {
+          if (b < nb) {  // key block b
             const uint32_t kk = kvc + b;
             const int st = kk % C::kNK;
             if (!(ok = mbar_wait(bar(kBarKFull + st), (kk / C::kNK) & 1, abort_flag, a.err, kErrTimeout)))
               break;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (!ok || b >= it.nb[t]) continue;
-              if (nev[t] > 0 &&
-                  !(ok = mbar_wait(bar(kBarSFree + t), (nev[t] - 1) & 1, abort_flag, a.err, kErrTimeout)))
-                continue;
+            if (b < nbt) {
+              if (nqk > 0 &&
+                  !(ok = mbar_wait(bar(kBarSFree + t), (nqk - 1) & 1, abort_flag, a.err, kErrTimeout)))
+                break;
               if (b == 0) {  // the item's Q_t, widened by the tile's softmax warps
-                if (!(ok = mbar_wait(bar(kBarQConv + t), nqc[t] & 1, abort_flag, a.err, kErrTimeout)))
-                  continue;
-                ++nqc[t];
+                if (!(ok = mbar_wait(bar(kBarQConv + t), nqc & 1, abort_flag, a.err, kErrTimeout)))
+                  break;
+                ++nqc;
               }
               tc_fence_after();
               issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st));
               mma_commit(bar(kBarSFull + t));
-              ++nev[t];
+              ++nqk;
             }
-            if (ok) mma_commit(bar(kBarKEmpty + st));
+            mma_commit(bar(kBarKEmpty + st));
+            if (b == nbt - 1) mma_commit(bar(kBarQEmpty + qs));  // the tile's last QK
           }
-          if (ok) mma_commit(bar(kBarQEmpty + qs));
-        } else {
-          for (int b = 0; ok && b < nb; ++b) {
-            const uint32_t vv = kvc + b;
+          if (b >= 1) {  // value block b - 1
+            const uint32_t vv = kvc + b - 1;
             const int st = vv % C::kNV;
             if (!(ok = mbar_wait(bar(kBarVFull + st), (vv / C::kNV) & 1, abort_flag, a.err, kErrTimeout)))
               break;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (!ok || b >= it.nb[t]) continue;
-              if (!(ok = mbar_wait(bar(kBarPFull + t), nev[t] & 1, abort_flag, a.err, kErrTimeout)))
-                continue;
+            if (b - 1 < nbt) {
+              if (!(ok = mbar_wait(bar(kBarPFull + t), npv & 1, abort_flag, a.err, kErrTimeout)))
+                break;
               tc_fence_after();
-              issue_pv<D>(tmem + 256 + 128 * t, sP(t), sV(st), b > 0);
+              issue_pv<D>(tmem + 256 + 128 * t, sP(t), sV(st), b > 1);
               mma_commit(bar(kBarPVDone + t));
-              ++nev[t];
+              ++npv;
             }
-            if (ok) mma_commit(bar(kBarVEmpty + st));
+            mma_commit(bar(kBarVEmpty + st));
           }
         }
         kvc += nb;
         ++i;
       }
       // Every MMA this thread issued finishes before TMEM is freed.
-      const int drain = kBarDrain + (qk_issuer ? 0 : 1);
+      const int drain = kBarDrain + t;
       mma_commit(bar(drain));
       volatile int never = 0;
       mbar_wait(bar(drain), 0, &never, a.err, kErrTimeout);
@@ -557,14 +557,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten by the next QK
-        const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
+        float c = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
         const int kbase = j * kBN;
         const bool need_mask = (kbase + kBN > a.Nk) || (kbase + kBN - 1 > tile_lim);
-        const int nvis = max(0, min(kBN, lim - kbase + 1));
+        const int nvis = need_mask ? max(0, min(kBN, lim - kbase + 1)) : kBN;
+        if (!BIAS) {
+          // Masked keys become -inf scores.  A zero (or subnormal) c would
+          // turn them into NaN; c = FLT_MIN leaves every visible t = S c at
+          // or within 2^-105 of the exact S c, so no P, alpha or l changes.
+          c = fmaxf(c, 0x1p-126f);
+          if (need_mask) {
+#pragma unroll
+            for (int k = 0; k < kBN; ++k)
+              if (k >= nvis) s[k] = 0xFF800000u;
+          }
+        }
         uint32_t pw[kBN / 4];
         const float* bk = BIAS ? brow + kbase : nullptr;
-        const float alpha = need_mask ? softmax_step<BIAS, true>(s, c, nvis, bk, m, l, pw)
-                                      : softmax_step<BIAS, false>(s, c, kBN, bk, m, l, pw);
+        const float alpha = softmax_step<BIAS>(s, c, nvis, bk, m, l, pw);
         if (j > 0) {  // PV(t, j-1) must be done with P_t and O_t
           ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);
           ++pvc;

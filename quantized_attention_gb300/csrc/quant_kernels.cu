@@ -78,58 +78,206 @@ __device__ __forceinline__ long long bf16_fix24(uint32_t b) {
   return (b & 0x8000u) ? -v : v;
 }
 
-// Channel sums of round(K * 2^24) over one chunk of kTokPerChunk tokens,
-// added into acc[bh][c] with 64-bit atomics (integer, so the order does not
-// matter).  The last CTA of each (batch, head) to finish turns the sums into
-// mu = fp32(fp64(sum) * 2^-24 / Nk).  acc and done must start at zero.
-template <int D>
-__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
-                                                         int nchunks,
-                                                         unsigned long long* __restrict__ acc,
-                                                         unsigned int* __restrict__ done,
-                                                         float* __restrict__ mu) {
-  constexpr int VPR = D / 8;               // 16-byte vectors per token row
-  constexpr int RPI = kThreads / VPR;      // rows per pass over the CTA
-  constexpr int NIT = kTokPerChunk / RPI;  // passes per chunk
-  __shared__ long long red64[RPI / 2][D];
-  __shared__ unsigned int last;
-  const int bh = blockIdx.y, chunk = blockIdx.x;
-  const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
-  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
-  uint4 raw[NIT];
+// round_half_even(x * 2^24) for many x at once, without 64-bit integer work.
+// With y = x * 2^24 (exact) and C1 = 1.5 * 2^46 (ulp 2^23):
+//   t  = fl(y + C1)            t = C1 + h * 2^23, h = rne(y / 2^23), |h| < 2^22
+//   lo = y - (t - C1)          exact, |lo| <= 2^22
+//   u  = fl(lo + C2)           C2 = 1.5 * 2^23 (ulp 1): u = C2 + rne(lo)
+// so rne(y) = h * 2^23 + rne(lo) (h * 2^23 is even, so ties round alike), with
+// h = bits(t) - bits(C1) and rne(lo) = bits(u) - bits(C2): integers that a
+// thread sums in 32 bits (the bias terms are removed once, at the end).  Valid
+// for |x| < 2^21; larger inputs take bf16_fix24.
+constexpr float kFixScale = 0x1p24f;
+constexpr float kFixC1 = 0x1.8p46f;
+constexpr float kFixC2 = 0x1.8p23f;
+constexpr uint32_t kFixC1Bits = 0x56C00000u;
+constexpr uint32_t kFixC2Bits = 0x4B400000u;
+constexpr uint32_t kFixMaxMag = 0x4A00u;  // bf16 magnitude bits of 2^21
+
+// Accumulates the fixed-point values of the 8 bf16 in `raw` into the biased
+// sums at/au (see above) and the largest magnitude pattern into mx.
+__device__ __forceinline__ void fix24_accumulate8(const uint4& raw, uint32_t (&at)[8],
+                                                  uint32_t (&au)[8], uint32_t& mx) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-  for (int it = 0; it < NIT; ++it) {
-    const int t = chunk * kTokPerChunk + r0 + it * RPI;
+  for (int e = 0; e < 4; ++e) {
+    mx = __vmaxu2(mx, w[e] & 0x7FFF7FFFu);
+    const float2 x = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+    const float2 t = ffma2(x, make_float2(kFixScale, kFixScale), make_float2(kFixC1, kFixC1));
+    const float2 nhi = ffma2(t, make_float2(-1.f, -1.f), make_float2(kFixC1, kFixC1));  // -(t - C1)
+    const float2 lo = ffma2(x, make_float2(kFixScale, kFixScale), nhi);
+    const float2 u = fadd2(lo, make_float2(kFixC2, kFixC2));
+    at[2 * e] += __float_as_uint(t.x);
+    at[2 * e + 1] += __float_as_uint(t.y);
+    au[2 * e] += __float_as_uint(u.x);
+    au[2 * e + 1] += __float_as_uint(u.y);
+  }
+}
+
+// Sum over NIT rows of one 16-byte column vector: the 8 channels' exact
+// sums of round(K * 2^24).  Rows past the end were loaded as zeros.
+template <int NIT>
+__device__ __forceinline__ void fix24_column_sums(const uint4 (&raw)[NIT], long long (&sum)[8]) {
+  uint32_t at[8], au[8], mx = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) at[e] = au[e] = 0u;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) fix24_accumulate8(raw[it], at, au, mx);
+  if (max(mx & 0xFFFFu, mx >> 16) < kFixMaxMag) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int h = static_cast<int>(at[e] - NIT * kFixC1Bits);
+      const int r = static_cast<int>(au[e] - NIT * kFixC2Bits);
+      sum[e] = static_cast<long long>(h) * (1ll << 23) + r;
+    }
+  } else {  // some |x| >= 2^21: the general integer decode
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] = 0;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sum[2 * e] += bf16_fix24(w[e] & 0xFFFFu);
+        sum[2 * e + 1] += bf16_fix24(w[e] >> 16);
+      }
+    }
+  }
+}
+
+// x = q * N + r (0 <= r < N) for x < 2^57, with M = floor((2^64 - 1) / N):
+// q_est = floor(x * M / 2^64) is floor(x / N) or one less.
+__device__ __forceinline__ void udivmod(unsigned long long x, uint32_t N, unsigned long long M,
+                                        unsigned long long& q, unsigned long long& r) {
+  q = __umul64hi(x, M);
+  r = x - q * N;
+  if (r >= N) {
+    ++q;
+    r -= N;
+  }
+}
+
+// mu = fp32(fp64(S) * 2^-24 / N), computed as the correctly rounded fp32
+// quotient |S| / N (then scaled by 2^-24) with integer long division -- no
+// fp64, whose throughput on this part is a small fraction of fp32's.
+// The two agree.  With A = |S| < 2^53 and N < 2^24, rounding A / N to fp64
+// first could change the fp32 result only by landing exactly on an fp32
+// rounding midpoint b != A / N, i.e. 0 < |A/N - b| <= 2^(e-53) for b in
+// [2^e, 2^(e+1)).  But N (A/N - b) is a nonzero multiple of 2^(e-24), so
+// |A/N - b| >= 2^(e-24) / N > 2^(e-48); and if e > 24, b is an integer, so
+// |A/N - b| >= 1/N, which is > 2^(e-53) unless N >= 2^(53-e), and then
+// A ~ N b > 2^53.  Both cases are impossible.
+__device__ __forceinline__ float mean_of_fix24(long long S, uint32_t N, unsigned long long M) {
+  if (S == 0) return 0.f;
+  const unsigned long long A = S < 0 ? 0ull - static_cast<unsigned long long>(S)
+                                     : static_cast<unsigned long long>(S);
+  unsigned long long Q, R;
+  udivmod(A, N, M, Q, R);  // A / N = (Q + R / N) * 2^-fr, fr = 0 so far
+  int fr = 0;
+  int bl = 64 - __clzll(static_cast<long long>(Q));
+  while (bl < 25) {  // append quotient bits until Q holds 25 (24 + a guard bit)
+    const int m = min(32, 25 - bl);
+    unsigned long long q2, r2;
+    udivmod(R << m, N, M, q2, r2);
+    Q = (Q << m) | q2;
+    R = r2;
+    fr += m;
+    bl = 64 - __clzll(static_cast<long long>(Q));
+  }
+  const int drop = bl - 25;
+  const bool sticky = (R != 0) || (drop > 0 && (Q & ((1ull << drop) - 1ull)) != 0);
+  const unsigned long long T = Q >> drop;  // 25 bits
+  fr -= drop;
+  uint32_t U = static_cast<uint32_t>(T >> 1);  // 24 bits, value U * 2^(1 - fr)
+  if ((T & 1ull) && (sticky || (U & 1u))) ++U;  // round half to even
+  int e = 1 - fr - 24;  // value / 2^24 = U * 2^e
+  if (U == (1u << 24)) {
+    U >>= 1;
+    ++e;
+  }
+  const uint32_t bits = (static_cast<uint32_t>(e + 23 + 127) << 23) | (U - (1u << 23));
+  return __uint_as_float(bits | (S < 0 ? 0x80000000u : 0u));
+}
+
+constexpr int kMeanRows = 8;  // rows per thread in the mean kernels
+
+// Channel mean for short heads: one warp per (batch, head), all Nk rows
+// (Nk <= 8 * 32 / (D / 8)); lanes = (row group, 16-byte column).
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const uint16_t* __restrict__ K,
+                                                              int BH, int Nk,
+                                                              unsigned long long magic,
+                                                              float* __restrict__ mu) {
+  constexpr int VPR = D / 8;
+  constexpr int RG = 32 / VPR;
+  const int bh = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (bh >= BH) return;
+  const int lane = threadIdx.x & 31;
+  const int v = lane % VPR, rg = lane / VPR;
+  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
+  uint4 raw[kMeanRows];
+#pragma unroll
+  for (int it = 0; it < kMeanRows; ++it) {
+    const int t = rg + it * RG;
     raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * D) + v)
                        : make_uint4(0u, 0u, 0u, 0u);
   }
-  long long a8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  long long sum[8];
+  fix24_column_sums<kMeanRows>(raw, sum);
 #pragma unroll
-  for (int it = 0; it < NIT; ++it) {
-    const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+  for (int o = VPR; o < 32; o <<= 1) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      a8[2 * e] += bf16_fix24(w[e] & 0xFFFFu);
-      a8[2 * e + 1] += bf16_fix24(w[e] >> 16);
-    }
+    for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
   }
-  // Fold the CTA's rows: the upper half into the lower half, then a column sum.
-  if (r0 >= RPI / 2) {
+  // Every lane now holds its column's 8 sums; the RG lanes of a column share
+  // the 8 divisions between them.
 #pragma unroll
-    for (int e = 0; e < 8; ++e) red64[r0 - RPI / 2][v * 8 + e] = a8[e];
+  for (int e = 0; e < 8; ++e) {
+    if (e % RG == rg)
+      mu[static_cast<size_t>(bh) * D + v * 8 + e] =
+          mean_of_fix24(sum[e], static_cast<uint32_t>(Nk), magic);
   }
-  __syncthreads();
-  if (r0 < RPI / 2) {
+}
+
+// Channel mean over CTA-sized chunks of kMeanRows * (256 / (D / 8)) rows.
+// MULTI = false: one chunk holds the whole head and the CTA writes mu.
+// MULTI = true: each chunk adds its sums into acc[bh][c] with 64-bit atomics
+// (integer, so the order does not matter) and the last CTA of the head to
+// finish writes mu; acc and done must start at zero.
+template <int D, bool MULTI>
+__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
+                                                         int nchunks, unsigned long long magic,
+                                                         unsigned long long* __restrict__ acc,
+                                                         unsigned int* __restrict__ done,
+                                                         float* __restrict__ mu) {
+  constexpr int VPR = D / 8;           // 16-byte vectors per row
+  constexpr int RG = kThreads / VPR;   // row groups per CTA
+  constexpr int kChunk = RG * kMeanRows;
+  __shared__ long long red[RG][D];
+  __shared__ unsigned int last;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int v = threadIdx.x % VPR, rg = threadIdx.x / VPR;
+  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
+  uint4 raw[kMeanRows];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) red64[r0][v * 8 + e] += a8[e];
+  for (int it = 0; it < kMeanRows; ++it) {
+    const int t = chunk * kChunk + rg + it * RG;
+    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * D) + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
   }
+  long long sum[8];
+  fix24_column_sums<kMeanRows>(raw, sum);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rg][v * 8 + e] = sum[e];
   __syncthreads();
   for (int c = threadIdx.x; c < D; c += kThreads) {
-    long long sum = 0;
-#pragma unroll
-    for (int r = 0; r < RPI / 2; ++r) sum += red64[r][c];
-    atomicAdd(acc + static_cast<size_t>(bh) * D + c, static_cast<unsigned long long>(sum));
+    long long tot = 0;
+#pragma unroll 8
+    for (int r = 0; r < RG; ++r) tot += red[r][c];
+    if (!MULTI) mu[static_cast<size_t>(bh) * D + c] = mean_of_fix24(tot, static_cast<uint32_t>(Nk), magic);
+    else atomicAdd(acc + static_cast<size_t>(bh) * D + c, static_cast<unsigned long long>(tot));
   }
+  if (!MULTI) return;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last = (atomicAdd(done + bh, 1u) == static_cast<unsigned int>(nchunks - 1));
@@ -139,8 +287,7 @@ __global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __rest
     for (int c = threadIdx.x; c < D; c += kThreads) {
       const long long tot =
           static_cast<long long>(atomicAdd(acc + static_cast<size_t>(bh) * D + c, 0ull));
-      const double m = (__ll2double_rn(tot) * 0x1p-24) / static_cast<double>(Nk);
-      mu[static_cast<size_t>(bh) * D + c] = __double2float_rn(m);
+      mu[static_cast<size_t>(bh) * D + c] = mean_of_fix24(tot, static_cast<uint32_t>(Nk), magic);
     }
   }
 }
@@ -430,19 +577,37 @@ size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d) {
   return static_cast<size_t>(BH * d) * sizeof(unsigned long long) + static_cast<size_t>(BH) * 4;
 }
 
+template <int D>
+static cudaError_t smooth_k_t(const uint16_t* K, int BH, int Nk, long long* ws, float* mu,
+                              cudaStream_t s) {
+  constexpr int kWarpRows = kMeanRows * 32 / (D / 8);
+  constexpr int kChunk = kMeanRows * kThreads / (D / 8);
+  const unsigned long long magic = ~0ull / static_cast<unsigned long long>(Nk);
+  if (Nk <= kWarpRows) {
+    const int per = kThreads / 32;
+    k_mean_warp_kernel<D><<<(BH + per - 1) / per, kThreads, 0, s>>>(K, BH, Nk, magic, mu);
+    return cudaGetLastError();
+  }
+  const int nchunks = (Nk + kChunk - 1) / kChunk;
+  const dim3 grid(nchunks, BH);
+  if (nchunks == 1) {
+    k_mean_kernel<D, false><<<grid, kThreads, 0, s>>>(K, Nk, 1, magic, nullptr, nullptr, mu);
+    return cudaGetLastError();
+  }
+  unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws);
+  unsigned int* done = reinterpret_cast<unsigned int*>(acc + static_cast<size_t>(BH) * D);
+  const cudaError_t e = cudaMemsetAsync(ws, 0, smooth_k_ws_bytes(BH, Nk, D), s);
+  if (e != cudaSuccess) return e;
+  k_mean_kernel<D, true><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, magic, acc, done, mu);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
                             cudaStream_t s) {
   if (Nk == 0) return cudaMemsetAsync(mu, 0, static_cast<size_t>(BH) * d * sizeof(float), s);
-  unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws);
-  unsigned int* done = reinterpret_cast<unsigned int*>(acc + static_cast<size_t>(BH) * d);
-  cudaError_t e = cudaMemsetAsync(ws, 0, smooth_k_ws_bytes(BH, Nk, d), s);
-  if (e != cudaSuccess) return e;
-  const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  const dim3 grid(nchunks, BH);
-  if (d == 32) k_mean_kernel<32><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
-  else if (d == 64) k_mean_kernel<64><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
-  else k_mean_kernel<128><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, acc, done, mu);
-  return cudaGetLastError();
+  if (d == 32) return smooth_k_t<32>(K, BH, Nk, ws, mu, s);
+  if (d == 64) return smooth_k_t<64>(K, BH, Nk, ws, mu, s);
+  return smooth_k_t<128>(K, BH, Nk, ws, mu, s);
 }
 
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran) {

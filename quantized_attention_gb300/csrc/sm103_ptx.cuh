@@ -272,6 +272,20 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
+// ---------------------------------------------------------------- registers
+// Per-thread register budget of the calling warpgroup (all four warps must
+// execute the same instruction).  inc waits until the CTA's pool holds enough
+// registers, so the budgets of all warpgroups must sum to at most the
+// registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- smem, sync
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
