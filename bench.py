@@ -53,6 +53,30 @@ def mixed_peak(peaks, sustained=True):
     return 1.0 / (0.5 / p16 + 0.5 / p8)
 
 
+def _attn_traffic(wl_name):
+    """DRAM bytes per attention-kernel launch from the committed ncu capture
+    (profiles/attn_fwd_<workload>_traffic.txt), or None when there is none for
+    this workload or the kernel source has changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{wl_name}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#") and "=" in line:
+                k, v = line.split("=", 1)
+                kv[k] = v
+    h = hashlib.sha256()
+    for name in ("attn_fwd.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "quantized_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if kv.get("workload") != wl_name or kv.get("kernel_source_sha256") != h.hexdigest():
+        return None
+    return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+
+
 # ----------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------
@@ -326,11 +350,12 @@ def gpu_arm(args):
     pmix = mixed_peak(peaks, sustained=True)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = ops / (attn_avg_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "qattn_fwd (fused attention)",
+    roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel (the one launch of qattn_fwd)",
                 "achieved": achieved, "peak": pmix, "unit": "TFLOP/s", "frac": achieved / pmix,
                 "peak_basis": (f"{peaks['source']}: QK^T at the sustained bf16 rate "
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
-                "traffic": None}
+                "traffic": _attn_traffic(args.workload),
+                "traffic_unit": "bytes per launch (ncu dram read + write)"}
     cpu = None
     if not args.no_cpu_baseline:
         c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)

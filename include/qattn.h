@@ -112,7 +112,8 @@ int64_t qattn_v_ld(int64_t Nk);
  *   k_mean  fp32 [B][Hkv][d] (out):
  *           mu = fp32( fp64( sum_t round_half_even(K * 2^24) ) * 2^-24 / Nk )
  *           The int64 fixed-point sum makes the result independent of the
- *           summation order.  Valid while |K| < 2^20; Nk = 0 gives mu = 0.
+ *           summation order.  Exact while Nk * max|K| < 2^29 (the sum stays
+ *           below 2^53); Nk = 0 gives mu = 0.
  */
 qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* k_mean,
                             void* workspace, size_t workspace_bytes, qattn_stream_t stream);
@@ -134,13 +135,17 @@ qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* 
  *   q_scales     fp32, params->q_gran layout (out)
  *   k_codes      int8 [B][Hkv][Nk][d] (out; BF16 K only, ignored for I8 K)
  *   k_scales     fp32, params->k_gran layout (out)
+ *   k_carrier    NULL, or fp16 [B][Hkv][Nk][d] (out): the K codes (those
+ *                written to k_codes, or the I8 K given) as exact fp16 values,
+ *                the operand form of the tensor-core product; hand it to
+ *                qattn_fwd to spare it a conversion pass.
  */
 qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
                                const float* k_mean, const float* k_chan_scale,
                                const qattn_shape* shape, const qattn_params* params,
                                int8_t* q_codes, float* q_scales, int8_t* k_codes,
-                               float* k_scales, void* workspace, size_t workspace_bytes,
-                               qattn_stream_t stream);
+                               float* k_scales, uint16_t* k_carrier, void* workspace,
+                               size_t workspace_bytes, qattn_stream_t stream);
 
 /* a3 -- V to e4m3 with one fp32 scale per (batch, KV head, channel) (ZINC
  * post, "fp8 is not faster": e4m3 PV; the per-channel scale factors out of the
@@ -185,6 +190,9 @@ qattn_status qattn_quantize_v_noalloc(const void* V, qattn_dtype v_dtype,
 
 /* a4-a10 -- fused attention forward (prefill).
  *   q_codes/q_scales, k_codes/k_scales   as written by qattn_quantize_qk
+ *   k_carrier  NULL, or the fp16 carriers qattn_quantize_qk wrote for these
+ *              K codes (then the workspace may be NULL / 0 bytes); with NULL
+ *              the call first converts k_codes itself, in the workspace.
  *   v8t, ldv, v_scales                    as written by qattn_quantize_v
  *   bias   NULL, or fp32 [Nq][Nk] in natural-log units added to the scaled
  *          scores (one matrix per head if params->bias_head_stride != 0).
@@ -204,8 +212,9 @@ qattn_status qattn_quantize_v_noalloc(const void* V, qattn_dtype v_dtype,
  * kind::f8f6f4 e4m3 x e4m3 with fp32 accumulation.
  */
 qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
-                       const float* k_scales, const uint8_t* v8t, int64_t ldv,
-                       const float* v_scales, const float* bias, const qattn_shape* shape,
+                       const uint16_t* k_carrier, const float* k_scales, const uint8_t* v8t,
+                       int64_t ldv, const float* v_scales, const float* bias,
+                       const qattn_shape* shape,
                        const qattn_params* params, void* O, float* lse, void* workspace,
                        size_t workspace_bytes, qattn_stream_t stream);
 

@@ -67,10 +67,11 @@ def lib() -> ctypes.CDLL:
     L.qattn_v_ld.restype = i64
     L.qattn_v_ld.argtypes = [i64]
     L.qattn_smooth_k.argtypes = [vp, PS, vp, vp, sz, vp]
-    L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, sz, vp]
+    L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp,
+                                    sz, vp]
     L.qattn_quantize_v.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
     L.qattn_quantize_v_noalloc.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp]
-    L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
+    L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
@@ -145,13 +146,16 @@ def smooth_k(K, shape, k_mean, workspace, stream=None):
 
 
 def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_scales,
-                k_codes, k_scales, workspace, stream=None):
+                k_codes, k_scales, workspace, stream=None, k_carrier=None):
     _dense(Q, torch.bfloat16, "Q")
     _dense(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")
+    if k_carrier is not None:
+        _dense(k_carrier, torch.float16, "k_carrier")
     _check(lib().qattn_quantize_qk(_p(Q), _p(K), k_dtype, _p(k_mean), _p(k_chan_scale),
                                    ctypes.byref(shape), ctypes.byref(params), _p(q_codes),
-                                   _p(q_scales), _p(k_codes), _p(k_scales), _p(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+                                   _p(q_scales), _p(k_codes), _p(k_scales), _p(k_carrier),
+                                   _p(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)),
            "qattn_quantize_qk")
 
 
@@ -173,11 +177,14 @@ def quantize_v_noalloc(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, stre
 
 
 def fwd(q_codes, q_scales, k_codes, k_scales, v8t, ldv, v_scales, bias, shape, params, O, lse,
-        workspace, stream=None):
-    _check(lib().qattn_fwd(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales), _p(v8t), ldv,
-                           _p(v_scales), _p(bias), ctypes.byref(shape), ctypes.byref(params),
-                           _p(O), _p(lse), _p(workspace),
-                           workspace.numel() * workspace.element_size(), _stream(stream)),
+        workspace, stream=None, k_carrier=None):
+    if k_carrier is not None:
+        _dense(k_carrier, torch.float16, "k_carrier")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qattn_fwd(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_carrier), _p(k_scales),
+                           _p(v8t), ldv, _p(v_scales), _p(bias), ctypes.byref(shape),
+                           ctypes.byref(params), _p(O), _p(lse), _p(workspace), ws_bytes,
+                           _stream(stream)),
            "qattn_fwd")
 
 

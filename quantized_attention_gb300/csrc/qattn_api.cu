@@ -182,8 +182,8 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
                                const float* k_mean, const float* k_chan_scale,
                                const qattn_shape* shape, const qattn_params* params,
                                int8_t* q_codes, float* q_scales, int8_t* k_codes,
-                               float* k_scales, void* workspace, size_t workspace_bytes,
-                               qattn_stream_t stream) {
+                               float* k_scales, uint16_t* k_carrier, void* workspace,
+                               size_t workspace_bytes, qattn_stream_t stream) {
   qattn_status st = check_shape(shape);
   if (st != QATTN_OK) return st;
   if ((st = check_params(params)) != QATTN_OK) return st;
@@ -194,6 +194,7 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   if (i8 && (!k_chan_scale || !aligned16(k_chan_scale))) return QATTN_ERR_INVALID_ARG;
   if (!i8 && shape->Nk > 0 && (!K || !aligned16(K) || !k_codes || !aligned16(k_codes))) return QATTN_ERR_INVALID_ARG;
   if (k_mean && (i8 || !aligned16(k_mean))) return QATTN_ERR_INVALID_ARG;
+  if (k_carrier && !aligned16(k_carrier)) return QATTN_ERR_INVALID_ARG;
   const size_t wq = align256(qattn::quantize_rows_ws_bytes(shape->B, shape->Hq, shape->Nq, params->q_gran));
   const size_t need = ws_quant_qk(shape, params);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
@@ -220,6 +221,11 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   if (i8) {
     cudaError_t e = qattn::launch_quantize_rows(jq, 2, jk, 0, d, s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
+    if (k_carrier && shape->Nk > 0) {
+      e = qattn::launch_codes_to_f16(static_cast<const int8_t*>(K), k_carrier,
+                                     static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * d), s);
+      if (e != cudaSuccess) return QATTN_ERR_CUDA;
+    }
     const int64_t n = params->k_gran == QATTN_GRAN_TENSOR ? 1
                       : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
                                                           : shape->B * shape->Hkv * nkb;
@@ -236,6 +242,7 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
     jk.codes = k_codes;
     jk.scales = k_scales;
     jk.ws_amax = ws_k;
+    jk.carrier = k_carrier;
     jk.nblk = static_cast<int>(nkb);
     jk.BH = B * Hkv;
   }
@@ -265,7 +272,8 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
 }
 
 qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
-                       const float* k_scales, const uint8_t* v8t, int64_t ldv,
+                       const uint16_t* k_carrier, const float* k_scales, const uint8_t* v8t,
+                       int64_t ldv,
                        const float* v_scales, const float* bias, const qattn_shape* shape,
                        const qattn_params* params, void* O, float* lse, void* workspace,
                        size_t workspace_bytes, qattn_stream_t stream) {
@@ -279,8 +287,13 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
   if (shape->Nk > 0) {
     if (!k_codes || !aligned16(k_codes) || !k_scales || !v8t || !aligned16(v8t) || !v_scales) return QATTN_ERR_INVALID_ARG;
+    if (k_carrier && !aligned16(k_carrier)) return QATTN_ERR_INVALID_ARG;
     if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return QATTN_ERR_INVALID_ARG;
+  }
+  if (!k_carrier) {  // the K codes are converted into the workspace
+    const size_t need = ws_fwd(shape);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned int* err = error_word();
@@ -312,13 +325,15 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
     // writes the zeros; give it valid (unused) maps.
     a.Nk = 0;
   }
-  const size_t need = ws_fwd(shape);
-  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
-  uint16_t* kc16 = static_cast<uint16_t*>(workspace);
-  if (shape->Nk > 0) {
-    const cudaError_t e = qattn::launch_codes_to_f16(
-        k_codes, kc16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
-    if (e != cudaSuccess) return QATTN_ERR_CUDA;
+  const uint16_t* kc16 = k_carrier;
+  if (!kc16) {  // convert the K codes into the workspace (checked above)
+    uint16_t* w16 = static_cast<uint16_t*>(workspace);
+    if (shape->Nk > 0) {
+      const cudaError_t e = qattn::launch_codes_to_f16(
+          k_codes, w16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+      if (e != cudaSuccess) return QATTN_ERR_CUDA;
+    }
+    kc16 = w16;
   }
   CUtensorMap tq, tk, tv;
   const int64_t nk_map = shape->Nk > 0 ? shape->Nk : 1;

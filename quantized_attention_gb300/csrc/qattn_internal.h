@@ -44,6 +44,7 @@ struct RowsJob {
   int8_t* codes;
   float* scales;
   float* ws_amax;  // B*H*nblk block maxima (tensor / head granules only)
+  uint16_t* carrier;  // nullable: the codes again as exact fp16, same layout
   int nblk, BH;    // 128-token blocks per head; B*H (0: no job)
 };
 // Quantizes j0 (mode m0) and j1 (mode m1) in the same launches.  Supported:

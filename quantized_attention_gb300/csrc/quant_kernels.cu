@@ -371,8 +371,14 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
         q = max(-127, min(127, q));
         w[e / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e % 4));
       }
-      *reinterpret_cast<uint2*>(j.codes + (static_cast<size_t>(bh) * j.N + t0 + r) * D + cv * 8) =
-          make_uint2(w[0], w[1]);
+      const size_t off = (static_cast<size_t>(bh) * j.N + t0 + r) * D + cv * 8;
+      *reinterpret_cast<uint2*>(j.codes + off) = make_uint2(w[0], w[1]);
+      if (j.carrier != nullptr) {
+        uint4 h;
+        codes4_to_f16x2(w[0], h.x, h.y);
+        codes4_to_f16x2(w[1], h.z, h.w);
+        *reinterpret_cast<uint4*>(j.carrier + off) = h;
+      }
     }
   }
   if (threadIdx.x == 0) {

@@ -17,7 +17,7 @@ from . import binding as qb
 class Problem:
     def __init__(self, B, Hq, Hkv, Nq, Nk, d, *, causal=False, q_gran=qb.GRAN_BLOCK,
                  k_gran=qb.GRAN_BLOCK, q_pos0=None, kv_codes=False, out_dtype=qb.DT_F32,
-                 bias_head_stride=0, want_lse=False, device="cuda"):
+                 bias_head_stride=0, want_lse=False, k_carrier=True, device="cuda"):
         self.B, self.Hq, self.Hkv, self.Nq, self.Nk, self.d = B, Hq, Hkv, Nq, Nk, d
         self.kv_codes = kv_codes
         self.shape = qb.make_shape(B, Hq, Hkv, Nq, Nk, d)
@@ -32,6 +32,10 @@ class Problem:
         self.k_codes = None if kv_codes else torch.empty((B, Hkv, Nk, d), dtype=i8, device=dev)
         self.k_scales = torch.empty((qb.n_scales(k_gran, B, Hkv, Nk),), dtype=f32, device=dev)
         self.k_mean = None if kv_codes else torch.empty((B, Hkv, d), dtype=f32, device=dev)
+        # fp16 carriers of the K codes, written by quantize_qk and read by fwd
+        # (None: fwd converts the codes itself, in the workspace)
+        self.k_carrier = (torch.empty((B, Hkv, Nk, d), dtype=torch.float16, device=dev)
+                          if k_carrier else None)
         self.v8t = torch.empty((B, Hkv, d, self.ldv), dtype=torch.uint8, device=dev)
         self.v_scales = torch.empty((B, Hkv, d), dtype=f32, device=dev)
         odt = torch.bfloat16 if out_dtype == qb.DT_BF16 else f32
@@ -45,7 +49,8 @@ class Problem:
         """a1-a3: codes and scales for Q, K and V."""
         if self.kv_codes:
             qb.quantize_qk(Q, K_codes, qb.DT_I8, None, K_scale, self.shape, self.params,
-                           self.q_codes, self.q_scales, None, self.k_scales, self.workspace, stream)
+                           self.q_codes, self.q_scales, None, self.k_scales, self.workspace, stream,
+                           k_carrier=self.k_carrier)
             qb.quantize_v(V_codes, qb.DT_I8, V_scale, self.shape, self.v8t, self.ldv,
                           self.v_scales, self.workspace, stream)
             self._k_codes = K_codes
@@ -53,7 +58,7 @@ class Problem:
             qb.smooth_k(K, self.shape, self.k_mean, self.workspace, stream)
             qb.quantize_qk(Q, K, qb.DT_BF16, self.k_mean, None, self.shape, self.params,
                            self.q_codes, self.q_scales, self.k_codes, self.k_scales,
-                           self.workspace, stream)
+                           self.workspace, stream, k_carrier=self.k_carrier)
             qb.quantize_v(V, qb.DT_BF16, None, self.shape, self.v8t, self.ldv, self.v_scales,
                           self.workspace, stream)
             self._k_codes = self.k_codes
@@ -62,20 +67,20 @@ class Problem:
         """a4-a10: the fused attention kernel on the quantized operands."""
         qb.fwd(self.q_codes, self.q_scales, self._k_codes, self.k_scales, self.v8t, self.ldv,
                self.v_scales, bias, self.shape, self.params, self.O, self.lse, self.workspace,
-               stream)
+               stream, k_carrier=self.k_carrier)
         return self.O
 
     def kernel_launches(self) -> int:
         """Kernels of this library that one ``run`` launches (memsets excluded)."""
-        two_pass_q = self.params.q_gran != qb.GRAN_BLOCK
-        two_pass_k = self.params.k_gran != qb.GRAN_BLOCK
-        n = 1 + int(two_pass_q)                      # Q codes
+        two_pass = (self.params.q_gran != qb.GRAN_BLOCK or
+                    (not self.kv_codes and self.params.k_gran != qb.GRAN_BLOCK))
+        n = 1 + int(two_pass)                        # Q and K codes (one grid)
         if self.kv_codes:
-            n += 1                                   # K scales set to 1
+            n += 1 + int(self.k_carrier is not None)  # K scales set to 1, K carriers
         else:
-            n += 2 + 1 + int(two_pass_k)             # channel mean (2), K codes
+            n += 1                                   # channel mean
         n += 2                                       # V amax, V e4m3 transpose
-        n += 3                                       # Q/K fp16 carriers, fused attention
+        n += 1 + int(self.k_carrier is None)         # [K carriers], fused attention
         return n
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,

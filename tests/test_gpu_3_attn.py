@@ -81,3 +81,21 @@ def test_repeat_calls_identical():
     a = run_gpu(wl, inp).O.cpu().numpy()
     b = run_gpu(wl, inp).O.cpu().numpy()
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("wl", [I.small("llm8k", Hq=4, Hkv=2, Nq=384, Nk=384),
+                                I.small("chunk32k", Hq=2, Hkv=1, Nq=128, Nk=512, q_pos0=384),
+                                I.small("swin", B=3)],
+                         ids=["llm8k", "chunk32k", "swin"])
+def test_without_k_carrier_identical(wl):
+    """qattn_fwd converting the K codes itself (no carrier from
+    qattn_quantize_qk) gives bit-identical outputs, and the carriers
+    qattn_quantize_qk writes are the K codes as fp16."""
+    import torch
+    inp = I.make_inputs(wl)
+    a = run_gpu(wl, inp, k_carrier=True)
+    b = run_gpu(wl, inp, k_carrier=False)
+    assert np.array_equal(a.O.cpu().numpy(), b.O.cpu().numpy())
+    assert np.array_equal(a.lse.cpu().numpy(), b.lse.cpu().numpy())
+    codes = a._k_codes.to(torch.float16)
+    assert torch.equal(a.k_carrier.view(torch.int16), codes.view(torch.int16))

@@ -52,11 +52,16 @@ def test_invalid_arguments_rejected_on_host(L):
     p = qb.make_params()
     fake = vp(1 << 20)  # aligned, never dereferenced: validation fails first
     # null outputs
-    assert L.qattn_fwd(None, fake, fake, fake, fake, 256, fake, None, ctypes.byref(s),
+    assert L.qattn_fwd(None, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
                        ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
-    # misaligned pointer
-    assert L.qattn_fwd(vp((1 << 20) + 4), fake, fake, fake, fake, 256, fake, None, ctypes.byref(s),
-                       ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
+    # misaligned pointers
+    assert L.qattn_fwd(vp((1 << 20) + 4), fake, fake, None, fake, fake, 256, fake, None,
+                       ctypes.byref(s), ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
+    assert L.qattn_fwd(fake, fake, fake, vp((1 << 20) + 2), fake, fake, 256, fake, None,
+                       ctypes.byref(s), ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
+    # no K carrier and no workspace
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p), fake, None, None, 0, None) == 5
     # unsupported head dim
     s96 = qb.make_shape(1, 4, 2, 256, 256, 96)
     assert L.qattn_smooth_k(fake, ctypes.byref(s96), fake, fake, 1 << 30, None) == 2
@@ -69,10 +74,14 @@ def test_invalid_arguments_rejected_on_host(L):
     # bad enum
     p_bad = qb.make_params(q_gran=7)
     assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p_bad),
-                               fake, fake, fake, fake, fake, 1 << 30, None) == 1
+                               fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    # misaligned K carrier
+    assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p),
+                               fake, fake, fake, fake, vp((1 << 20) + 8), fake, 1 << 30,
+                               None) == 1
     # workspace too small
     assert L.qattn_smooth_k(fake, ctypes.byref(s), fake, fake, 16, None) == 5
     # empty problem: ok, nothing launched
     s0 = qb.make_shape(0, 4, 2, 256, 256, 64)
-    assert L.qattn_fwd(None, None, None, None, None, 0, None, None, ctypes.byref(s0),
+    assert L.qattn_fwd(None, None, None, None, None, None, 0, None, None, ctypes.byref(s0),
                        ctypes.byref(p), None, None, None, 0, None) == 0
