@@ -223,6 +223,8 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
 //   s      the row's 128 scores: fp32 bit patterns of the integer scores, with
 //          -inf for masked keys (without BIAS); with BIAS they are
 //          overwritten by t = S c + bias log2e, and keys >= nvis are masked
+//          (their bias is never read)
+//   brow   BIAS: the row's bias for this block
 //   c      the block's score scale (> 0 without BIAS, so -inf * c = -inf)
 // Updates the running max m and sum l (l in units of 448 P), returns alpha
 // and the e4m3 codes of 448 P packed four per word (key 4q + e in byte e).
@@ -234,11 +236,11 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
                                               uint32_t (&pw)[kBN / 4]) {
   float mx;
   {
-    if (BIAS) {
+    if (BIAS) {  // only visible keys' bias is read: the row may end inside the block
 #pragma unroll
       for (int k = 0; k < kBN; ++k) {
-        float t = fmaf(__uint_as_float(s[k]), c, __fmul_rn(__ldg(brow + k), kLog2e));
-        if (k >= nvis) t = kNegInf;
+        float t = kNegInf;
+        if (k < nvis) t = fmaf(__uint_as_float(s[k]), c, __fmul_rn(__ldg(brow + k), kLog2e));
         s[k] = __float_as_uint(t);
       }
     }
@@ -520,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      // the item's scales first: their loads overlap the Q widening
+      const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
+      float sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, 0);
       {  // widen this tile's Q codes for the item's QK MMAs
         const int qs = i % C::kQS;
         ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout);
@@ -531,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarQConv + t));
       }
-      const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
       const int lim = a.causal ? min(a.Nk - 1, a.pos0 + qi) : a.Nk - 1;  // last visible key
       const int tile_lim = a.causal ? a.pos0 + q0t : a.Nk;  // blocks ending <= this need no causal mask
       const float* brow = nullptr;
@@ -539,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         brow = a.bias + static_cast<size_t>(it.h) * a.bias_head_stride +
                static_cast<size_t>(min(qi, a.Nq - 1)) * a.Nk;
       float m = kNegInf, l = 0.f;
-      float sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, 0);
       for (int j = 0; j < nbt; ++j) {
         const float sk = sk_next;
         if (j + 1 < nbt) sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j + 1);
@@ -615,6 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarPFull + t));
       }
       if (!ok) break;
+      // V scales of the first 32 channels, loaded while the last PV runs
+      const float4* sv4 = reinterpret_cast<const float4*>(a.v_scales + static_cast<size_t>(it.bkv) * D);
+      float4 svn[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) svn[q] = __ldg(sv4 + q);
       ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);  // last PV
       ++pvc;
       if (!__all_sync(0xffffffffu, ok)) {
@@ -623,16 +631,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const float* sv = a.v_scales + static_cast<size_t>(it.bkv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
+        float svc[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          svc[4 * q] = svn[q].x;
+          svc[4 * q + 1] = svn[q].y;
+          svc[4 * q + 2] = svn[q].z;
+          svc[4 * q + 3] = svn[q].w;
+        }
+        if (cc + 1 < D / 32) {  // the next chunk's scales load under this chunk's TMEM read
+#pragma unroll
+          for (int q = 0; q < 8; ++q) svn[q] = __ldg(sv4 + 8 * (cc + 1) + q);
+        }
         uint32_t o[32];
         tmem_ld32(tO + lane_base + cc * 32, o);
         tmem_wait_ld();
         if (qi < a.Nq) {
           float v[32];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(o[q]) * (__ldg(sv + cc * 32 + q) * inv_l);
+          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(o[q]) * (svc[q] * inv_l);
           if (a.out_bf16) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + cc * 32);
 #pragma unroll

@@ -286,7 +286,9 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   const int64_t pos0 = pos0_of(shape, params);
   if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
   if (shape->Nk > 0) {
-    if (!k_codes || !aligned16(k_codes) || !k_scales || !v8t || !aligned16(v8t) || !v_scales) return QATTN_ERR_INVALID_ARG;
+    if (!k_codes || !aligned16(k_codes) || !k_scales || !v8t || !aligned16(v8t) || !v_scales ||
+        !aligned16(v_scales))
+      return QATTN_ERR_INVALID_ARG;
     if (k_carrier && !aligned16(k_carrier)) return QATTN_ERR_INVALID_ARG;
     if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return QATTN_ERR_INVALID_ARG;
