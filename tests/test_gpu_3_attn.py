@@ -27,6 +27,11 @@ CASES = [
     I.small("tiny", causal=False, Nq=3, Nk=1000),                   # few rows, many keys
     I.small("chunk32k", Hq=4, Hkv=2, Nq=256, Nk=1024, q_pos0=768),
     I.small("chunk32k", Hq=2, Hkv=2, Nq=100, Nk=301, q_pos0=201, d=32),
+    # bias read from global memory: several key blocks with a ragged last one,
+    # every head dim, causal and not (the shared-memory copy covers Swin)
+    I.small("tiny", has_bias=True, Nq=300, Nk=300),
+    I.small("swin", B=2, Nq=200, Nk=200),
+    I.small("tiny", has_bias=True, d=128, Nq=130, Nk=257, causal=True),
 ]
 
 
