@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, int n_items) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
+  pdl_trigger();
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel's outputs (codes, scales, carriers) are visible
 
   if (warp == 0) {
     if (lane == 0) {
@@ -789,8 +791,8 @@ cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const long long n_items = static_cast<long long>(a.B) * a.Hq * ((n_qt + 1) / 2);
   if (n_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
-  attn_fwd_kernel<D, BIAS><<<grid, kThreads, smem, s>>>(tq, tk, tv, a, static_cast<int>(n_items));
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel<D, BIAS>, dim3(grid), dim3(kThreads), smem, s, tq, tk, tv, a,
+                    static_cast<int>(n_items));
 }
 
 template <int D>

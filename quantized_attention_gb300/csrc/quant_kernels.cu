@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const uint16_t* _
                                                               int BH, int Nk,
                                                               unsigned long long magic,
                                                               float* __restrict__ mu) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VPR = D / 8;
   constexpr int RG = 32 / VPR;
   const int bh = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -250,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __rest
                                                          unsigned long long* __restrict__ acc,
                                                          unsigned int* __restrict__ done,
                                                          float* __restrict__ mu) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VPR = D / 8;           // 16-byte vectors per row
   constexpr int RG = kThreads / VPR;   // row groups per CTA
   constexpr int kChunk = RG * kMeanRows;
@@ -300,14 +304,11 @@ __global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __rest
 // recomputed when quantizing, which halves the registers and doubles the
 // CTAs per SM.
 template <int D, int MODE>
-__device__ __forceinline__ void load_x8(const uint4& raw, const float* crow, int cv, float (&x)[8]) {
+__device__ __forceinline__ void load_x8(const uint4& raw, const float (&ch)[8], float (&x)[8]) {
   unpack_bf16x8(raw, x);
   if (MODE != 0) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float cc = __ldg(crow + cv * 8 + e);
-      x[e] = (MODE == 1) ? __fsub_rn(x[e], cc) : __fmul_rn(x[e], cc);
-    }
+    for (int e = 0; e < 8; ++e) x[e] = (MODE == 1) ? __fsub_rn(x[e], ch[e]) : __fmul_rn(x[e], ch[e]);
   }
 }
 
@@ -321,8 +322,14 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
   const int t0 = blk * 128;
   const int rows = min(128, j.N - t0);
   const uint16_t* src = j.X + (static_cast<size_t>(bh) * j.N + t0) * D;
-  const float* crow = nullptr;
-  if (MODE != 0) crow = j.chan + (static_cast<size_t>(b) * j.Hchan + h / j.group) * D;
+  // Every vector a thread handles is the same 8 channels (kThreads % VPR == 0).
+  static_assert(kThreads % VPR == 0, "fixed channel group per thread");
+  float ch[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (MODE != 0) {
+    const float* crow = j.chan + (static_cast<size_t>(b) * j.Hchan + h / j.group) * D;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ch[e] = __ldg(crow + (threadIdx.x % VPR) * 8 + e);
+  }
 
   uint4 raw[NV];
 #pragma unroll
@@ -338,7 +345,7 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
     const int v = threadIdx.x + i * kThreads;
     if (v / VPR < rows) {
       float x[8];
-      load_x8<D, MODE>(raw[i], crow, v % VPR, x);
+      load_x8<D, MODE>(raw[i], ch, x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
     }
@@ -363,7 +370,7 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
     const int r = v / VPR, cv = v % VPR;
     if (r < rows) {
       float x[8];
-      load_x8<D, MODE>(raw[i], crow, cv, x);
+      load_x8<D, MODE>(raw[i], ch, x);
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -394,6 +401,8 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
 template <int D, int M0, int M1>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsJob j0, const RowsJob j1,
                                                              int pass) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[kThreads / 32];
   const int x = blockIdx.x, blk = blockIdx.y;
   if (x < j0.BH) {
@@ -404,6 +413,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsJob j0, 
 }
 
 __global__ void fill_ones_kernel(float* p, long long n) {
+  pdl_trigger();
+  pdl_wait();
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x)
     p[i] = 1.0f;
@@ -415,6 +426,8 @@ __global__ void fill_ones_kernel(float* p, long long n) {
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
                                                          unsigned int* __restrict__ amax_bits) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int EPV = I8 ? 16 : 8;
   constexpr int VPR = D / EPV;
   constexpr int RPI = kThreads / VPR;
@@ -472,6 +485,8 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     const void* __restrict__ V, int Nk, const unsigned int* __restrict__ amax_bits,
     const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
     float* __restrict__ v_scales) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int EPV = I8 ? 16 : 8;        // channels per 16-byte vector
   constexpr int kSlices = D / (2 * EPV);  // 32-byte channel slices per key row
   constexpr int kWarps = kThreads / 32;
@@ -547,6 +562,8 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
 // int8 codes -> fp16 values (exact: |code| <= 127).
 __global__ void codes_to_f16_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst,
                                     size_t n16) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + i);
@@ -591,21 +608,22 @@ static cudaError_t smooth_k_t(const uint16_t* K, int BH, int Nk, long long* ws, 
   const unsigned long long magic = ~0ull / static_cast<unsigned long long>(Nk);
   if (Nk <= kWarpRows) {
     const int per = kThreads / 32;
-    k_mean_warp_kernel<D><<<(BH + per - 1) / per, kThreads, 0, s>>>(K, BH, Nk, magic, mu);
-    return cudaGetLastError();
+    return launch_pdl(k_mean_warp_kernel<D>, dim3((BH + per - 1) / per), dim3(kThreads), 0, s, K, BH, Nk,
+                      magic, mu);
   }
   const int nchunks = (Nk + kChunk - 1) / kChunk;
   const dim3 grid(nchunks, BH);
   if (nchunks == 1) {
-    k_mean_kernel<D, false><<<grid, kThreads, 0, s>>>(K, Nk, 1, magic, nullptr, nullptr, mu);
-    return cudaGetLastError();
+    return launch_pdl(k_mean_kernel<D, false>, grid, dim3(kThreads), 0, s, K, Nk, 1, magic,
+                      static_cast<unsigned long long*>(nullptr),
+                      static_cast<unsigned int*>(nullptr), mu);
   }
   unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws);
   unsigned int* done = reinterpret_cast<unsigned int*>(acc + static_cast<size_t>(BH) * D);
   const cudaError_t e = cudaMemsetAsync(ws, 0, smooth_k_ws_bytes(BH, Nk, D), s);
   if (e != cudaSuccess) return e;
-  k_mean_kernel<D, true><<<grid, kThreads, 0, s>>>(K, Nk, nchunks, magic, acc, done, mu);
-  return cudaGetLastError();
+  return launch_pdl(k_mean_kernel<D, true>, grid, dim3(kThreads), 0, s, K, Nk, nchunks, magic, acc,
+                    done, mu);
 }
 
 cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
@@ -622,11 +640,12 @@ size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran) {
 }
 
 template <int D>
-static void quant_rows_dispatch(dim3 grid, cudaStream_t s, const RowsJob& j0, int m0,
-                                const RowsJob& j1, int m1, int pass) {
-  if (m0 == 0 && m1 == 1) quant_rows_kernel<D, 0, 1><<<grid, kThreads, 0, s>>>(j0, j1, pass);
-  else if (m0 == 0) quant_rows_kernel<D, 0, 0><<<grid, kThreads, 0, s>>>(j0, j1, pass);
-  else quant_rows_kernel<D, 2, 0><<<grid, kThreads, 0, s>>>(j0, j1, pass);
+static cudaError_t quant_rows_dispatch(dim3 grid, cudaStream_t s, const RowsJob& j0, int m0,
+                                       const RowsJob& j1, int m1, int pass) {
+  if (m0 == 0 && m1 == 1)
+    return launch_pdl(quant_rows_kernel<D, 0, 1>, grid, dim3(kThreads), 0, s, j0, j1, pass);
+  if (m0 == 0) return launch_pdl(quant_rows_kernel<D, 0, 0>, grid, dim3(kThreads), 0, s, j0, j1, pass);
+  return launch_pdl(quant_rows_kernel<D, 2, 0>, grid, dim3(kThreads), 0, s, j0, j1, pass);
 }
 
 cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, int m1, int d,
@@ -638,27 +657,33 @@ cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, i
   const dim3 grid(nx, nblk);
   const bool two_pass = (j0.BH > 0 && j0.gran != 2) || (j1.BH > 0 && j1.gran != 2);
   for (int pass = two_pass ? 0 : 1; pass < 2; ++pass) {
+    cudaError_t e;
     switch (d) {
-      case 32: quant_rows_dispatch<32>(grid, s, j0, m0, j1, m1, pass); break;
-      case 64: quant_rows_dispatch<64>(grid, s, j0, m0, j1, m1, pass); break;
-      default: quant_rows_dispatch<128>(grid, s, j0, m0, j1, m1, pass);
+      case 32: e = quant_rows_dispatch<32>(grid, s, j0, m0, j1, m1, pass); break;
+      case 64: e = quant_rows_dispatch<64>(grid, s, j0, m0, j1, m1, pass); break;
+      default: e = quant_rows_dispatch<128>(grid, s, j0, m0, j1, m1, pass);
     }
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_fill_ones(float* p, long long n, cudaStream_t s) {
-  if (n > 0) fill_ones_kernel<<<grid_for(static_cast<size_t>(n), 256), 256, 0, s>>>(p, n);
-  return cudaGetLastError();
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(fill_ones_kernel, dim3(grid_for(static_cast<size_t>(n), 256)), dim3(256), 0, s,
+                    p, n);
 }
 
 template <int D, bool I8>
-static void quantize_v_impl(const void* V, const float* chan, int BH, int Nk, uint8_t* v8t,
-                            long long ldv, float* v_scales, unsigned int* ws, cudaStream_t s) {
+static cudaError_t quantize_v_impl(const void* V, const float* chan, int BH, int Nk,
+                                   uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws,
+                                   cudaStream_t s) {
   const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  v_amax_kernel<D, I8><<<dim3(nchunks, BH), kThreads, 0, s>>>(V, Nk, ws);
+  cudaError_t e = launch_pdl(v_amax_kernel<D, I8>, dim3(nchunks, BH), dim3(kThreads), 0, s, V, Nk, ws);
+  if (e != cudaSuccess) return e;
   const int nt = static_cast<int>((ldv + 127) / 128);
-  v_convert_kernel<D, I8><<<dim3(nt, BH), kThreads, 0, s>>>(V, Nk, ws, chan, v8t, ldv, v_scales);
+  return launch_pdl(v_convert_kernel<D, I8>, dim3(nt, BH), dim3(kThreads), 0, s, V, Nk,
+                    static_cast<const unsigned int*>(ws), chan, v8t, ldv, v_scales);
 }
 
 cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,
@@ -667,24 +692,21 @@ cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int B
   cudaError_t e = cudaMemsetAsync(ws_amax, 0, static_cast<size_t>(BH) * d * sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
   if (Nk == 0) return cudaMemsetAsync(v_scales, 0, static_cast<size_t>(BH) * d * sizeof(float), s);
-#define QATTN_QV(DD)                                                             \
-  if (is_i8)                                                                     \
-    quantize_v_impl<DD, true>(V, chan, BH, Nk, v8t, ldv, v_scales, ws_amax, s);  \
-  else                                                                           \
-    quantize_v_impl<DD, false>(V, chan, BH, Nk, v8t, ldv, v_scales, ws_amax, s);
+#define QATTN_QV(DD)                                                                  \
+  return is_i8 ? quantize_v_impl<DD, true>(V, chan, BH, Nk, v8t, ldv, v_scales, ws_amax, s) \
+               : quantize_v_impl<DD, false>(V, chan, BH, Nk, v8t, ldv, v_scales, ws_amax, s);
   switch (d) {
-    case 32: QATTN_QV(32) break;
-    case 64: QATTN_QV(64) break;
+    case 32: QATTN_QV(32)
+    case 64: QATTN_QV(64)
     default: QATTN_QV(128)
   }
 #undef QATTN_QV
-  return cudaGetLastError();
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t s) {
   const size_t n16 = n / 16;
-  if (n16 > 0) codes_to_f16_kernel<<<grid_for(n16, 256), 256, 0, s>>>(src, dst, n16);
-  return cudaGetLastError();
+  if (n16 == 0) return cudaSuccess;
+  return launch_pdl(codes_to_f16_kernel, dim3(grid_for(n16, 256)), dim3(256), 0, s, src, dst, n16);
 }
 
 }  // namespace qattn

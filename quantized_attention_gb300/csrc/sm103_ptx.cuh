@@ -272,6 +272,18 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the
+// stream start launching (its CTAs are placed once every CTA of this grid has
+// triggered or exited); pdl_wait blocks until the previous grid of the stream
+// has completed and its writes are visible.  Every kernel here triggers at
+// entry and waits before it reads any input, so the overlap is limited to
+// launch latency and set-up.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- registers
 // Per-thread register budget of the calling warpgroup (all four warps must
 // execute the same instruction).  inc waits until the CTA's pool holds enough
