@@ -80,6 +80,14 @@ typedef struct {
   int64_t B, Hq, Hkv, Nq, Nk, d;
 } qattn_shape;
 
+/* How P is quantized for the PV product (qattn_params.pv_mode). */
+typedef enum {
+  QATTN_PV_E4M3 = 0,  /* the recipe: e4m3(448 P), static scale 448              */
+  QATTN_PV_INT8 = 1   /* ablation: int8 rint(127 P), static scale 127 ("int8 Flash
+                         Attention on RDNA4", "Then the easy matmul turns out to be
+                         the hard one": the int8 PV that flushes P < 1/254 to 0) */
+} qattn_pv_mode;
+
 typedef struct {
   int32_t causal;           /* 1: key k is visible to query i iff k <= q_pos0 + i   */
   int32_t q_gran;           /* qattn_gran of the Q codes                           */
@@ -87,7 +95,7 @@ typedef struct {
   int32_t out_dtype;        /* QATTN_F32 or QATTN_BF16                             */
   int64_t q_pos0;           /* key position of query row 0, or QATTN_POS0_BOTTOM_RIGHT */
   float sm_scale;           /* softmax scale; 0 -> fp32(1/sqrt(d))                 */
-  int32_t reserved;         /* must be 0                                           */
+  int32_t pv_mode;          /* qattn_pv_mode; 0 for the recipe                     */
   int64_t bias_head_stride; /* elements between heads' bias matrices; 0 = shared   */
 } qattn_params;
 

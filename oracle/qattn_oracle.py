@@ -294,8 +294,9 @@ def online_softmax_pv(S, c, V8, s_v, *, visible, bias2=None, p_quant="e4m3",
     Finally O * s_v / l (0 where l == 0).
 
     With want_bound, also returns a per-element bound on how far the output
-    can move if any e4m3 code of P * 448 whose value lies within the
-    exp2-accuracy window of a rounding midpoint is rounded the other way.
+    can move if any code of P (e4m3 of P * 448, or the int8 rint(P * 127))
+    whose value lies within the exp2-accuracy window of a rounding midpoint
+    is rounded the other way.
     """
     S = np.asarray(S)
     R, Nk = S.shape
@@ -334,14 +335,20 @@ def online_softmax_pv(S, c, V8, s_v, *, visible, bias2=None, p_quant="e4m3",
             Pq = P.astype(F64)
         O = alpha.astype(F64)[:, None] * O + Pq @ np.asarray(V8[k0:k1], dtype=F64)
         if want_bound:
-            assert p_quant == "e4m3"
-            dist, step = e4m3_midpoint_distance(P448)
+            assert p_quant in ("e4m3", "int8")
             span = np.abs(t.astype(F64)) + np.abs(m_new.astype(F64))[:, None]
             span = np.where(np.isfinite(span), span, 0.0)
-            window = 2.0 ** -20 * (4.0 + span) * P448.astype(F64)
-            amb = (dist <= window) & (P448 > 0)
+            if p_quant == "e4m3":
+                dist, step = e4m3_midpoint_distance(P448)
+                Ps, scale = P448.astype(F64), P_SCALE
+            else:  # int8: midpoints at k + 1/2, a flip moves the code by 1
+                Ps = (P * ftype(QMAX)).astype(F64)
+                dist = np.abs(Ps - (np.floor(Ps) + 0.5))
+                step, scale = np.ones_like(Ps), float(QMAX)
+            window = 2.0 ** -20 * (4.0 + span) * Ps
+            amb = (dist <= window) & (Ps > 0)
             n_amb += int(amb.sum())
-            Bacc = alpha.astype(F64)[:, None] * Bacc + (amb * step / P_SCALE) @ absV[k0:k1]
+            Bacc = alpha.astype(F64)[:, None] * Bacc + (amb * step / scale) @ absV[k0:k1]
         m = m_new
     with np.errstate(divide="ignore", invalid="ignore"):
         inv_l = np.where(l > 0, 1.0 / l, 0.0)
@@ -495,14 +502,15 @@ def prepare(inp) -> dict:
             "v8": v8, "s_v": s_v}
 
 
-def run_workload(inp, prep=None, *, heads=None, rows=None, want_bound=False):
-    """Recipe output for chosen heads/rows of a workload (parity target)."""
+def run_workload(inp, prep=None, *, heads=None, rows=None, want_bound=False, p_quant="e4m3"):
+    """Recipe output for chosen heads/rows of a workload (parity target).
+    p_quant="int8" gives the static-127 int8 PV ablation instead."""
     wl = inp.wl
     prep = prepare(inp) if prep is None else prep
     return attn_fwd(prep["q_codes"], prep["q_scales"], prep["k_codes"], prep["k_scales"],
                     prep["v8"], prep["s_v"], q_gran=wl.q_gran, k_gran=wl.k_gran,
                     causal=wl.causal, q_pos0=wl.q_pos0, bias=inp.bias, heads=heads,
-                    rows=rows, want_bound=want_bound)
+                    rows=rows, want_bound=want_bound, p_quant=p_quant)
 
 
 def real_kv(inp):
@@ -514,3 +522,66 @@ def real_kv(inp):
         V = inp.V_codes.astype(F64) * inp.V_scale[:, :, None, :].astype(F64)
         return K, V
     return inp.K, inp.V
+
+
+# ---------------------------------------------------------------------------
+# Probability-mass diagnostic (ZINC-ATTN, "Then the easy matmul turns out to be
+# the hard one" and its figure): how much of an attention row's probability
+# mass lies below what a static-127 int8 grid can hold.  Round to nearest sends
+# every probability below half a step, 0.5 / 127 ~ 0.0039, to zero.
+# ---------------------------------------------------------------------------
+
+INT8_ZERO_THRESHOLD = 0.5 / QMAX
+
+# The figure's magnitude decades: < 1e-4, [1e-4, 1e-3), [1e-3, 1e-2),
+# [1e-2, 1e-1), >= 1e-1.
+MASS_DECADE_EDGES = (1e-4, 1e-3, 1e-2, 1e-1)
+
+
+def attn_probs_fp64(Q, K, *, causal, q_pos0=None, sm_scale=None, bias=None, heads=None,
+                    rows=None):
+    """softmax(Q K^T * sm_scale + bias) of the chosen rows, dense, float64.
+    Returns [len(heads), len(rows), Nk] (masked keys have probability 0)."""
+    Q = np.asarray(Q, dtype=F64)
+    K = np.asarray(K, dtype=F64)
+    B, Hq, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    g = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = float(default_sm_scale(d))
+    q0 = (Nk - Nq) if q_pos0 is None else q_pos0
+    heads = [(b, h) for b in range(B) for h in range(Hq)] if heads is None else heads
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    vis = visible_mask(rows, Nk, causal, q0)
+    out = np.zeros((len(heads), len(rows), Nk), dtype=F64)
+    for i, (b, h) in enumerate(heads):
+        s = Q[b, h][rows] @ K[b, h // g].T * float(sm_scale)
+        if bias is not None:
+            s = s + np.asarray(bias, F64)[rows]
+        s = np.where(vis, s, -np.inf)
+        mx = s.max(axis=1, keepdims=True)
+        e = np.where(vis, np.exp(s - np.where(np.isfinite(mx), mx, 0.0)), 0.0)
+        tot = e.sum(axis=1, keepdims=True)
+        out[i] = np.where(tot > 0, e / np.where(tot > 0, tot, 1.0), 0.0)
+    return out
+
+
+def mass_profile(probs, edges=MASS_DECADE_EDGES, threshold=INT8_ZERO_THRESHOLD):
+    """Per row: the fraction of the row's probability mass in each magnitude
+    bin (len(edges) + 1 bins) and below `threshold`.  probs [..., N] rows of
+    probabilities (each row sums to 1, or to 0 for a fully masked row)."""
+    p = np.asarray(probs, dtype=F64)
+    tot = p.sum(axis=-1)
+    safe = np.where(tot > 0, tot, 1.0)
+    bounds = (0.0,) + tuple(edges) + (np.inf,)
+    bins = np.stack([np.where((p >= lo) & (p < hi), p, 0.0).sum(axis=-1) / safe
+                     for lo, hi in zip(bounds[:-1], bounds[1:])], axis=-1)
+    # zeroed by the static-127 grid: rint(127 p) == 0, i.e. 127 p <= 1/2 (the
+    # tie rounds to the even code 0)
+    below = np.where(p * QMAX <= threshold * QMAX, p, 0.0).sum(axis=-1) / safe
+    # the same threshold applied to p / max p: the flash-attention P = exp(s - m)
+    # <= 1 is quantized relative to the row max, not after normalization
+    pmax = p.max(axis=-1, keepdims=True)
+    rel = p / np.where(pmax > 0, pmax, 1.0)
+    below_rel = np.where(rel * QMAX <= threshold * QMAX, p, 0.0).sum(axis=-1) / safe
+    return {"bins": bins, "below": below, "below_rel_max": below_rel}

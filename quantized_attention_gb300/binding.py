@@ -19,6 +19,7 @@ OK = 0
 GRAN_TENSOR, GRAN_HEAD, GRAN_BLOCK = 0, 1, 2
 DT_BF16, DT_F32, DT_I8, DT_E4M3 = 0, 1, 2, 3
 POS0_BOTTOM_RIGHT = -(2 ** 63)
+PV_E4M3, PV_INT8 = 0, 1
 
 EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
@@ -42,7 +43,7 @@ class Params(ctypes.Structure):
     _fields_ = [("causal", ctypes.c_int32), ("q_gran", ctypes.c_int32),
                 ("k_gran", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("q_pos0", ctypes.c_int64), ("sm_scale", ctypes.c_float),
-                ("reserved", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64)]
+                ("pv_mode", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -115,10 +116,10 @@ def make_shape(B, Hq, Hkv, Nq, Nk, d) -> Shape:
 
 
 def make_params(causal=False, q_gran=GRAN_BLOCK, k_gran=GRAN_BLOCK, out_dtype=DT_F32,
-                q_pos0=None, sm_scale=0.0, bias_head_stride=0) -> Params:
+                q_pos0=None, sm_scale=0.0, bias_head_stride=0, pv_mode=PV_E4M3) -> Params:
     return Params(int(bool(causal)), q_gran, k_gran, out_dtype,
-                  POS0_BOTTOM_RIGHT if q_pos0 is None else int(q_pos0), float(sm_scale), 0,
-                  int(bias_head_stride))
+                  POS0_BOTTOM_RIGHT if q_pos0 is None else int(q_pos0), float(sm_scale),
+                  int(pv_mode), int(bias_head_stride))
 
 
 def version() -> int:

@@ -40,6 +40,7 @@ constexpr int kBN = 128;  // keys per block
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.44269502162933349609375f;  // fp32(log2 e)
 constexpr float kLog2_448 = 8.8073549220576041f;      // log2(448)
+constexpr float kLog2_127 = 6.9886846867721655f;      // log2(127)
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -48,7 +49,9 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // layout (128-byte rows and the 128B swizzle; 64-byte rows and the 64B
 // swizzle for D = 32).  V is e4m3 transposed, [D rows][128 keys]; P is e4m3
 // [128 rows][128 keys]; both 128-byte rows with the 128B swizzle.
-template <int D>
+// PQ: the int8 P ablation, whose P occupies two e4m3 planes per tile (see
+// softmax_step); it buys that room with a 2-stage K ring for D >= 64.
+template <int D, bool PQ = false>
 struct Cfg {
   static constexpr int kColBlock = (D >= 64) ? 64 : D;  // fp16 elements per row of a block
   static constexpr int kRowBytes = kColBlock * 2;
@@ -57,12 +60,13 @@ struct Cfg {
   static constexpr uint32_t kSwz = (kRowBytes == 128) ? kSwizzle128B : kSwizzle64B;
   static constexpr uint32_t kSBO = 8 * kRowBytes;  // bytes between 8-row groups
   static constexpr int kQS = (D == 128) ? 1 : 2;   // Q stages (each holds both tiles)
-  static constexpr int kNK = (D == 128) ? 3 : 4;   // K ring stages
+  static constexpr int kNK = (PQ && D >= 64) ? 2 : (D == 128) ? 3 : 4;  // K ring stages
   static constexpr int kNV = (D == 128) ? 2 : 4;   // V ring stages
   static constexpr int kQTileBytes = kBM * D * 2;
   static constexpr int kKBytes = kBN * D * 2;
   static constexpr int kVBytes = D * kBN;
-  static constexpr int kPBytes = kBM * kBN;
+  static constexpr int kPBytes = kBM * kBN;  // one e4m3 plane of P
+  static constexpr int kPPlanes = PQ ? 2 : 1;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQS * 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + kNK * kKBytes;
@@ -71,7 +75,7 @@ struct Cfg {
   // (see convert_q_tile), in a region of their own for smaller D.
   static constexpr bool kQ8InPlace = (D == 128);
   static constexpr int kQ8Bytes = kBM * D;
-  static constexpr int kOffQ8 = kOffP + 2 * kPBytes;
+  static constexpr int kOffQ8 = kOffP + 2 * kPPlanes * kPBytes;
   static constexpr int kOffBar = kOffQ8 + (kQ8InPlace ? 0 : kQS * 2 * kQ8Bytes);
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
   static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kVBytes % 1024 == 0,
@@ -105,14 +109,19 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t sq, uint32_t 
   }
 }
 
-// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3.
-template <int D>
+// O (+)= P8 . V8 for one key block: 4 MMAs of K = 32 e4m3 per P plane (PQ:
+// the high plane, then the low plane at sp + one plane, same V).
+template <int D, bool PQ>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t sp, uint32_t sv, bool acc) {
   constexpr uint32_t idesc = make_idesc(kBM, D, 0, 0);  // E4M3 x E4M3 -> F32
 #pragma unroll
-  for (int s = 0; s < kBN / 32; ++s) {
-    mma_f8(tmem_o, smem_desc(sp + s * 32, 1024, kSwizzle128B),
-           smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc, (acc || s > 0) ? 1u : 0u);
+  for (int pl = 0; pl < (PQ ? 2 : 1); ++pl) {
+#pragma unroll
+    for (int s = 0; s < kBN / 32; ++s) {
+      mma_f8(tmem_o, smem_desc(sp + pl * kBM * kBN + s * 32, 1024, kSwizzle128B),
+             smem_desc(sv + s * 32, 1024, kSwizzle128B), idesc,
+             (acc || pl > 0 || s > 0) ? 1u : 0u);
+    }
   }
 }
 
@@ -230,10 +239,10 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
 // and the e4m3 codes of 448 P packed four per word (key 4q + e in byte e).
 // One body serves masked and unmasked blocks: a second, masked copy of this
 // fully unrolled code would double the loop's instruction footprint.
-template <bool BIAS>
+template <bool BIAS, bool PQ>
 __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int nvis,
                                               const float* brow, float& m, float& l,
-                                              uint32_t (&pw)[kBN / 4]) {
+                                              uint32_t (&pw)[kBN / 4], uint32_t (&pw2)[kBN / 4]) {
   float mx;
   {
     if (BIAS) {  // only visible keys' bias is read: the row may end inside the block
@@ -260,12 +269,12 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
   const float m_new = fmaxf(m, m_blk);
   const bool dead = (m_new == kNegInf);
   const float alpha = dead ? 1.f : ex2_approx(m - m_new);
-  const float kneg = dead ? 0.f : (kLog2_448 - m_new);
+  const float kneg = dead ? 0.f : ((PQ ? kLog2_127 : kLog2_448) - m_new);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                    make_float2(0.f, 0.f)};
 #pragma unroll
   for (int k = 0; k < kBN; k += 4) {
-    uint32_t half[2];
+    uint32_t half[2], half2[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int kk = k + 2 * e;
@@ -279,9 +288,16 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
       }
       const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
       acc[(k / 2 + e) & 3] = fadd2(acc[(k / 2 + e) & 3], p);
-      half[e] = cvt_e4m3x2(p.x, p.y);
+      if (PQ) {  // code = rint(127 P) = 16 hi + lo; 16 hi and lo are exact e4m3 values
+        const int ca = min(__float2int_rn(p.x), 127), cb = min(__float2int_rn(p.y), 127);
+        half[e] = cvt_e4m3x2(static_cast<float>(ca & 0x70), static_cast<float>(cb & 0x70));
+        half2[e] = cvt_e4m3x2(static_cast<float>(ca & 15), static_cast<float>(cb & 15));
+      } else {
+        half[e] = cvt_e4m3x2(p.x, p.y);
+      }
     }
     pw[k / 4] = half[0] | (half[1] << 16);
+    if (PQ) pw2[k / 4] = half2[0] | (half2[1] << 16);
   }
   const float2 a01 = fadd2(acc[0], acc[1]);
   const float2 a23 = fadd2(acc[2], acc[3]);
@@ -291,11 +307,11 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
   return alpha;
 }
 
-template <int D, bool BIAS>
+template <int D, bool BIAS, bool PQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, int n_items) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PQ>;
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
   const uint32_t raw = smem_u32(smem_raw);
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sQ = [&](int qs, int t) { return base + C::kOffQ + (qs * 2 + t) * C::kQTileBytes; };
   auto sK = [&](int st) { return base + C::kOffK + st * C::kKBytes; };
   auto sV = [&](int st) { return base + C::kOffV + st * C::kVBytes; };
-  auto sP = [&](int t) { return base + C::kOffP + t * C::kPBytes; };
+  auto sP = [&](int t) { return base + C::kOffP + t * C::kPPlanes * C::kPBytes; };
   auto sQ8 = [&](int qs, int t) {
     return C::kQ8InPlace ? sQ(qs, t) + C::kQTileBytes / 2
                          : base + C::kOffQ8 + (qs * 2 + t) * C::kQ8Bytes;
@@ -472,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait(bar(kBarPFull + t), npv & 1, abort_flag, a.err, kErrTimeout)))
                 break;
               tc_fence_after();
-              issue_pv<D>(tmem + 256 + 128 * t, sP(t), sV(st), b > 1);
+              issue_pv<D, PQ>(tmem + 256 + 128 * t, sP(t), sV(st), b > 1);
               mma_commit(bar(kBarPVDone + t));
               ++npv;
             }
@@ -577,9 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (k >= nvis) s[k] = 0xFF800000u;
           }
         }
-        uint32_t pw[kBN / 4];
+        uint32_t pw[kBN / 4], pw2[kBN / 4];
         const float* bk = BIAS ? brow + kbase : nullptr;
-        const float alpha = softmax_step<BIAS>(s, c, nvis, bk, m, l, pw);
+        const float alpha = softmax_step<BIAS, PQ>(s, c, nvis, bk, m, l, pw, pw2);
         if (j > 0) {  // PV(t, j-1) must be done with P_t and O_t
           ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);
           ++pvc;
@@ -595,6 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pw[4 * ch]),
                        "r"(pw[4 * ch + 1]), "r"(pw[4 * ch + 2]), "r"(pw[4 * ch + 3])
                        : "memory");
+          if (PQ)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr + C::kPBytes),
+                         "r"(pw2[4 * ch]), "r"(pw2[4 * ch + 1]), "r"(pw2[4 * ch + 2]),
+                         "r"(pw2[4 * ch + 3])
+                         : "memory");
         }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // Rescale the O_t row: one TMEM round trip for all D columns.
@@ -673,7 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (a.lse && qi < a.Nq) a.lse[row] = (l > 0.f) ? (m + __log2f(l) - kLog2_448) * kLn2 : kNegInf;
+      if (a.lse && qi < a.Nq)
+        a.lse[row] = (l > 0.f) ? (m + __log2f(l) - (PQ ? kLog2_127 : kLog2_448)) * kLn2 : kNegInf;
     }
     if (!ok) *abort_flag = 1;
   }
@@ -780,19 +802,19 @@ int num_sms() {
   return n;
 }
 
-template <int D, bool BIAS>
+template <int D, bool BIAS, bool PQ = false>
 cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnArgs& a, cudaStream_t s) {
-  const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BIAS>,
+  const int smem = Cfg<D, PQ>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BIAS, PQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_qt = (a.Nq + kBM - 1) / kBM;
   const long long n_items = static_cast<long long>(a.B) * a.Hq * ((n_qt + 1) / 2);
   if (n_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
-  return launch_pdl(attn_fwd_kernel<D, BIAS>, dim3(grid), dim3(kThreads), smem, s, tq, tk, tv, a,
-                    static_cast<int>(n_items));
+  return launch_pdl(attn_fwd_kernel<D, BIAS, PQ>, dim3(grid), dim3(kThreads), smem, s, tq, tk, tv,
+                    a, static_cast<int>(n_items));
 }
 
 template <int D>
@@ -811,6 +833,13 @@ cudaError_t launch_dbg_t(const CUtensorMap& tq, const CUtensorMap& tk, int B, in
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& a, cudaStream_t s) {
+  if (a.pv_int8) {  // the int8 P ablation (no bias)
+    switch (a.d) {
+      case 32: return launch_attn_t<32, false, true>(tq, tk, tv, a, s);
+      case 64: return launch_attn_t<64, false, true>(tq, tk, tv, a, s);
+      default: return launch_attn_t<128, false, true>(tq, tk, tv, a, s);
+    }
+  }
   const bool bias = a.bias != nullptr;
   switch (a.d) {
     case 32: return bias ? launch_attn_t<32, true>(tq, tk, tv, a, s) : launch_attn_t<32, false>(tq, tk, tv, a, s);

@@ -79,7 +79,8 @@ qattn_status check_params(const qattn_params* p) {
   if (p->q_gran < 0 || p->q_gran > 2 || p->k_gran < 0 || p->k_gran > 2) return QATTN_ERR_INVALID_ARG;
   if (p->out_dtype != QATTN_F32 && p->out_dtype != QATTN_BF16) return QATTN_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return QATTN_ERR_INVALID_ARG;
-  if (p->reserved != 0 || p->bias_head_stride < 0) return QATTN_ERR_INVALID_ARG;
+  if (p->pv_mode != QATTN_PV_E4M3 && p->pv_mode != QATTN_PV_INT8) return QATTN_ERR_INVALID_ARG;
+  if (p->bias_head_stride < 0) return QATTN_ERR_INVALID_ARG;
   if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return QATTN_ERR_INVALID_ARG;
   return QATTN_OK;
 }
@@ -283,6 +284,7 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   if (empty_problem(shape)) return QATTN_OK;
   if (!q_codes || !aligned16(q_codes) || !q_scales || !O || !aligned16(O)) return QATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return QATTN_ERR_INVALID_ARG;
+  if (params->pv_mode == QATTN_PV_INT8 && bias) return QATTN_ERR_UNSUPPORTED;  // ablation: no bias
   const int64_t pos0 = pos0_of(shape, params);
   if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
   if (shape->Nk > 0) {
@@ -318,6 +320,7 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   a.v_scales = v_scales;
   a.bias = bias;
   a.bias_head_stride = params->bias_head_stride;
+  a.pv_int8 = params->pv_mode == QATTN_PV_INT8 ? 1 : 0;
   a.out = O;
   a.out_bf16 = params->out_dtype == QATTN_BF16;
   a.lse = lse;

@@ -41,6 +41,7 @@ struct AttnArgs {
   const float* v_scales;
   const float* bias;
   long long bias_head_stride;
+  int pv_int8;  // P quantized as int8 rint(127 P) (ablation) instead of e4m3(448 P)
   void* out;
   int out_bf16;
   float* lse;

@@ -18,8 +18,9 @@ def ensure_library():
     qb.lib()
 
 
-def run_gpu(wl, inp, out_dtype=qb.DT_F32, want_lse=True, k_carrier=True):
-    P = problem_for(wl, out_dtype=out_dtype, want_lse=want_lse, k_carrier=k_carrier)
+def run_gpu(wl, inp, out_dtype=qb.DT_F32, want_lse=True, k_carrier=True, pv_mode=qb.PV_E4M3):
+    P = problem_for(wl, out_dtype=out_dtype, want_lse=want_lse, k_carrier=k_carrier,
+                    pv_mode=pv_mode)
     dev = device_inputs(inp)
     bias = dev.pop("bias", None)
     P.run(**dev, bias=bias)

@@ -104,3 +104,32 @@ def test_without_k_carrier_identical(wl):
     assert np.array_equal(a.lse.cpu().numpy(), b.lse.cpu().numpy())
     codes = a._k_codes.to(torch.float16)
     assert torch.equal(a.k_carrier.view(torch.int16), codes.view(torch.int16))
+
+
+INT8_PV_CASES = [
+    I.small("llm8k", Hq=4, Hkv=2, Nq=640, Nk=640),
+    I.small("llm8k", Hq=2, Hkv=1, Nq=333, Nk=333, d=64),
+    I.small("llm8k", Hq=2, Hkv=2, Nq=300, Nk=300, d=32),
+    I.small("vit", B=2),
+    I.small("chunk32k", Hq=4, Hkv=2, Nq=256, Nk=1024, q_pos0=768),
+]
+
+
+@pytest.mark.parametrize("wl", INT8_PV_CASES, ids=[_ids(w) for w in INT8_PV_CASES])
+def test_int8_pv_ablation_matches_oracle(wl):
+    """pv_mode = QATTN_PV_INT8: P quantized as rint(127 P) (the int8 PV the ZINC
+    post rejects), against the oracle's int8 mode, with the same 2e-3 gate and
+    its flip allowance for codes next to a rounding midpoint."""
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P = run_gpu(wl, inp, pv_mode=qb.PV_INT8)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)][:8]
+    rows = np.arange(wl.Nq)
+    ref = O.run_workload(inp, prep, heads=heads, rows=rows, want_bound=True, p_quant="int8")
+    check_output(gpu_out_rows(P, heads, rows), ref["O"], ref["bound"], _ids(wl))
+    lse = gpu_lse_rows(P, heads, rows)
+    fin = np.isfinite(ref["lse"])
+    np.testing.assert_allclose(lse[fin], ref["lse"][fin], rtol=0, atol=1e-4)
+    # and it is not the e4m3 recipe
+    e4 = O.run_workload(inp, prep, heads=heads, rows=rows)["O"]
+    assert np.abs(gpu_out_rows(P, heads, rows) - e4).max() > 1e-3

@@ -71,6 +71,14 @@ def test_invalid_arguments_rejected_on_host(L):
     # ldv too small
     assert L.qattn_quantize_v(fake, 0, None, ctypes.byref(s), fake, 128, fake, fake, 1 << 30,
                               None) == 1
+    # int8 P ablation with a bias: unsupported
+    p_i8 = qb.make_params(pv_mode=qb.PV_INT8)
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, fake, ctypes.byref(s),
+                       ctypes.byref(p_i8), fake, None, fake, 1 << 30, None) == 2
+    # bad P mode
+    p_pv = qb.make_params(pv_mode=3)
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p_pv), fake, None, fake, 1 << 30, None) == 1
     # bad enum
     p_bad = qb.make_params(q_gran=7)
     assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p_bad),
