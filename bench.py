@@ -264,13 +264,23 @@ def gpu_arm(args):
     inp = I.make_inputs(wl)
     dev = device_inputs(inp)
     bias = dev.pop("bias", None)
-    P = problem_for(wl, out_dtype=qb.DT_BF16)
+    decode = wl.name.startswith("decode")
+    P = problem_for(wl, out_dtype=qb.DT_BF16, k_carrier=not decode)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
 
     ops = 4 * wl.d * wl.unmasked_pairs()
+    if decode:  # the int8 cache is device state; a step quantizes the new token and decodes
+        P.set_cache(dev["K_codes"], dev["V_codes"], dev["V_scale"])
+        cache_bytes = 2 * wl.B * wl.Hkv * wl.Nk * wl.d  # K and V codes, read once
 
     def step():
+        if decode:
+            P.quantize_q(dev["Q"], dev["K_scale"], stream)
+            ev_a.record(stream)
+            P.decode(stream)
+            ev_b.record(stream)
+            return
         P.quantize(**dev, stream=stream)
         ev_a.record(stream)
         P.attend(bias, stream)
@@ -312,7 +322,7 @@ def gpu_arm(args):
     value = world * ops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, host buffers, copies timed
-    host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+    host = {k: v.cpu().pin_memory() for k, v in dev.items() if not decode or k == "Q"}
     out_host = torch.empty(P.O.shape, dtype=P.O.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -320,7 +330,11 @@ def gpu_arm(args):
     def e2e_step():
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
-        P.run(**dev, bias=bias, stream=stream)
+        if decode:
+            P.quantize_q(dev["Q"], dev["K_scale"], stream)
+            P.decode(stream)
+        else:
+            P.run(**dev, bias=bias, stream=stream)
         out_host.copy_(P.O, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -356,6 +370,13 @@ def gpu_arm(args):
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
                 "traffic": _attn_traffic(args.workload),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
+    if decode:  # memory-bound: the cache's bytes over the decode call's time
+        gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "qattn_decode (3 launches: scores, PV, combine)",
+                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"],
+                    "peak_basis": f"{peaks['source']} HBM copy rate",
+                    "algorithmic_bytes": cache_bytes, "traffic": None}
     cpu = None
     if not args.no_cpu_baseline:
         c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
@@ -370,7 +391,7 @@ def gpu_arm(args):
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": P.kernel_launches() * args.steps,
+            "gpu_launches": (P.decode_launches() if decode else P.kernel_launches()) * args.steps,
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
     if world > 1:

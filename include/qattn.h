@@ -226,6 +226,36 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
                        const qattn_params* params, void* O, float* lse, void* workspace,
                        size_t workspace_bytes, qattn_stream_t stream);
 
+/* Decode on an int8 KV cache ("int8 Flash Attention on RDNA4", "What actually
+ * changed for decode": at batch one both products are matrix-vector products
+ * bound by the bytes of the cache, and an int8 cache halves them).  A few query
+ * tokens per (batch, head) against Nk cached keys, read as stored: the K codes
+ * for the scores and the V codes row-major, each V code rounded to e4m3 on the
+ * fly as qattn_quantize_v rounds it.  The result is qattn_fwd's recipe on the
+ * same codes (key blocks of 128 in ascending order, P relative to the running
+ * max at each block), computed by a split over key blocks: every block's
+ * scores and row maxima first, then each block's running max as a prefix
+ * maximum, the chunks' shares of O and l, and their combination.
+ *   q_codes/q_scales  as written by qattn_quantize_qk with k_dtype QATTN_I8
+ *   k_codes      int8 [B][Hkv][Nk][d]: the cache's K codes (of the mean-
+ *                subtracted K; the mean lives in the cache header, "K's
+ *                outliers, and the subtraction softmax does not notice")
+ *   k_scales     as written by qattn_quantize_qk (all 1 for I8 K)
+ *   v_codes      int8 [B][Hkv][Nk][d]: the cache's V codes
+ *   v_chan_scale fp32 [B][Hkv][d]: scale of each V channel's codes
+ *   v_code_amax  fp32 [B][Hkv][d]: max |code| of each V channel over the
+ *                cache (the cache header keeps it as tokens arrive)
+ *   O, lse       as for qattn_fwd; params as for qattn_fwd (pv_mode 0, no bias)
+ * Limits: 1 <= (Hq / Hkv) * Nq <= 16, d in {64, 128}.  Workspace: at least
+ * qattn_workspace_size() for this shape.
+ */
+qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
+                          const float* k_scales, const int8_t* v_codes,
+                          const float* v_chan_scale, const float* v_code_amax,
+                          const qattn_shape* shape, const qattn_params* params, void* O,
+                          float* lse, void* workspace, size_t workspace_bytes,
+                          qattn_stream_t stream);
+
 /* a4 alone (debug) -- the int32 score tiles S = q_codes . k_codes^T
  * ("QFlash", eq. (3)), through the same tensor-core path as qattn_fwd.
  *   S (out) int32 [B][Hq][Nq][Nk]

@@ -24,7 +24,7 @@ PV_E4M3, PV_INT8 = 0, 1
 EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-    "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
+    "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
 )
 
 
@@ -74,8 +74,10 @@ def lib() -> ctypes.CDLL:
     L.qattn_quantize_v_noalloc.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp]
     L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
+    L.qattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
+                 "qattn_decode",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -187,6 +189,18 @@ def fwd(q_codes, q_scales, k_codes, k_scales, v8t, ldv, v_scales, bias, shape, p
                            ctypes.byref(params), _p(O), _p(lse), _p(workspace), ws_bytes,
                            _stream(stream)),
            "qattn_fwd")
+
+
+def decode(q_codes, q_scales, k_codes, k_scales, v_codes, v_chan_scale, v_code_amax, shape,
+           params, O, lse, workspace, stream=None):
+    """Decode step on an int8 KV cache (see qattn_decode in include/qattn.h)."""
+    _dense(k_codes, torch.int8, "k_codes")
+    _dense(v_codes, torch.int8, "v_codes")
+    _check(lib().qattn_decode(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales), _p(v_codes),
+                              _p(v_chan_scale), _p(v_code_amax), ctypes.byref(shape),
+                              ctypes.byref(params), _p(O), _p(lse), _p(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_decode")
 
 
 def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):

@@ -168,9 +168,9 @@ __device__ __forceinline__ void convert_q_tile(uint32_t tile, uint32_t codes, in
 }
 
 __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int nblk, int blk) {
-  if (gran == 0) return __ldg(s);
-  if (gran == 1) return __ldg(s + bh);
-  return __ldg(s + static_cast<size_t>(bh) * nblk + blk);
+  if (gran == 0) return s[0];
+  if (gran == 1) return s[bh];
+  return s[static_cast<size_t>(bh) * nblk + blk];
 }
 
 // Barrier slots.
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* sv4 = reinterpret_cast<const float4*>(a.v_scales + static_cast<size_t>(it.bkv) * D);
       float4 svn[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) svn[q] = __ldg(sv4 + q);
+      for (int q = 0; q < 8; ++q) svn[q] = sv4[q];
       ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);  // last PV
       ++pvc;
       if (!__all_sync(0xffffffffu, ok)) {
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (cc + 1 < D / 32) {  // the next chunk's scales load under this chunk's TMEM read
 #pragma unroll
-          for (int q = 0; q < 8; ++q) svn[q] = __ldg(sv4 + 8 * (cc + 1) + q);
+          for (int q = 0; q < 8; ++q) svn[q] = sv4[8 * (cc + 1) + q];
         }
         uint32_t o[32];
         tmem_ld32(tO + lane_base + cc * 32, o);

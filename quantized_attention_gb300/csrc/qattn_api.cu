@@ -135,6 +135,12 @@ bool encode_carrier(CUtensorMap* map, const void* ptr, int64_t planes, int64_t r
                    128, swz);
 }
 
+// Shapes the decode path serves: (Hq / Hkv) * Nq rows per KV head.
+bool decode_shape_ok(const qattn_shape* s) {
+  return s->Hkv > 0 && s->Nq >= 1 && (s->Hq / s->Hkv) * s->Nq <= qattn::kMaxDecodeRows &&
+         (s->d == 64 || s->d == 128);
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,6 +168,11 @@ size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params
   if (q > m) m = q;
   if (ws_quant_v(shape) > m) m = ws_quant_v(shape);
   if (ws_fwd(shape) > m) m = ws_fwd(shape);
+  if (decode_shape_ok(shape)) {
+    const size_t dws = qattn::decode_ws_bytes(shape->B, shape->Hq, shape->Hkv, shape->Nq,
+                                              shape->Nk, shape->d);
+    if (dws > m) m = dws;
+  }
   return m;
 }
 
@@ -350,6 +361,60 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
                  static_cast<uint32_t>(shape->d), CU_TENSOR_MAP_SWIZZLE_128B))
     return QATTN_ERR_CUDA;
   return from_cuda(qattn::launch_attn_fwd(tq, tk, tv, a, s));
+}
+
+qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
+                          const float* k_scales, const int8_t* v_codes,
+                          const float* v_chan_scale, const float* v_code_amax,
+                          const qattn_shape* shape, const qattn_params* params, void* O,
+                          float* lse, void* workspace, size_t workspace_bytes,
+                          qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (empty_problem(shape)) return QATTN_OK;
+  if (!decode_shape_ok(shape) || shape->Nk == 0 || params->pv_mode != QATTN_PV_E4M3)
+    return QATTN_ERR_UNSUPPORTED;
+  if (!q_codes || !aligned16(q_codes) || !q_scales || !k_codes || !aligned16(k_codes) ||
+      !k_scales || !v_codes || !aligned16(v_codes) || !v_chan_scale || !v_code_amax || !O ||
+      !aligned16(O))
+    return QATTN_ERR_INVALID_ARG;
+  for (const void* f : {static_cast<const void*>(q_scales), static_cast<const void*>(k_scales),
+                        static_cast<const void*>(v_chan_scale),
+                        static_cast<const void*>(v_code_amax), static_cast<const void*>(lse)})
+    if (reinterpret_cast<uintptr_t>(f) & 3u) return QATTN_ERR_INVALID_ARG;
+  const int64_t pos0 = pos0_of(shape, params);
+  if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
+  const size_t need = qattn::decode_ws_bytes(shape->B, shape->Hq, shape->Hkv, shape->Nq,
+                                             shape->Nk, shape->d);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  unsigned int* err = error_word();
+  if (!err) return QATTN_ERR_CUDA;
+  qattn::DecodeArgs a{};
+  a.err = err;
+  a.B = static_cast<int>(shape->B);
+  a.Hq = static_cast<int>(shape->Hq);
+  a.Hkv = static_cast<int>(shape->Hkv);
+  a.Nq = static_cast<int>(shape->Nq);
+  a.Nk = static_cast<int>(shape->Nk);
+  a.d = static_cast<int>(shape->d);
+  a.causal = params->causal;
+  a.pos0 = params->causal ? static_cast<int>(pos0) : 0;
+  a.sm_scale = params->sm_scale > 0.f ? params->sm_scale
+                                      : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
+  a.q_gran = params->q_gran;
+  a.k_gran = params->k_gran;
+  a.q_codes = q_codes;
+  a.q_scales = q_scales;
+  a.k_codes = k_codes;
+  a.k_scales = k_scales;
+  a.v_codes = v_codes;
+  a.v_chan_scale = v_chan_scale;
+  a.v_code_amax = v_code_amax;
+  a.out = O;
+  a.out_bf16 = params->out_dtype == QATTN_BF16;
+  a.lse = lse;
+  return from_cuda(qattn::launch_decode(a, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,

@@ -80,6 +80,38 @@ cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int B
 
 cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t s);
 
+// ---- decode.cu
+constexpr int kMaxDecodeRows = 16;  // (Hq / Hkv) * Nq rows per KV head
+constexpr int kDecodeChunk = 2;     // key blocks per chunk of the split
+
+struct DecodeArgs {
+  int B, Hq, Hkv, Nq, Nk, d;
+  int causal;
+  int pos0;
+  float sm_scale;
+  int q_gran, k_gran;
+  const int8_t* q_codes;
+  const float* q_scales;
+  const int8_t* k_codes;
+  const float* k_scales;
+  const int8_t* v_codes;       // [B*Hkv][Nk][d], row-major as cached
+  const float* v_chan_scale;   // [B*Hkv][d]
+  const float* v_code_amax;    // [B*Hkv][d]: max |code| per channel
+  void* out;
+  int out_bf16;
+  float* lse;
+  // workspace regions, set by launch_decode
+  float* t;
+  float* mblk;
+  float* part_o;
+  float* part_l;
+  float* part_m;
+  unsigned int* err;  // device error word (a bounded wait that ran out)
+};
+size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
+                       long long d);
+cudaError_t launch_decode(DecodeArgs a, void* ws, cudaStream_t s);
+
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& a, cudaStream_t s);

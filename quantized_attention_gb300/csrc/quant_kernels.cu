@@ -328,7 +328,7 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
   if (MODE != 0) {
     const float* crow = j.chan + (static_cast<size_t>(b) * j.Hchan + h / j.group) * D;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ch[e] = __ldg(crow + (threadIdx.x % VPR) * 8 + e);
+    for (int e = 0; e < 8; ++e) ch[e] = crow[(threadIdx.x % VPR) * 8 + e];  // written by the K mean pass
   }
 
   uint4 raw[NV];
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict
 // the write stops at the row stride ldv.
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_convert_kernel(
-    const void* __restrict__ V, int Nk, const unsigned int* __restrict__ amax_bits,
+    const void* __restrict__ V, int Nk, const unsigned int* amax_bits,
     const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
     float* __restrict__ v_scales) {
   pdl_trigger();
@@ -560,13 +560,13 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
 
 // ------------------------------------------------------------------ carriers
 // int8 codes -> fp16 values (exact: |code| <= 127).
-__global__ void codes_to_f16_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst,
+__global__ void codes_to_f16_kernel(const int8_t* src, uint16_t* __restrict__ dst,
                                     size_t n16) {
   pdl_trigger();
   pdl_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    const uint4 raw = reinterpret_cast<const uint4*>(src)[i];  // may come from the kernel before
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t o[8];
 #pragma unroll

@@ -88,6 +88,9 @@ WORKLOADS = {
     "llm8k": Workload("llm8k", 1, 32, 8, 8192, 8192, 128, True, GRAN_BLOCK, GRAN_BLOCK, 4),
     "chunk32k": Workload("chunk32k", 1, 32, 8, 2048, 32768, 128, True, GRAN_BLOCK, GRAN_BLOCK,
                          5, q_pos0=30720, kv_codes=True),
+    # one decode token at position 32767 against the chunk32k-shaped int8 cache
+    "decode32k": Workload("decode32k", 1, 32, 8, 1, 32768, 128, True, GRAN_BLOCK, GRAN_BLOCK,
+                          6, kv_codes=True),
 }
 
 

@@ -64,6 +64,25 @@ class Problem:
                           self.workspace, stream)
             self._k_codes = self.k_codes
 
+    def quantize_q(self, Q, K_scale, stream=None):
+        """Decode on an int8 cache: only the new tokens' Q codes (K's channel
+        scales folded in) and the K scales; the cache itself stays as stored."""
+        qb.quantize_qk(Q, self._cache_k, qb.DT_I8, None, K_scale, self.shape, self.params,
+                       self.q_codes, self.q_scales, None, self.k_scales, self.workspace, stream)
+
+    def set_cache(self, K_codes, V_codes, V_scale):
+        """The int8 KV cache qattn_decode reads, and its header's per-channel
+        max |V code|."""
+        self._cache_k, self._cache_v, self._cache_vs = K_codes, V_codes, V_scale
+        self._cache_vamax = V_codes.to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+
+    def decode(self, stream=None):
+        """qattn_decode on the cache given to set_cache."""
+        qb.decode(self.q_codes, self.q_scales, self._cache_k, self.k_scales, self._cache_v,
+                  self._cache_vs, self._cache_vamax, self.shape, self.params, self.O, self.lse,
+                  self.workspace, stream)
+        return self.O
+
     def attend(self, bias: Optional[torch.Tensor] = None, stream=None):
         """a4-a10: the fused attention kernel on the quantized operands."""
         qb.fwd(self.q_codes, self.q_scales, self._k_codes, self.k_scales, self.v8t, self.ldv,
@@ -83,6 +102,11 @@ class Problem:
         n += 2                                       # V amax, V e4m3 transpose
         n += 1 + int(self.k_carrier is None)         # [K carriers], fused attention
         return n
+
+    def decode_launches(self) -> int:
+        """Kernels one quantize_q + decode launches: Q codes (two passes for a
+        tensor/head granule), K scales set to 1, then the decode's three."""
+        return 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 3
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
             V_scale=None, bias=None, stream=None):

@@ -1,0 +1,91 @@
+"""Decode on an int8 KV cache (qattn_decode) against the oracle's recipe on the
+same codes: a few query tokens per head, long caches with a ragged last
+block, GQA groups, both head dims, and the full 32K-key decode shape on
+sampled heads."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import qattn_oracle as O
+from quantized_attention_gb300 import binding as qb
+from quantized_attention_gb300 import inputs as I
+from quantized_attention_gb300.pipeline import device_inputs, problem_for
+from tests.gpu_common import ensure_library
+from tests.parity import check_output
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    I.small("chunk32k", Hq=8, Hkv=2, Nq=1, Nk=4173, q_pos0=None),
+    I.small("chunk32k", Hq=8, Hkv=2, Nq=2, Nk=1500, q_pos0=None),
+    I.small("chunk32k", Hq=4, Hkv=1, Nq=4, Nk=700, q_pos0=None, d=64),
+    I.small("chunk32k", Hq=2, Hkv=2, Nq=1, Nk=100, q_pos0=None),
+    I.small("chunk32k", Hq=8, Hkv=4, Nq=3, Nk=2048, q_pos0=1000),  # tokens mid-cache
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def _ids(w):
+    return f"H{w.Hq}/{w.Hkv}-q{w.Nq}-k{w.Nk}-d{w.d}-p{w.pos0}"
+
+
+def run_decode(wl, inp, out_dtype=qb.DT_F32):
+    P = problem_for(wl, out_dtype=out_dtype, want_lse=True)
+    dev = device_inputs(inp)
+    P.quantize(**dev)
+    amax = dev["V_codes"].to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+    ws = torch.empty(max(qb.workspace_size(P.shape, P.params), 256), dtype=torch.uint8,
+                     device="cuda")
+    qb.decode(P.q_codes, P.q_scales, dev["K_codes"], P.k_scales, dev["V_codes"],
+              dev["V_scale"], amax, P.shape, P.params, P.O, P.lse, ws)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    return P
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
+def test_decode_matches_oracle(wl):
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P = run_decode(wl, inp)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+    rows = np.arange(wl.Nq)
+    ref = O.run_workload(inp, prep, heads=heads, rows=rows, want_bound=True)
+    gpu = P.O.cpu().numpy().reshape(len(heads), wl.Nq, wl.d).astype(np.float64)
+    check_output(gpu, ref["O"], ref["bound"], _ids(wl))
+    lse = P.lse.cpu().numpy().reshape(len(heads), wl.Nq).astype(np.float64)
+    fin = np.isfinite(ref["lse"])
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref["lse"][fin], rtol=0, atol=1e-4)
+
+
+def test_decode_32k_full_shape_sampled_heads():
+    """The decode32k shape: 32 query heads / 8 KV heads, one token against
+    32768 cached int8 keys; every head checked against the oracle."""
+    wl = I.WORKLOADS["decode32k"]
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P = run_decode(wl, inp, out_dtype=qb.DT_BF16)
+    heads = [(0, h) for h in range(wl.Hq)]
+    ref = O.run_workload(inp, prep, heads=heads, rows=np.arange(wl.Nq), want_bound=True)
+    gpu = P.O.float().cpu().numpy().reshape(len(heads), wl.Nq, wl.d).astype(np.float64)
+    # bf16 output: the oracle's fp32-exact output rounded to bf16 is within 2^-9 relative
+    want = torch.from_numpy(ref["O"].astype(np.float32)).to(torch.bfloat16).double().numpy()
+    check_output(gpu, want, ref["bound"] + np.abs(ref["O"]) * 2.0 ** -8, "decode32k")
+
+
+def test_decode_same_as_prefill_kernel():
+    """qattn_decode and qattn_fwd (after qattn_quantize_v) on the same codes."""
+    wl = I.small("chunk32k", Hq=8, Hkv=2, Nq=2, Nk=3000, q_pos0=None)
+    inp = I.make_inputs(wl)
+    Pd = run_decode(wl, inp)
+    P = problem_for(wl, want_lse=True)
+    dev = device_inputs(inp)
+    P.run(**dev)
+    torch.cuda.synchronize()
+    a, b = Pd.O.cpu().numpy(), P.O.cpu().numpy()
+    assert np.abs(a - b).max() <= 2e-3 * np.abs(b).max()
