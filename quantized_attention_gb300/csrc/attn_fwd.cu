@@ -795,13 +795,6 @@ __global__ void __launch_bounds__(160, 1)
   }
 }
 
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
-  return n;
-}
-
 template <int D, bool BIAS, bool PQ = false>
 cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnArgs& a, cudaStream_t s) {

@@ -414,7 +414,16 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
   a.out = O;
   a.out_bf16 = params->out_dtype == QATTN_BF16;
   a.lse = lse;
-  return from_cuda(qattn::launch_decode(a, workspace, reinterpret_cast<cudaStream_t>(stream)));
+  // the cache's K and V codes, tiles of 128 keys swizzled for conflict-free reads
+  CUtensorMap tk, tv;
+  const CUtensorMapSwizzle swz = shape->d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const uint64_t planes = static_cast<uint64_t>(shape->B * shape->Hkv);
+  if (!encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k_codes, shape->d, shape->Nk, planes,
+                 shape->d, static_cast<uint32_t>(shape->d), 128, swz) ||
+      !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_codes, shape->d, shape->Nk, planes,
+                 shape->d, static_cast<uint32_t>(shape->d), 128, swz))
+    return QATTN_ERR_CUDA;
+  return from_cuda(qattn::launch_decode(tk, tv, a, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,

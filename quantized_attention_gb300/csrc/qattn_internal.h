@@ -27,6 +27,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Streaming multiprocessors of the current device (1 if the query fails).
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
 // Bits of the device error word.
 constexpr unsigned int kErrTimeout = 1u;
 
@@ -82,7 +90,6 @@ cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cuda
 
 // ---- decode.cu
 constexpr int kMaxDecodeRows = 16;  // (Hq / Hkv) * Nq rows per KV head
-constexpr int kDecodeChunk = 2;     // key blocks per chunk of the split
 
 struct DecodeArgs {
   int B, Hq, Hkv, Nq, Nk, d;
@@ -110,7 +117,10 @@ struct DecodeArgs {
 };
 size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
                        long long d);
-cudaError_t launch_decode(DecodeArgs a, void* ws, cudaStream_t s);
+// tk, tv: maps over the int8 K and V codes [B*Hkv][Nk][d], box d x 128 x 1,
+// 128-byte swizzle for d = 128, 64-byte for d = 64.
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, void* ws,
+                          cudaStream_t s);
 
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

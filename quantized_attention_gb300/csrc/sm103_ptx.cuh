@@ -352,4 +352,17 @@ __device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t& lo, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
+// D(16x8 fp32) += A(16x32 e4m3) * B(32x8 e4m3), warp-wide.  Fragments
+// (g = lane / 4, t = lane % 4): a0/a2 hold row g, k = 4t..4t+3 / 16+4t..;
+// a1/a3 the same for row g + 8; b0/b1 hold column g, k = 4t..4t+3 /
+// 16+4t..; d0,d1 are row g, columns 2t, 2t+1 and d2,d3 row g + 8.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 }  // namespace qattn

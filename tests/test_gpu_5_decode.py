@@ -21,6 +21,14 @@ CASES = [
     I.small("chunk32k", Hq=4, Hkv=1, Nq=4, Nk=700, q_pos0=None, d=64),
     I.small("chunk32k", Hq=2, Hkv=2, Nq=1, Nk=100, q_pos0=None),
     I.small("chunk32k", Hq=8, Hkv=4, Nq=3, Nk=2048, q_pos0=1000),  # tokens mid-cache
+    I.small("chunk32k", Hq=16, Hkv=2, Nq=2, Nk=1100, q_pos0=None),  # 16 rows per KV head
+]
+
+# Enough key blocks that pass 2 gives each CTA a chunk of several blocks, so the
+# accumulators are rescaled as the running max grows inside a chunk.
+LONG_CASES = [
+    I.small("chunk32k", Hq=32, Hkv=16, Nq=8, Nk=8192, q_pos0=None),          # 16 rows, d 128
+    I.small("chunk32k", Hq=16, Hkv=16, Nq=1, Nk=16384, q_pos0=None, d=64),   # 1 row, d 64
 ]
 
 
@@ -61,6 +69,19 @@ def test_decode_matches_oracle(wl):
     fin = np.isfinite(ref["lse"])
     assert np.array_equal(np.isfinite(lse), fin)
     np.testing.assert_allclose(lse[fin], ref["lse"][fin], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("wl", LONG_CASES, ids=[_ids(w) for w in LONG_CASES])
+def test_decode_multi_block_chunks_sampled_heads(wl):
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    P = run_decode(wl, inp)
+    G = wl.Hq // wl.Hkv
+    picked = [0, 1, wl.Hq - G, wl.Hq - 1]  # both ends of the first and last KV groups
+    heads = [(0, h) for h in picked]
+    ref = O.run_workload(inp, prep, heads=heads, rows=np.arange(wl.Nq), want_bound=True)
+    gpu = P.O.cpu().numpy().reshape(wl.Hq, wl.Nq, wl.d)[picked].astype(np.float64)
+    check_output(gpu, ref["O"], ref["bound"], _ids(wl))
 
 
 def test_decode_32k_full_shape_sampled_heads():
