@@ -372,7 +372,7 @@ def gpu_arm(args):
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     if decode:  # memory-bound: the cache's bytes over the decode call's time
         gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "qattn_decode (3 launches: scores, PV, combine)",
+        roofline = {"bound": "hbm", "kernel": "qattn_decode (2 launches: fused scores + PV over key chunks, chunk combine)",
                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"],
                     "peak_basis": f"{peaks['source']} HBM copy rate",

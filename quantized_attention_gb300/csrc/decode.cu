@@ -7,20 +7,17 @@
 //
 // It computes the recipe of the prefill kernel on the same codes: blocks of
 // 128 keys in ascending order, each block's P relative to the running max at
-// that block.  The split keeps that exactly: pass 1 writes every block's
-// scores t = S c and each row's block maximum; pass 2 rebuilds the running max
-// of each block as a prefix maximum of the block maxima, so P = 2^(t - m_j)
-// and its e4m3 code are the recipe's, and accumulates a chunk of blocks'
-// share of O and l scaled to the running max at the chunk's end; pass 3
-// combines the chunks.  Rows are (query head of the KV group, token):
-// r = g * Nq + i.
+// that block.  The split over key blocks keeps that exactly: a chunk of blocks
+// computes its scores, learns the running max before it from the chunk maxima
+// of the earlier chunks (so each block's P = 2^(t - m_j) and its e4m3 code are
+// the recipe's), and accumulates its share of O and l scaled to the running
+// max at its last block; a second pass combines the chunks.  Rows are (query
+// head of the KV group, token): r = g * Nq + i.
 //
-// Both streaming passes move key blocks into shared memory with TMA (128-byte
-// swizzle for d = 128, 64-byte for d = 64) through a ring of stages, so a CTA
-// keeps several blocks in flight.  Pass 1 waits on the kernels before it and
-// only then lets pass 2 launch; pass 2 can therefore start its V loads before
-// its own wait (the cache was written before this call), overlapping the tail
-// of pass 1.
+// The K and V tiles move by TMA (128-byte swizzle for d = 128, 64-byte for
+// d = 64) through one ring of stages per CTA: a chunk's K tiles, then its V
+// tiles, so the V reads start while the last scores are computed.
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,10 +27,7 @@
 namespace qattn {
 namespace {
 
-constexpr int kBlk = 128;         // keys per block (the recipe's key block)
-constexpr int kScoreStages = 2;   // pass 1 ring depth (many CTAs per SM)
-constexpr int kPvStages = 3;      // pass 2 ring depth
-constexpr int kPvThreads = 128;   // four warps: warp w takes keys 32w .. 32w+31 of a block
+constexpr int kBlk = 128;  // keys per block (the recipe's key block)
 constexpr int kCombineThreads = 256;
 constexpr float kLog2e = 1.44269502162933349609375f;  // fp32(log2 e)
 constexpr float kLog2_448 = 8.8073549220576041f;
@@ -91,455 +85,504 @@ __device__ __forceinline__ float scale_at(const float* s, int gran, int bh, int 
   return s[static_cast<size_t>(bh) * nblk + blk];
 }
 
-// ------------------------------------------------------------------ pass 1
-// Persistent CTAs of 128 threads; CTA c takes the key blocks gb = c, c + grid,
-// ... of all (batch * KV head, block j) pairs, gb = bkv * nkb + j, through a
-// ring of kScoreStages stages (the block's K codes by TMA, swizzled, and the
-// head's Q rows by a bulk copy).  Thread k owns key j * 128 + k: the exact
-// int32 dot products run on dp4a; the swizzle puts the 8 keys of a shared-
-// memory phase in 8 different bank groups, and every lane reads the same Q
-// chunk (a broadcast).  Writes t = S c (masked keys -inf) and each row's block
-// maximum.
-template <int D, int RMAX>
-struct ScoreSmem {
-  static constexpr int kK = kBlk * D;                           // K codes of a block
-  static constexpr int kStage = round_up(kK + RMAX * D, 1024);  // + the head's Q codes
-  static constexpr int kBytes = kScoreStages * kStage + 1024;   // + alignment slack
-};
+// Chunk records: one 64-bit word per (chunk, row) holding this call's tag in
+// the high half and the chunk maximum's bits in the low half, so the value and
+// its tag land in one store and need no fence (a fence here would wait for the
+// tiles the CTA has in flight).
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
-template <int D, int RMAX>
-__global__ void __launch_bounds__(kBlk) decode_scores_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                             const DecodeArgs a) {
-  constexpr int NC = D / 16;  // 16-byte chunks per key row
-  using SM = ScoreSmem<D, RMAX>;
-  extern __shared__ uint8_t dsm_raw[];
-  uint8_t* dsm = dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u);
-  __shared__ float cfv[2][RMAX];
-  __shared__ float wmax[2][kBlk / 32][RMAX];
-  __shared__ __align__(8) uint64_t full[kScoreStages];
-  __shared__ int abort_flag;
-  const int G = a.Hq / a.Hkv, R = G * a.Nq;
-  const int nkb = (a.Nk + kBlk - 1) / kBlk, nqb = (a.Nq + kBlk - 1) / kBlk;
-  const int total = nkb * a.B * a.Hkv;
-  const int n_my = (total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                   static_cast<int>(gridDim.x);
-  const size_t tstride = static_cast<size_t>(nkb) * kBlk;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScoreStages; ++s) mbar_init(smem_u32(&full[s]), 1);
-    abort_flag = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tmK);
-  }
-  __syncthreads();
-  pdl_wait();     // Q codes and scales come from the kernels before; the cache may too
-  pdl_trigger();  // only now: pass 2 may read the cache before its own wait
-  // thread 0: the i-th block of this CTA into stage i % kScoreStages
-  auto issue = [&](int i) {
-    const int gb = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int bkv = gb / nkb, j = gb % nkb;
-    const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
-    const uint32_t st = smem_u32(dsm + (i % kScoreStages) * SM::kStage);
-    const uint32_t bar = smem_u32(&full[i % kScoreStages]);
-    // the TMA box is always 128 full rows (rows past Nk arrive as zeros)
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>((kBlk + R) * D));
-    tma_load_3d(st, &tmK, bar, 0, j * kBlk, bkv);
-    // rows r = g * Nq + i of the head are contiguous: heads hkv*G .. hkv*G+G-1
-    bulk_g2s(st + SM::kK, a.q_codes + (static_cast<size_t>(b) * a.Hq + hkv * G) * a.Nq * D,
-             static_cast<uint32_t>(R * D), bar);
-  };
-  if (threadIdx.x == 0)
-    for (int i = 0; i < min(kScoreStages, n_my); ++i) issue(i);
-  // the scales of row r for the i-th block (threads r < R)
-  auto load_scales = [&](int i, int r, float& sq, float& sk) {
-    const int gb = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int bkv = gb / nkb, j = gb % nkb;
-    const int b = bkv / a.Hkv, hkv = bkv % a.Hkv, g = r / a.Nq, ii = r % a.Nq;
-    sq = scale_at(a.q_scales, a.q_gran, b * a.Hq + hkv * G + g, nqb, ii / kBlk);
-    sk = scale_at(a.k_scales, a.k_gran, bkv, nkb, j);
-  };
-  auto cfac = [&](float sq, float sk) {
-    return __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
-  };
-  if (threadIdx.x < R && n_my > 0) {
-    float sq, sk;
-    load_scales(0, threadIdx.x, sq, sk);
-    cfv[0][threadIdx.x] = cfac(sq, sk);
-  }
-  __syncthreads();
-  const int k = threadIdx.x;
-  for (int i = 0; i < n_my; ++i) {
-    const int s = i % kScoreStages;
-    const int gb = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int bkv = gb / nkb, j = gb % nkb;
-    float nsq = 0.f, nsk = 0.f;  // the next block's scales, in flight during the wait
-    if (threadIdx.x < R && i + 1 < n_my) load_scales(i + 1, threadIdx.x, nsq, nsk);
-    if (!mbar_wait(smem_u32(&full[s]), (i / kScoreStages) & 1, &abort_flag, a.err, kErrTimeout))
-      return;
-    const int8_t* ks = reinterpret_cast<const int8_t*>(dsm + s * SM::kStage);
-    const int8_t* qs = ks + SM::kK;
-    int acc[RMAX];
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc[r] = 0;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const uint4 kw = *reinterpret_cast<const uint4*>(ks + swz_chunk<D>(k, c));
-#pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-          const uint4 qw = *reinterpret_cast<const uint4*>(qs + r * D + c * 16);
-          acc[r] = __dp4a(static_cast<int>(kw.x), static_cast<int>(qw.x), acc[r]);
-          acc[r] = __dp4a(static_cast<int>(kw.y), static_cast<int>(qw.y), acc[r]);
-          acc[r] = __dp4a(static_cast<int>(kw.z), static_cast<int>(qw.z), acc[r]);
-          acc[r] = __dp4a(static_cast<int>(kw.w), static_cast<int>(qw.w), acc[r]);
-        }
+// Waits (bounded, like mbar_wait) until the record carries tag; returns its value.
+__device__ __forceinline__ bool wait_record(const unsigned long long* rec, uint32_t tag, float& v,
+                                            volatile int* abort_flag, unsigned int* err) {
+  const unsigned long long t0 = cycles();
+  for (uint32_t n = 0;; ++n) {
+    const unsigned long long w = ld_relaxed_u64(rec);
+    if (static_cast<uint32_t>(w >> 32) == tag) {
+      v = __uint_as_float(static_cast<uint32_t>(w));
+      return true;
+    }
+    if ((n & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (cycles() - t0 > kWaitTimeoutCycles) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
       }
     }
-    const int key = j * kBlk + k;
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < R) {
-        const int ii = r % a.Nq;
-        const bool vis = key < a.Nk && (!a.causal || key <= a.pos0 + ii);
-        const float t = vis ? __fmul_rn(static_cast<float>(acc[r]), cfv[i & 1][r]) : kNegInf;
-        a.t[(static_cast<size_t>(bkv) * R + r) * tstride + key] = t;
-        float mx = t;
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-        if ((k & 31) == 0) wmax[i & 1][k >> 5][r] = mx;
-      }
-    }
-    if (threadIdx.x < R && i + 1 < n_my) cfv[(i + 1) & 1][threadIdx.x] = cfac(nsq, nsk);
-    __syncthreads();  // stage s is read; the block's warp maxima are in
-    if (threadIdx.x == 0 && i + kScoreStages < n_my) issue(i + kScoreStages);
-    if (threadIdx.x < R) {
-      const int r = threadIdx.x;
-      const float mx = fmaxf(fmaxf(wmax[i & 1][0][r], wmax[i & 1][1][r]),
-                             fmaxf(wmax[i & 1][2][r], wmax[i & 1][3][r]));
-      a.mblk[(static_cast<size_t>(bkv) * nkb + j) * R + r] = mx;
-    }
+    __nanosleep(64);
   }
 }
 
-// ------------------------------------------------------------------ pass 2
-// One CTA of four warps per (chunk of bpc key blocks, batch * KV head).  The
-// chunk's t rows arrive by bulk copy and become the e4m3 codes of 448 P
-// relative to each block's running max (the recipe's P8), stored in the
-// A-fragment order of mma.m16n8k32; V blocks stream through a ring of TMA
-// stages.  For each block, warp w multiplies P8 (rows x keys 32w..32w+31) by
-// the block's V8 on the tensor cores (e4m3 x e4m3, fp32 accumulation): every
-// lane reads 16 (d = 128) or 8 (d = 64) channels of 8 keys, rounds the codes
-// to e4m3 as qattn_quantize_v does, and transposes 4x4 byte groups into B
-// fragments.  Keys of a 32-key step are permuted (fragment position
-// 4t + i <-> key 8i + 2t, 16 + 4t + i <-> key 8i + 2t + 1) so the 8 lanes of a
-// shared-memory phase hit 8 bank groups of the swizzled tile; P8 uses the same
-// permutation.  Channels: lane group g = lane / 4 owns channels CPT*g ..
-// CPT*g + CPT-1; n-tile (word w, byte e) column n is channel CPT*n + 4w + e.
-// Between blocks the accumulators are rescaled by 2^(m_prev - m_j), so the
-// chunk's share ends relative to the running max at its last block.
+// ------------------------------------------------------------------ pass 1+2
+// One kernel: CTA-units u = bkv * nch + c, each a chunk of bpc key blocks of
+// one (batch, KV head), taken by persistent CTAs in increasing u.  A unit
+// first computes its blocks' scores t = S c (the K tiles streamed through a
+// ring of TMA stages) into shared memory and publishes its rows' chunk maximum
+// (a record tagged with this call's epoch, release/acquire at GPU scope).  It
+// then looks back at the records of the earlier chunks of its head -- the
+// running max before the chunk -- and runs PV on the V tiles, which stream
+// through the same ring right behind the K tiles.  A unit waits only on
+// lower-numbered units, taken earlier by running CTAs, so the waits always
+// end; each is bounded anyway.
+//
+// Scores: thread k owns key k of a block; exact int32 dot products on dp4a;
+// the swizzled tile puts the 8 keys of a shared-memory phase in 8 bank groups
+// and every lane reads the same Q chunk (a broadcast).
+//
+// PV: warp w multiplies P8 (rows x keys 32w..32w+31 of a block) by the
+// block's V8 on the tensor cores (mma.m16n8k32, e4m3 x e4m3, fp32
+// accumulation): every lane reads 16 (d = 128) or 8 (d = 64) channels of 8
+// keys, rounds the codes to e4m3 as qattn_quantize_v does, and transposes 4x4
+// byte groups into B fragments.  Keys of a 32-key step are permuted (fragment
+// position 4t + i <-> key 8i + 2t, 16 + 4t + i <-> key 8i + 2t + 1) so the 8
+// lanes of a shared-memory phase hit 8 bank groups; P8 uses the same
+// permutation.  Lane group g = lane / 4 owns channels CPT*g .. CPT*g + CPT-1;
+// n-tile (word w, byte e) column n is channel CPT*n + 4w + e.  Between blocks
+// the accumulators are rescaled by 2^(m_prev - m_j), so the chunk's share ends
+// relative to the running max at its last block.
+constexpr int kThreads = 128;  // four warps
+constexpr int kStages = 3;     // ring of K then V tiles
+
 template <int D, int RMAX>
-struct PvSmem {
+struct FusedSmem {
   static constexpr int kMaxBlocks = (RMAX <= 4) ? 8 : 4;  // key blocks per chunk, at most
   static constexpr int kChunkKeys = kMaxBlocks * kBlk;
-  static constexpr int kStage = kBlk * D;  // 1024-byte multiple
-  static constexpr int kRing = kPvStages * kStage;
-  static constexpr int kT = RMAX * kChunkKeys * 4;               // t rows of the chunk (fp32)
+  static constexpr int kTile = kBlk * D;  // 1024-byte multiple
+  static constexpr int kRing = kStages * kTile;
+  static constexpr int kQ = round_up(RMAX * D, 1024);           // the head's Q codes
+  static constexpr int kT = RMAX * kChunkKeys * 4;               // t of the chunk (fp32)
   static constexpr int kP8 = kMaxBlocks * 4 * RMAX * 32;         // [block][step][row][32]
-  static constexpr int kBytes = kRing + kT + kP8 + 1024;         // + alignment slack
-  static constexpr int kRed = (kPvThreads / 32) * RMAX * D * 4;  // [warp][row][d]
+  static constexpr int kBytes = kRing + kQ + kT + kP8 + 1024;    // + alignment slack
+  static constexpr int kRed = (kThreads / 32) * RMAX * D * 4;    // [warp][row][d]
   static_assert(kRed <= kRing, "reduction buffer does not fit");
 };
 
 template <int D, int RMAX>
-__global__ void __launch_bounds__(kPvThreads) decode_pv_kernel(const __grid_constant__ CUtensorMap tmV,
-                                                               const DecodeArgs a, int bpc) {
-  constexpr int CPT = D / 8;    // channels per lane group
+__global__ void __launch_bounds__(kThreads)
+    decode_fused_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
+  constexpr int NC = D / 16;    // 16-byte chunks per key row
+  constexpr int CPT = D / 8;    // PV: channels per lane group
   constexpr int WPT = CPT / 4;  // their 32-bit words
   constexpr int NT = 4 * WPT;   // n-tiles a lane accumulates
-  using SM = PvSmem<D, RMAX>;
+  using SM = FusedSmem<D, RMAX>;
   constexpr int CK = SM::kChunkKeys;
+  constexpr int MB = SM::kMaxBlocks;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u);
-  float* tb = reinterpret_cast<float*>(dsm + SM::kRing);
-  uint8_t* p8 = dsm + SM::kRing + SM::kT;
+  int8_t* qs = reinterpret_cast<int8_t*>(dsm + SM::kRing);
+  float* tb = reinterpret_cast<float*>(dsm + SM::kRing + SM::kQ);
+  uint8_t* p8 = dsm + SM::kRing + SM::kQ + SM::kT;
   float* red = reinterpret_cast<float*>(dsm);
-  __shared__ float mrun[SM::kMaxBlocks][RMAX];
-  __shared__ float lblk[SM::kMaxBlocks][RMAX];
-  __shared__ float mpre[kPvThreads];
+  __shared__ float cf[MB][RMAX];    // score factor of block i, row r
+  __shared__ float bmax[MB][RMAX];  // block maxima of the chunk
+  __shared__ float mrun[MB][RMAX];  // running max at each block
+  __shared__ float lblk[MB][RMAX];
+  __shared__ float wmax[2][kThreads / 32][RMAX];
+  __shared__ float mpoll[kThreads];
   __shared__ __align__(16) float inv_s[D];
-  __shared__ __align__(8) uint64_t full[kPvStages];
-  __shared__ __align__(8) uint64_t tbar;
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t qbar;
   __shared__ int abort_flag;
-  const int ch = blockIdx.x, bkv = blockIdx.y;
-  const int c0 = ch * bpc;
-  const int G = a.Hq / a.Hkv, R = G * a.Nq;
-  const int nkb = (a.Nk + kBlk - 1) / kBlk;
-  const int nb = min(bpc, nkb - c0);
+  __shared__ int unit_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t4 = lane & 3;
+  const int G = a.Hq / a.Hkv, R = G * a.Nq;
+  const int nkb = (a.Nk + kBlk - 1) / kBlk, nqb = (a.Nq + kBlk - 1) / kBlk;
+  const int units = a.B * a.Hkv * a.nch;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPvStages; ++s) mbar_init(smem_u32(&full[s]), 1);
-    mbar_init(smem_u32(&tbar), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    mbar_init(smem_u32(&qbar), 1);
     abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  __syncthreads();
-  // thread 0: V codes of the chunk's block jj into stage jj % kPvStages
-  auto issue_v = [&](int jj) {
-    const uint32_t bar = smem_u32(&full[jj % kPvStages]);
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kBlk * D));
-    tma_load_3d(smem_u32(dsm + (jj % kPvStages) * SM::kStage), &tmV, bar, 0, (c0 + jj) * kBlk, bkv);
+  // Units are taken in increasing order from a counter whose high half is this
+  // call's tag: the first taker finds another value there (an earlier call's,
+  // or whatever the workspace held) and claims the counter with a swap, so it
+  // needs no reset.  A unit is only ever held by a running CTA, so the smallest
+  // unfinished unit always has its predecessors done, whatever the residency
+  // of the grid.  The kernels before this one in the stream do not touch it.
+  const uint32_t tag = static_cast<uint32_t>(a.epoch);
+  auto take = [&]() -> int {
+    for (int attempt = 0; attempt < 64; ++attempt) {
+      const unsigned long long cur = ld_relaxed_u64(a.ctr);
+      if (static_cast<uint32_t>(cur >> 32) == tag)
+        return static_cast<int>(static_cast<uint32_t>(atomicAdd(a.ctr, 1ull)));
+      // another value (an earlier call's, or garbage): claim it for this call, unit 0
+      if (atomicCAS(a.ctr, cur, (static_cast<unsigned long long>(tag) << 32) | 1ull) == cur) return 0;
+    }
+    atomicOr(a.err, kErrTimeout);  // unreachable while one call owns the workspace
+    return units;
   };
-  // The cache (V codes, their channel maxima) precedes this call; pass 1
-  // released this grid only after its own wait, so it is complete here.
-  if (threadIdx.x == 0)
-    for (int jj = 0; jj < min(kPvStages, nb); ++jj) issue_v(jj);
-  for (int c = threadIdx.x; c < D; c += kPvThreads) {
-    const float am = __ldg(a.v_code_amax + static_cast<size_t>(bkv) * D + c);
-    inv_s[c] = (am > 0.f) ? __fdiv_rn(448.0f, am) : 0.f;
-  }
-  pdl_wait();  // t and the block maxima come from pass 1
-  pdl_trigger();
-  const size_t tstride = static_cast<size_t>(nkb) * kBlk;
-  if (threadIdx.x == 0) {
-    const uint32_t bar = smem_u32(&tbar);
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(R * nb * kBlk * 4));
-    for (int r = 0; r < R; ++r)
-      bulk_g2s(smem_u32(tb + r * CK),
-               a.t + (static_cast<size_t>(bkv) * R + r) * tstride + static_cast<size_t>(c0) * kBlk,
-               static_cast<uint32_t>(nb * kBlk * 4), bar);
-  }
-  const float* mb = a.mblk + static_cast<size_t>(bkv) * nkb * R;
-  // the running max before the chunk: max of the earlier blocks' maxima
-  {
-    const int r = threadIdx.x % R, part = threadIdx.x / R, parts = kPvThreads / R;
-    float mx = kNegInf;
-    if (part < parts)
-      for (int jj = part; jj < c0; jj += parts) mx = fmaxf(mx, mb[static_cast<size_t>(jj) * R + r]);
-    mpre[threadIdx.x] = mx;
-  }
+  if (threadIdx.x == 0) unit_s = take();
   __syncthreads();
-  if (threadIdx.x < R) {
-    const int r = threadIdx.x, parts = kPvThreads / R;
-    float m = kNegInf;
-    for (int p = 0; p < parts; ++p) m = fmaxf(m, mpre[p * R + r]);
-    for (int jj = 0; jj < nb; ++jj) {
-      m = fmaxf(m, mb[static_cast<size_t>(c0 + jj) * R + r]);
-      mrun[jj][r] = m;
+  pdl_wait();  // Q codes and scales come from the kernels before; the cache precedes this call
+  uint32_t q0 = 0;  // ring items consumed by earlier units (every thread keeps the same count)
+  uint32_t nu = 0;  // units done by this CTA (phase of qbar)
+  for (int u = unit_s; u < units; ++nu) {
+    const int bkv = u / a.nch, c = u % a.nch;
+    const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
+    const int j0 = c * a.bpc, nb = min(a.bpc, nkb - j0);
+    const int items = 2 * nb;  // K tiles of the chunk, then its V tiles
+    // thread 0: ring item i of this unit (K tile i, or V tile i - nb)
+    auto issue = [&](int i) {
+      const uint32_t q = q0 + i, slot = q % kStages;
+      const uint32_t bar = smem_u32(&full[slot]);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kBlk * D));
+      if (i < nb) tma_load_3d(smem_u32(dsm + slot * SM::kTile), &tmK, bar, 0, (j0 + i) * kBlk, bkv);
+      else tma_load_3d(smem_u32(dsm + slot * SM::kTile), &tmV, bar, 0, (j0 + i - nb) * kBlk, bkv);
+    };
+    if (threadIdx.x == 0) {
+      const uint32_t bar = smem_u32(&qbar);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(R * D));
+      // rows r = g * Nq + i of the head are contiguous: heads hkv*G .. hkv*G+G-1
+      bulk_g2s(smem_u32(qs), a.q_codes + (static_cast<size_t>(b) * a.Hq + hkv * G) * a.Nq * D,
+               static_cast<uint32_t>(R * D), bar);
     }
-  }
-  __syncthreads();
-  if (!mbar_wait(smem_u32(&tbar), 0, &abort_flag, a.err, kErrTimeout)) return;
-  // P8 = e4m3(448 P), P = 2^(t - m_j) relative to the block's running max,
-  // written in fragment order; the block's sum of 448 P (unquantized).  One
-  // warp per row; lane = key within a 32-key step.
-  {
-    const int f = (lane & 1) ? (16 + 4 * ((lane >> 1) & 3) + (lane >> 3))
-                             : (4 * ((lane >> 1) & 3) + (lane >> 3));
-    for (int r = warp; r < R; r += kPvThreads / 32) {
-      const float* tr = tb + r * CK;
-      for (int jj = 0; jj < nb; ++jj) {
-        const float mj = mrun[jj][r];
-        const float kneg = (mj == kNegInf) ? 0.f : (kLog2_448 - mj);
-        float sum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float p = ex2_approx(__fadd_rn(tr[jj * kBlk + 32 * q + lane], kneg));
-          sum += p;
-          p8[((jj * 4 + q) * RMAX + r) * 32 + f] = static_cast<uint8_t>(cvt_e4m3x2(p, 0.f) & 0xFFu);
-        }
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-        if (lane == 0) lblk[jj][r] = sum;
-      }
+    // score factors c = fp32(fp32(fp32(sq * sk) * sm_scale) * log2 e) and 448 / amax
+    // (their loads go out ahead of the tiles)
+    for (int idx = threadIdx.x; idx < nb * R; idx += kThreads) {
+      const int i = idx / R, r = idx % R, g = r / a.Nq, ii = r % a.Nq;
+      const float sq = scale_at(a.q_scales, a.q_gran, b * a.Hq + hkv * G + g, nqb, ii / kBlk);
+      const float sk = scale_at(a.k_scales, a.k_gran, bkv, nkb, j0 + i);
+      cf[i][r] = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), a.sm_scale), kLog2e);
     }
-  }
-  __syncthreads();
-  float acc[NT][4];
+    for (int cc = threadIdx.x; cc < D; cc += kThreads) {
+      const float am = __ldg(a.v_code_amax + static_cast<size_t>(bkv) * D + cc);
+      inv_s[cc] = (am > 0.f) ? __fdiv_rn(448.0f, am) : 0.f;
+    }
+    if (threadIdx.x == 0)
+      for (int i = 0; i < min(kStages, items); ++i) issue(i);
+    __syncthreads();
+    if (!mbar_wait(smem_u32(&qbar), nu & 1, &abort_flag, a.err, kErrTimeout)) return;
+    // ---- scores of the chunk's blocks
+    const int k = threadIdx.x;
+    for (int i = 0; i < nb; ++i) {
+      const uint32_t q = q0 + i;
+      if (!mbar_wait(smem_u32(&full[q % kStages]), (q / kStages) & 1, &abort_flag, a.err,
+                     kErrTimeout))
+        return;
+      const int8_t* ks = reinterpret_cast<const int8_t*>(dsm + (q % kStages) * SM::kTile);
+      int acc[RMAX];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  const bool row_lo = g < R, row_hi = (RMAX > 8) && (g + 8 < R);
-  for (int jj = 0; jj < nb; ++jj) {
-    const int s = jj % kPvStages;
-    if (!mbar_wait(smem_u32(&full[s]), (jj / kPvStages) & 1, &abort_flag, a.err, kErrTimeout))
-      return;
-    if (jj > 0) {  // rescale to this block's running max (skipped while it holds)
-      const float f0 =
-          (row_lo && mrun[jj][g] != kNegInf) ? ex2_approx(mrun[jj - 1][g] - mrun[jj][g]) : 1.f;
-      const float f1 = (row_hi && mrun[jj][g + 8] != kNegInf)
-                           ? ex2_approx(mrun[jj - 1][g + 8] - mrun[jj][g + 8])
-                           : 1.f;
-      if (!__all_sync(0xffffffffu, f0 == 1.f && f1 == 1.f)) {
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0;
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          acc[n][0] *= f0;
-          acc[n][1] *= f0;
-          acc[n][2] *= f1;
-          acc[n][3] *= f1;
+      for (int cc = 0; cc < NC; ++cc) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(ks + swz_chunk<D>(k, cc));
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            const uint4 qw = *reinterpret_cast<const uint4*>(qs + r * D + cc * 16);
+            acc[r] = __dp4a(static_cast<int>(kw.x), static_cast<int>(qw.x), acc[r]);
+            acc[r] = __dp4a(static_cast<int>(kw.y), static_cast<int>(qw.y), acc[r]);
+            acc[r] = __dp4a(static_cast<int>(kw.z), static_cast<int>(qw.z), acc[r]);
+            acc[r] = __dp4a(static_cast<int>(kw.w), static_cast<int>(qw.w), acc[r]);
+          }
         }
       }
+      const int key = (j0 + i) * kBlk + k;
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        if (r < R) {
+          const int ii = r % a.Nq;
+          const bool vis = key < a.Nk && (!a.causal || key <= a.pos0 + ii);
+          const float t = vis ? __fmul_rn(static_cast<float>(acc[r]), cf[i][r]) : kNegInf;
+          tb[r * CK + i * kBlk + k] = t;
+          float mx = t;
+#pragma unroll
+          for (int sh = 16; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+          if (lane == 0) wmax[i & 1][warp][r] = mx;
+        }
+      }
+      __syncthreads();  // the tile is read; the block's warp maxima are in
+      if (threadIdx.x == 0 && i + kStages < items) issue(i + kStages);
+      if (threadIdx.x < R) {
+        const int r = threadIdx.x;
+        bmax[i][r] = fmaxf(fmaxf(wmax[i & 1][0][r], wmax[i & 1][1][r]),
+                           fmaxf(wmax[i & 1][2][r], wmax[i & 1][3][r]));
+      }
     }
-    // A fragments: P8 rows g, g + 8 of this warp's 32-key step
-    const uint8_t* pa = p8 + ((jj * 4 + warp) * RMAX) * 32;
-    const uint32_t a0 = row_lo ? *reinterpret_cast<const uint32_t*>(pa + g * 32 + 4 * t4) : 0u;
-    const uint32_t a2 = row_lo ? *reinterpret_cast<const uint32_t*>(pa + g * 32 + 16 + 4 * t4) : 0u;
-    const uint32_t a1 =
-        row_hi ? *reinterpret_cast<const uint32_t*>(pa + (g + 8) * 32 + 4 * t4) : 0u;
-    const uint32_t a3 =
-        row_hi ? *reinterpret_cast<const uint32_t*>(pa + (g + 8) * 32 + 16 + 4 * t4) : 0u;
-    // this lane's channels of its 8 keys: key 8i + 2t4 (+1 for h = 1) of the step
-    const uint8_t* vs = dsm + s * SM::kStage;
-    uint32_t raw[8][WPT];
+    __syncthreads();
+    // ---- publish the chunk's maxima, then look back at the earlier chunks'
+    const size_t rec0 = static_cast<size_t>(bkv) * a.nch;
+    if (threadIdx.x < R) {
+      const int r = threadIdx.x;
+      float m = kNegInf;
+      for (int i = 0; i < nb; ++i) m = fmaxf(m, bmax[i][r]);
+      st_relaxed_u64(a.rec + (rec0 + c) * R + r,
+                     (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(m));
+    }
+    // warps 1-3 poll: thread 32 + p * R + r reads row r of chunks p, p + pt, ...
+    const int pt = (kThreads - 32) / R;
+    const int pi = static_cast<int>(threadIdx.x) - 32;
+    float mb = kNegInf;
+    if (pi >= 0 && pi < pt * R) {
+      const int r = pi % R;
+      for (int cp = pi / R; cp < c; cp += pt) {
+        float v;
+        if (!wait_record(a.rec + (rec0 + cp) * R + r, tag, v, &abort_flag, a.err)) break;
+        mb = fmaxf(mb, v);
+      }
+    }
+    mpoll[threadIdx.x] = mb;
+    __syncthreads();
+    if (abort_flag) return;  // a look-back wait ran out (every thread sees it here)
+    if (threadIdx.x < R) {
+      const int r = threadIdx.x;
+      float m = kNegInf;
+      for (int p = 0; p < pt; ++p) m = fmaxf(m, mpoll[32 + p * R + r]);
+      for (int i = 0; i < nb; ++i) {
+        m = fmaxf(m, bmax[i][r]);
+        mrun[i][r] = m;
+      }
+    }
+    __syncthreads();
+    // ---- P8 = e4m3(448 P), P = 2^(t - m_j), in fragment order; the block's
+    // sum of 448 P (unquantized).  One warp per row; lane = key within a step.
+    {
+      const int f = (lane & 1) ? (16 + 4 * ((lane >> 1) & 3) + (lane >> 3))
+                               : (4 * ((lane >> 1) & 3) + (lane >> 3));
+      for (int r = warp; r < R; r += kThreads / 32) {
+        const float* tr = tb + r * CK;
+        for (int i = 0; i < nb; ++i) {
+          const float mj = mrun[i][r];
+          const float kneg = (mj == kNegInf) ? 0.f : (kLog2_448 - mj);
+          float sum = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+          for (int st = 0; st < 4; ++st) {
+            const float p = ex2_approx(__fadd_rn(tr[i * kBlk + 32 * st + lane], kneg));
+            sum += p;
+            p8[((i * 4 + st) * RMAX + r) * 32 + f] = static_cast<uint8_t>(cvt_e4m3x2(p, 0.f) & 0xFFu);
+          }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = 32 * warp + 8 * i + 2 * t4 + h;
-        const uint8_t* src = vs + swz_chunk<D>(row, (CPT * g) >> 4) + ((CPT * g) & 15);
-        if constexpr (WPT == 4) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
-          raw[4 * h + i][0] = v.x;
-          raw[4 * h + i][1] = v.y;
-          raw[4 * h + i][2] = v.z;
-          raw[4 * h + i][3] = v.w;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          raw[4 * h + i][0] = v.x;
-          raw[4 * h + i][1] = v.y;
+          for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+          if (lane == 0) lblk[i][r] = sum;
         }
       }
     }
+    __syncthreads();
+    // ---- PV on the V tiles
+    const int g = lane >> 2, t4 = lane & 3;
+    const bool row_lo = g < R, row_hi = (RMAX > 8) && (g + 8 < R);
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int i = 0; i < nb; ++i) {
+      const uint32_t q = q0 + nb + i;
+      if (!mbar_wait(smem_u32(&full[q % kStages]), (q / kStages) & 1, &abort_flag, a.err,
+                     kErrTimeout))
+        return;
+      if (i > 0) {  // rescale to this block's running max (skipped while it holds)
+        const float f0 =
+            (row_lo && mrun[i][g] != kNegInf) ? ex2_approx(mrun[i - 1][g] - mrun[i][g]) : 1.f;
+        const float f1 = (row_hi && mrun[i][g + 8] != kNegInf)
+                             ? ex2_approx(mrun[i - 1][g + 8] - mrun[i][g + 8])
+                             : 1.f;
+        if (!__all_sync(0xffffffffu, f0 == 1.f && f1 == 1.f)) {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[n][0] *= f0;
+            acc[n][1] *= f0;
+            acc[n][2] *= f1;
+            acc[n][3] *= f1;
+          }
+        }
+      }
+      const uint8_t* pa = p8 + ((i * 4 + warp) * RMAX) * 32;
+      const uint32_t a0 = row_lo ? *reinterpret_cast<const uint32_t*>(pa + g * 32 + 4 * t4) : 0u;
+      const uint32_t a2 = row_lo ? *reinterpret_cast<const uint32_t*>(pa + g * 32 + 16 + 4 * t4) : 0u;
+      const uint32_t a1 =
+          row_hi ? *reinterpret_cast<const uint32_t*>(pa + (g + 8) * 32 + 4 * t4) : 0u;
+      const uint32_t a3 =
+          row_hi ? *reinterpret_cast<const uint32_t*>(pa + (g + 8) * 32 + 16 + 4 * t4) : 0u;
+      const uint8_t* vs = dsm + (q % kStages) * SM::kTile;
+      uint32_t raw[8][WPT];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          const int row = 32 * warp + 8 * ii + 2 * t4 + h;
+          const uint8_t* src = vs + swz_chunk<D>(row, (CPT * g) >> 4) + ((CPT * g) & 15);
+          if constexpr (WPT == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src);
+            raw[4 * h + ii][0] = v.x;
+            raw[4 * h + ii][1] = v.y;
+            raw[4 * h + ii][2] = v.z;
+            raw[4 * h + ii][3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            raw[4 * h + ii][0] = v.x;
+            raw[4 * h + ii][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < WPT; ++w) {
+        const float4 iv = *reinterpret_cast<const float4*>(inv_s + CPT * g + 4 * w);
+        uint32_t e0[4], e1[4], b0[4], b1[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          e0[ii] = v_codes_to_e4m3(raw[ii][w], iv);
+          e1[ii] = v_codes_to_e4m3(raw[4 + ii][w], iv);
+        }
+        transpose4x4(e0, b0);
+        transpose4x4(e1, b1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mma_e4m3_16832(acc[4 * w + e], a0, a1, a2, a3, b0[e], b1[e]);
+      }
+      __syncthreads();  // the tile is read
+      if (threadIdx.x == 0 && nb + i + kStages < items) issue(nb + i + kStages);
+    }
+    q0 += items;
+    // ---- reduce the four warps' shares; write the chunk's O share, l and m
 #pragma unroll
     for (int w = 0; w < WPT; ++w) {
-      const float4 iv = *reinterpret_cast<const float4*>(inv_s + CPT * g + 4 * w);
-      uint32_t e0[4], e1[4], b0[4], b1[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        e0[i] = v_codes_to_e4m3(raw[i][w], iv);
-        e1[i] = v_codes_to_e4m3(raw[4 + i][w], iv);
-      }
-      transpose4x4(e0, b0);
-      transpose4x4(e1, b1);
+      for (int e = 0; e < 4; ++e) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) mma_e4m3_16832(acc[4 * w + e], a0, a1, a2, a3, b0[e], b1[e]);
-    }
-    __syncthreads();  // stage s is read
-    if (threadIdx.x == 0 && jj + kPvStages < nb) issue_v(jj + kPvStages);
-  }
-  // reduce the four warps' shares; write the chunk's O share
-#pragma unroll
-  for (int w = 0; w < WPT; ++w) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = CPT * (2 * t4 + cc) + 4 * w + e;
-        if (row_lo) red[(warp * RMAX + g) * D + c] = acc[4 * w + e][cc];
-        if (row_hi) red[(warp * RMAX + g + 8) * D + c] = acc[4 * w + e][2 + cc];
+        for (int cc = 0; cc < 2; ++cc) {
+          const int ch = CPT * (2 * t4 + cc) + 4 * w + e;
+          if (row_lo) red[(warp * RMAX + g) * D + ch] = acc[4 * w + e][cc];
+          if (row_hi) red[(warp * RMAX + g + 8) * D + ch] = acc[4 * w + e][2 + cc];
+        }
       }
     }
-  }
-  __syncthreads();
-  const size_t pbase = (static_cast<size_t>(bkv) * gridDim.x + ch) * R;
-  for (int idx = threadIdx.x; idx < R * D; idx += kPvThreads) {
-    const int r = idx / D, c = idx % D;
-    float sum = 0.f;
+    __syncthreads();
+    const size_t pbase = (rec0 + c) * R;
+    for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+      const int r = idx / D, ch = idx % D;
+      float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPvThreads / 32; ++w) sum += red[(w * RMAX + r) * D + c];
-    a.part_o[(pbase + r) * D + c] = sum;
+      for (int w = 0; w < kThreads / 32; ++w) sum += red[(w * RMAX + r) * D + ch];
+      a.part_o[(pbase + r) * D + ch] = sum;
+    }
+    if (threadIdx.x < R) {
+      const int r = threadIdx.x;
+      const float mend = mrun[nb - 1][r];
+      float l = 0.f;
+      if (mend != kNegInf)
+        for (int i = 0; i < nb; ++i) l += lblk[i][r] * ex2_approx(mrun[i][r] - mend);
+      a.part_l[pbase + r] = l;
+      a.part_m[pbase + r] = mend;
+    }
+    // the next unit only now: taken earlier, a fast CTA would take units from
+    // CTAs that have not started their first one yet.  With no more units
+    // than CTAs, the first takes got them all.
+    if (threadIdx.x == 0) unit_s = (units > static_cast<int>(gridDim.x)) ? take() : units;
+    __syncthreads();  // red (the ring) and the unit's shared state are free again
+    u = unit_s;
   }
-  if (threadIdx.x < R) {
-    const int r = threadIdx.x;
-    const float mend = mrun[nb - 1][r];
-    float l = 0.f;
-    if (mend != kNegInf)
-      for (int jj = 0; jj < nb; ++jj) l += lblk[jj][r] * ex2_approx(mrun[jj][r] - mend);
-    a.part_l[pbase + r] = l;
-    a.part_m[pbase + r] = mend;
-  }
+  pdl_trigger();  // after every wait of this CTA: the combine pass may take the SM
 }
 
-// ------------------------------------------------------------------ pass 3
+// ------------------------------------------------------------------ combine
 // One CTA per (row, batch * KV head).  Thread (chunk group cg, channel word
-// c4) sums chunks cg, cg + CG, ... scaled to the final max.
+// c4) loads chunks cg, cg + CG, ... (their m, l and O slice in one batch),
+// then scales them to the final max and the groups are summed.
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeArgs a,
                                                                         int nchunks) {
   constexpr int TPC = D / 4;                 // threads per chunk row
   constexpr int CG = kCombineThreads / TPC;  // chunk groups
-  constexpr int U = 4;                       // chunks in flight per thread
+  constexpr int U = 8;                       // chunks per thread in one batch
   __shared__ float wm[kCombineThreads / 32];
   __shared__ __align__(16) float red[CG][D];
   __shared__ float redl[CG];
-  pdl_wait();
-  pdl_trigger();
   const int r = blockIdx.x, bkv = blockIdx.y;
   const int b = bkv / a.Hkv, hkv = bkv % a.Hkv;
   const int G = a.Hq / a.Hkv, R = G * a.Nq;
+  // V scale s_v = fp32(fp32(chan * amax) / 448), as qattn_quantize_v writes it; the
+  // cache header precedes this call and the scores/PV pass released this grid
+  // only after all its waits, so it is read before the dependency wait
+  float sv = 0.f;
+  if (threadIdx.x < D) {
+    const size_t vc = static_cast<size_t>(bkv) * D + threadIdx.x;
+    sv = __fdiv_rn(__fmul_rn(__ldg(a.v_chan_scale + vc), __ldg(a.v_code_amax + vc)), 448.0f);
+  }
+  pdl_wait();
+  pdl_trigger();
   const size_t p0 = static_cast<size_t>(bkv) * nchunks * R + r;  // chunk c: p0 + c * R
-  float mf = kNegInf;
-  for (int c = threadIdx.x; c < nchunks; c += kCombineThreads)
-    mf = fmaxf(mf, a.part_m[p0 + static_cast<size_t>(c) * R]);
-#pragma unroll
-  for (int sh = 16; sh > 0; sh >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, sh));
-  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = mf;
-  __syncthreads();
-  mf = wm[0];
-#pragma unroll
-  for (int w = 1; w < kCombineThreads / 32; ++w) mf = fmaxf(mf, wm[w]);
   const int c4 = threadIdx.x % TPC, cg = threadIdx.x / TPC;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.f;
-  if (mf != kNegInf) {
-    for (int cb = cg; cb < nchunks; cb += U * CG) {
-      float mc[U], lc[U];
-      float4 oc[U];
+  float l = 0.f, mf = kNegInf;
+  for (int cb = cg; cb < nchunks; cb += U * CG) {
+    float mc[U], lc[U];
+    float4 oc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = cb + u * CG;
+      const size_t pi = p0 + static_cast<size_t>(c) * R;
+      const bool in = c < nchunks;
+      mc[u] = in ? a.part_m[pi] : kNegInf;
+      lc[u] = in ? a.part_l[pi] : 0.f;
+      oc[u] = in ? *reinterpret_cast<const float4*>(a.part_o + pi * D + 4 * c4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // the batch's max, then everything so far rescaled to it (online, in the
+    // order of the recipe's combination: weights 2^(m_c - m_final))
+    float mx = mf;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mx = fmaxf(mx, mc[u]);
+    if (mx != kNegInf) {
+      const float f = (mf == kNegInf) ? 0.f : ex2_approx(mf - mx);
+      l *= f;
+      o.x *= f;
+      o.y *= f;
+      o.z *= f;
+      o.w *= f;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int c = cb + u * CG;
-        const size_t pi = p0 + static_cast<size_t>(c) * R;
-        const bool in = c < nchunks;
-        mc[u] = in ? a.part_m[pi] : kNegInf;
-        lc[u] = in ? a.part_l[pi] : 0.f;
-        oc[u] = in ? *reinterpret_cast<const float4*>(a.part_o + pi * D + 4 * c4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float wgt = (mc[u] == kNegInf) ? 0.f : ex2_approx(mc[u] - mf);
+        const float wgt = (mc[u] == kNegInf) ? 0.f : ex2_approx(mc[u] - mx);
         l = fmaf(wgt, lc[u], l);
         o.x = fmaf(wgt, oc[u].x, o.x);
         o.y = fmaf(wgt, oc[u].y, o.y);
         o.z = fmaf(wgt, oc[u].z, o.z);
         o.w = fmaf(wgt, oc[u].w, o.w);
       }
+      mf = mx;
     }
   }
-  *reinterpret_cast<float4*>(&red[cg][4 * c4]) = o;
-  if (c4 == 0) redl[cg] = l;
+  // the groups' maxima -> the final max; each group's sums rescaled to it
+  float gm = mf;
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, sh));
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = gm;
+  __syncthreads();
+  float mfin = wm[0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) mfin = fmaxf(mfin, wm[w]);
+  const float f = (mf == kNegInf) ? 0.f : ex2_approx(mf - mfin);
+  *reinterpret_cast<float4*>(&red[cg][4 * c4]) = make_float4(o.x * f, o.y * f, o.z * f, o.w * f);
+  if (c4 == 0) redl[cg] = l * f;
   __syncthreads();
   const int g = r / a.Nq, i = r % a.Nq;
   const size_t row = (static_cast<size_t>(b) * a.Hq + hkv * G + g) * a.Nq + i;
   float lt = 0.f;
 #pragma unroll
   for (int g2 = 0; g2 < CG; ++g2) lt += redl[g2];
-  for (int c = threadIdx.x; c < D; c += kCombineThreads) {
+  if (threadIdx.x < D) {
+    const int c = threadIdx.x;
     float s = 0.f;
 #pragma unroll
     for (int g2 = 0; g2 < CG; ++g2) s += red[g2][c];
-    // V scale s_v = fp32(fp32(chan * amax) / 448), as qattn_quantize_v writes it
-    const size_t vc = static_cast<size_t>(bkv) * D + c;
-    const float sv = __fdiv_rn(__fmul_rn(__ldg(a.v_chan_scale + vc), __ldg(a.v_code_amax + vc)), 448.0f);
     const float out = (lt > 0.f) ? s * (sv * (1.f / lt)) : 0.f;
     if (a.out_bf16) reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + c] = __float2bfloat16(out);
     else reinterpret_cast<float*>(a.out)[row * D + c] = out;
   }
   if (threadIdx.x == 0 && a.lse)
-    a.lse[row] = (lt > 0.f) ? (mf + __log2f(lt) - kLog2_448) * kLn2 : kNegInf;
+    a.lse[row] = (lt > 0.f) ? (mfin + __log2f(lt) - kLog2_448) * kLn2 : kNegInf;
 }
 
 // CTAs of a kernel resident per SM.  Callers cache it: it depends only on the
-// kernel and the device model, and a wrong value changes the grid, not results.
+// kernel and the device model.
 template <typename Kernel>
 int ctas_per_sm(Kernel kernel, int threads, int smem) {
   int n = 0;
@@ -550,53 +593,45 @@ int ctas_per_sm(Kernel kernel, int threads, int smem) {
 }
 
 template <int D, int RMAX>
-cudaError_t launch_decode_r(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+cudaError_t launch_decode_r(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a,
                             cudaStream_t s) {
+  using SM = FusedSmem<D, RMAX>;
   const int BHkv = a.B * a.Hkv;
   const int nkb = (a.Nk + kBlk - 1) / kBlk;
-  const int sms = num_sms();
   const int total = nkb * BHkv;
-  // pass 1: a persistent grid filling every SM
-  constexpr int ssmem = ScoreSmem<D, RMAX>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_scores_kernel<D, RMAX>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<D, RMAX>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (e != cudaSuccess) return e;
-  static const int occ1 = ctas_per_sm(decode_scores_kernel<D, RMAX>, kBlk, ssmem);
-  const int g1 = min(total, sms * occ1);
-  e = launch_pdl(decode_scores_kernel<D, RMAX>, dim3(g1), dim3(kBlk), ssmem, s, tk, a);
-  if (e != cudaSuccess) return e;
-  // pass 2: chunks sized so every resident CTA slot gets one
-  using PS = PvSmem<D, RMAX>;
-  e = cudaFuncSetAttribute(decode_pv_kernel<D, RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PS::kBytes);
-  if (e != cudaSuccess) return e;
-  static const int occ2 = ctas_per_sm(decode_pv_kernel<D, RMAX>, kPvThreads, PS::kBytes);
-  const int target = sms * occ2;
-  const int bpc = max(1, min(PS::kMaxBlocks, (total + target - 1) / target));
-  const int nchunks = (nkb + bpc - 1) / bpc;
-  e = launch_pdl(decode_pv_kernel<D, RMAX>, dim3(nchunks, BHkv), dim3(kPvThreads), PS::kBytes, s,
-                 tv, a, bpc);
+  static const int occ = ctas_per_sm(decode_fused_kernel<D, RMAX>, kThreads, SM::kBytes);
+  const int slots = num_sms() * occ;
+  // chunks of about total / slots blocks (at most kMaxBlocks), one per resident CTA
+  a.bpc = max(1, min(SM::kMaxBlocks, (total + slots - 1) / slots));
+  a.nch = (nkb + a.bpc - 1) / a.bpc;
+  const int units = a.nch * BHkv;
+  e = launch_pdl(decode_fused_kernel<D, RMAX>, dim3(min(units, slots)), dim3(kThreads),
+                 SM::kBytes, s, tk, tv, a);
   if (e != cudaSuccess) return e;
   const int R = (a.Hq / a.Hkv) * a.Nq;
   return launch_pdl(decode_combine_kernel<D>, dim3(R, BHkv), dim3(kCombineThreads), 0, s, a,
-                    nchunks);
+                    a.nch);
 }
 
 }  // namespace
 
-// Workspace: t [B*Hkv][R][nkb*128], block maxima [B*Hkv][nkb][R], and the
-// chunk shares O [B*Hkv][chunks][R][d], l and m [B*Hkv][chunks][R], sized for
-// the most chunks (one block each) so the layout does not depend on the GPU.
+// Workspace, sized for the most chunks (one block each) so the layout does not
+// depend on the GPU: the unit counter (64-bit), chunk shares O
+// [B*Hkv][chunks][R][d], their l and m [B*Hkv][chunks][R], and the tagged
+// chunk maxima [B*Hkv][chunks][R] (64-bit).
 size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
                        long long d) {
   const long long R = (Hq / Hkv) * Nq;
   const long long nkb = (Nk + kBlk - 1) / kBlk;
   const long long BH = B * Hkv;
   auto a256 = [](long long x) { return static_cast<size_t>((x + 255) / 256 * 256); };
-  return a256(BH * R * nkb * kBlk * 4) +  // t
-         a256(BH * nkb * R * 4) +          // block maxima
-         a256(BH * nkb * R * d * 4) +      // chunk O
-         2 * a256(BH * nkb * R * 4);       // chunk l, m
+  return a256(8) +                     // unit counter
+         a256(BH * nkb * R * d * 4) +  // chunk O
+         2 * a256(BH * nkb * R * 4) +  // chunk l, m
+         a256(BH * nkb * R * 8);       // chunk maxima records
 }
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, void* ws,
@@ -606,15 +641,15 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, DecodeAr
   const long long BH = static_cast<long long>(a.B) * a.Hkv;
   auto a256 = [](long long x) { return static_cast<size_t>((x + 255) / 256 * 256); };
   char* p = static_cast<char*>(ws);
-  a.t = reinterpret_cast<float*>(p);
-  p += a256(BH * R * nkb * kBlk * 4);
-  a.mblk = reinterpret_cast<float*>(p);
-  p += a256(BH * nkb * R * 4);
+  a.ctr = reinterpret_cast<unsigned long long*>(p);
+  p += a256(8);
   a.part_o = reinterpret_cast<float*>(p);
   p += a256(BH * nkb * R * a.d * 4);
   a.part_l = reinterpret_cast<float*>(p);
   p += a256(BH * nkb * R * 4);
   a.part_m = reinterpret_cast<float*>(p);
+  p += a256(BH * nkb * R * 4);
+  a.rec = reinterpret_cast<unsigned long long*>(p);
   if (R <= 4)
     return a.d == 64 ? launch_decode_r<64, 4>(tk, tv, a, s) : launch_decode_r<128, 4>(tk, tv, a, s);
   return a.d == 64 ? launch_decode_r<64, kMaxDecodeRows>(tk, tv, a, s)

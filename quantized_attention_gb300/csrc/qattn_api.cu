@@ -4,7 +4,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <random>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -22,6 +24,20 @@ __device__ unsigned int g_qattn_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+// Tags of qattn_decode calls: a per-call count XOR a random per-process salt
+// marks the chunk records and the unit counter a call writes in its workspace,
+// so neither needs clearing between calls (stale contents carry another tag;
+// the salt keeps zeros or small integers left in the memory from matching).
+std::atomic<uint32_t> g_decode_count{0};
+const uint32_t g_decode_salt = static_cast<uint32_t>(std::random_device{}());
+
+uint32_t next_decode_tag() {
+  for (;;) {
+    const uint32_t t = (g_decode_count.fetch_add(1) + 1u) ^ g_decode_salt;
+    if (t != 0u && t != 0xFFFFFFFFu) return t;
+  }
+}
 
 unsigned int* error_word() {
   int dev = 0;
@@ -392,6 +408,7 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
   if (!err) return QATTN_ERR_CUDA;
   qattn::DecodeArgs a{};
   a.err = err;
+  a.epoch = next_decode_tag();
   a.B = static_cast<int>(shape->B);
   a.Hq = static_cast<int>(shape->Hq);
   a.Hkv = static_cast<int>(shape->Hkv);

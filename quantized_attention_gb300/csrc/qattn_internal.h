@@ -107,12 +107,15 @@ struct DecodeArgs {
   void* out;
   int out_bf16;
   float* lse;
-  // workspace regions, set by launch_decode
-  float* t;
-  float* mblk;
-  float* part_o;
-  float* part_l;
-  float* part_m;
+  // set by launch_decode: the split and the workspace regions
+  int bpc;                        // key blocks per chunk
+  int nch;                        // chunks per (batch, KV head)
+  unsigned long long epoch;       // this call's tag (low 32 bits), unique per call
+  unsigned long long* ctr;        // unit counter: (tag << 32) | units taken
+  float* part_o;                  // [B*Hkv][nch][R][d]  chunk shares of O
+  float* part_l;                  // [B*Hkv][nch][R]     their l
+  float* part_m;                  // [B*Hkv][nch][R]     their running max
+  unsigned long long* rec;        // [B*Hkv][nch][R]     chunk maxima: (tag << 32) | bits
   unsigned int* err;  // device error word (a bounded wait that ran out)
 };
 size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,

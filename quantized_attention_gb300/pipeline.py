@@ -105,8 +105,8 @@ class Problem:
 
     def decode_launches(self) -> int:
         """Kernels one quantize_q + decode launches: Q codes (two passes for a
-        tensor/head granule), K scales set to 1, then the decode's three."""
-        return 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 3
+        tensor/head granule), K scales set to 1, then the decode's two."""
+        return 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 2
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
             V_scale=None, bias=None, stream=None):

@@ -110,3 +110,39 @@ def test_decode_same_as_prefill_kernel():
     torch.cuda.synchronize()
     a, b = Pd.O.cpu().numpy(), P.O.cpu().numpy()
     assert np.abs(a - b).max() <= 2e-3 * np.abs(b).max()
+
+
+def test_decode_ignores_workspace_contents():
+    """The chunk records and the unit counter carry a per-call tag, so the
+    workspace needs no clearing: zeros, 0xFF bytes, random bytes or a previous
+    call's records for another shape give bit-identical outputs."""
+    wl = I.small("chunk32k", Hq=8, Hkv=2, Nq=2, Nk=5000, q_pos0=None)
+    inp = I.make_inputs(wl)
+    P = problem_for(wl, want_lse=True)
+    dev = device_inputs(inp)
+    P.quantize(**dev)
+    amax = dev["V_codes"].to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+    n = max(qb.workspace_size(P.shape, P.params), 256)
+
+    def run(ws):
+        qb.decode(P.q_codes, P.q_scales, dev["K_codes"], P.k_scales, dev["V_codes"],
+                  dev["V_scale"], amax, P.shape, P.params, P.O, P.lse, ws)
+        torch.cuda.synchronize()
+        assert qb.get_error() == 0
+        return P.O.clone(), P.lse.clone()
+
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    fills = [torch.zeros(n, dtype=torch.uint8, device="cuda"),
+             torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda"),
+             torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=gen)]
+    o0, l0 = run(fills[0])
+    for ws in fills[1:]:
+        o, l = run(ws)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    # the same workspace after a decode of another shape, then twice in a row
+    other = I.small("chunk32k", Hq=4, Hkv=1, Nq=4, Nk=3000, q_pos0=None)
+    run_decode(other, I.make_inputs(other))  # its own workspace; then reuse ours below
+    ws = fills[2]
+    for _ in range(2):
+        o, l = run(ws)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
