@@ -372,11 +372,15 @@ def gpu_arm(args):
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     if decode:  # memory-bound: the cache's bytes over the decode call's time
         gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
+        ref_us = _stream_ref_us(dev["K_codes"], dev["V_codes"], flush, stream)
         roofline = {"bound": "hbm", "kernel": "qattn_decode (2 launches: fused scores + PV over key chunks, chunk combine)",
                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"],
                     "peak_basis": f"{peaks['source']} HBM copy rate",
-                    "algorithmic_bytes": cache_bytes, "traffic": None}
+                    "algorithmic_bytes": cache_bytes, "traffic": None,
+                    "stream_ref": {"op": "torch.sum over one buffer holding the cache's bytes (as fp32), "
+                                         "same L2 flush before each launch",
+                                   "us": ref_us, "GB/s": cache_bytes / (ref_us * 1e-6) / 1e9}}
     cpu = None
     if not args.no_cpu_baseline:
         c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
@@ -397,6 +401,26 @@ def gpu_arm(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _stream_ref_us(k_codes, v_codes, flush, stream, reps=20):
+    """Device time of one library streaming read (torch.sum over the bytes
+    viewed as fp32, its vectorized reduction) of a buffer with the cache's
+    bytes, after the same L2 flush as the timed steps: what a plain read of
+    these bytes costs at this size, launch and ramp included."""
+    import torch
+    buf = torch.cat([k_codes.reshape(-1), v_codes.reshape(-1)])
+    evs = []
+    for i in range(reps + 3):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        buf.view(torch.float32).sum()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs[3:]]
+    return sum(ms) / len(ms) * 1e3
 
 
 def main():
