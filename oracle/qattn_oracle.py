@@ -538,6 +538,46 @@ INT8_ZERO_THRESHOLD = 0.5 / QMAX
 MASS_DECADE_EDGES = (1e-4, 1e-3, 1e-2, 1e-1)
 
 
+def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax,
+              k_codes, v_codes):
+    """Append T tokens to an int8 KV cache whose header keeps a running channel
+    mean of K ([ZINC-ATTN] "K's outliers, and the subtraction softmax does not
+    notice": during decode K arrives one token at a time, the cache header
+    keeps a running channel mean, and the mean lags by one token).
+
+    For token t at cache position n = pos + t, per (batch, KV head, channel):
+        k_code = clip(rint(fp32(fp32(K - mu) / s_k)), -127, 127)  (mu of the n earlier tokens)
+        mu     = fp32(mu + fp32(fp32(K - mu) / (n + 1)))          (then the header moves on)
+        v_code = clip(rint(fp32(V / s_v)), -127, 127);  amax = max(amax, |v_code|)
+    Readings (the page gives none of these): the cache's codes use fixed
+    per-channel scales s_k, s_v from its header; codes are x / s rounded half
+    to even; the running mean is the plain fp32 recurrence above.
+
+    K_new, V_new: [B, Hkv, T, d] values (bf16 inputs as float32).  k_mean,
+    v_code_amax, k_chan_scale, v_chan_scale: [B, Hkv, d] float32.  k_codes,
+    v_codes: [B, Hkv, capacity, d] int8.  Returns updated copies
+    (k_mean, v_code_amax, k_codes, v_codes).
+    """
+    K_new = np.asarray(K_new, dtype=np.float32)
+    V_new = np.asarray(V_new, dtype=np.float32)
+    mu = np.array(k_mean, dtype=np.float32, copy=True)
+    amax = np.array(v_code_amax, dtype=np.float32, copy=True)
+    kc = np.array(k_codes, dtype=np.int8, copy=True)
+    vc = np.array(v_codes, dtype=np.int8, copy=True)
+    sk = np.asarray(k_chan_scale, dtype=np.float32)
+    sv = np.asarray(v_chan_scale, dtype=np.float32)
+    T = K_new.shape[2]
+    for t in range(T):
+        n = pos + t
+        diff = (K_new[:, :, t, :] - mu).astype(np.float32)
+        kc[:, :, n, :] = np.clip(np.rint((diff / sk).astype(np.float32)), -127, 127).astype(np.int8)
+        mu = (mu + (diff / np.float32(n + 1)).astype(np.float32)).astype(np.float32)
+        code_v = np.clip(np.rint((V_new[:, :, t, :] / sv).astype(np.float32)), -127, 127)
+        vc[:, :, n, :] = code_v.astype(np.int8)
+        amax = np.maximum(amax, np.abs(code_v).astype(np.float32))
+    return mu, amax, kc, vc
+
+
 def attn_probs_fp64(Q, K, *, causal, q_pos0=None, sm_scale=None, bias=None, heads=None,
                     rows=None):
     """softmax(Q K^T * sm_scale + bias) of the chosen rows, dense, float64.
