@@ -238,7 +238,10 @@ def _config(wl_name):
                         f"d={wl.d} causal={int(wl.causal)} q_pos0={wl.pos0}",
             "granularity": {0: "tensor", 1: "head", 2: "block128"}[wl.q_gran],
             "kv_input": "int8 codes" if wl.kv_codes else "bf16",
-            "output": "bf16", "l2": "flushed (256 MB write) before every timed step"}
+            "output": "bf16", "l2": "flushed (256 MB write) before every timed step",
+            **({"step": "append the new token's K/V to the int8 cache (running K mean), "
+                        "quantize its Q, decode over all Nk cached keys"} if wl.kv_codes and
+               wl_name.startswith("decode") else {})}
 
 
 # ----------------------------------------------------------------------------
@@ -270,12 +273,17 @@ def gpu_arm(args):
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
 
     ops = 4 * wl.d * wl.unmasked_pairs()
-    if decode:  # the int8 cache is device state; a step quantizes the new token and decodes
-        P.set_cache(dev["K_codes"], dev["V_codes"], dev["V_scale"])
+    if decode:  # the int8 cache is device state; a step appends the new token, quantizes its Q, decodes
+        hdr = torch.from_numpy(inp.K_header_mean).to("cuda")
+        P.set_cache(dev["K_codes"], dev["V_codes"], dev["V_scale"], K_scale=dev["K_scale"], K_mean=hdr)
+        k_new, v_new = I.make_append_tokens(inp, 1)
+        dev["K_new"] = torch.from_numpy(k_new).to(device="cuda", dtype=torch.bfloat16)
+        dev["V_new"] = torch.from_numpy(v_new).to(device="cuda", dtype=torch.bfloat16)
         cache_bytes = 2 * wl.B * wl.Hkv * wl.Nk * wl.d  # K and V codes, read once
 
     def step():
         if decode:
+            P.append(dev["K_new"], dev["V_new"], wl.Nk - 1, stream)  # the token at row Nk-1
             P.quantize_q(dev["Q"], dev["K_scale"], stream)
             ev_a.record(stream)
             P.decode(stream)
@@ -322,7 +330,8 @@ def gpu_arm(args):
     value = world * ops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, host buffers, copies timed
-    host = {k: v.cpu().pin_memory() for k, v in dev.items() if not decode or k == "Q"}
+    host = {k: v.cpu().pin_memory() for k, v in dev.items()
+            if not decode or k in ("Q", "K_new", "V_new")}
     out_host = torch.empty(P.O.shape, dtype=P.O.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -331,6 +340,7 @@ def gpu_arm(args):
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
         if decode:
+            P.append(dev["K_new"], dev["V_new"], wl.Nk - 1, stream)
             P.quantize_q(dev["Q"], dev["K_scale"], stream)
             P.decode(stream)
         else:
@@ -395,7 +405,7 @@ def gpu_arm(args):
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (P.decode_launches() if decode else P.kernel_launches()) * args.steps,
+            "gpu_launches": (P.decode_launches(append=True) if decode else P.kernel_launches()) * args.steps,
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -97,6 +97,8 @@ typedef struct {
   float sm_scale;           /* softmax scale; 0 -> fp32(1/sqrt(d))                 */
   int32_t pv_mode;          /* qattn_pv_mode; 0 for the recipe                     */
   int64_t bias_head_stride; /* elements between heads' bias matrices; 0 = shared   */
+  int64_t kv_capacity;      /* qattn_decode: rows per (batch, KV head) in the cache
+                               arrays (>= Nk, the rows in use); 0 = Nk               */
 } qattn_params;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -237,11 +239,12 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
  * scores and row maxima first, then each block's running max as a prefix
  * maximum, the chunks' shares of O and l, and their combination.
  *   q_codes/q_scales  as written by qattn_quantize_qk with k_dtype QATTN_I8
- *   k_codes      int8 [B][Hkv][Nk][d]: the cache's K codes (of the mean-
+ *   k_codes      int8 [B][Hkv][cap][d], cap = params->kv_capacity (or Nk): the
+ *                cache's K codes, rows 0..Nk-1 in use (of the mean-
  *                subtracted K; the mean lives in the cache header, "K's
  *                outliers, and the subtraction softmax does not notice")
  *   k_scales     as written by qattn_quantize_qk (all 1 for I8 K)
- *   v_codes      int8 [B][Hkv][Nk][d]: the cache's V codes
+ *   v_codes      int8 [B][Hkv][cap][d]: the cache's V codes
  *   v_chan_scale fp32 [B][Hkv][d]: scale of each V channel's codes
  *   v_code_amax  fp32 [B][Hkv][d]: max |code| of each V channel over the
  *                cache (the cache header keeps it as tokens arrive)
@@ -255,6 +258,31 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
                           const qattn_shape* shape, const qattn_params* params, void* O,
                           float* lse, void* workspace, size_t workspace_bytes,
                           qattn_stream_t stream);
+
+/* Append T tokens to an int8 KV cache whose header keeps a running channel
+ * mean of K (ZINC post, "K's outliers, and the subtraction softmax does not
+ * notice": during decode K arrives one token at a time and the header keeps a
+ * running mean, which lags by one token).  For token t at position
+ * n = pos + t, per (batch, KV head, channel c), in fp32 with round-to-nearest:
+ *   k_code = clamp(rint((K - mu) / s_k), -127, 127)   (mu of the n earlier tokens)
+ *   mu     = mu + (K - mu) / (n + 1)
+ *   v_code = clamp(rint(V / s_v), -127, 127);  amax = max(amax, |v_code|)
+ *   K_new, V_new  bf16 [B][Hkv][T][d], device
+ *   k_chan_scale, v_chan_scale  fp32 [B][Hkv][d], positive, device (the
+ *                 cache's fixed per-channel scales)
+ *   k_mean, v_code_amax  fp32 [B][Hkv][d], device, read and updated (the
+ *                 header; zeros for an empty cache)
+ *   k_codes, v_codes  int8 [B][Hkv][capacity][d], device; rows pos..pos+T-1
+ *                 are written
+ * Limits: 0 <= pos, pos + T <= capacity <= 2^24, 1 <= d <= 1024,
+ * B * Hkv * d < 2^31.  T = 0 does nothing.  Pointers: non-null; bf16 2-byte
+ * and fp32 4-byte aligned.  Asynchronous on the stream; no workspace.
+ */
+qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,
+                             int64_t T, int64_t d, int64_t pos, int64_t capacity,
+                             const float* k_chan_scale, const float* v_chan_scale,
+                             float* k_mean, float* v_code_amax, int8_t* k_codes,
+                             int8_t* v_codes, qattn_stream_t stream);
 
 /* a4 alone (debug) -- the int32 score tiles S = q_codes . k_codes^T
  * ("QFlash", eq. (3)), through the same tensor-core path as qattn_fwd.

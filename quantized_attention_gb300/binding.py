@@ -25,6 +25,7 @@ EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
+    "qattn_kv_append",
 )
 
 
@@ -43,7 +44,8 @@ class Params(ctypes.Structure):
     _fields_ = [("causal", ctypes.c_int32), ("q_gran", ctypes.c_int32),
                 ("k_gran", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("q_pos0", ctypes.c_int64), ("sm_scale", ctypes.c_float),
-                ("pv_mode", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64)]
+                ("pv_mode", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64),
+                ("kv_capacity", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -75,9 +77,10 @@ def lib() -> ctypes.CDLL:
     L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
     L.qattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
+    L.qattn_kv_append.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-                 "qattn_decode",
+                 "qattn_decode", "qattn_kv_append",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -118,10 +121,11 @@ def make_shape(B, Hq, Hkv, Nq, Nk, d) -> Shape:
 
 
 def make_params(causal=False, q_gran=GRAN_BLOCK, k_gran=GRAN_BLOCK, out_dtype=DT_F32,
-                q_pos0=None, sm_scale=0.0, bias_head_stride=0, pv_mode=PV_E4M3) -> Params:
+                q_pos0=None, sm_scale=0.0, bias_head_stride=0, pv_mode=PV_E4M3,
+                kv_capacity=0) -> Params:
     return Params(int(bool(causal)), q_gran, k_gran, out_dtype,
                   POS0_BOTTOM_RIGHT if q_pos0 is None else int(q_pos0), float(sm_scale),
-                  int(pv_mode), int(bias_head_stride))
+                  int(pv_mode), int(bias_head_stride), int(kv_capacity))
 
 
 def version() -> int:
@@ -201,6 +205,25 @@ def decode(q_codes, q_scales, k_codes, k_scales, v_codes, v_chan_scale, v_code_a
                               ctypes.byref(params), _p(O), _p(lse), _p(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
            "qattn_decode")
+
+
+def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes,
+              v_codes, stream=None):
+    """Append tokens to an int8 KV cache with a running-mean header (see
+    qattn_kv_append in include/qattn.h).  K_new, V_new: bf16 [B, Hkv, T, d];
+    k_codes, v_codes: int8 [B, Hkv, capacity, d]; scales and header fp32 [B, Hkv, d]."""
+    _dense(K_new, torch.bfloat16, "K_new")
+    _dense(V_new, torch.bfloat16, "V_new")
+    _dense(k_codes, torch.int8, "k_codes")
+    _dense(v_codes, torch.int8, "v_codes")
+    for t, nm in ((k_chan_scale, "k_chan_scale"), (v_chan_scale, "v_chan_scale"),
+                  (k_mean, "k_mean"), (v_code_amax, "v_code_amax")):
+        _dense(t, torch.float32, nm)
+    B, H, T, d = K_new.shape
+    _check(lib().qattn_kv_append(_p(K_new), _p(V_new), B, H, T, d, int(pos), k_codes.shape[2],
+                                 _p(k_chan_scale), _p(v_chan_scale), _p(k_mean), _p(v_code_amax),
+                                 _p(k_codes), _p(v_codes), _stream(stream)),
+           "qattn_kv_append")
 
 
 def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):

@@ -581,6 +581,40 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     a.lse[row] = (lt > 0.f) ? (mfin + __log2f(lt) - kLog2_448) * kLn2 : kNegInf;
 }
 
+// ------------------------------------------------------------------ cache append
+// One thread per (batch * KV head, channel), the T new tokens in order: a
+// token's K is quantized against the header's running mean of the tokens
+// before it, then the mean moves (the lag of one token the ZINC post
+// describes); V codes raise the header's max |code|.  All steps are single
+// IEEE fp32 operations, so the result is exact.
+__global__ void kv_append_kernel(const uint16_t* K_new, const uint16_t* V_new, int BHd, int d,
+                                 int T, int pos, long long cap, const float* k_chan_scale,
+                                 const float* v_chan_scale, float* k_mean, float* v_code_amax,
+                                 int8_t* k_codes, int8_t* v_codes) {
+  pdl_trigger();
+  pdl_wait();
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= BHd) return;
+  const int bh = idx / d, c = idx % d;
+  float mu = k_mean[idx], am = v_code_amax[idx];
+  const float sk = k_chan_scale[idx], sv = v_chan_scale[idx];
+  for (int t = 0; t < T; ++t) {
+    const size_t in = (static_cast<size_t>(bh) * T + t) * d + c;
+    const float k = bf16_bits_to_f32(K_new[in]), v = bf16_bits_to_f32(V_new[in]);
+    const int n = pos + t;
+    const float diff = __fsub_rn(k, mu);
+    const float qk = fminf(fmaxf(rintf(__fdiv_rn(diff, sk)), -127.f), 127.f);
+    mu = __fadd_rn(mu, __fdiv_rn(diff, static_cast<float>(n + 1)));
+    const float qv = fminf(fmaxf(rintf(__fdiv_rn(v, sv)), -127.f), 127.f);
+    am = fmaxf(am, fabsf(qv));
+    const size_t out = (static_cast<size_t>(bh) * cap + n) * d + c;
+    k_codes[out] = static_cast<int8_t>(qk);
+    v_codes[out] = static_cast<int8_t>(qv);
+  }
+  k_mean[idx] = mu;
+  v_code_amax[idx] = am;
+}
+
 // CTAs of a kernel resident per SM.  Callers cache it: it depends only on the
 // kernel and the device model.
 template <typename Kernel>
@@ -632,6 +666,15 @@ size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, l
          a256(BH * nkb * R * d * 4) +  // chunk O
          2 * a256(BH * nkb * R * 4) +  // chunk l, m
          a256(BH * nkb * R * 8);       // chunk maxima records
+}
+
+cudaError_t launch_kv_append(const uint16_t* K_new, const uint16_t* V_new, int BH, int d, int T,
+                             int pos, long long cap, const float* k_chan_scale,
+                             const float* v_chan_scale, float* k_mean, float* v_code_amax,
+                             int8_t* k_codes, int8_t* v_codes, cudaStream_t s) {
+  const int n = BH * d;
+  return launch_pdl(kv_append_kernel, dim3((n + 255) / 256), dim3(256), 0, s, K_new, V_new, n, d, T,
+                    pos, cap, k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes, v_codes);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, void* ws,

@@ -96,7 +96,7 @@ qattn_status check_params(const qattn_params* p) {
   if (p->out_dtype != QATTN_F32 && p->out_dtype != QATTN_BF16) return QATTN_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return QATTN_ERR_INVALID_ARG;
   if (p->pv_mode != QATTN_PV_E4M3 && p->pv_mode != QATTN_PV_INT8) return QATTN_ERR_INVALID_ARG;
-  if (p->bias_head_stride < 0) return QATTN_ERR_INVALID_ARG;
+  if (p->bias_head_stride < 0 || p->kv_capacity < 0) return QATTN_ERR_INVALID_ARG;
   if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return QATTN_ERR_INVALID_ARG;
   return QATTN_OK;
 }
@@ -123,11 +123,12 @@ size_t ws_fwd(const qattn_shape* s) { return ws_carriers_k(s); }
 // 3-D tiled map over a dense [planes][rows][inner] tensor.
 bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const void* ptr,
                uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride_bytes,
-               uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+               uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz,
+               uint64_t plane_rows = 0) {  // rows between planes in memory; 0 = rows
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {inner, rows, planes};
-  const cuuint64_t strides[2] = {row_stride_bytes, row_stride_bytes * rows};
+  const cuuint64_t strides[2] = {row_stride_bytes, row_stride_bytes * (plane_rows ? plane_rows : rows)};
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   (void)esize;
@@ -391,6 +392,9 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
   if (empty_problem(shape)) return QATTN_OK;
   if (!decode_shape_ok(shape) || shape->Nk == 0 || params->pv_mode != QATTN_PV_E4M3)
     return QATTN_ERR_UNSUPPORTED;
+  if (params->kv_capacity != 0 &&
+      (params->kv_capacity < shape->Nk || params->kv_capacity > (int64_t{1} << 31)))
+    return QATTN_ERR_INVALID_ARG;
   if (!q_codes || !aligned16(q_codes) || !q_scales || !k_codes || !aligned16(k_codes) ||
       !k_scales || !v_codes || !aligned16(v_codes) || !v_chan_scale || !v_code_amax || !O ||
       !aligned16(O))
@@ -435,10 +439,11 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
   CUtensorMap tk, tv;
   const CUtensorMapSwizzle swz = shape->d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const uint64_t planes = static_cast<uint64_t>(shape->B * shape->Hkv);
+  const uint64_t cap = static_cast<uint64_t>(params->kv_capacity ? params->kv_capacity : shape->Nk);
   if (!encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k_codes, shape->d, shape->Nk, planes,
-                 shape->d, static_cast<uint32_t>(shape->d), 128, swz) ||
+                 shape->d, static_cast<uint32_t>(shape->d), 128, swz, cap) ||
       !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_codes, shape->d, shape->Nk, planes,
-                 shape->d, static_cast<uint32_t>(shape->d), 128, swz))
+                 shape->d, static_cast<uint32_t>(shape->d), 128, swz, cap))
     return QATTN_ERR_CUDA;
   return from_cuda(qattn::launch_decode(tk, tv, a, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -467,6 +472,30 @@ qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
   return from_cuda(qattn::launch_qk_debug(tq, tk, static_cast<int>(shape->B), static_cast<int>(shape->Hq),
                                           static_cast<int>(shape->Hkv), static_cast<int>(shape->Nq),
                                           static_cast<int>(shape->Nk), static_cast<int>(shape->d), S, err, s));
+}
+
+qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,
+                             int64_t T, int64_t d, int64_t pos, int64_t capacity,
+                             const float* k_chan_scale, const float* v_chan_scale,
+                             float* k_mean, float* v_code_amax, int8_t* k_codes,
+                             int8_t* v_codes, qattn_stream_t stream) {
+  if (B <= 0 || Hkv <= 0 || T < 0 || d < 1 || d > 1024 || pos < 0 || capacity < 0 ||
+      pos + T > capacity || capacity > (int64_t{1} << 24) || B * Hkv * d >= (int64_t{1} << 31))
+    return QATTN_ERR_INVALID_ARG;
+  if (!K_new || !V_new || !k_chan_scale || !v_chan_scale || !k_mean || !v_code_amax ||
+      !k_codes || !v_codes)
+    return QATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(K_new) & 1u) || (reinterpret_cast<uintptr_t>(V_new) & 1u))
+    return QATTN_ERR_INVALID_ARG;
+  for (const void* f : {static_cast<const void*>(k_chan_scale), static_cast<const void*>(v_chan_scale),
+                        static_cast<const void*>(k_mean), static_cast<const void*>(v_code_amax)})
+    if (reinterpret_cast<uintptr_t>(f) & 3u) return QATTN_ERR_INVALID_ARG;
+  if (T == 0) return QATTN_OK;
+  return from_cuda(qattn::launch_kv_append(
+      static_cast<const uint16_t*>(K_new), static_cast<const uint16_t*>(V_new),
+      static_cast<int>(B * Hkv), static_cast<int>(d), static_cast<int>(T), static_cast<int>(pos),
+      static_cast<long long>(capacity), k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes,
+      v_codes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_get_error(qattn_stream_t stream) {

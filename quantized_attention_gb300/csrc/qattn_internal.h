@@ -124,6 +124,10 @@ size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, l
 // 128-byte swizzle for d = 128, 64-byte for d = 64.
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, void* ws,
                           cudaStream_t s);
+cudaError_t launch_kv_append(const uint16_t* K_new, const uint16_t* V_new, int BH, int d, int T,
+                             int pos, long long cap, const float* k_chan_scale,
+                             const float* v_chan_scale, float* k_mean, float* v_code_amax,
+                             int8_t* k_codes, int8_t* v_codes, cudaStream_t s);
 
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

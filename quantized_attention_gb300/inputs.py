@@ -191,6 +191,19 @@ def _make_cache_inputs(rng: np.random.Generator, wl: Workload, Q: np.ndarray) ->
                   V_codes=V_codes, V_scale=V_scale)
 
 
+def make_append_tokens(inp: Inputs, T: int, seed: int = 0):
+    """T new tokens for an int8-cache workload, shaped like its cache: raw K =
+    the header's channel mean + N(0, sigma_c) with the cache's channel spread,
+    V = N(0, 1) at the V codes' scale; bf16 values as fp32, [B, Hkv, T, d]."""
+    wl = inp.wl
+    rng = np.random.Generator(np.random.PCG64(10007 * wl.seed + seed))
+    span = np.float32(127.0 / 4.5)
+    sig = (inp.K_scale * span)[:, :, None, :]
+    K = inp.K_header_mean[:, :, None, :] + _normal(rng, (wl.B, wl.Hkv, T, wl.d)) * sig
+    V = _normal(rng, (wl.B, wl.Hkv, T, wl.d)) * (inp.V_scale * span)[:, :, None, :]
+    return to_bf16(K.astype(np.float32)), to_bf16(V.astype(np.float32))
+
+
 def small(name: str, **kw) -> Workload:
     """A reduced-size copy of a named workload (same structure, new sizes)."""
     return WORKLOADS[name].replace(name=name + "@small", **kw)

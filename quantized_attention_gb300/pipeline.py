@@ -70,11 +70,24 @@ class Problem:
         qb.quantize_qk(Q, self._cache_k, qb.DT_I8, None, K_scale, self.shape, self.params,
                        self.q_codes, self.q_scales, None, self.k_scales, self.workspace, stream)
 
-    def set_cache(self, K_codes, V_codes, V_scale):
-        """The int8 KV cache qattn_decode reads, and its header's per-channel
-        max |V code|."""
+    def set_cache(self, K_codes, V_codes, V_scale, K_scale=None, K_mean=None):
+        """The int8 KV cache qattn_decode reads ([B, Hkv, capacity, d], rows
+        0..Nk-1 in use) and its header: the per-channel max |V code| of the
+        rows in use, and for qattn_kv_append the channel scales and the
+        running channel mean of K (zeros if not given)."""
         self._cache_k, self._cache_v, self._cache_vs = K_codes, V_codes, V_scale
-        self._cache_vamax = V_codes.to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+        used = V_codes[:, :, : self.shape.Nk]
+        self._cache_vamax = used.to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+        self._cache_ks = K_scale
+        self._cache_kmean = (K_mean.clone().contiguous() if K_mean is not None
+                             else torch.zeros_like(V_scale))
+        self.params.kv_capacity = K_codes.shape[2]
+
+    def append(self, K_new, V_new, pos: int, stream=None):
+        """qattn_kv_append: tokens K_new, V_new (bf16 [B, Hkv, T, d]) into the
+        cache at rows pos.., updating the header (running K mean, V max)."""
+        qb.kv_append(K_new, V_new, pos, self._cache_ks, self._cache_vs, self._cache_kmean,
+                     self._cache_vamax, self._cache_k, self._cache_v, stream)
 
     def decode(self, stream=None):
         """qattn_decode on the cache given to set_cache."""
@@ -103,10 +116,11 @@ class Problem:
         n += 1 + int(self.k_carrier is None)         # [K carriers], fused attention
         return n
 
-    def decode_launches(self) -> int:
-        """Kernels one quantize_q + decode launches: Q codes (two passes for a
-        tensor/head granule), K scales set to 1, then the decode's two."""
-        return 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 2
+    def decode_launches(self, append: bool = False) -> int:
+        """Kernels one [append +] quantize_q + decode launches: [the cache
+        append,] Q codes (two passes for a tensor/head granule), K scales set
+        to 1, then the decode's two."""
+        return int(append) + 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 2
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
             V_scale=None, bias=None, stream=None):

@@ -93,3 +93,26 @@ def test_invalid_arguments_rejected_on_host(L):
     s0 = qb.make_shape(0, 4, 2, 256, 256, 64)
     assert L.qattn_fwd(None, None, None, None, None, None, 0, None, None, ctypes.byref(s0),
                        ctypes.byref(p), None, None, None, 0, None) == 0
+
+
+def test_decode_and_append_arguments_rejected_on_host(L):
+    from quantized_attention_gb300 import binding as qb
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    # qattn_kv_append: pos + T beyond the capacity, negative pos, d out of range,
+    # misaligned bf16 / fp32 pointers, null codes; T = 0 is a no-op (no launch)
+    assert L.qattn_kv_append(fake, fake, 1, 2, 3, 64, 6, 8, fake, fake, fake, fake, fake, fake, None) == 1
+    assert L.qattn_kv_append(fake, fake, 1, 2, 3, 64, -1, 8, fake, fake, fake, fake, fake, fake, None) == 1
+    assert L.qattn_kv_append(fake, fake, 1, 2, 3, 2048, 0, 8, fake, fake, fake, fake, fake, fake, None) == 1
+    assert L.qattn_kv_append(vp((1 << 20) + 1), fake, 1, 2, 3, 64, 0, 8, fake, fake, fake, fake,
+                             fake, fake, None) == 1
+    assert L.qattn_kv_append(fake, fake, 1, 2, 3, 64, 0, 8, fake, fake, vp((1 << 20) + 2), fake,
+                             fake, fake, None) == 1
+    assert L.qattn_kv_append(fake, fake, 1, 2, 3, 64, 0, 8, fake, fake, fake, fake, None, fake, None) == 1
+    assert L.qattn_kv_append(fake, fake, 1, 2, 0, 64, 8, 8, fake, fake, fake, fake, fake, fake, None) == 0
+    # qattn_decode: a capacity below the rows in use, a negative capacity
+    s = qb.make_shape(1, 8, 2, 1, 1000, 128)
+    for cap, st in ((999, 1), (-5, 1)):
+        p = qb.make_params(causal=True, kv_capacity=cap)
+        assert L.qattn_decode(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(s),
+                              ctypes.byref(p), fake, None, fake, 1 << 30, None) == st
