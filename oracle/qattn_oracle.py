@@ -578,6 +578,110 @@ def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax
     return mu, amax, kc, vc
 
 
+EXACT24_GROUP = 64   # q scaled per (head, 64-channel group)
+EXACT24_CHUNK = 64   # P scaled per (row, 64-key chunk); also the online-softmax block
+
+
+def split24(x):
+    """x (fp32, |x| <= 127) -> int64 parts (h, l, m) with
+    X = rint(fp32(x * 65536)) = h * 65536 + l * 256 + m, h and l signed bytes and
+    m an unsigned byte (Strata PR, "What it does", "Operands": 24 bits, each
+    part's product sum exact in int32)."""
+    X = np.rint((np.asarray(x, np.float32) * np.float32(65536.0)).astype(np.float32)).astype(np.int64)
+    m = X & 255
+    r = (X - m) >> 8
+    l = ((r + 128) & 255) - 128
+    h = (r - l) >> 8
+    return h, l, m
+
+
+def attn_exact24(Q, k_codes, k_chan_scale, v_codes, v_chan_scale, *, causal, q_pos0=None,
+                 sm_scale=None, heads=None, rows=None):
+    """High-accuracy attention on an int8 KV cache with operands split exact to
+    24 bits (Strata PR, "What it does", "Operands"; parity "Measured": max
+    relative error ~2e-6 against FP64).  Steps, per (batch, query head):
+
+    1. q' = fp32(q * s_k[c]) (the cache's K channel scales folded into q);
+       per 64-channel group g over all the head's query rows,
+       s_g = fp32(max|q'| / 127), x = fp32(q' / s_g), split24(x) -> (h, l, m).
+    2. Per group, three exact integer dots with the K codes; S = sum over
+       groups of fp32(s_g * Sh) + fp32(s_g/256 * Sl) + fp32(s_g/65536 * Sm),
+       accumulated in fp32 in group order; t = fp32(S * fp32(sm_scale * log2 e)).
+    3. Online softmax over 64-key chunks in order (running max m, P = 2^(t - m)
+       in float64 here); per (row, chunk) s_p = fp32(max P / 127),
+       x = fp32(P / s_p), split24(x) -> (h, l, m); three exact integer dots
+       with the V codes give O_chunk = s_p * (Oh + Ol/256 + Om/65536).
+    4. O = alpha * O + O_chunk, l = alpha * l + sum P (float64); out = O * s_v / l.
+
+    Readings (not on the page): the K and V channel scales of the int8 cache
+    are factored out of the dots (K's folded into q, V's applied at the end, so
+    "p . v_scale" reduces to p); the chunk is 64 keys; P's chunk maximum is
+    taken over the visible keys.  Q: [B, Hq, Nq, d] values; k_codes, v_codes:
+    [B, Hkv, Nk, d] int8; scales [B, Hkv, d].  Returns out [len(heads), R, d]
+    and lse (natural log of the softmax denominator of the scaled scores).
+    """
+    Q = np.asarray(Q, np.float32)
+    B, Hq, Nq, d = Q.shape
+    Hkv, Nk = k_codes.shape[1], k_codes.shape[2]
+    G = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = default_sm_scale(d)
+    cfac = np.float32(np.float32(sm_scale) * LOG2E_F32)
+    if q_pos0 is None:
+        q_pos0 = Nk - Nq
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    out = np.zeros((len(heads), len(rows), d))
+    lse = np.zeros((len(heads), len(rows)))
+    ng = d // EXACT24_GROUP
+    for hi, (b, h) in enumerate(heads):
+        kv = h // G
+        qp = (Q[b, h] * k_chan_scale[b, kv][None, :]).astype(np.float32)          # [Nq, d]
+        kc = k_codes[b, kv].astype(np.int64)                                       # [Nk, d]
+        vc = v_codes[b, kv].astype(np.int64)
+        S = np.zeros((len(rows), Nk), np.float32)
+        for g in range(ng):
+            cs = slice(g * EXACT24_GROUP, (g + 1) * EXACT24_GROUP)
+            sg = np.float32(np.abs(qp[:, cs]).max() / np.float32(127.0))
+            if sg == 0:
+                continue
+            x = (qp[rows][:, cs] / sg).astype(np.float32)
+            ph, pl, pm = split24(x)
+            Sh, Sl, Sm = ph @ kc[:, cs].T, pl @ kc[:, cs].T, pm @ kc[:, cs].T        # exact int64
+            S = (S + (sg * Sh.astype(np.float32)).astype(np.float32)).astype(np.float32)
+            S = (S + (np.float32(sg / 256) * Sl.astype(np.float32)).astype(np.float32)).astype(np.float32)
+            S = (S + (np.float32(sg / 65536) * Sm.astype(np.float32)).astype(np.float32)).astype(np.float32)
+        t = (S * cfac).astype(np.float32).astype(np.float64)
+        vis = visible_mask(rows, Nk, causal, q_pos0)
+        t[~vis] = -np.inf
+        m = np.full(len(rows), -np.inf)
+        l = np.zeros(len(rows))
+        O = np.zeros((len(rows), d))
+        for k0 in range(0, Nk, EXACT24_CHUNK):
+            tk = t[:, k0:k0 + EXACT24_CHUNK]
+            m_new = np.maximum(m, tk.max(axis=1))
+            live = np.isfinite(m_new)
+            prev = live & np.isfinite(m)
+            alpha = np.where(prev, np.exp2(np.where(prev, m, 0.0) - np.where(prev, m_new, 0.0)), 0.0)
+            P = np.where(live[:, None], np.exp2(tk - np.where(live, m_new, 0.0)[:, None]), 0.0)
+            pmax = P.max(axis=1)
+            sp = (pmax.astype(np.float32) / np.float32(127.0)).astype(np.float32)
+            safe = np.where(sp > 0, sp, np.float32(1.0))
+            x = (P.astype(np.float32) / safe[:, None]).astype(np.float32)
+            x[sp == 0] = 0
+            ph, pl, pm = split24(x)
+            vcb = vc[k0:k0 + EXACT24_CHUNK]
+            Oc = (ph @ vcb) + (pl @ vcb) / 256.0 + (pm @ vcb) / 65536.0
+            O = alpha[:, None] * O + sp.astype(np.float64)[:, None] * Oc
+            l = alpha * l + P.sum(axis=1)
+            m = m_new
+        sv = v_chan_scale[b, kv].astype(np.float64)
+        ok = l > 0
+        out[hi] = np.where(ok[:, None], O * sv[None, :] / np.where(ok, l, 1.0)[:, None], 0.0)
+        lse[hi] = np.where(ok, (m + np.log2(np.where(ok, l, 1.0))) * np.log(2.0), -np.inf)
+    return out, lse
+
+
 def attn_probs_fp64(Q, K, *, causal, q_pos0=None, sm_scale=None, bias=None, heads=None,
                     rows=None):
     """softmax(Q K^T * sm_scale + bias) of the chosen rows, dense, float64.
