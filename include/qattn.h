@@ -259,6 +259,30 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
                           float* lse, void* workspace, size_t workspace_bytes,
                           qattn_stream_t stream);
 
+/* High-accuracy attention on an int8 KV cache with both products' other
+ * operand split exact to 24 bits (Strata PR "prompt_attn_i8v3_kernel", "What
+ * it does", "Operands"; "Measured": ~2e-6 max relative error against FP64).
+ * Per (batch, query head): q' = fp32(q * k_chan_scale); per 64-channel group
+ * s_g = fp32(max |q'| / 127) over the head's rows; X = rint(q'/s_g * 65536)
+ * = h * 65536 + l * 256 + m; S = sum over groups of s_g * (h.k + l.k/256 +
+ * m.k/65536) with exact integer dots against the K codes, combined in fp32;
+ * an online softmax over 64-key chunks (fp32, P = 2^(t - m)); per (row,
+ * chunk) s_p = max P / 127 and P's parts; O += s_p * (h.v + l.v/256 +
+ * m.v/65536) against the V codes; out = O * v_chan_scale / l.
+ *   Q            bf16 [B][Hq][Nq][d], device
+ *   k_codes, v_codes  int8 [B][Hkv][cap][d] (cap = params->kv_capacity or Nk)
+ *   k_chan_scale, v_chan_scale  fp32 [B][Hkv][d]: the codes' channel scales
+ *   O, lse       as for qattn_fwd; params: causal, q_pos0, sm_scale,
+ *                out_dtype, kv_capacity (granules, pv_mode and bias unused)
+ * Limits: d in {64, 128}, B * Hq <= 65535.  Workspace: at least
+ * qattn_workspace_size() (three fp16 planes of Q's parts and the group scales).
+ */
+qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float* k_chan_scale,
+                               const int8_t* v_codes, const float* v_chan_scale,
+                               const qattn_shape* shape, const qattn_params* params, void* O,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               qattn_stream_t stream);
+
 /* Append T tokens to an int8 KV cache whose header keeps a running channel
  * mean of K (ZINC post, "K's outliers, and the subtraction softmax does not
  * notice": during decode K arrives one token at a time and the header keeps a

@@ -25,7 +25,7 @@ EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
-    "qattn_kv_append",
+    "qattn_kv_append", "qattn_fwd_exact24",
 )
 
 
@@ -78,9 +78,10 @@ def lib() -> ctypes.CDLL:
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
     L.qattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_kv_append.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+    L.qattn_fwd_exact24.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-                 "qattn_decode", "qattn_kv_append",
+                 "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -205,6 +206,19 @@ def decode(q_codes, q_scales, k_codes, k_scales, v_codes, v_chan_scale, v_code_a
                               ctypes.byref(params), _p(O), _p(lse), _p(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
            "qattn_decode")
+
+
+def fwd_exact24(Q, k_codes, k_chan_scale, v_codes, v_chan_scale, shape, params, O, lse,
+                workspace, stream=None):
+    """24-bit exact split attention on an int8 KV cache (see qattn_fwd_exact24)."""
+    _dense(Q, torch.bfloat16, "Q")
+    _dense(k_codes, torch.int8, "k_codes")
+    _dense(v_codes, torch.int8, "v_codes")
+    _check(lib().qattn_fwd_exact24(_p(Q), _p(k_codes), _p(k_chan_scale), _p(v_codes),
+                                   _p(v_chan_scale), ctypes.byref(shape), ctypes.byref(params),
+                                   _p(O), _p(lse), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "qattn_fwd_exact24")
 
 
 def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes,

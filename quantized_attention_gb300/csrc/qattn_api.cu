@@ -190,6 +190,8 @@ size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params
                                               shape->Nk, shape->d);
     if (dws > m) m = dws;
   }
+  const size_t e24 = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Nq, shape->d);
+  if (e24 > m) m = e24;
   return m;
 }
 
@@ -472,6 +474,55 @@ qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
   return from_cuda(qattn::launch_qk_debug(tq, tk, static_cast<int>(shape->B), static_cast<int>(shape->Hq),
                                           static_cast<int>(shape->Hkv), static_cast<int>(shape->Nq),
                                           static_cast<int>(shape->Nk), static_cast<int>(shape->d), S, err, s));
+}
+
+qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float* k_chan_scale,
+                              const int8_t* v_codes, const float* v_chan_scale,
+                              const qattn_shape* shape, const qattn_params* params, void* O,
+                              float* lse, void* workspace, size_t workspace_bytes,
+                              qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (empty_problem(shape)) return QATTN_OK;
+  if (shape->d != 64 && shape->d != 128) return QATTN_ERR_UNSUPPORTED;
+  if (shape->B * shape->Hq > 65535) return QATTN_ERR_UNSUPPORTED;
+  if (!Q || !aligned16(Q) || !O || !aligned16(O) || !k_chan_scale || !v_chan_scale)
+    return QATTN_ERR_INVALID_ARG;
+  if (shape->Nk > 0 && (!k_codes || !aligned16(k_codes) || !v_codes || !aligned16(v_codes)))
+    return QATTN_ERR_INVALID_ARG;
+  for (const void* f : {static_cast<const void*>(k_chan_scale), static_cast<const void*>(v_chan_scale),
+                        static_cast<const void*>(lse)})
+    if (reinterpret_cast<uintptr_t>(f) & 3u) return QATTN_ERR_INVALID_ARG;
+  if (params->kv_capacity != 0 &&
+      (params->kv_capacity < shape->Nk || params->kv_capacity > (int64_t{1} << 31)))
+    return QATTN_ERR_INVALID_ARG;
+  const int64_t pos0 = pos0_of(shape, params);
+  if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
+  const size_t need = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Nq, shape->d);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  qattn::Exact24Args a{};
+  a.B = static_cast<int>(shape->B);
+  a.Hq = static_cast<int>(shape->Hq);
+  a.Hkv = static_cast<int>(shape->Hkv);
+  a.Nq = static_cast<int>(shape->Nq);
+  a.Nk = static_cast<int>(shape->Nk);
+  a.d = static_cast<int>(shape->d);
+  a.causal = params->causal;
+  a.pos0 = params->causal ? static_cast<int>(pos0) : 0;
+  a.sm_scale = params->sm_scale > 0.f ? params->sm_scale
+                                      : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
+  a.cap = params->kv_capacity ? params->kv_capacity : shape->Nk;
+  a.Q = Q;
+  a.k_chan_scale = k_chan_scale;
+  a.k_codes = k_codes;
+  a.v_codes = v_codes;
+  a.v_chan_scale = v_chan_scale;
+  a.out = O;
+  a.out_bf16 = params->out_dtype == QATTN_BF16;
+  a.lse = lse;
+  a.ws = workspace;
+  return from_cuda(qattn::launch_exact24(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,

@@ -129,6 +129,26 @@ cudaError_t launch_kv_append(const uint16_t* K_new, const uint16_t* V_new, int B
                              const float* v_chan_scale, float* k_mean, float* v_code_amax,
                              int8_t* k_codes, int8_t* v_codes, cudaStream_t s);
 
+// ---- exact24.cu
+struct Exact24Args {
+  int B, Hq, Hkv, Nq, Nk, d;
+  int causal;
+  int pos0;
+  float sm_scale;
+  long long cap;                // cache rows per (batch, KV head)
+  const void* Q;                // bf16 [B][Hq][Nq][d]
+  const float* k_chan_scale;    // [B][Hkv][d]
+  const int8_t* k_codes;        // [B][Hkv][cap][d]
+  const int8_t* v_codes;
+  const float* v_chan_scale;
+  void* out;
+  int out_bf16;
+  float* lse;
+  void* ws;                     // exact24_ws_bytes
+};
+size_t exact24_ws_bytes(long long B, long long Hq, long long Nq, long long d);
+cudaError_t launch_exact24(const Exact24Args& x, cudaStream_t s);
+
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& a, cudaStream_t s);
