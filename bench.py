@@ -281,7 +281,24 @@ def gpu_arm(args):
         dev["V_new"] = torch.from_numpy(v_new).to(device="cuda", dtype=torch.bfloat16)
         cache_bytes = 2 * wl.B * wl.Hkv * wl.Nk * wl.d  # K and V codes, read once
 
+    if args.exact24:  # the 24-bit exact split mode on the int8 cache
+        if not wl.kv_codes:
+            raise SystemExit("--exact24 needs an int8-cache workload (chunk32k, decode32k)")
+        e24_shape = qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
+        e24_params = qb.make_params(causal=wl.causal, q_pos0=wl.q_pos0, out_dtype=qb.DT_BF16)
+        e24_ws = torch.empty(max(qb.workspace_size(e24_shape, e24_params), 256), dtype=torch.uint8,
+                             device="cuda")
+
+    def run_exact24():
+        qb.fwd_exact24(dev["Q"], dev["K_codes"], dev["K_scale"], dev["V_codes"], dev["V_scale"],
+                       e24_shape, e24_params, P.O, P.lse, e24_ws, stream)
+
     def step():
+        if args.exact24:
+            ev_a.record(stream)
+            run_exact24()
+            ev_b.record(stream)
+            return
         if decode:
             P.append(dev["K_new"], dev["V_new"], wl.Nk - 1, stream)  # the token at row Nk-1
             P.quantize_q(dev["Q"], dev["K_scale"], stream)
@@ -331,7 +348,7 @@ def gpu_arm(args):
 
     # ---- end to end through the public API, host buffers, copies timed
     host = {k: v.cpu().pin_memory() for k, v in dev.items()
-            if not decode or k in ("Q", "K_new", "V_new")}
+            if (not decode and not args.exact24) or k in ("Q", "K_new", "V_new")}
     out_host = torch.empty(P.O.shape, dtype=P.O.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -339,7 +356,9 @@ def gpu_arm(args):
     def e2e_step():
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
-        if decode:
+        if args.exact24:
+            run_exact24()
+        elif decode:
             P.append(dev["K_new"], dev["V_new"], wl.Nk - 1, stream)
             P.quantize_q(dev["Q"], dev["K_scale"], stream)
             P.decode(stream)
@@ -380,7 +399,15 @@ def gpu_arm(args):
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
                 "traffic": _attn_traffic(args.workload),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
-    if decode:  # memory-bound: the cache's bytes over the decode call's time
+    if args.exact24:  # three exact fp16 tensor-core products per attention product
+        mma_tflops = 3 * ops / (attn_avg_ms * 1e-3) / 1e12
+        pb = peaks["bf16_sustained"]
+        roofline = {"bound": "tensor", "kernel": "exact24_attn_kernel + q_split_kernel (qattn_fwd_exact24)",
+                    "achieved": mma_tflops, "peak": pb, "unit": "TFLOP/s", "frac": mma_tflops / pb,
+                    "peak_basis": f"{peaks['source']} sustained bf16 (fp16 MMA runs at the bf16 rate); "
+                                  "achieved counts the 3 fp16 products per attention product",
+                    "traffic": None}
+    if decode and not args.exact24:  # memory-bound: the cache's bytes over the decode call's time
         gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
         ref_us = _stream_ref_us(dev["K_codes"], dev["V_codes"], flush, stream)
         roofline = {"bound": "hbm", "kernel": "qattn_decode (2 launches: fused scores + PV over key chunks, chunk combine)",
@@ -392,20 +419,23 @@ def gpu_arm(args):
                                          "same L2 flush before each launch",
                                    "us": ref_us, "GB/s": cache_bytes / (ref_us * 1e-6) / 1e9}}
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not args.exact24:
         c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {c_s:.1f} s"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3", "data": "synthetic",
-            "config": _config(args.workload),
+            "config": {**_config(args.workload),
+                       **({"mode": "24-bit exact split (qattn_fwd_exact24)",
+                           "step": "split Q, attention with exact fp16 products"} if args.exact24 else {})},
             "frac_of_mixed_peak": value / pmix,
             "attn_kernel_ms": attn_avg_ms,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (P.decode_launches(append=True) if decode else P.kernel_launches()) * args.steps,
+            "gpu_launches": (2 if args.exact24 else P.decode_launches(append=True) if decode
+                             else P.kernel_launches()) * args.steps,
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -441,6 +471,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llm8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--exact24", action="store_true",
+                    help="time the 24-bit exact split mode (qattn_fwd_exact24) on an int8-cache workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -6,9 +6,9 @@
 // against FP64).
 //
 // The exact products run on the tensor cores as fp16 x fp16 with fp32
-// accumulation (mma.m16n8k16): h, l, m and the int8 codes are exact fp16
-// values, and a part's sum over 64 channels (or 64 keys) is an integer below
-// 64 * 255 * 127 < 2^24, so no rounding occurs.  (GB300 runs the warp-level
+// accumulation (mma.m16n8k16, fragments by ldmatrix): h, l, m and the int8
+// codes are exact fp16 values, and a part's sum over 64 channels (or 64 keys)
+// is an integer below 64 * 255 * 127 < 2^24, so no rounding occurs.  (GB300 runs the warp-level
 // fp16 MMA about four times faster than its int8 one.)  The K and V channel
 // scales of the cache are factored out: K's is folded into q before the
 // split, V's applied to the output.
@@ -40,6 +40,22 @@ __device__ __forceinline__ void split24(float x, __half& h, __half& l, __half& m
   h = __int2half_rn(hh);
   l = __int2half_rn(ll);
   m = __int2half_rn(mm);
+}
+
+// The same split for X = rint(y) given y = x * 65536 >= 0 (P's side), in fp32
+// arithmetic only: every value below 2^24 is an exact integer, so floor, the
+// products by 2^-8 and the differences are exact.  Returns (h, l, m) as floats.
+__device__ __forceinline__ void split24_pos(float y, float& h, float& l, float& m) {
+  const float X = rintf(y);
+  const float r = floorf(X * 0.00390625f);           // X >> 8
+  m = fmaf(-256.0f, r, X);                           // X & 255
+  h = floorf((r + 128.0f) * 0.00390625f);            // so that l is a signed byte
+  l = fmaf(-256.0f, h, r);
+}
+
+__device__ __forceinline__ uint32_t pack_f2h2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);  // exact: small integers
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
@@ -111,13 +127,10 @@ __global__ void __launch_bounds__(256) q_split_kernel(const uint16_t* Q, const f
 // ---------------------------------------------------------------- attention
 template <int D>
 struct Ex24Smem {
-  static constexpr int kQPitch = D * 2 + 32;            // bytes per q row of a part
-  static constexpr int kQ = 3 * kRows * kQPitch;        // three parts
-  static constexpr int kKPitch = D + 16;                // bytes per key row
-  static constexpr int kK = kChunk * kKPitch;
-  static constexpr int kVPitch = kChunk + 16;           // bytes per channel row of V^T
-  static constexpr int kV = D * kVPitch;
-  static constexpr int kBytes = kQ + kK + kV;
+  static constexpr int kPitch = D * 2 + 16;         // bytes per fp16 row (8 rows hit 8 bank groups)
+  static constexpr int kQ = 3 * kRows * kPitch;     // the three q parts
+  static constexpr int kKV = kChunk * kPitch;       // K or V codes of a chunk as fp16
+  static constexpr int kBytes = kQ + 2 * kKV;
 };
 
 struct Ex24Args {
@@ -137,13 +150,25 @@ struct Ex24Args {
   float* lse;
 };
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // CTA: 64 query rows of one (batch, query head); warp w owns rows 16w..16w+15.
-// Per 64-key chunk: the K codes (padded rows) and V codes (transposed, keys of
-// each 16-key step stored at position 4t + e for key 2t + e and 4t + 2 + e for
-// key 2t + 8 + e, so a lane's PV fragment is one 32-bit word) go to shared
-// memory; S = sum over groups and parts of weight * (part . K codes) in the
-// oracle's fp32 order; the online softmax; P per (row, chunk) to 127 and its
-// parts; O += sum of part weights * (part . V codes).
+// Per 64-key chunk the K and V codes are converted once to exact fp16 rows in
+// shared memory; fragments come from ldmatrix (V transposed).  S = sum over
+// groups and parts of weight * (part . K codes), fp32 multiply-adds;
+// the online softmax; P per (row, chunk) to 127 and its three parts;
+// O += sum of part weights * (part . V codes).
 template <int D>
 __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a) {
   using SM = Ex24Smem<D>;
@@ -152,7 +177,8 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* sq = smem;
   uint8_t* sk = smem + SM::kQ;
-  uint8_t* sv = smem + SM::kQ + SM::kK;
+  uint8_t* sv = smem + SM::kQ + SM::kKV;
+  __shared__ float gs[NG];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,15 +194,19 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
     if (q0 + r < a.Nq)
       x = *reinterpret_cast<const uint4*>(a.parts + p * a.plane +
                                           (static_cast<size_t>(bh) * a.Nq + q0 + r) * D + c8 * 8);
-    *reinterpret_cast<uint4*>(sq + (p * kRows + r) * SM::kQPitch + c8 * 16) = x;
+    *reinterpret_cast<uint4*>(sq + (p * kRows + r) * SM::kPitch + c8 * 16) = x;
   }
-  __shared__ float gs[NG];
   if (threadIdx.x < NG) gs[threadIdx.x] = a.group_scale[static_cast<size_t>(bh) * NG + threadIdx.x];
   const int r_lo = q0 + 16 * warp + g, r_hi = r_lo + 8;  // this lane's two rows
   float m_lo = kNegInf, m_hi = kNegInf, l_lo = 0.f, l_hi = 0.f;
   float o[NTO][4];
 #pragma unroll
   for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8
+  const int mrow = lane & 7, mat = lane >> 3;
+  const uint32_t q_addr = smem_u32(sq) + (16 * warp + mrow + (mat & 1) * 8) * SM::kPitch + (mat >> 1) * 16;
+  const uint32_t k_addr = smem_u32(sk) + (mrow + (mat >> 1) * 8) * SM::kPitch + (mat & 1) * 16;
+  const uint32_t v_addr = smem_u32(sv) + (mrow + (mat & 1) * 8) * SM::kPitch + (mat >> 1) * 16;
   // keys visible to the CTA's last row
   const int last_row = min(q0 + kRows, a.Nq) - 1;
   const int kend = a.causal ? min(a.Nk, a.pos0 + last_row + 1) : a.Nk;
@@ -184,33 +214,21 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
   const int8_t* vg = a.v_codes + static_cast<size_t>(bkv) * a.cap * D;
   for (int k0 = 0; k0 < kend; k0 += kChunk) {
     __syncthreads();  // the previous chunk's tiles are read
-    // K codes -> padded rows (zeros past Nk)
-    for (int v = threadIdx.x; v < kChunk * (D / 16); v += kThreads) {
-      const int key = v / (D / 16), c16 = v % (D / 16);
+    // K and V codes -> exact fp16 rows (zeros past Nk)
+    for (int v = threadIdx.x; v < 2 * kChunk * (D / 16); v += kThreads) {
+      const int which = v / (kChunk * (D / 16)), rem = v % (kChunk * (D / 16));
+      const int key = rem / (D / 16), c16 = rem % (D / 16);
+      const int8_t* src = which ? vg : kg;
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (k0 + key < a.Nk) x = __ldg(reinterpret_cast<const uint4*>(kg + static_cast<size_t>(k0 + key) * D) + c16);
-      *reinterpret_cast<uint4*>(sk + key * SM::kKPitch + c16 * 16) = x;
-    }
-    // V codes -> V^T: item (step s, quad t, channel word cw) gathers keys
-    // 16s + 2t, 2t + 1, 2t + 8, 2t + 9 of 4 channels and stores each channel's
-    // four bytes at positions 16s + 4t .. 16s + 4t + 3
-    for (int v = threadIdx.x; v < 4 * 4 * (D / 4); v += kThreads) {
-      const int s = v / (4 * (D / 4)), rem = v % (4 * (D / 4));
-      const int t = rem / (D / 4), cw = rem % (D / 4);
-      uint32_t x[4];
-      const int keys[4] = {16 * s + 2 * t, 16 * s + 2 * t + 1, 16 * s + 2 * t + 8, 16 * s + 2 * t + 9};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        x[e] = (k0 + keys[e] < a.Nk)
-                   ? __ldg(reinterpret_cast<const uint32_t*>(vg + static_cast<size_t>(k0 + keys[e]) * D) + cw)
-                   : 0u;
-      const uint32_t u0 = __byte_perm(x[0], x[1], 0x5140u), u1 = __byte_perm(x[0], x[1], 0x7362u);
-      const uint32_t u2 = __byte_perm(x[2], x[3], 0x5140u), u3 = __byte_perm(x[2], x[3], 0x7362u);
-      const uint32_t y[4] = {__byte_perm(u0, u2, 0x5410u), __byte_perm(u0, u2, 0x7632u),
-                             __byte_perm(u1, u3, 0x5410u), __byte_perm(u1, u3, 0x7632u)};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        *reinterpret_cast<uint32_t*>(sv + (4 * cw + e) * SM::kVPitch + 16 * s + 4 * t) = y[e];
+      if (k0 + key < a.Nk) x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(k0 + key) * D) + c16);
+      uint32_t hv[8];
+      codes4_to_f16x2(x.x, hv[0], hv[1]);
+      codes4_to_f16x2(x.y, hv[2], hv[3]);
+      codes4_to_f16x2(x.z, hv[4], hv[5]);
+      codes4_to_f16x2(x.w, hv[6], hv[7]);
+      uint8_t* dst = (which ? sv : sk) + key * SM::kPitch + c16 * 32;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(dst + 16) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
     }
     __syncthreads();
     // ---- scores: 16 rows x 64 keys per warp, in the oracle's order
@@ -224,25 +242,24 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
         float Sp[8][4];
 #pragma unroll
         for (int j = 0; j < 8; ++j) Sp[j][0] = Sp[j][1] = Sp[j][2] = Sp[j][3] = 0.f;
-#pragma unroll 2
+#pragma unroll 1
         for (int kk = 0; kk < kGroup / 16; ++kk) {
           const int ks = gr * (kGroup / 16) + kk;
-          const uint8_t* qa = sq + (p * kRows + 16 * warp + g) * SM::kQPitch + ks * 32 + t4 * 8;
-          const uint2 alo = *reinterpret_cast<const uint2*>(qa);
-          const uint2 ahi = *reinterpret_cast<const uint2*>(qa + 8 * SM::kQPitch);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(q_addr + p * kRows * SM::kPitch + ks * 32, a0, a1, a2, a3);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(sk + (8 * j + g) * SM::kKPitch + ks * 16 + 4 * t4);
-            uint32_t b0, b1;
-            codes4_to_f16x2(w, b0, b1);
-            mma_f16_16816(Sp[j], alo.x, ahi.x, alo.y, ahi.y, b0, b1);
+          for (int j = 0; j < 8; j += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(k_addr + 8 * j * SM::kPitch + ks * 32, b0, b1, b2, b3);
+            mma_f16_16816(Sp[j], a0, a1, a2, a3, b0, b1);
+            mma_f16_16816(Sp[j + 1], a0, a1, a2, a3, b2, b3);
           }
         }
-        const float wgt = (p == 0) ? gs[gr] : (p == 1) ? __fdiv_rn(gs[gr], 256.0f) : __fdiv_rn(gs[gr], 65536.0f);
+        const float wgt = gs[gr] * ((p == 0) ? 1.f : (p == 1) ? (1.f / 256.f) : (1.f / 65536.f));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) S[j][e] = __fadd_rn(S[j][e], __fmul_rn(wgt, Sp[j][e]));
+          for (int e = 0; e < 4; ++e) S[j][e] = fmaf(wgt, Sp[j][e], S[j][e]);
       }
     }
     // ---- t, mask, online softmax (rows r_lo, r_hi; a row's 64 keys sit in
@@ -287,6 +304,9 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
     const float pm_lo = (mx_lo == kNegInf) ? 0.f : ex2_approx(mx_lo - ref_lo);
     const float pm_hi = (mx_hi == kNegInf) ? 0.f : ex2_approx(mx_hi - ref_hi);
     const float sp_lo = __fdiv_rn(pm_lo, 127.0f), sp_hi = __fdiv_rn(pm_hi, 127.0f);
+    // x * 65536 = P * (65536 / s_p): one reciprocal per row
+    const float ci_lo = (sp_lo > 0.f) ? __fdiv_rn(65536.0f, sp_lo) : 0.f;
+    const float ci_hi = (sp_hi > 0.f) ? __fdiv_rn(65536.0f, sp_hi) : 0.f;
 #pragma unroll
     for (int n = 0; n < NTO; ++n) {
       o[n][0] *= al_lo;
@@ -303,17 +323,14 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int j = 2 * s + half;
-        __half v[3][4];
+        float v[3][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float sp = (e < 2) ? sp_lo : sp_hi;
-          const float x = (sp > 0.f) ? __fdiv_rn(S[j][e], sp) : 0.f;
-          split24(x, v[0][e], v[1][e], v[2][e]);
-        }
+        for (int e = 0; e < 4; ++e)
+          split24_pos(S[j][e] * ((e < 2) ? ci_lo : ci_hi), v[0][e], v[1][e], v[2][e]);
 #pragma unroll
         for (int p = 0; p < 3; ++p) {
-          af[p][s][2 * half] = pack_h2(v[p][0], v[p][1]);      // a0 / a2: row g
-          af[p][s][2 * half + 1] = pack_h2(v[p][2], v[p][3]);  // a1 / a3: row g + 8
+          af[p][s][2 * half] = pack_f2h2(v[p][0], v[p][1]);      // a0 / a2: row g
+          af[p][s][2 * half + 1] = pack_f2h2(v[p][2], v[p][3]);  // a1 / a3: row g + 8
         }
       }
     }
@@ -327,12 +344,12 @@ __global__ void __launch_bounds__(kThreads) exact24_attn_kernel(const Ex24Args a
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
 #pragma unroll
-          for (int n = 0; n < NTO / 2; ++n) {
+          for (int n = 0; n < NTO / 2; n += 2) {
             const int nt = hc * (NTO / 2) + n;
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(sv + (8 * nt + g) * SM::kVPitch + 16 * s + 4 * t4);
-            uint32_t b0, b1;
-            codes4_to_f16x2(w, b0, b1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(v_addr + 16 * s * SM::kPitch + nt * 16, b0, b1, b2, b3);
             mma_f16_16816(op[n], af[p][s][0], af[p][s][1], af[p][s][2], af[p][s][3], b0, b1);
+            mma_f16_16816(op[n + 1], af[p][s][0], af[p][s][1], af[p][s][2], af[p][s][3], b2, b3);
           }
         }
         const float pw = (p == 0) ? 1.f : (p == 1) ? (1.f / 256.f) : (1.f / 65536.f);
