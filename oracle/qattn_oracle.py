@@ -682,6 +682,94 @@ def attn_exact24(Q, k_codes, k_chan_scale, v_codes, v_chan_scale, *, causal, q_p
     return out, lse
 
 
+INTSM_TILE = 64          # key tile of the integer online softmax (Bc)
+INTSM_M0 = -(1 << 21)    # initial running max (QFlash Algorithm 1)
+
+
+def intsm_constants(sq, sk, sm_scale):
+    """Integer constants of QFlash's integer softmax, from the per-tensor
+    scales ("QFlash", section 4.3 eq. (5)-(8), section 4.4 eq. (9)-(10)):
+    s~ = fp32(fp32(fp32(sq * sk) * sm_scale) * log2 e) (the scale of an
+    exponent in base 2); X0 = rint(fp32(1 / s~)) (the integer that stands for
+    -1 in the exponent); the requantization of P (scale s~) to int8 codes of
+    scale 1/127: ratio = fp32(127 * s~), n = ceil(log2 ratio), r = 8 - n,
+    M = rint(ratio * 2^r).  Returns (s~, X0, M, r)."""
+    st = np.float32(np.float32(np.float32(np.float32(sq) * np.float32(sk)) * np.float32(sm_scale)) * LOG2E_F32)
+    x0 = int(np.rint(np.float32(np.float32(1.0) / st)))
+    ratio = np.float32(np.float32(127.0) * st)
+    f, e = np.frexp(np.float64(ratio))          # ratio = f * 2^e, f in [0.5, 1): exact
+    n = int(e) - 1 if f == 0.5 else int(e)      # ceil(log2 ratio)
+    r = 8 - n
+    M = int(np.rint(np.float64(ratio) * 2.0 ** r))
+    return st, max(x0, 1), M, r
+
+
+def shift_exp2(X, x0):
+    """QFlash's ShiftExp2 ("QFlash", section 4.3): for integer X <= 0,
+    2^(s~ X) ~= s~ ((R >> 1) + X0) >> -Q with X = Q X0 + R, Q = X / X0
+    truncated toward zero and R in (-X0, 0] (eq. (6)); 2^(s~ R) ~= s~ R / 2 + 1
+    (eq. (7)).  Integer in, integer out (scale s~); int64 arrays."""
+    X = np.asarray(X, dtype=np.int64)
+    q = -((-X) // x0)                  # truncation toward zero for X <= 0
+    R = X - q * x0                     # in (-x0, 0]
+    base = (R >> 1) + x0               # arithmetic shift: floor(R / 2)
+    sh = np.minimum(-q, 62)
+    return np.where(-q >= 62, 0, base >> sh)
+
+
+def requant_p(P, M, r):
+    """QFlash's requantization (section 4.4, eq. (10)): Y = (X * M) >> r,
+    clamped to the int8 codes [0, 127] of P's scale 1/127."""
+    return np.minimum((np.asarray(P, np.int64) * M) >> r, 127)
+
+
+def scale_release(x, alpha, x0):
+    """ScaleRelease (named in "QFlash" section 4.6; its definition, Appendix
+    B.1, is not in the pages -- PARITY UNPINNED): the reading taken here
+    multiplies by the max-offset factor alpha (scale s~) and divides by the
+    integer X0 ~= 1/s~ that stands for the inverse scale, floor division in
+    int64: floor(x * alpha / X0)."""
+    return (np.asarray(x, np.int64) * np.asarray(alpha, np.int64)) // x0
+
+
+def attn_intsoftmax(q_codes, sq, k_codes, sk, v_codes, *, sm_scale=None, heads=None, rows=None):
+    """QFlash's integer-only attention ("QFlash", Algorithm 1, sections 4.2-4.6):
+    per query row, over key tiles of 64 in order: S = q.k (int32),
+    m' = max(m, rowmax S) (m starts at -2^21), alpha = ShiftExp2(m - m'),
+    P = ShiftExp2(S - m'), Y = requant(P), l = ScaleRelease(l, alpha) + sum Y,
+    O = ScaleRelease(O, alpha) + Y.v (int32 dots); out = floor(O / l), int8
+    codes of V's scale (s_O = s_V).  Per-tensor scales sq, sk (floats);
+    q_codes [B, Hq, N, d], k/v codes [B, Hkv, N, d] int8.  No mask (the
+    workloads are ViT/DeiT/Swin windows).  Returns int64 [len(heads), R, d]."""
+    B, Hq, N, d = q_codes.shape
+    Hkv = k_codes.shape[1]
+    G = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = default_sm_scale(d)
+    _, x0, M, r = intsm_constants(sq, sk, sm_scale)
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    Nk = k_codes.shape[2]
+    out = np.zeros((len(heads), len(rows), d), np.int64)
+    for hi, (b, h) in enumerate(heads):
+        q = q_codes[b, h][rows].astype(np.int64)
+        k = k_codes[b, h // G].astype(np.int64)
+        v = v_codes[b, h // G].astype(np.int64)
+        m = np.full(len(rows), INTSM_M0, np.int64)
+        l = np.zeros(len(rows), np.int64)
+        O = np.zeros((len(rows), d), np.int64)
+        for k0 in range(0, Nk, INTSM_TILE):
+            S = q @ k[k0:k0 + INTSM_TILE].T                   # exact int32 values
+            m_new = np.maximum(m, S.max(axis=1))
+            alpha = shift_exp2(m - m_new, x0)
+            Y = requant_p(shift_exp2(S - m_new[:, None], x0), M, r)
+            l = scale_release(l, alpha, x0) + Y.sum(axis=1)
+            O = scale_release(O, alpha[:, None], x0) + Y @ v[k0:k0 + INTSM_TILE]
+            m = m_new
+        out[hi] = np.clip(O // np.maximum(l, 1)[:, None], -127, 127)
+    return out
+
+
 def attn_probs_fp64(Q, K, *, causal, q_pos0=None, sm_scale=None, bias=None, heads=None,
                     rows=None):
     """softmax(Q K^T * sm_scale + bias) of the chosen rows, dense, float64.
