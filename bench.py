@@ -289,11 +289,33 @@ def gpu_arm(args):
         e24_ws = torch.empty(max(qb.workspace_size(e24_shape, e24_params), 256), dtype=torch.uint8,
                              device="cuda")
 
+    if args.intsoftmax:  # QFlash integer-only attention on per-tensor int8 codes
+        if wl.kv_codes or wl.causal:
+            raise SystemExit("--intsoftmax needs an unmasked bf16 workload (vit, tiny)")
+        def tensor_codes(x):
+            sc = np.float32(np.abs(x).max() / np.float32(127.0))
+            return (torch.from_numpy(np.clip(np.rint(x / sc), -127, 127).astype(np.int8)).to("cuda"),
+                    torch.tensor([sc], dtype=torch.float32, device="cuda"))
+        ism_q, ism_sq = tensor_codes(inp.Q)
+        ism_k, ism_sk = tensor_codes(inp.K)
+        ism_v, _ = tensor_codes(inp.V)
+        ism_out = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d), dtype=torch.int8, device="cuda")
+        ism_shape = qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
+        ism_params = qb.make_params()
+
+    def run_intsoftmax():
+        qb.fwd_intsoftmax(ism_q, ism_sq, ism_k, ism_sk, ism_v, ism_shape, ism_params, ism_out, stream)
+
     def run_exact24():
         qb.fwd_exact24(dev["Q"], dev["K_codes"], dev["K_scale"], dev["V_codes"], dev["V_scale"],
                        e24_shape, e24_params, P.O, P.lse, e24_ws, stream)
 
     def step():
+        if args.intsoftmax:
+            ev_a.record(stream)
+            run_intsoftmax()
+            ev_b.record(stream)
+            return
         if args.exact24:
             ev_a.record(stream)
             run_exact24()
@@ -347,16 +369,24 @@ def gpu_arm(args):
     value = world * ops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API, host buffers, copies timed
-    host = {k: v.cpu().pin_memory() for k, v in dev.items()
-            if (not decode and not args.exact24) or k in ("Q", "K_new", "V_new")}
-    out_host = torch.empty(P.O.shape, dtype=P.O.dtype).pin_memory()
+    if args.intsoftmax:  # the int8 codes in, the int8 output codes back
+        dev = {"q": ism_q, "k": ism_k, "v": ism_v}
+        host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        out_dev = ism_out
+    else:
+        host = {k: v.cpu().pin_memory() for k, v in dev.items()
+                if (not decode and not args.exact24) or k in ("Q", "K_new", "V_new")}
+        out_dev = P.O
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
-        if args.exact24:
+        if args.intsoftmax:
+            run_intsoftmax()
+        elif args.exact24:
             run_exact24()
         elif decode:
             P.append(dev["K_new"], dev["V_new"], wl.Nk - 1, stream)
@@ -364,7 +394,7 @@ def gpu_arm(args):
             P.decode(stream)
         else:
             P.run(**dev, bias=bias, stream=stream)
-        out_host.copy_(P.O, non_blocking=True)
+        out_host.copy_(out_dev, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -399,6 +429,14 @@ def gpu_arm(args):
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
                 "traffic": _attn_traffic(args.workload),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
+    if args.intsoftmax:  # both products on the warp-level int8 tensor cores
+        ism_tops = ops / (attn_avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "intsm_attn_kernel (qattn_fwd_intsoftmax)",
+                    "achieved": ism_tops, "peak": peaks["bf16_sustained"], "unit": "TOPS",
+                    "frac": ism_tops / peaks["bf16_sustained"],
+                    "peak_basis": f"{peaks['source']} sustained bf16 (the int8 warp MMA on this "
+                                  "GPU runs far below it)",
+                    "traffic": None}
     if args.exact24:  # three exact fp16 tensor-core products per attention product
         mma_tflops = 3 * ops / (attn_avg_ms * 1e-3) / 1e12
         pb = peaks["bf16_sustained"]
@@ -419,7 +457,7 @@ def gpu_arm(args):
                                          "same L2 flush before each launch",
                                    "us": ref_us, "GB/s": cache_bytes / (ref_us * 1e-6) / 1e9}}
     cpu = None
-    if not args.no_cpu_baseline and not args.exact24:
+    if not args.no_cpu_baseline and not args.exact24 and not args.intsoftmax:
         c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {c_s:.1f} s"}
@@ -428,13 +466,16 @@ def gpu_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3", "data": "synthetic",
             "config": {**_config(args.workload),
                        **({"mode": "24-bit exact split (qattn_fwd_exact24)",
-                           "step": "split Q, attention with exact fp16 products"} if args.exact24 else {})},
+                           "step": "split Q, attention with exact fp16 products"} if args.exact24 else {}),
+                       **({"mode": "integer-only softmax (qattn_fwd_intsoftmax)",
+                           "step": "attention on resident per-tensor int8 codes"} if args.intsoftmax else {})},
             "frac_of_mixed_peak": value / pmix,
             "attn_kernel_ms": attn_avg_ms,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (2 if args.exact24 else P.decode_launches(append=True) if decode
+            "gpu_launches": (1 if args.intsoftmax else 2 if args.exact24
+                             else P.decode_launches(append=True) if decode
                              else P.kernel_launches()) * args.steps,
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
@@ -471,6 +512,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llm8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--intsoftmax", action="store_true",
+                    help="time QFlash's integer-only attention (qattn_fwd_intsoftmax) on int8 codes")
     ap.add_argument("--exact24", action="store_true",
                     help="time the 24-bit exact split mode (qattn_fwd_exact24) on an int8-cache workload")
     args = ap.parse_args()

@@ -283,6 +283,33 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
                                float* lse, void* workspace, size_t workspace_bytes,
                                qattn_stream_t stream);
 
+/* QFlash's integer-only attention ("QFlash: Bridging Quantization and Memory
+ * Efficiency in Vision Transformer Attention", Algorithm 1, sections 4.2-4.6)
+ * on per-tensor int8 codes.  With s~ = fp32(fp32(fp32(sq * sk) * sm_scale) *
+ * log2 e) and X0 = rint(1 / s~), per query row over key tiles of 64:
+ *   S = q.k (int32);  m' = max(m, rowmax S), m starting at -2^21
+ *   ShiftExp2(X <= 0) = ((R >> 1) + X0) >> -Q, X = Q X0 + R, Q = X / X0
+ *       truncated toward zero (section 4.3, eq. (5)-(8))
+ *   alpha = ShiftExp2(m - m');  P = ShiftExp2(S - m')
+ *   Y = min((P * M) >> r, 127): P to int8 codes of scale 1/127, with
+ *       ratio = fp32(127 s~), n = ceil(log2 ratio), r = 8 - n,
+ *       M = rint(ratio 2^r) (section 4.4, eq. (9)-(10))
+ *   l = floor(l * alpha / X0) + rowsum Y;  O = floor(O * alpha / X0) + Y.V
+ *       (ScaleRelease, section 4.6: its definition is not given; this is the
+ *       reading taken: the inverse scale 1/s~ approximated by the integer X0)
+ *   out = clamp(floor(O / l), -127, 127): int8 codes of V's scale.
+ *   q_codes  int8 [B][Hq][Nq][d], q_scale fp32[1] (device): its scale
+ *   k_codes, v_codes  int8 [B][Hkv][Nk][d]; k_scale fp32[1] (device)
+ *   O_codes  (out) int8 [B][Hq][Nq][d]
+ *   params: sm_scale (0 -> fp32(1/sqrt(d))); causal must be 0
+ * Limits: d in {32, 64, 128}, B * Hq <= 65535, no mask.  No workspace.
+ */
+qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
+                                  const int8_t* k_codes, const float* k_scale,
+                                  const int8_t* v_codes, const qattn_shape* shape,
+                                  const qattn_params* params, int8_t* O_codes,
+                                  qattn_stream_t stream);
+
 /* Append T tokens to an int8 KV cache whose header keeps a running channel
  * mean of K (ZINC post, "K's outliers, and the subtraction softmax does not
  * notice": during decode K arrives one token at a time and the header keeps a

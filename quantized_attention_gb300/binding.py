@@ -25,7 +25,7 @@ EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
-    "qattn_kv_append", "qattn_fwd_exact24",
+    "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
 )
 
 
@@ -79,9 +79,10 @@ def lib() -> ctypes.CDLL:
     L.qattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_kv_append.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
     L.qattn_fwd_exact24.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
+    L.qattn_fwd_intsoftmax.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp]
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
-                 "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24",
+                 "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -219,6 +220,19 @@ def fwd_exact24(Q, k_codes, k_chan_scale, v_codes, v_chan_scale, shape, params, 
                                    _p(O), _p(lse), _p(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)),
            "qattn_fwd_exact24")
+
+
+def fwd_intsoftmax(q_codes, q_scale, k_codes, k_scale, v_codes, shape, params, O_codes,
+                   stream=None):
+    """QFlash integer-only attention on per-tensor int8 codes (see
+    qattn_fwd_intsoftmax); O_codes: int8 codes of V's scale."""
+    for t, nm in ((q_codes, "q_codes"), (k_codes, "k_codes"), (v_codes, "v_codes"),
+                  (O_codes, "O_codes")):
+        _dense(t, torch.int8, nm)
+    _check(lib().qattn_fwd_intsoftmax(_p(q_codes), _p(q_scale), _p(k_codes), _p(k_scale),
+                                      _p(v_codes), ctypes.byref(shape), ctypes.byref(params),
+                                      _p(O_codes), _stream(stream)),
+           "qattn_fwd_intsoftmax")
 
 
 def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes,

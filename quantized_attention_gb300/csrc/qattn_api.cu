@@ -525,6 +525,30 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
   return from_cuda(qattn::launch_exact24(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
+                                 const int8_t* k_codes, const float* k_scale,
+                                 const int8_t* v_codes, const qattn_shape* shape,
+                                 const qattn_params* params, int8_t* O_codes,
+                                 qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (empty_problem(shape)) return QATTN_OK;
+  if (shape->d != 32 && shape->d != 64 && shape->d != 128) return QATTN_ERR_UNSUPPORTED;
+  if (params->causal || shape->Nk == 0 || shape->B * shape->Hq > 65535) return QATTN_ERR_UNSUPPORTED;
+  if (!q_codes || !aligned16(q_codes) || !k_codes || !aligned16(k_codes) || !v_codes ||
+      !aligned16(v_codes) || !O_codes || !q_scale || !k_scale)
+    return QATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_scale) & 3u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u))
+    return QATTN_ERR_INVALID_ARG;
+  const float sm = params->sm_scale > 0.f ? params->sm_scale
+                                          : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
+  return from_cuda(qattn::launch_intsoftmax(
+      static_cast<int>(shape->B), static_cast<int>(shape->Hq), static_cast<int>(shape->Hkv),
+      static_cast<int>(shape->Nq), static_cast<int>(shape->Nk), static_cast<int>(shape->d), sm, q_codes,
+      q_scale, k_codes, k_scale, v_codes, O_codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,
                              int64_t T, int64_t d, int64_t pos, int64_t capacity,
                              const float* k_chan_scale, const float* v_chan_scale,

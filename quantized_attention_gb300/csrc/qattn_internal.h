@@ -149,6 +149,12 @@ struct Exact24Args {
 size_t exact24_ws_bytes(long long B, long long Hq, long long Nq, long long d);
 cudaError_t launch_exact24(const Exact24Args& x, cudaStream_t s);
 
+// ---- intsm.cu
+cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, float sm_scale,
+                              const int8_t* q_codes, const float* q_scale, const int8_t* k_codes,
+                              const float* k_scale, const int8_t* v_codes, int8_t* out,
+                              cudaStream_t s);
+
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& a, cudaStream_t s);

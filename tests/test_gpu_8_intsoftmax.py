@@ -1,0 +1,63 @@
+"""qattn_fwd_intsoftmax (QFlash's integer-only attention) against the oracle's
+attn_intsoftmax: every step is integer arithmetic, so the int8 output codes
+must match bit for bit, on the ViT/DeiT and Swin-window shapes."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import qattn_oracle as O
+from quantized_attention_gb300 import binding as qb
+from quantized_attention_gb300 import inputs as I
+from tests.gpu_common import ensure_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+CASES = [
+    I.small("vit", B=2, Hq=3, Hkv=3),                       # DeiT-Tiny heads, N 197, d 64
+    I.small("vit", B=1, Hq=12, Hkv=12),                     # ViT-Base heads
+    I.small("swin", B=16, Hq=3, Hkv=3, has_bias=False),     # Swin stage-1 windows, N 49, d 32
+    I.small("vit", B=1, Hq=4, Hkv=2, Nq=100, Nk=300),       # GQA, ragged tiles
+    I.small("vit", B=1, Hq=2, Hkv=2, Nq=70, Nk=150, d=128),
+]
+
+
+def _ids(w):
+    return f"B{w.B}-H{w.Hq}/{w.Hkv}-q{w.Nq}-k{w.Nk}-d{w.d}"
+
+
+def _tensor_codes(x):
+    s = np.float32(np.abs(x).max() / np.float32(127.0))
+    return np.clip(np.rint(x / s), -127, 127).astype(np.int8), s
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
+def test_intsoftmax_bit_exact(wl):
+    inp = I.make_inputs(wl)
+    qc, sq = _tensor_codes(inp.Q * 2.0)   # sharper rows than N(0, 1) scores give
+    kc, sk = _tensor_codes(inp.K * 2.0)
+    vc, _ = _tensor_codes(inp.V)
+    want = O.attn_intsoftmax(qc, sq, kc, sk, vc)
+    dev = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dt)
+    out = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d), dtype=torch.int8, device="cuda")
+    qb.fwd_intsoftmax(dev(qc, torch.int8), dev(np.array([sq]), torch.float32), dev(kc, torch.int8),
+                      dev(np.array([sk]), torch.float32), dev(vc, torch.int8),
+                      qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d), qb.make_params(), out)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    got = out.cpu().numpy().reshape(want.shape).astype(np.int64)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
+
+
+def test_intsoftmax_rejects_causal():
+    p = qb.make_params(causal=True)
+    z = torch.zeros(64 * 64, dtype=torch.int8, device="cuda")
+    f = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(qb.QattnError):
+        qb.fwd_intsoftmax(z, f, z, f, z, qb.make_shape(1, 1, 1, 64, 64, 64), p, z)
