@@ -719,8 +719,10 @@ def shift_exp2(X, x0):
 
 def requant_p(P, M, r):
     """QFlash's requantization (section 4.4, eq. (10)): Y = (X * M) >> r,
-    clamped to the int8 codes [0, 127] of P's scale 1/127."""
-    return np.minimum((np.asarray(P, np.int64) * M) >> r, 127)
+    clamped to the int8 codes [0, 127] of P's scale 1/127.  The shift is a
+    multiplication by 2^-r, so a negative r (s~ > 2) shifts left."""
+    PM = np.asarray(P, np.int64) * M
+    return np.minimum(PM >> r if r >= 0 else PM << -r, 127)
 
 
 def scale_release(x, alpha, x0):

@@ -54,6 +54,15 @@ def test_requant_maps_one_to_the_top_code():
         assert np.all(np.diff(Y) >= 0) and np.abs(Y - P * 127.0 / x0).max() <= 1.5
 
 
+def test_requant_with_a_negative_shift_saturates():
+    """s~ > 2 (coarse scales): ratio = 127 s~ > 256, so n > 8 and r < 0; every
+    P >= 1 is worth more than 127 codes and saturates, P = 0 stays 0."""
+    st, x0, M, r = O.intsm_constants(4.0, 4.0, 0.125)
+    assert float(st) > 2 and r < 0 and x0 == 1
+    assert O.requant_p(np.array([0, 1, 2, 5]), M, r).tolist() == [0, 127, 127, 127]
+    assert np.floor(1 * 127 * float(st)) > 127
+
+
 def test_single_tile_against_python_integers():
     """One key tile: no rescale happens; Python-integer loops give the same
     codes (exp by the page's decomposition, requantization, floor division)."""
