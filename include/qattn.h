@@ -302,7 +302,10 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
  *   k_codes, v_codes  int8 [B][Hkv][Nk][d]; k_scale fp32[1] (device)
  *   O_codes  (out) int8 [B][Hq][Nq][d]
  *   params: sm_scale (0 -> fp32(1/sqrt(d))); causal must be 0
- * Limits: d in {32, 64, 128}, B * Hq <= 65535, no mask.  No workspace.
+ * Limits: d in {32, 64, 128}, B * Hq <= 65535, Nk <= 131072 (int32 O), no
+ * mask, O_codes 16-byte aligned.  No workspace.  The scales are read on the
+ * device: if s~ is not a positive finite number or 1/s~ > 2^30 the kernel
+ * writes nothing and qattn_get_error() returns QATTN_ERR_INVALID_ARG.
  */
 qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
                                   const int8_t* k_codes, const float* k_scale,
@@ -344,7 +347,9 @@ qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
                                    size_t workspace_bytes, qattn_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of
- * the current device (QATTN_ERR_TIMEOUT if a kernel gave up on a wait). */
+ * the current device (QATTN_ERR_TIMEOUT if a kernel gave up on a wait,
+ * QATTN_ERR_INVALID_ARG if a kernel found device-held scales outside its
+ * domain). */
 qattn_status qattn_get_error(qattn_stream_t stream);
 
 #ifdef __cplusplus

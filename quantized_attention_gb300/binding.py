@@ -16,6 +16,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 _lib = None
 
 OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = 1, 2, 3, 4, 5
 GRAN_TENSOR, GRAN_HEAD, GRAN_BLOCK = 0, 1, 2
 DT_BF16, DT_F32, DT_I8, DT_E4M3 = 0, 1, 2, 3
 POS0_BOTTOM_RIGHT = -(2 ** 63)

@@ -8,11 +8,22 @@
 // its definition, the paper's Appendix B.1, is not in the pages) and O += P.V
 // in int32; out = floor(O / l) as int8 codes of V's scale.
 //
-// Both products run on the warp-level int8 tensor cores (mma.m16n8k32 s8,
-// exact int32); the workloads (ViT/DeiT/Swin windows, N <= 197) are small.
-// Every step is integer arithmetic, so the result is bit-exact with the
-// oracle.
+// Both products run on the warp-level fp16 tensor cores (mma.m16n8k16, fp32
+// accumulation), which on this GPU run about four times the int8 warp MMA:
+// the int8 codes and the P codes (0..127) are exact fp16 values and every
+// partial sum is an integer below 2^24 (|q.k| <= 128^2 * 128 = 2^21; a tile's
+// P.V <= 64 * 127 * 128), so the fp32 accumulator holds it exactly and the
+// products are the int32 ones.  Every other step is integer arithmetic, so the
+// result is bit-exact with the oracle.
+//
+// CTA: 16 * W query rows of one (batch, head), W <= 8 warps sized to Nq so a
+// ViT row count (197) splits into two CTAs of 7 warps.  Per 64-key tile the
+// K and V codes are staged by cp.async while the previous tile computes, then
+// converted once to fp16 rows that ldmatrix reads (V transposed); S stays in
+// registers and the P codes go straight into the A fragments of the PV
+// product.
 #include <climits>
+#include <cmath>
 #include <cuda_runtime.h>
 
 #include "qattn_internal.h"
@@ -21,73 +32,140 @@
 namespace qattn {
 namespace {
 
-constexpr int kTile = 64;   // keys per tile (Bc)
-constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
-constexpr int kThreads = 128;
+constexpr int kTile = 64;        // keys per tile (Bc): the points where O is rescaled
+constexpr int kMaxWarps = 8;     // 16 query rows per warp
 constexpr int kM0 = -(1 << 21);  // initial running max
+constexpr float kMaxX0 = 1073741824.0f;               // 2^30: a larger X0 leaves the int32 domain
 constexpr float kLog2e = 1.44269502162933349609375f;  // fp32(log2 e)
 
-__device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                             uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 struct IntsmConst {
-  int x0;        // rint(1 / s~)
-  float inv_x0;  // 1 / x0 (for the quotient estimate)
-  int M, r;      // P requantization: (P * M) >> r
+  int x0;                   // rint(1 / s~)
+  int M, r;                 // P requantization (P * M) >> r; r < 0 is stored as M = 128, r = 0
+  uint32_t dm;              // floor(n / x0) = umulhi(n * 2^9, dm) >> dl for n < 2^23
+  int dl;                   // ceil(log2 x0)
+  unsigned long long cfix;  // floor(2^62 / x0)
 };
 
 // The constants from the per-tensor scales, in the oracle's fp32 steps.
-__device__ __forceinline__ IntsmConst intsm_constants(float sq, float sk, float sm_scale) {
-  IntsmConst c;
+// False when s~ is not a positive finite number or X0 exceeds 2^30.
+__device__ __forceinline__ bool intsm_constants(float sq, float sk, float sm_scale, IntsmConst& c) {
   const float st = __fmul_rn(__fmul_rn(__fmul_rn(sq, sk), sm_scale), kLog2e);
-  c.x0 = max(1, __float2int_rn(__fdiv_rn(1.0f, st)));
-  c.inv_x0 = 1.0f / static_cast<float>(c.x0);
+  const float inv = __fdiv_rn(1.0f, st);
+  if (!(st > 0.f) || !(inv <= kMaxX0)) return false;
+  c.x0 = max(1, __float2int_rn(inv));
   const float ratio = __fmul_rn(127.0f, st);
   int e;
-  const float f = frexpf(ratio, &e);  // ratio = f * 2^e, f in [0.5, 1)
+  const float f = frexpf(ratio, &e);      // ratio = f * 2^e, f in [0.5, 1)
   const int n = (f == 0.5f) ? e - 1 : e;  // ceil(log2 ratio)
   c.r = 8 - n;
   c.M = __float2int_rn(ldexpf(ratio, c.r));  // exact scaling, then round
-  return c;
-}
-
-// ShiftExp2 for X <= 0 (|X| < 2^23): Q = X / X0 truncated toward zero, R in
-// (-X0, 0]; the quotient comes from a float estimate corrected once.
-__device__ __forceinline__ int shift_exp2(int X, const IntsmConst& c) {
-  int q = static_cast<int>(truncf(static_cast<float>(X) * c.inv_x0));
-  int R = X - q * c.x0;
-  if (R > 0) {  // the estimate was one too negative
-    ++q;
-    R -= c.x0;
-  } else if (R <= -c.x0) {  // one too large
-    --q;
-    R += c.x0;
+  if (c.r < 0) {  // ratio > 256: any P >= 1 saturates, as with a multiplier of 128
+    c.M = 128;
+    c.r = 0;
   }
-  const int sh = -q;
-  const int base = (R >> 1) + c.x0;
-  return (sh >= 31) ? 0 : (base >> sh);
+  // division by the invariant x0 (Granlund and Montgomery, "Division by
+  // Invariant Integers using Multiplication", 1994): with l = ceil(log2 x0)
+  // and m = ceil(2^(23 + l) / x0) < 2^24 + 1, floor(n m / 2^(23 + l)) =
+  // floor(n / x0) for every n < 2^23
+  const unsigned long long x0u = static_cast<unsigned long long>(c.x0);
+  c.dl = (c.x0 == 1) ? 0 : 32 - __clz(c.x0 - 1);
+  c.dm = static_cast<uint32_t>(((1ull << (23 + c.dl)) + x0u - 1) / x0u);
+  c.cfix = (1ull << 62) / x0u;
+  return true;
 }
 
-// floor(x * alpha / X0); the identity at alpha = X0 and 0 at alpha = 0.
-__device__ __forceinline__ int scale_release(int x, int alpha, const IntsmConst& c) {
-  if (alpha == c.x0) return x;
-  if (alpha == 0) return 0;
-  const long long p = static_cast<long long>(x) * alpha;
-  long long q = p / c.x0;
-  if (p % c.x0 != 0 && p < 0) --q;
-  return static_cast<int>(q);
+// ShiftExp2 of X = -n <= 0 (n < 2^23): X = Q X0 + R with Q = -floor(n / X0)
+// (truncation toward zero) and R = -(n mod X0); ((R >> 1) + X0) >> -Q, where
+// floor(-rr / 2) = -ceil(rr / 2) for rr = n mod X0.
+__device__ __forceinline__ int shift_exp2_neg(uint32_t n, const IntsmConst& c) {
+  const uint32_t q = __umulhi(n << 9, c.dm) >> c.dl;
+  const uint32_t rr = n - q * static_cast<uint32_t>(c.x0);
+  const int base = c.x0 - static_cast<int>((rr + 1) >> 1);
+  return base >> min(q, 31u);  // base < 2^31: a shift of 31 leaves 0
 }
+
+// P (scale s~) -> int8 code of scale 1/127: min((P * M) >> r, 127), the
+// 64-bit product as its two halves and a funnel shift (r <= 31).
+__device__ __forceinline__ int requant(int P, const IntsmConst& c) {
+  const uint32_t lo = static_cast<uint32_t>(P) * static_cast<uint32_t>(c.M);
+  const uint32_t hi = __umulhi(static_cast<uint32_t>(P), static_cast<uint32_t>(c.M));
+  return static_cast<int>(min(__funnelshift_r(lo, hi, c.r), 127u));
+}
+
+// ScaleRelease's per-row factor F = min(floor(alpha 2^31 / X0), 2^31 - 1):
+// alpha * floor(2^62 / X0) / 2^31 falls short of alpha 2^31 / X0 by less
+// than 1/2, so one step against the exact remainder completes the floor.
+__device__ __forceinline__ int rescale_factor(int alpha, const IntsmConst& c) {
+  const unsigned long long a = static_cast<unsigned long long>(alpha);
+  const unsigned long long x0u = static_cast<unsigned long long>(c.x0);
+  unsigned long long f = __umul64hi(a << 33, c.cfix);
+  if ((a << 31) - f * x0u >= x0u) ++f;
+  return static_cast<int>(min(f, 0x7fffffffull));
+}
+
+// ScaleRelease, floor(x * alpha / X0), for |x| < 2^31 and 0 <= alpha <= X0:
+// (x F) >> 31 is within one of the quotient, and the remainder (in
+// [-X0, 2 X0), exact in wrapping 32-bit arithmetic) gives the last step.
+__device__ __forceinline__ int scale_release(int x, int alpha, int F, const IntsmConst& c) {
+  int q = static_cast<int>((static_cast<long long>(x) * F) >> 31);
+  const int rem = static_cast<int>(static_cast<uint32_t>(x) * static_cast<uint32_t>(alpha) -
+                                   static_cast<uint32_t>(q) * static_cast<uint32_t>(c.x0));
+  if (rem < 0) --q;
+  else if (rem >= c.x0) ++q;
+  return q;
+}
+
+// An fp32 holding an integer v with |v| <= 2^22 -> v: v + 1.5 * 2^23 is exact
+// and carries v in its low mantissa bits.
+constexpr float kMagic = 12582912.0f;
+constexpr int kMagicBits = 0x4B400000;
+__device__ __forceinline__ int f2i_small(float v) { return __float_as_int(v + kMagic) - kMagicBits; }
 
 __device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
   int q = a / b;
   if ((a % b != 0) && (a < 0)) --q;
   return q;
 }
+
+// Two P codes (0..127) -> one f16x2 word: 0x6400 | y is the fp16 1024 + y,
+// and one f16x2 subtraction of 1024 leaves y (exact).
+__device__ __forceinline__ uint32_t codes2_to_f16x2(int y0, int y1) {
+  const uint32_t w = 0x64006400u | static_cast<uint32_t>(y0) | (static_cast<uint32_t>(y1) << 16);
+  uint32_t out;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(w), "r"(0x64006400u));
+  return out;
+}
+
+// D(16x8 f32) += A(16x16 f16) * B(16x8 f16).  a0/a2: row g, k = 2t, 2t+1 /
+// 2t+8, 2t+9; a1/a3: row g + 8; b0/b1: column g, k = 2t, 2t+1 / 2t+8, 2t+9;
+// d0, d1: row g, columns 2t, 2t+1; d2, d3: row g + 8.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// 16 bytes global -> shared through L2; src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 struct IntsmArgs {
   int B, Hq, Hkv, Nq, Nk;
@@ -98,182 +176,266 @@ struct IntsmArgs {
   const float* k_scale;
   const int8_t* v_codes;
   int8_t* out;
+  unsigned int* err;
 };
 
 template <int D>
 struct IntsmSmem {
-  static constexpr int kQPitch = D + 16;     // bytes per row (conflict-free fragment reads)
-  static constexpr int kQ = kRows * kQPitch;
-  static constexpr int kK = kTile * kQPitch;
-  static constexpr int kVPitch = kTile + 16;  // V^T rows: one per channel
-  static constexpr int kV = D * kVPitch;
-  static constexpr int kYPitch = kTile + 16;  // P codes, one row per query row
-  static constexpr int kY = kRows * kYPitch;
-  static constexpr int kBytes = kQ + kK + kV + kY;
+  static constexpr int kPitch = 2 * D + 16;     // bytes per fp16 row (conflict-free ldmatrix)
+  static constexpr int kKV = kTile * kPitch;    // one tile of K or V as fp16 rows
+  static constexpr int kStage = 2 * kTile * D;  // the next tile's K then V codes (int8)
+  static constexpr int bytes(int warps) { return 16 * warps * kPitch + 2 * kKV + kStage; }
 };
 
+// The codes of keys k0..k0+63 into the staging area (zeros past Nk).
 template <int D>
-__global__ void __launch_bounds__(kThreads) intsm_attn_kernel(const IntsmArgs a) {
+__device__ __forceinline__ void stage_tile(uint32_t st, const int8_t* kg, const int8_t* vg, int k0,
+                                           int Nk) {
+  constexpr int kChunks = kTile * D / 16;
+  for (int v = threadIdx.x; v < 2 * kChunks; v += blockDim.x) {
+    const int which = v / kChunks, rem = v % kChunks;
+    const int key = rem / (D / 16), c16 = rem % (D / 16);
+    const bool in = k0 + key < Nk;
+    const int8_t* src = (which ? vg : kg) + (in ? static_cast<size_t>(k0 + key) * D + 16 * c16 : 0);
+    cp_async16(st + 16 * v, src, in ? 16u : 0u);
+  }
+}
+
+// Staged codes -> exact fp16 rows of K and V.
+template <int D>
+__device__ __forceinline__ void convert_tile(const uint8_t* st, uint8_t* sk, uint8_t* sv) {
   using SM = IntsmSmem<D>;
-  constexpr int KS = D / 32;   // k-steps of the QK product
-  constexpr int NTO = D / 8;   // PV n-tiles
+  constexpr int kChunks = kTile * D / 16;
+  for (int v = threadIdx.x; v < 2 * kChunks; v += blockDim.x) {
+    const int which = v / kChunks, rem = v % kChunks;
+    const int key = rem / (D / 16), c16 = rem % (D / 16);
+    const uint4 x = *reinterpret_cast<const uint4*>(st + 16 * v);
+    uint32_t hv[8];
+    codes4_to_f16x2(x.x, hv[0], hv[1]);
+    codes4_to_f16x2(x.y, hv[2], hv[3]);
+    codes4_to_f16x2(x.z, hv[4], hv[5]);
+    codes4_to_f16x2(x.w, hv[6], hv[7]);
+    uint8_t* dst = (which ? sv : sk) + key * SM::kPitch + c16 * 32;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+  }
+}
+
+// One tile's softmax step for a lane's two rows (g and g + 8) from the exact
+// fp32 scores S (the m16n8 accumulator layout): the new running max m'
+// (quad-reduced), alpha = ShiftExp2(m - m'), the P codes Y =
+// requant(ShiftExp2(S - m')) packed as the PV A fragments (the accumulator
+// layout of 8 n-tiles is the A layout of 4 k-steps), and the lane's share of
+// the row sums, quad-reduced.  Tail: keys at or past nvalid take no part.
+template <bool Tail>
+__device__ __forceinline__ void softmax_tile(const float (&S)[8][4], int nvalid, int t4, const IntsmConst& c,
+                                             float& m_lo, float& m_hi, int& al_lo, int& al_hi, int& sum_lo,
+                                             int& sum_hi, uint32_t (&af)[4][4]) {
+  float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool v0 = !Tail || 8 * j + 2 * t4 < nvalid, v1 = !Tail || 8 * j + 2 * t4 + 1 < nvalid;
+    mx_lo = fmaxf(mx_lo, fmaxf(v0 ? S[j][0] : -INFINITY, v1 ? S[j][1] : -INFINITY));
+    mx_hi = fmaxf(mx_hi, fmaxf(v0 ? S[j][2] : -INFINITY, v1 ? S[j][3] : -INFINITY));
+  }
+#pragma unroll
+  for (int sh = 1; sh < 4; sh <<= 1) {
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, sh));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, sh));
+  }
+  const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+  // every score and the initial max are integers within 2^21 of zero, so all
+  // differences below are exact and at most 2^22
+  al_lo = shift_exp2_neg(static_cast<uint32_t>(f2i_small(mn_lo - m_lo)), c);
+  al_hi = shift_exp2_neg(static_cast<uint32_t>(f2i_small(mn_hi - m_hi)), c);
+  m_lo = mn_lo;
+  m_hi = mn_hi;
+  const float mb_lo = mn_lo + kMagic, mb_hi = mn_hi + kMagic;  // exact
+  int s_lo = 0, s_hi = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    int Y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t n = static_cast<uint32_t>(__float_as_int(((e < 2) ? mb_lo : mb_hi) - S[j][e]) - kMagicBits);
+      Y[e] = requant(shift_exp2_neg(n, c), c);
+      if (Tail && 8 * j + 2 * t4 + (e & 1) >= nvalid) Y[e] = 0;
+    }
+    s_lo += Y[0] + Y[1];
+    s_hi += Y[2] + Y[3];
+    af[j >> 1][2 * (j & 1)] = codes2_to_f16x2(Y[0], Y[1]);      // a0 / a2: row g
+    af[j >> 1][2 * (j & 1) + 1] = codes2_to_f16x2(Y[2], Y[3]);  // a1 / a3: row g + 8
+  }
+#pragma unroll
+  for (int sh = 1; sh < 4; sh <<= 1) {
+    s_lo += __shfl_xor_sync(0xffffffffu, s_lo, sh);
+    s_hi += __shfl_xor_sync(0xffffffffu, s_hi, sh);
+  }
+  sum_lo = s_lo;
+  sum_hi = s_hi;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_kernel(const IntsmArgs a) {
+  using SM = IntsmSmem<D>;
+  constexpr int KS = D / 16;              // k-steps of QK^T
+  constexpr int NTO = D / 8;              // PV n-tiles (8 channels each)
+  constexpr int NTH = NTO < 8 ? NTO : 8;  // n-tiles per PV pass
   extern __shared__ __align__(16) uint8_t smem[];
+  const int W = blockDim.x >> 5;
   uint8_t* sq = smem;
-  uint8_t* sk = smem + SM::kQ;
-  uint8_t* sv = smem + SM::kQ + SM::kK;
-  uint8_t* sy = smem + SM::kQ + SM::kK + SM::kV;
+  uint8_t* sk = sq + 16 * W * SM::kPitch;
+  uint8_t* sv = sk + SM::kKV;
+  uint8_t* sst = sv + SM::kKV;
   pdl_trigger();
   pdl_wait();
-  const IntsmConst c = intsm_constants(a.q_scale[0], a.k_scale[0], a.sm_scale);
+  IntsmConst c;
+  if (!intsm_constants(a.q_scale[0], a.k_scale[0], a.sm_scale, c)) {  // the same in every thread
+    if (threadIdx.x == 0) atomicOr(a.err, kErrDomain);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int bh = blockIdx.y, b = bh / a.Hq, h = bh % a.Hq;
   const int bkv = b * a.Hkv + h / (a.Hq / a.Hkv);
-  const int q0 = blockIdx.x * kRows;
+  const int q0 = blockIdx.x * 16 * W;
   const int8_t* qg = a.q_codes + static_cast<size_t>(bh) * a.Nq * D;
   const int8_t* kg = a.k_codes + static_cast<size_t>(bkv) * a.Nk * D;
   const int8_t* vg = a.v_codes + static_cast<size_t>(bkv) * a.Nk * D;
-  for (int v = threadIdx.x; v < kRows * (D / 16); v += kThreads) {
+  const uint32_t st_addr = smem_u32(sst);
+  stage_tile<D>(st_addr, kg, vg, 0, a.Nk);
+  // the CTA's Q rows as exact fp16 (zeros past Nq)
+  for (int v = threadIdx.x; v < 16 * W * (D / 16); v += blockDim.x) {
     const int r = v / (D / 16), c16 = v % (D / 16);
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (q0 + r < a.Nq) x = __ldg(reinterpret_cast<const uint4*>(qg + static_cast<size_t>(q0 + r) * D) + c16);
-    *reinterpret_cast<uint4*>(sq + r * SM::kQPitch + c16 * 16) = x;
+    if (q0 + r < a.Nq) x = *reinterpret_cast<const uint4*>(qg + static_cast<size_t>(q0 + r) * D + 16 * c16);
+    uint32_t hv[8];
+    codes4_to_f16x2(x.x, hv[0], hv[1]);
+    codes4_to_f16x2(x.y, hv[2], hv[3]);
+    codes4_to_f16x2(x.z, hv[4], hv[5]);
+    codes4_to_f16x2(x.w, hv[6], hv[7]);
+    uint8_t* dst = sq + r * SM::kPitch + c16 * 32;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
   }
-  int m_lo = kM0, m_hi = kM0, l_lo = 0, l_hi = 0;
+  cp_async_wait_all();
+  __syncthreads();
+  convert_tile<D>(sst, sk, sv);
+  __syncthreads();
+
+  float m_lo = static_cast<float>(kM0), m_hi = static_cast<float>(kM0);  // running max (integers)
+  int l_lo = 0, l_hi = 0;
   int o[NTO][4];
 #pragma unroll
   for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0;
-  const int rq = 16 * warp + g;  // this lane's rows rq, rq + 8 within the CTA
+  const bool active = q0 + 16 * warp < a.Nq;  // the warp has rows to compute
+  // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8
+  const int mrow = lane & 7, mat = lane >> 3;
+  const uint32_t q_addr = smem_u32(sq) + (16 * warp + mrow + (mat & 1) * 8) * SM::kPitch + (mat >> 1) * 16;
+  const uint32_t k_addr = smem_u32(sk) + (mrow + (mat >> 1) * 8) * SM::kPitch + (mat & 1) * 16;
+  const uint32_t v_addr = smem_u32(sv) + (mrow + (mat & 1) * 8) * SM::kPitch + (mat >> 1) * 16;
   for (int k0 = 0; k0 < a.Nk; k0 += kTile) {
-    __syncthreads();  // the previous tile is read
-    for (int v = threadIdx.x; v < kTile * (D / 16); v += kThreads) {
-      const int key = v / (D / 16), c16 = v % (D / 16);
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (k0 + key < a.Nk) x = __ldg(reinterpret_cast<const uint4*>(kg + static_cast<size_t>(k0 + key) * D) + c16);
-      *reinterpret_cast<uint4*>(sk + key * SM::kQPitch + c16 * 16) = x;
-    }
-    // V^T: item (4-key group kq, channel word cw) transposes 4 keys x 4 channels
-    for (int v = threadIdx.x; v < (kTile / 4) * (D / 4); v += kThreads) {
-      const int kq = v / (D / 4), cw = v % (D / 4);
-      uint32_t x[4];
+    const bool more = k0 + kTile < a.Nk;
+    if (more) stage_tile<D>(st_addr, kg, vg, k0 + kTile, a.Nk);  // overlaps this tile's math
+    if (active) {
+      // ---- S = q.k for the warp's 16 rows and the tile's 64 keys (exact in fp32)
+      float S[8][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + 4 * kq + e;
-        x[e] = (key < a.Nk) ? __ldg(reinterpret_cast<const uint32_t*>(vg + static_cast<size_t>(key) * D) + cw) : 0u;
+      for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(q_addr + ks * 32, a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(k_addr + 8 * j * SM::kPitch + ks * 32, b0, b1, b2, b3);
+          mma_f16_16816(S[j], a0, a1, a2, a3, b0, b1);
+          mma_f16_16816(S[j + 1], a0, a1, a2, a3, b2, b3);
+        }
       }
-      const uint32_t u0 = __byte_perm(x[0], x[1], 0x5140u), u1 = __byte_perm(x[0], x[1], 0x7362u);
-      const uint32_t u2 = __byte_perm(x[2], x[3], 0x5140u), u3 = __byte_perm(x[2], x[3], 0x7362u);
-      const uint32_t y[4] = {__byte_perm(u0, u2, 0x5410u), __byte_perm(u0, u2, 0x7632u),
-                             __byte_perm(u1, u3, 0x5410u), __byte_perm(u1, u3, 0x7632u)};
+      // ---- the running max, alpha, and the P codes as the PV A fragments
+      int al_lo, al_hi, sum_lo, sum_hi;
+      uint32_t af[4][4];
+      if (a.Nk - k0 >= kTile)
+        softmax_tile<false>(S, kTile, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+      else
+        softmax_tile<true>(S, a.Nk - k0, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+      // ---- l and O rescaled by alpha (ScaleRelease); the identity where the
+      // max stayed (alpha = X0), nothing to do on the first tile (l = O = 0)
+      if (k0 > 0 && __any_sync(0xffffffffu, (al_lo != c.x0) | (al_hi != c.x0))) {
+        const int F_lo = rescale_factor(al_lo, c), F_hi = rescale_factor(al_hi, c);
+        l_lo = scale_release(l_lo, al_lo, F_lo, c);
+        l_hi = scale_release(l_hi, al_hi, F_hi, c);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        *reinterpret_cast<uint32_t*>(sv + (4 * cw + e) * SM::kVPitch + 4 * kq) = y[e];
-    }
-    __syncthreads();
-    // ---- S = q.k for the warp's 16 rows and the tile's 64 keys (int32)
-    int S[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint8_t* qa = sq + rq * SM::kQPitch + 32 * ks + 4 * t4;
-      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(qa);
-      const uint32_t a2 = *reinterpret_cast<const uint32_t*>(qa + 16);
-      const uint32_t a1 = *reinterpret_cast<const uint32_t*>(qa + 8 * SM::kQPitch);
-      const uint32_t a3 = *reinterpret_cast<const uint32_t*>(qa + 8 * SM::kQPitch + 16);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint8_t* kb = sk + (8 * j + g) * SM::kQPitch + 32 * ks + 4 * t4;
-        mma_s8_16832(S[j], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(kb),
-                     *reinterpret_cast<const uint32_t*>(kb + 16));
+        for (int n = 0; n < NTO; ++n) {
+          o[n][0] = scale_release(o[n][0], al_lo, F_lo, c);
+          o[n][1] = scale_release(o[n][1], al_lo, F_lo, c);
+          o[n][2] = scale_release(o[n][2], al_hi, F_hi, c);
+          o[n][3] = scale_release(o[n][3], al_hi, F_hi, c);
+        }
       }
-    }
-    // keys past Nk take no part (every tile holds at least one valid key)
-    int mx_lo = INT_MIN, mx_hi = INT_MIN;
+      l_lo += sum_lo;
+      l_hi += sum_hi;
+      // ---- O += Y.V, 64 channels per pass (exact: a tile's sums stay below 2^24)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool v0 = k0 + 8 * j + 2 * t4 < a.Nk, v1 = k0 + 8 * j + 2 * t4 + 1 < a.Nk;
-      mx_lo = max(mx_lo, max(v0 ? S[j][0] : INT_MIN, v1 ? S[j][1] : INT_MIN));
-      mx_hi = max(mx_hi, max(v0 ? S[j][2] : INT_MIN, v1 ? S[j][3] : INT_MIN));
-    }
+      for (int hc = 0; hc < NTO / NTH; ++hc) {
+        float op[NTH][4];
 #pragma unroll
-    for (int sh = 1; sh < 4; sh <<= 1) {
-      mx_lo = max(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, sh));
-      mx_hi = max(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, sh));
-    }
-    const int mn_lo = max(m_lo, mx_lo), mn_hi = max(m_hi, mx_hi);
-    const int al_lo = shift_exp2(m_lo - mn_lo, c), al_hi = shift_exp2(m_hi - mn_hi, c);
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    // ---- P codes Y = requant(ShiftExp2(S - m)), row sums
-    int sum_lo = 0, sum_hi = 0;
-    uint8_t* yrow = sy + rq * SM::kYPitch;
+        for (int n = 0; n < NTH; ++n) op[n][0] = op[n][1] = op[n][2] = op[n][3] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+        for (int s = 0; s < 4; ++s) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // |X| < 2^23: scores lie within 127^2 * D of each other
-        const bool valid = k0 + 8 * j + 2 * t4 + (e & 1) < a.Nk;
-        const int P = valid ? shift_exp2(S[j][e] - ((e < 2) ? mn_lo : mn_hi), c) : 0;
-        const int Y = min((P * c.M) >> c.r, 127);
-        if (e < 2) sum_lo += Y;
-        else sum_hi += Y;
-        yrow[((e < 2) ? 0 : 8 * SM::kYPitch) + 8 * j + 2 * t4 + (e & 1)] = static_cast<uint8_t>(Y);
+          for (int n = 0; n < NTH; n += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(v_addr + 16 * s * SM::kPitch + (hc * NTH + n) * 16, b0, b1, b2, b3);
+            mma_f16_16816(op[n], af[s][0], af[s][1], af[s][2], af[s][3], b0, b1);
+            mma_f16_16816(op[n + 1], af[s][0], af[s][1], af[s][2], af[s][3], b2, b3);
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < NTH; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[hc * NTH + n][e] += f2i_small(op[n][e]);
+        }
       }
     }
-#pragma unroll
-    for (int sh = 1; sh < 4; sh <<= 1) {
-      sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, sh);
-      sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, sh);
+    if (more) {
+      cp_async_wait_all();
+      __syncthreads();  // this tile's fp16 rows are read; the next tile's codes have landed
+      convert_tile<D>(sst, sk, sv);
+      __syncthreads();
     }
-    l_lo = scale_release(l_lo, al_lo, c) + sum_lo;
-    l_hi = scale_release(l_hi, al_hi, c) + sum_hi;
-#pragma unroll
-    for (int n = 0; n < NTO; ++n) {
-      o[n][0] = scale_release(o[n][0], al_lo, c);
-      o[n][1] = scale_release(o[n][1], al_lo, c);
-      o[n][2] = scale_release(o[n][2], al_hi, c);
-      o[n][3] = scale_release(o[n][3], al_hi, c);
-    }
-    __syncwarp();  // the warp's P codes are written
-    // ---- O += Y.V: A = P codes (rows x 32 keys), B = V^T (4 keys of a channel per word)
-#pragma unroll
-    for (int ks = 0; ks < kTile / 32; ++ks) {
-      const uint8_t* ya = yrow + 32 * ks + 4 * t4;
-      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(ya);
-      const uint32_t a2 = *reinterpret_cast<const uint32_t*>(ya + 16);
-      const uint32_t a1 = *reinterpret_cast<const uint32_t*>(ya + 8 * SM::kYPitch);
-      const uint32_t a3 = *reinterpret_cast<const uint32_t*>(ya + 8 * SM::kYPitch + 16);
-#pragma unroll
-      for (int n = 0; n < NTO; ++n) {
-        const uint8_t* vb = sv + (8 * n + g) * SM::kVPitch + 32 * ks + 4 * t4;
-        mma_s8_16832(o[n], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(vb),
-                     *reinterpret_cast<const uint32_t*>(vb + 16));
-      }
-    }
-    __syncwarp();  // the P codes are read before the next tile rewrites them
   }
+  if (!active) return;
   // ---- out = floor(O / l), int8 codes of V's scale
-  const int r_lo = q0 + rq, r_hi = r_lo + 8;
+  const int r_lo = q0 + 16 * warp + g, r_hi = r_lo + 8;
+  const int dl_lo = max(l_lo, 1), dl_hi = max(l_hi, 1);
 #pragma unroll
   for (int n = 0; n < NTO; ++n) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = (e < 2) ? r_lo : r_hi;
+    for (int half = 0; half < 2; ++half) {
+      const int row = half ? r_hi : r_lo;
       if (row >= a.Nq) continue;
-      const int l = max((e < 2) ? l_lo : l_hi, 1);
-      const int val = min(127, max(-127, floor_div(o[n][e], l)));
-      a.out[(static_cast<size_t>(bh) * a.Nq + row) * D + 8 * n + 2 * t4 + (e & 1)] = static_cast<int8_t>(val);
+      const int dl = half ? dl_hi : dl_lo;
+      const int v0 = min(127, max(-127, floor_div(o[n][2 * half], dl)));
+      const int v1 = min(127, max(-127, floor_div(o[n][2 * half + 1], dl)));
+      const uint16_t pair = static_cast<uint16_t>((v0 & 0xff) | ((v1 & 0xff) << 8));
+      *reinterpret_cast<uint16_t*>(a.out + (static_cast<size_t>(bh) * a.Nq + row) * D + 8 * n + 2 * t4) = pair;
     }
   }
 }
 
 template <int D>
 cudaError_t launch_t(const IntsmArgs& a, cudaStream_t s) {
-  constexpr int smem = IntsmSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(intsm_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the 16-row blocks split evenly over the fewest CTAs of at most 8 warps
+  const int nblk = (a.Nq + 15) / 16;
+  const int per_head = (nblk + kMaxWarps - 1) / kMaxWarps;
+  const int W = (nblk + per_head - 1) / per_head;
+  cudaError_t e = cudaFuncSetAttribute(intsm_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       IntsmSmem<D>::bytes(kMaxWarps));
   if (e != cudaSuccess) return e;
-  return launch_pdl(intsm_attn_kernel<D>, dim3((a.Nq + kRows - 1) / kRows, a.B * a.Hq), dim3(kThreads), smem,
+  return launch_pdl(intsm_attn_kernel<D>, dim3(per_head, a.B * a.Hq), dim3(32 * W), IntsmSmem<D>::bytes(W),
                     s, a);
 }
 
@@ -282,8 +444,8 @@ cudaError_t launch_t(const IntsmArgs& a, cudaStream_t s) {
 cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, float sm_scale,
                               const int8_t* q_codes, const float* q_scale, const int8_t* k_codes,
                               const float* k_scale, const int8_t* v_codes, int8_t* out,
-                              cudaStream_t s) {
-  IntsmArgs a{B, Hq, Hkv, Nq, Nk, sm_scale, q_codes, q_scale, k_codes, k_scale, v_codes, out};
+                              unsigned int* err, cudaStream_t s) {
+  IntsmArgs a{B, Hq, Hkv, Nq, Nk, sm_scale, q_codes, q_scale, k_codes, k_scale, v_codes, out, err};
   if (d == 32) return launch_t<32>(a, s);
   if (d == 64) return launch_t<64>(a, s);
   return launch_t<128>(a, s);

@@ -535,9 +535,11 @@ qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
   if ((st = check_params(params)) != QATTN_OK) return st;
   if (empty_problem(shape)) return QATTN_OK;
   if (shape->d != 32 && shape->d != 64 && shape->d != 128) return QATTN_ERR_UNSUPPORTED;
-  if (params->causal || shape->Nk == 0 || shape->B * shape->Hq > 65535) return QATTN_ERR_UNSUPPORTED;
+  // Nk <= 2^17 keeps |O| <= 127 * 128 * Nk inside int32
+  if (params->causal || shape->Nk == 0 || shape->Nk > (int64_t{1} << 17) || shape->B * shape->Hq > 65535)
+    return QATTN_ERR_UNSUPPORTED;
   if (!q_codes || !aligned16(q_codes) || !k_codes || !aligned16(k_codes) || !v_codes ||
-      !aligned16(v_codes) || !O_codes || !q_scale || !k_scale)
+      !aligned16(v_codes) || !O_codes || !aligned16(O_codes) || !q_scale || !k_scale)
     return QATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q_scale) & 3u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u))
     return QATTN_ERR_INVALID_ARG;
@@ -546,7 +548,7 @@ qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
   return from_cuda(qattn::launch_intsoftmax(
       static_cast<int>(shape->B), static_cast<int>(shape->Hq), static_cast<int>(shape->Hkv),
       static_cast<int>(shape->Nq), static_cast<int>(shape->Nk), static_cast<int>(shape->d), sm, q_codes,
-      q_scale, k_codes, k_scale, v_codes, O_codes, reinterpret_cast<cudaStream_t>(stream)));
+      q_scale, k_codes, k_scale, v_codes, O_codes, error_word(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,
@@ -581,7 +583,8 @@ qattn_status qattn_get_error(qattn_stream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_qattn_error_word, &zero, sizeof(zero)) != cudaSuccess) return QATTN_ERR_CUDA;
   }
-  return (v & qattn::kErrTimeout) ? QATTN_ERR_TIMEOUT : QATTN_OK;
+  if (v & qattn::kErrTimeout) return QATTN_ERR_TIMEOUT;
+  return (v & qattn::kErrDomain) ? QATTN_ERR_INVALID_ARG : QATTN_OK;
 }
 
 }  // extern "C"

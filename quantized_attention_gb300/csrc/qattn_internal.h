@@ -37,6 +37,7 @@ inline int num_sms() {
 
 // Bits of the device error word.
 constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrDomain = 2u;  // device-held scales outside a kernel's domain
 
 struct AttnArgs {
   int B, Hq, Hkv, Nq, Nk, d;
@@ -153,7 +154,7 @@ cudaError_t launch_exact24(const Exact24Args& x, cudaStream_t s);
 cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, float sm_scale,
                               const int8_t* q_codes, const float* q_scale, const int8_t* k_codes,
                               const float* k_scale, const int8_t* v_codes, int8_t* out,
-                              cudaStream_t s);
+                              unsigned int* err, cudaStream_t s);
 
 // ---- attn_fwd.cu
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

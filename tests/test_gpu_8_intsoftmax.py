@@ -24,6 +24,8 @@ CASES = [
     I.small("swin", B=16, Hq=3, Hkv=3, has_bias=False),     # Swin stage-1 windows, N 49, d 32
     I.small("vit", B=1, Hq=4, Hkv=2, Nq=100, Nk=300),       # GQA, ragged tiles
     I.small("vit", B=1, Hq=2, Hkv=2, Nq=70, Nk=150, d=128),
+    I.small("vit", B=1, Hq=2, Hkv=1, Nq=300, Nk=129),       # 3 CTAs per head; a 1-key tail tile
+    I.small("vit", B=1, Hq=1, Hkv=1, Nq=1, Nk=1, d=32),      # one row, one key
 ]
 
 
@@ -36,6 +38,23 @@ def _tensor_codes(x):
     return np.clip(np.rint(x / s), -127, 127).astype(np.int8), s
 
 
+def _run(wl, qc, sq, kc, sk, vc, fill=0):
+    dev = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dt)
+    out = torch.full((wl.B, wl.Hq, wl.Nq, wl.d), fill, dtype=torch.int8, device="cuda")
+    qb.fwd_intsoftmax(dev(qc, torch.int8), dev(np.array([sq], np.float32), torch.float32),
+                      dev(kc, torch.int8), dev(np.array([sk], np.float32), torch.float32),
+                      dev(vc, torch.int8), qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d),
+                      qb.make_params(), out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.int64)
+
+
+def _check(got, want):
+    got = got.reshape(want.shape)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
+
+
 @pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
 def test_intsoftmax_bit_exact(wl):
     inp = I.make_inputs(wl)
@@ -43,16 +62,37 @@ def test_intsoftmax_bit_exact(wl):
     kc, sk = _tensor_codes(inp.K * 2.0)
     vc, _ = _tensor_codes(inp.V)
     want = O.attn_intsoftmax(qc, sq, kc, sk, vc)
-    dev = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dt)
-    out = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d), dtype=torch.int8, device="cuda")
-    qb.fwd_intsoftmax(dev(qc, torch.int8), dev(np.array([sq]), torch.float32), dev(kc, torch.int8),
-                      dev(np.array([sk]), torch.float32), dev(vc, torch.int8),
-                      qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d), qb.make_params(), out)
-    torch.cuda.synchronize()
+    got = _run(wl, qc, sq, kc, sk, vc)
     assert qb.get_error() == 0
-    got = out.cpu().numpy().reshape(want.shape).astype(np.int64)
-    bad = np.argwhere(got != want)
-    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
+    _check(got, want)
+
+
+def test_intsoftmax_coarse_scales_bit_exact():
+    """s~ > 2: X0 = 1 and the requantization shift is negative (every P >= 1
+    saturates); the rescale runs with alpha in {0, 1}."""
+    wl = CASES[0]
+    inp = I.make_inputs(wl)
+    qc, _ = _tensor_codes(inp.Q)
+    kc, _ = _tensor_codes(inp.K)
+    vc, _ = _tensor_codes(inp.V)
+    want = O.attn_intsoftmax(qc, np.float32(4.0), kc, np.float32(4.0), vc)
+    got = _run(wl, qc, np.float32(4.0), kc, np.float32(4.0), vc)
+    assert qb.get_error() == 0
+    _check(got, want)
+
+
+def test_intsoftmax_scales_outside_the_domain_flagged():
+    """1/s~ above 2^30: the kernel writes nothing and the error word reports
+    an invalid argument (the scales live on the device)."""
+    wl = CASES[0]
+    inp = I.make_inputs(wl)
+    qc, _ = _tensor_codes(inp.Q)
+    kc, _ = _tensor_codes(inp.K)
+    vc, _ = _tensor_codes(inp.V)
+    got = _run(wl, qc, np.float32(1e-6), kc, np.float32(1e-6), vc, fill=55)
+    assert qb.get_error() == qb.ERR_INVALID_ARG
+    assert np.all(got == 55)
+    assert qb.get_error() == 0  # read and cleared
 
 
 def test_intsoftmax_rejects_causal():
