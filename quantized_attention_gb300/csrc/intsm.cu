@@ -43,8 +43,21 @@ struct IntsmConst {
   int M, r;                 // P requantization (P * M) >> r; r < 0 is stored as M = 128, r = 0
   uint32_t dm;              // floor(n / x0) = umulhi(n * 2^9, dm) >> dl for n < 2^23
   int dl;                   // ceil(log2 x0)
+  uint32_t k0, k1;          // ShiftExp2 from an fp32's bits (below): -512 * kMagicBits, 2 x0 + kMagicBits
   unsigned long long cfix;  // floor(2^62 / x0)
 };
+
+// An fp32 holding an integer v with |v| <= 2^22 -> v: v + 1.5 * 2^23 is exact
+// and carries v in its low mantissa bits.
+constexpr float kMagic = 12582912.0f;
+constexpr int kMagicBits = 0x4B400000;
+__device__ __forceinline__ int f2i_small(float v) { return __float_as_int(v + kMagic) - kMagicBits; }
+
+__device__ __forceinline__ uint32_t shr_clamped(uint32_t v, uint32_t s) {  // 0 once s >= 32
+  uint32_t r;
+  asm("shr.u32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
 
 // The constants from the per-tensor scales, in the oracle's fp32 steps.
 // False when s~ is not a positive finite number or X0 exceeds 2^30.
@@ -71,23 +84,28 @@ __device__ __forceinline__ bool intsm_constants(float sq, float sk, float sm_sca
   c.dl = (c.x0 == 1) ? 0 : 32 - __clz(c.x0 - 1);
   c.dm = static_cast<uint32_t>(((1ull << (23 + c.dl)) + x0u - 1) / x0u);
   c.cfix = (1ull << 62) / x0u;
+  c.k0 = 0u - 512u * static_cast<uint32_t>(kMagicBits);
+  c.k1 = 2u * static_cast<uint32_t>(c.x0) + static_cast<uint32_t>(kMagicBits);
   return true;
 }
 
-// ShiftExp2 of X = -n <= 0 (n < 2^23): X = Q X0 + R with Q = -floor(n / X0)
-// (truncation toward zero) and R = -(n mod X0); ((R >> 1) + X0) >> -Q, where
-// floor(-rr / 2) = -ceil(rr / 2) for rr = n mod X0.
-__device__ __forceinline__ int shift_exp2_neg(uint32_t n, const IntsmConst& c) {
-  const uint32_t q = __umulhi(n << 9, c.dm) >> c.dl;
-  const uint32_t rr = n - q * static_cast<uint32_t>(c.x0);
-  const int base = c.x0 - static_cast<int>((rr + 1) >> 1);
-  return base >> min(q, 31u);  // base < 2^31: a shift of 31 leaves 0
+// ShiftExp2 of X = -n <= 0 (0 <= n <= 2^22), given bits = the fp32 bits of
+// n + 1.5 * 2^23: X = Q X0 + R with Q = -floor(n / X0) (truncation toward
+// zero) and R = -(n mod X0), and ((R >> 1) + X0) >> -Q = (2 X0 - (n mod X0))
+// >> (1 - Q), where 2 X0 - (n mod X0) = (floor(n / X0) + 2) X0 - n.
+__device__ __forceinline__ int shift_exp2_bits(uint32_t bits, const IntsmConst& c) {
+  const uint32_t q = __umulhi(bits * 512u + c.k0, c.dm) >> c.dl;  // floor(n / X0)
+  const uint32_t u = q * static_cast<uint32_t>(c.x0) + (c.k1 - bits);
+  return static_cast<int>(shr_clamped(u, q + 1));  // u <= 2 X0 <= 2^31
 }
 
-// P (scale s~) -> int8 code of scale 1/127: min((P * M) >> r, 127), the
-// 64-bit product as its two halves and a funnel shift (r <= 31).
+// P (scale s~) -> int8 code of scale 1/127: min((P * M) >> r, 127).  Narrow
+// (X0 < 2^23, so P M < 2^31): one 32-bit product; else the 64-bit product as
+// its two halves and a funnel shift (r <= 31).
+template <bool Narrow>
 __device__ __forceinline__ int requant(int P, const IntsmConst& c) {
   const uint32_t lo = static_cast<uint32_t>(P) * static_cast<uint32_t>(c.M);
+  if (Narrow) return static_cast<int>(min(lo >> c.r, 127u));
   const uint32_t hi = __umulhi(static_cast<uint32_t>(P), static_cast<uint32_t>(c.M));
   return static_cast<int>(min(__funnelshift_r(lo, hi, c.r), 127u));
 }
@@ -115,15 +133,14 @@ __device__ __forceinline__ int scale_release(int x, int alpha, int F, const Ints
   return q;
 }
 
-// An fp32 holding an integer v with |v| <= 2^22 -> v: v + 1.5 * 2^23 is exact
-// and carries v in its low mantissa bits.
-constexpr float kMagic = 12582912.0f;
-constexpr int kMagicBits = 0x4B400000;
-__device__ __forceinline__ int f2i_small(float v) { return __float_as_int(v + kMagic) - kMagicBits; }
-
-__device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
-  int q = a / b;
-  if ((a % b != 0) && (a < 0)) --q;
+// floor(o / l) for |o| < 2^31 and 1 <= l < 2^30, with Fi = min(floor(2^31 / l),
+// 2^31 - 1): (o Fi) >> 31 is within one of the quotient and the remainder
+// (in [-l, 2 l), exact in wrapping 32-bit arithmetic) gives the last step.
+__device__ __forceinline__ int floor_div_recip(int o, int l, uint32_t Fi) {
+  int q = static_cast<int>((static_cast<long long>(o) * static_cast<long long>(Fi)) >> 31);
+  const int rem = static_cast<int>(static_cast<uint32_t>(o) - static_cast<uint32_t>(q) * static_cast<uint32_t>(l));
+  if (rem < 0) --q;
+  else if (rem >= l) ++q;
   return q;
 }
 
@@ -227,7 +244,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t* st, uint8_t* sk, uin
 // requant(ShiftExp2(S - m')) packed as the PV A fragments (the accumulator
 // layout of 8 n-tiles is the A layout of 4 k-steps), and the lane's share of
 // the row sums, quad-reduced.  Tail: keys at or past nvalid take no part.
-template <bool Tail>
+template <bool Tail, bool Narrow>
 __device__ __forceinline__ void softmax_tile(const float (&S)[8][4], int nvalid, int t4, const IntsmConst& c,
                                              float& m_lo, float& m_hi, int& al_lo, int& al_hi, int& sum_lo,
                                              int& sum_hi, uint32_t (&af)[4][4]) {
@@ -246,8 +263,8 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[8][4], int nvalid,
   const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
   // every score and the initial max are integers within 2^21 of zero, so all
   // differences below are exact and at most 2^22
-  al_lo = shift_exp2_neg(static_cast<uint32_t>(f2i_small(mn_lo - m_lo)), c);
-  al_hi = shift_exp2_neg(static_cast<uint32_t>(f2i_small(mn_hi - m_hi)), c);
+  al_lo = shift_exp2_bits(__float_as_uint((mn_lo - m_lo) + kMagic), c);
+  al_hi = shift_exp2_bits(__float_as_uint((mn_hi - m_hi) + kMagic), c);
   m_lo = mn_lo;
   m_hi = mn_hi;
   const float mb_lo = mn_lo + kMagic, mb_hi = mn_hi + kMagic;  // exact
@@ -257,8 +274,7 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[8][4], int nvalid,
     int Y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t n = static_cast<uint32_t>(__float_as_int(((e < 2) ? mb_lo : mb_hi) - S[j][e]) - kMagicBits);
-      Y[e] = requant(shift_exp2_neg(n, c), c);
+      Y[e] = requant<Narrow>(shift_exp2_bits(__float_as_uint(((e < 2) ? mb_lo : mb_hi) - S[j][e]), c), c);
       if (Tail && 8 * j + 2 * t4 + (e & 1) >= nvalid) Y[e] = 0;
     }
     s_lo += Y[0] + Y[1];
@@ -294,6 +310,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_ke
     if (threadIdx.x == 0) atomicOr(a.err, kErrDomain);
     return;
   }
+  const bool narrow = c.x0 < (1 << 23);  // P * M < 2^31
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int bh = blockIdx.y, b = bh / a.Hq, h = bh % a.Hq;
@@ -357,10 +374,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_ke
       // ---- the running max, alpha, and the P codes as the PV A fragments
       int al_lo, al_hi, sum_lo, sum_hi;
       uint32_t af[4][4];
-      if (a.Nk - k0 >= kTile)
-        softmax_tile<false>(S, kTile, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
-      else
-        softmax_tile<true>(S, a.Nk - k0, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+      const int nvalid = a.Nk - k0;
+      if (narrow) {
+        if (nvalid >= kTile)
+          softmax_tile<false, true>(S, kTile, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+        else
+          softmax_tile<true, true>(S, nvalid, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+      } else {
+        if (nvalid >= kTile)
+          softmax_tile<false, false>(S, kTile, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+        else
+          softmax_tile<true, false>(S, nvalid, t4, c, m_lo, m_hi, al_lo, al_hi, sum_lo, sum_hi, af);
+      }
       // ---- l and O rescaled by alpha (ScaleRelease); the identity where the
       // max stayed (alpha = X0), nothing to do on the first tile (l = O = 0)
       if (k0 > 0 && __any_sync(0xffffffffu, (al_lo != c.x0) | (al_hi != c.x0))) {
@@ -411,6 +436,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_ke
   // ---- out = floor(O / l), int8 codes of V's scale
   const int r_lo = q0 + 16 * warp + g, r_hi = r_lo + 8;
   const int dl_lo = max(l_lo, 1), dl_hi = max(l_hi, 1);
+  const uint32_t fi_lo = (dl_lo == 1) ? 0x7fffffffu : 0x80000000u / static_cast<uint32_t>(dl_lo);
+  const uint32_t fi_hi = (dl_hi == 1) ? 0x7fffffffu : 0x80000000u / static_cast<uint32_t>(dl_hi);
 #pragma unroll
   for (int n = 0; n < NTO; ++n) {
 #pragma unroll
@@ -418,8 +445,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_ke
       const int row = half ? r_hi : r_lo;
       if (row >= a.Nq) continue;
       const int dl = half ? dl_hi : dl_lo;
-      const int v0 = min(127, max(-127, floor_div(o[n][2 * half], dl)));
-      const int v1 = min(127, max(-127, floor_div(o[n][2 * half + 1], dl)));
+      const uint32_t fi = half ? fi_hi : fi_lo;
+      const int v0 = min(127, max(-127, floor_div_recip(o[n][2 * half], dl, fi)));
+      const int v1 = min(127, max(-127, floor_div_recip(o[n][2 * half + 1], dl, fi)));
       const uint16_t pair = static_cast<uint16_t>((v0 & 0xff) | ((v1 & 0xff) << 8));
       *reinterpret_cast<uint16_t*>(a.out + (static_cast<size_t>(bh) * a.Nq + row) * D + 8 * n + 2 * t4) = pair;
     }

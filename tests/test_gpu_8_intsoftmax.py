@@ -81,6 +81,23 @@ def test_intsoftmax_coarse_scales_bit_exact():
     _check(got, want)
 
 
+def test_intsoftmax_fine_scales_bit_exact():
+    """Fine scales: X0 ~ 2.2e7 > 2^23, so P * M needs 64 bits (the kernel's
+    wide requantization path)."""
+    wl = CASES[3]
+    inp = I.make_inputs(wl)
+    qc, _ = _tensor_codes(inp.Q)
+    kc, _ = _tensor_codes(inp.K)
+    vc, _ = _tensor_codes(inp.V)
+    sq = sk = np.float32(5e-4)
+    _, x0, _, _ = O.intsm_constants(sq, sk, O.default_sm_scale(wl.d))
+    assert x0 > 2 ** 23
+    want = O.attn_intsoftmax(qc, sq, kc, sk, vc)
+    got = _run(wl, qc, sq, kc, sk, vc)
+    assert qb.get_error() == 0
+    _check(got, want)
+
+
 def test_intsoftmax_scales_outside_the_domain_flagged():
     """1/s~ above 2^30: the kernel writes nothing and the error word reports
     an invalid argument (the scales live on the device)."""
