@@ -429,13 +429,21 @@ def gpu_arm(args):
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
                 "traffic": _attn_traffic(args.workload),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
-    if args.intsoftmax:  # both products on the warp-level int8 tensor cores
-        ism_tops = ops / (attn_avg_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "intsm_attn_kernel (qattn_fwd_intsoftmax)",
-                    "achieved": ism_tops, "peak": peaks["bf16_sustained"], "unit": "TOPS",
-                    "frac": ism_tops / peaks["bf16_sustained"],
-                    "peak_basis": f"{peaks['source']} sustained bf16 (the int8 warp MMA on this "
-                                  "GPU runs far below it)",
+    if args.intsoftmax:  # the integer softmax dominates: an ALU roofline
+        # algorithmic integer operations per score: S - m, ShiftExp2's five
+        # (quotient, remainder, halving, + X0, shift), requantization's three
+        # (multiply, shift, clamp), the row-sum add and the max compare
+        int_ops = INTSM_OPS_PER_SCORE * wl.unmasked_pairs()
+        alu_tops = int_ops / (attn_avg_ms * 1e-3) / 1e12
+        alu_peak = NUM_SMS * INT32_LANES_PER_SM * SM_MAX_GHZ / 1e3
+        roofline = {"bound": "alu", "kernel": "intsm_attn_kernel (qattn_fwd_intsoftmax)",
+                    "achieved": alu_tops, "peak": alu_peak, "unit": "TOP/s (int32)",
+                    "frac": alu_tops / alu_peak,
+                    "peak_basis": (f"{NUM_SMS} SMs x {INT32_LANES_PER_SM} int32 lanes per clock "
+                                   f"(64 ALU-pipe + 64 FMA-pipe, from ncu pipe counters) x "
+                                   f"{SM_MAX_GHZ} GHz"),
+                    "algorithmic_ops": int_ops, "ops_per_score": INTSM_OPS_PER_SCORE,
+                    "tensor_tops": ops / (attn_avg_ms * 1e-3) / 1e12,
                     "traffic": None}
     if args.exact24:  # three exact fp16 tensor-core products per attention product
         mma_tflops = 3 * ops / (attn_avg_ms * 1e-3) / 1e12
@@ -482,6 +490,13 @@ def gpu_arm(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# GB300 unit counts for the ALU roofline of the integer-only mode
+NUM_SMS = 152
+INT32_LANES_PER_SM = 128
+SM_MAX_GHZ = 2.07
+INTSM_OPS_PER_SCORE = 11
 
 
 def _stream_ref_us(k_codes, v_codes, flush, stream, reps=20):
