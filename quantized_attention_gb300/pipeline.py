@@ -96,12 +96,17 @@ class Problem:
                   self.workspace, stream)
         return self.O
 
-    def attend(self, bias: Optional[torch.Tensor] = None, stream=None):
-        """a4-a10: the fused attention kernel on the quantized operands."""
+    def attend(self, bias: Optional[torch.Tensor] = None, stream=None,
+               out: Optional[torch.Tensor] = None):
+        """a4-a10: the fused attention kernel on the quantized operands, into
+        ``out`` (shaped and typed like ``self.O``) or ``self.O``."""
+        O = self.O if out is None else out
+        if O.shape != self.O.shape or O.dtype != self.O.dtype or not O.is_contiguous():
+            raise ValueError("out must be a contiguous tensor like Problem.O")
         qb.fwd(self.q_codes, self.q_scales, self._k_codes, self.k_scales, self.v8t, self.ldv,
-               self.v_scales, bias, self.shape, self.params, self.O, self.lse, self.workspace,
+               self.v_scales, bias, self.shape, self.params, O, self.lse, self.workspace,
                stream, k_carrier=self.k_carrier)
-        return self.O
+        return O
 
     def kernel_launches(self) -> int:
         """Kernels of this library that one ``run`` launches (memsets excluded)."""
@@ -123,10 +128,79 @@ class Problem:
         return int(append) + 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 2
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
-            V_scale=None, bias=None, stream=None):
+            V_scale=None, bias=None, stream=None, out=None):
         self.quantize(Q, K, V, K_codes=K_codes, K_scale=K_scale, V_codes=V_codes,
                       V_scale=V_scale, stream=stream)
-        return self.attend(bias, stream)
+        return self.attend(bias, stream, out)
+
+
+class OverlappedSteps:
+    """Steps whose inputs come from pinned host memory and whose result goes
+    back to pinned host memory, with step i's host-to-device copies, step
+    i-1's kernels and step i-2's device-to-host copy in flight together.
+
+    Two device sets of inputs and outputs and two pinned host outputs
+    alternate; three streams (copy in, compute, copy out) are ordered by
+    events: a set's inputs are overwritten only after the compute that read
+    them, its output only after the copy that read it.  ``compute(dev_in,
+    dev_out, stream)`` issues one step's kernels on ``stream``.  Device
+    buffers are allocated once, like those of ``Problem``.
+    """
+
+    def __init__(self, host_inputs, out_like: torch.Tensor, compute, device="cuda"):
+        # host_inputs: one dict of pinned tensors, or a list of them used in turn
+        self.host_inputs = host_inputs if isinstance(host_inputs, list) else [host_inputs]
+        for h in self.host_inputs:
+            for t in h.values():
+                if not t.is_pinned():
+                    raise ValueError("host inputs must be pinned")
+        first = self.host_inputs[0]
+        dev = torch.device(device)
+        self.dev_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in first.items()}
+                       for _ in range(2)]
+        self.dev_out = [torch.empty_like(out_like, device=dev) for _ in range(2)]
+        self.host_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory()
+                         for _ in range(2)]
+        self.compute = compute
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.steps = 0
+        self.last = None  # set index of the most recent step
+
+    def step(self, before=None):
+        """Issue one step (asynchronously); ``before(stream)`` runs on the
+        compute stream ahead of the step's kernels.  Returns the pinned host
+        tensor that receives the step's result once ``sync()`` returns (it is
+        reused two steps later)."""
+        b = self.steps & 1
+        host = self.host_inputs[self.steps % len(self.host_inputs)]
+        if self.steps >= 2:
+            self.s_in.wait_event(self.ev_comp[b])    # the compute two steps back read dev_in[b]
+        with torch.cuda.stream(self.s_in):
+            for k, v in host.items():
+                self.dev_in[b][k].copy_(v, non_blocking=True)
+        self.ev_in[b].record(self.s_in)
+        self.s_comp.wait_event(self.ev_in[b])
+        if self.steps >= 2:
+            self.s_comp.wait_event(self.ev_out[b])   # dev_out[b]'s copy two steps back is done
+        if before is not None:
+            before(self.s_comp)
+        self.compute(self.dev_in[b], self.dev_out[b], self.s_comp)
+        self.ev_comp[b].record(self.s_comp)
+        self.s_out.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.s_out):
+            self.host_out[b].copy_(self.dev_out[b], non_blocking=True)
+        self.ev_out[b].record(self.s_out)
+        self.steps += 1
+        self.last = b
+        return self.host_out[b]
+
+    def sync(self):
+        """Wait for every step issued so far."""
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()
 
 
 def problem_for(wl, **kw) -> Problem:
