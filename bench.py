@@ -399,6 +399,7 @@ def gpu_arm(args):
     # decode steps are sequential (each appends the token the next one reads);
     # the other modes' steps are independent and run overlapped
     overlapped = not decode
+    copy_ms = None
     e_s = torch.cuda.Event(enable_timing=True)
     e_e = torch.cuda.Event(enable_timing=True)
     e_ms = 0.0
@@ -440,6 +441,18 @@ def gpu_arm(args):
         e_e.record(runner.s_out)
         runner.sync()
         e_ms = e_s.elapsed_time(e_e)
+        # the host link alone: the same copies and schedule with no kernels
+        copies = OverlappedSteps(host, out_dev, lambda d_in, d_out, s: None)
+        for _ in range(max(1, args.warmup)):
+            copies.step()
+        copies.sync()
+        c_s, c_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c_s.record(copies.s_in)
+        for _ in range(args.steps):
+            copies.step()
+        c_e.record(copies.s_out)
+        copies.sync()
+        copy_ms = c_s.elapsed_time(c_e) / args.steps
     else:
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -532,7 +545,10 @@ def gpu_arm(args):
                     "schedule": ("overlapped: step i's host-to-device copies, step i-1's kernels "
                                  "and step i-2's device-to-host copy in flight together "
                                  "(pipeline.OverlappedSteps); L2 flush inside the timed interval"
-                                 if overlapped else "serial: copies in, kernels, copy out")},
+                                 if overlapped else "serial: copies in, kernels, copy out"),
+                    **({"copy_only_ms_per_step": copy_ms,
+                        "copy_bound_value": world * ops / (copy_ms * 1e-3) / 1e12}
+                       if copy_ms else {})},
             "gpu_launches": (1 if args.intsoftmax else 2 if args.exact24
                              else P.decode_launches(append=True) if decode
                              else P.kernel_launches()) * args.steps,
