@@ -214,6 +214,44 @@ def time_cpu_baseline(wl_name, warmup=1, steps=1):
     return ops, secs, cores, desc
 
 
+def time_cpu_mode_baseline(mode, wl_name, budget_s=10.0):
+    """The oracle of an extra mode, as it stands, on whole items of the
+    workload (one process) until about budget_s seconds of CPU time; returns
+    (ops, seconds, cores, description).  ops counts 4 d per visible (query,
+    key) pair, as the GPU line does."""
+    from oracle import qattn_oracle as O
+    from quantized_attention_gb300 import inputs as I
+    wl = I.WORKLOADS[wl_name]
+    inp = I.make_inputs(wl)
+    ops, n, t0 = 0, 0, time.perf_counter()
+    if mode == "intsoftmax":
+        qc, sq = _tensor_codes_np(inp.Q)
+        kc, sk = _tensor_codes_np(inp.K)
+        vc, _ = _tensor_codes_np(inp.V)
+        heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+        while n < len(heads) and time.perf_counter() - t0 < budget_s:
+            O.attn_intsoftmax(qc, sq, kc, sk, vc, heads=[heads[n]])
+            ops += 4 * wl.d * wl.Nq * wl.Nk
+            n += 1
+        desc = f"{n} whole (image, head) attentions of {wl_name}, int64 NumPy, one process"
+    else:  # exact24: 128-row query blocks of head 0 against the whole cache
+        nblk = (wl.Nq + 127) // 128
+        while n < nblk and time.perf_counter() - t0 < budget_s:
+            rows = np.arange(n * 128, min(wl.Nq, n * 128 + 128))
+            O.attn_exact24(inp.Q, inp.K_codes, inp.K_scale, inp.V_codes, inp.V_scale,
+                           causal=wl.causal, q_pos0=wl.q_pos0, heads=[(0, 0)], rows=rows)
+            ops += 4 * wl.d * int(O.visible_mask(rows, wl.Nk, wl.causal, wl.pos0).sum())
+            n += 1
+        desc = f"{n} blocks of 128 query rows of head 0 of {wl_name} over the whole cache, one process"
+    return ops, time.perf_counter() - t0, 1, desc
+
+
+def _tensor_codes_np(x):
+    """Per-tensor int8 codes: scale fp32(max |x| / 127), codes rint(x / scale)."""
+    sc = np.float32(np.abs(x).max() / np.float32(127.0))
+    return np.clip(np.rint(x / sc), -127, 127).astype(np.int8), sc
+
+
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -293,8 +331,8 @@ def gpu_arm(args):
         if wl.kv_codes or wl.causal:
             raise SystemExit("--intsoftmax needs an unmasked bf16 workload (vit, tiny)")
         def tensor_codes(x):
-            sc = np.float32(np.abs(x).max() / np.float32(127.0))
-            return (torch.from_numpy(np.clip(np.rint(x / sc), -127, 127).astype(np.int8)).to("cuda"),
+            codes, sc = _tensor_codes_np(x)
+            return (torch.from_numpy(codes).to("cuda"),
                     torch.tensor([sc], dtype=torch.float32, device="cuda"))
         ism_q, ism_sq = tensor_codes(inp.Q)
         ism_k, ism_sk = tensor_codes(inp.K)
@@ -520,8 +558,12 @@ def gpu_arm(args):
                                          "same L2 flush before each launch",
                                    "us": ref_us, "GB/s": cache_bytes / (ref_us * 1e-6) / 1e9}}
     cpu = None
-    if not args.no_cpu_baseline and not args.exact24 and not args.intsoftmax:
-        c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
+    if not args.no_cpu_baseline:
+        if args.exact24 or args.intsoftmax:
+            c_ops, c_s, cores, desc = time_cpu_mode_baseline(
+                "intsoftmax" if args.intsoftmax else "exact24", args.workload)
+        else:
+            c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {c_s:.1f} s"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
