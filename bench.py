@@ -286,6 +286,25 @@ def _config(wl_name):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it), then a barrier; the
+    identity for one process."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_value(ops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """TOPS of the whole job: every rank runs its own copy of the workload
+    (weak scaling), over the slowest rank's time per step."""
+    return world * ops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -397,14 +416,9 @@ def gpu_arm(args):
         raise RuntimeError("device error word set during the timed steps")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     attn_ms = [a.elapsed_time(b) for a, b in zip(attn_a, attn_b)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
+    total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
-    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_value(ops, world, ms_per_step)
 
     # ---- end to end through the public API, host buffers, copies timed
     if args.intsoftmax:  # the int8 codes in, the int8 output codes back
@@ -504,11 +518,8 @@ def gpu_arm(args):
             e_e.record(stream)
             torch.cuda.synchronize()
             e_ms += e_s.elapsed_time(e_e)
-    if world > 1:
-        t = torch.tensor([e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e_value = world * ops / (e_ms / args.steps * 1e-3) / 1e12
+    e_ms = max_over_ranks(e_ms, world)
+    e2e_value = whole_job_value(ops, world, e_ms / args.steps)
 
     if rank != 0:
         return 0
