@@ -26,7 +26,7 @@ EXPORTED = (
     "qattn_version", "qattn_status_string", "qattn_workspace_size", "qattn_v_ld",
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
-    "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
+    "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
 )
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
     L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp,
                                     sz, vp]
     L.qattn_quantize_v.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
+    L.qattn_prepare.argtypes = [vp, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, sz, vp]
     L.qattn_quantize_v_noalloc.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp]
     L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
@@ -84,7 +85,8 @@ def lib() -> ctypes.CDLL:
     L.qattn_get_error.argtypes = [vp]
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
-                 "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc"):
+                 "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
+                 "qattn_prepare"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -167,6 +169,21 @@ def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_s
                                    _p(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)),
            "qattn_quantize_qk")
+
+
+def prepare(Q, K, V, shape, params, q_codes, q_scales, k_codes, k_scales, k_mean, v8t, ldv,
+            v_scales, workspace, stream=None, k_carrier=None):
+    """qattn_prepare: K mean, Q/K codes and V's e4m3 codes in two launches."""
+    for t, name in ((Q, "Q"), (K, "K"), (V, "V")):
+        _dense(t, torch.bfloat16, name)
+    if k_carrier is not None:
+        _dense(k_carrier, torch.float16, "k_carrier")
+    _check(lib().qattn_prepare(_p(Q), _p(K), _p(V), ctypes.byref(shape), ctypes.byref(params),
+                               _p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales),
+                               _p(k_carrier), _p(k_mean), _p(v8t), ldv, _p(v_scales),
+                               _p(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream)),
+           "qattn_prepare")
 
 
 def quantize_v(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, workspace, stream=None):

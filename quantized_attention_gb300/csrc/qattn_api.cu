@@ -119,6 +119,7 @@ size_t ws_quant_v(const qattn_shape* s) { return align256(static_cast<size_t>(s-
 // fp16 carriers of the K codes (Q codes are widened inside the kernels).
 size_t ws_carriers_k(const qattn_shape* s) { return align256(static_cast<size_t>(s->B * s->Hkv * s->Nk * s->d) * 2); }
 size_t ws_fwd(const qattn_shape* s) { return ws_carriers_k(s); }
+size_t ws_prepare(const qattn_shape* s) { return align256(qattn::prepare_ws_bytes(s->B * s->Hkv, s->d)); }
 
 // 3-D tiled map over a dense [planes][rows][inner] tensor.
 bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const void* ptr,
@@ -185,6 +186,7 @@ size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params
   if (q > m) m = q;
   if (ws_quant_v(shape) > m) m = ws_quant_v(shape);
   if (ws_fwd(shape) > m) m = ws_fwd(shape);
+  if (ws_prepare(shape) > m) m = ws_prepare(shape);
   if (decode_shape_ok(shape)) {
     const size_t dws = qattn::decode_ws_bytes(shape->B, shape->Hq, shape->Hkv, shape->Nq,
                                               shape->Nk, shape->d);
@@ -278,6 +280,58 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
     jk.BH = B * Hkv;
   }
   return from_cuda(qattn::launch_quantize_rows(jq, 0, jk, k_mean ? 1 : 0, d, s));
+}
+
+qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                           const qattn_shape* shape, const qattn_params* params,
+                           int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
+                           uint16_t* k_carrier, float* k_mean, uint8_t* v8t, int64_t ldv,
+                           float* v_scales, void* workspace, size_t workspace_bytes,
+                           qattn_stream_t stream) {
+  qattn_status st = check_shape(shape);
+  if (st != QATTN_OK) return st;
+  if ((st = check_params(params)) != QATTN_OK) return st;
+  if (empty_problem(shape)) return QATTN_OK;
+  if (params->q_gran != QATTN_GRAN_BLOCK || params->k_gran != QATTN_GRAN_BLOCK || shape->Nk < 1)
+    return QATTN_ERR_UNSUPPORTED;
+  for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K),
+                        static_cast<const void*>(V), static_cast<const void*>(q_codes),
+                        static_cast<const void*>(q_scales), static_cast<const void*>(k_codes),
+                        static_cast<const void*>(k_scales), static_cast<const void*>(k_mean),
+                        static_cast<const void*>(v8t), static_cast<const void*>(v_scales)})
+    if (!p || !aligned16(p)) return QATTN_ERR_INVALID_ARG;
+  if (k_carrier && !aligned16(k_carrier)) return QATTN_ERR_INVALID_ARG;
+  if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
+  const size_t need = ws_prepare(shape);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  const int B = static_cast<int>(shape->B), Hq = static_cast<int>(shape->Hq);
+  const int Hkv = static_cast<int>(shape->Hkv), d = static_cast<int>(shape->d);
+  qattn::RowsJob jq{};
+  jq.X = Q;
+  jq.H = Hq;
+  jq.N = static_cast<int>(shape->Nq);
+  jq.Hchan = 1;
+  jq.group = 1;
+  jq.gran = QATTN_GRAN_BLOCK;
+  jq.codes = q_codes;
+  jq.scales = q_scales;
+  jq.nblk = static_cast<int>((shape->Nq + 127) / 128);
+  jq.BH = B * Hq;
+  qattn::RowsJob jk{};
+  jk.X = K;
+  jk.H = Hkv;
+  jk.N = static_cast<int>(shape->Nk);
+  jk.chan = k_mean;
+  jk.Hchan = Hkv;
+  jk.group = 1;
+  jk.gran = QATTN_GRAN_BLOCK;
+  jk.codes = k_codes;
+  jk.scales = k_scales;
+  jk.carrier = k_carrier;
+  jk.nblk = static_cast<int>((shape->Nk + 127) / 128);
+  jk.BH = B * Hkv;
+  return from_cuda(qattn::launch_prepare(jq, jk, V, d, v8t, ldv, v_scales, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,

@@ -81,6 +81,12 @@ struct RowsJob {
 cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, int m1, int d,
                                  cudaStream_t s);
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
+// The pre-pass for bf16 Q, K, V with block granules in two launches: jq (Q,
+// mode 0), jk (K minus jk.chan = the mean it writes, mode 1), V's e4m3
+// transpose.  ws: prepare_ws_bytes(), zeroed here.
+cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
+                           uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
+size_t prepare_ws_bytes(long long BH, long long d);
 cudaError_t launch_fill_ones(float* p, long long n, cudaStream_t s);
 
 cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,

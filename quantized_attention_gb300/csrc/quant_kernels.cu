@@ -246,20 +246,24 @@ __global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const uint16_t* _
 // MULTI = true: each chunk adds its sums into acc[bh][c] with 64-bit atomics
 // (integer, so the order does not matter) and the last CTA of the head to
 // finish writes mu; acc and done must start at zero.
+template <int D>
+struct KMeanSmem {
+  static constexpr int RG = kThreads / (D / 8);  // row groups per CTA
+  long long red[RG][D];
+  unsigned int last;
+};
+
 template <int D, bool MULTI>
-__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
-                                                         int nchunks, unsigned long long magic,
-                                                         unsigned long long* __restrict__ acc,
-                                                         unsigned int* __restrict__ done,
-                                                         float* __restrict__ mu) {
-  pdl_trigger();
-  pdl_wait();
+__device__ __forceinline__ void k_mean_chunk(const uint16_t* __restrict__ K, int Nk, int nchunks,
+                                             unsigned long long magic,
+                                             unsigned long long* __restrict__ acc,
+                                             unsigned int* __restrict__ done, float* __restrict__ mu,
+                                             int chunk, int bh, KMeanSmem<D>& sm) {
   constexpr int VPR = D / 8;           // 16-byte vectors per row
-  constexpr int RG = kThreads / VPR;   // row groups per CTA
+  constexpr int RG = KMeanSmem<D>::RG;
   constexpr int kChunk = RG * kMeanRows;
-  __shared__ long long red[RG][D];
-  __shared__ unsigned int last;
-  const int bh = blockIdx.y, chunk = blockIdx.x;
+  auto& red = sm.red;
+  unsigned int& last = sm.last;
   const int v = threadIdx.x % VPR, rg = threadIdx.x / VPR;
   const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
   uint4 raw[kMeanRows];
@@ -294,6 +298,18 @@ __global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __rest
       mu[static_cast<size_t>(bh) * D + c] = mean_of_fix24(tot, static_cast<uint32_t>(Nk), magic);
     }
   }
+}
+
+template <int D, bool MULTI>
+__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
+                                                         int nchunks, unsigned long long magic,
+                                                         unsigned long long* __restrict__ acc,
+                                                         unsigned int* __restrict__ done,
+                                                         float* __restrict__ mu) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ KMeanSmem<D> sm;
+  k_mean_chunk<D, MULTI>(K, Nk, nchunks, magic, acc, done, mu, blockIdx.x, blockIdx.y, sm);
 }
 
 // ------------------------------------------------------------------ a2
@@ -424,16 +440,20 @@ __global__ void fill_ones_kernel(float* p, long long n) {
 // Per-channel amax of V over one chunk of tokens (every load issued before any
 // is used), merged with atomicMax on the (non-negative) float bit patterns.
 template <int D, bool I8>
-__global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
-                                                         unsigned int* __restrict__ amax_bits) {
-  pdl_trigger();
-  pdl_wait();
+struct VAmaxSmem {
+  static constexpr int RPI = kThreads / (D / (I8 ? 16 : 8));  // rows per iteration
+  float red[RPI * D];
+};
+
+template <int D, bool I8>
+__device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
+                                             unsigned int* __restrict__ amax_bits, int chunk, int bh,
+                                             VAmaxSmem<D, I8>& sm) {
   constexpr int EPV = I8 ? 16 : 8;
   constexpr int VPR = D / EPV;
-  constexpr int RPI = kThreads / VPR;
+  constexpr int RPI = VAmaxSmem<D, I8>::RPI;
   constexpr int NIT = (kTokPerChunk + RPI - 1) / RPI;
-  __shared__ float red[RPI * D];
-  const int bh = blockIdx.y, chunk = blockIdx.x;
+  float* red = sm.red;
   const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
   const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
   const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
@@ -472,6 +492,15 @@ __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict
   }
 }
 
+template <int D, bool I8>
+__global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
+                                                         unsigned int* __restrict__ amax_bits) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ VAmaxSmem<D, I8> sm;
+  v_amax_chunk<D, I8>(V, Nk, amax_bits, blockIdx.x, blockIdx.y, sm);
+}
+
 // Quantize a 128-key slice of one (batch, KV head) to e4m3 and write it
 // transposed: v8t[bh][c][t0 .. t0+127].  Lane l of a warp owns keys
 // 4l .. 4l+3 and reads, for each, 32 contiguous bytes of the row (two 16-byte
@@ -480,21 +509,26 @@ __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict
 // [D][128]-byte tile: the 32 lanes write 32 consecutive words (no bank
 // conflict).  The tile leaves as 16-byte rows.  Keys >= Nk are written as 0;
 // the write stops at the row stride ldv.
+template <int D>
+struct VConvSmem {
+  __align__(16) uint8_t tile[D * 128];
+  float inv_s[D];
+};
+
 template <int D, bool I8>
-__global__ void __launch_bounds__(kThreads) v_convert_kernel(
-    const void* __restrict__ V, int Nk, const unsigned int* amax_bits,
-    const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
-    float* __restrict__ v_scales) {
-  pdl_trigger();
-  pdl_wait();
+__device__ __forceinline__ void v_convert_slice(const void* __restrict__ V, int Nk,
+                                                const unsigned int* amax_bits,
+                                                const float* __restrict__ chan,
+                                                uint8_t* __restrict__ v8t, long long ldv,
+                                                float* __restrict__ v_scales, int tblk, int bh,
+                                                VConvSmem<D>& sm) {
   constexpr int EPV = I8 ? 16 : 8;        // channels per 16-byte vector
   constexpr int kSlices = D / (2 * EPV);  // 32-byte channel slices per key row
   constexpr int kWarps = kThreads / 32;
   constexpr int NS = (kSlices + kWarps - 1) / kWarps;  // slices per warp
-  __shared__ __align__(16) uint8_t tile[D * 128];
-  __shared__ float inv_s[D];
-  const int bh = blockIdx.y;
-  const int t0 = blockIdx.x * 128;
+  uint8_t* tile = sm.tile;
+  float* inv_s = sm.inv_s;
+  const int t0 = tblk * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
   const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
@@ -514,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
   for (int c = threadIdx.x; c < D; c += kThreads) {
     const float a = __uint_as_float(amax_bits[static_cast<size_t>(bh) * D + c]);
     inv_s[c] = (a > 0.f) ? __fdiv_rn(448.0f, a) : 0.f;
-    if (blockIdx.x == 0) {
+    if (tblk == 0) {
       const size_t i = static_cast<size_t>(bh) * D + c;
       v_scales[i] = I8 ? __fdiv_rn(__fmul_rn(chan[i], a), 448.0f) : __fdiv_rn(a, 448.0f);
     }
@@ -556,6 +590,90 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
     const uint4 w = *reinterpret_cast<const uint4*>(tile + c * 128 + 16 * k);
     *reinterpret_cast<uint4*>(v8t + (static_cast<size_t>(bh) * D + c) * ldv + pos) = w;
   }
+}
+
+template <int D, bool I8>
+__global__ void __launch_bounds__(kThreads) v_convert_kernel(
+    const void* __restrict__ V, int Nk, const unsigned int* amax_bits,
+    const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
+    float* __restrict__ v_scales) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ VConvSmem<D> sm;
+  v_convert_slice<D, I8>(V, Nk, amax_bits, chan, v8t, ldv, v_scales, blockIdx.x, blockIdx.y, sm);
+}
+
+// ------------------------------------------------------------------ a1-a3 in two launches
+// The whole pre-pass for bf16 Q, K, V with block granules.  Launch 1: Q's
+// codes | K's channel sums (the last CTA of a head writes its mean) | V's
+// channel maxima -- three independent jobs in one grid.  Launch 2: K's codes
+// (and carriers) from K minus its mean | V's e4m3 transpose.  Each CTA runs
+// one of the bodies the separate kernels run, so the outputs are the same.
+struct Prep1Args {
+  RowsJob jq;
+  const uint16_t* K;
+  const uint16_t* V;
+  int BHk, Nk, nkc, nvc;
+  unsigned long long magic;
+  unsigned long long* acc;
+  unsigned int* done;
+  float* mu;
+  unsigned int* amax;
+};
+
+struct Prep2Args {
+  RowsJob jk;
+  const uint16_t* V;
+  int Nk, nvt;
+  const unsigned int* amax;
+  uint8_t* v8t;
+  long long ldv;
+  float* v_scales;
+};
+
+constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
+
+// 64 registers: four CTAs per SM, as the separate Q/K quantizer runs.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 4) prepare1_kernel(const Prep1Args p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr size_t kBytes =
+      cmax(cmax(sizeof(KMeanSmem<D>), sizeof(VAmaxSmem<D, false>)), (kThreads / 32) * sizeof(float));
+  __shared__ __align__(16) unsigned char sm[kBytes];
+  int x = blockIdx.x;
+  const int nq = p.jq.BH * p.jq.nblk;
+  if (x < nq) {
+    quant_rows_body<D, 0>(p.jq, x / p.jq.nblk, x % p.jq.nblk, 1, reinterpret_cast<float*>(sm));
+    return;
+  }
+  x -= nq;
+  const int nk = p.nkc * p.BHk;
+  if (x < nk) {
+    k_mean_chunk<D, true>(p.K, p.Nk, p.nkc, p.magic, p.acc, p.done, p.mu, x % p.nkc, x / p.nkc,
+                          *reinterpret_cast<KMeanSmem<D>*>(sm));
+    return;
+  }
+  x -= nk;
+  v_amax_chunk<D, false>(p.V, p.Nk, p.amax, x % p.nvc, x / p.nvc,
+                         *reinterpret_cast<VAmaxSmem<D, false>*>(sm));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) prepare2_kernel(const Prep2Args p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr size_t kBytes = cmax(sizeof(VConvSmem<D>), (kThreads / 32) * sizeof(float));
+  __shared__ __align__(16) unsigned char sm[kBytes];
+  const int nk = p.jk.BH * p.jk.nblk;
+  const int x = blockIdx.x;
+  if (x < nk) {
+    quant_rows_body<D, 1>(p.jk, x / p.jk.nblk, x % p.jk.nblk, 1, reinterpret_cast<float*>(sm));
+    return;
+  }
+  const int y = x - nk;
+  v_convert_slice<D, false>(p.V, p.Nk, p.amax, nullptr, p.v8t, p.ldv, p.v_scales, y % p.nvt, y / p.nvt,
+                            *reinterpret_cast<VConvSmem<D>*>(sm));
 }
 
 // ------------------------------------------------------------------ carriers
@@ -632,6 +750,56 @@ cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long*
   if (d == 32) return smooth_k_t<32>(K, BH, Nk, ws, mu, s);
   if (d == 64) return smooth_k_t<64>(K, BH, Nk, ws, mu, s);
   return smooth_k_t<128>(K, BH, Nk, ws, mu, s);
+}
+
+size_t prepare_ws_bytes(long long BH, long long d) {
+  auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  return a256(smooth_k_ws_bytes(BH, 0, d)) + a256(static_cast<size_t>(BH * d) * sizeof(unsigned int));
+}
+
+template <int D>
+static cudaError_t prepare_t(const Prep1Args& p1, const Prep2Args& p2, cudaStream_t s) {
+  const int g1 = p1.jq.BH * p1.jq.nblk + (p1.nkc + p1.nvc) * p1.BHk;
+  cudaError_t e = launch_pdl(prepare1_kernel<D>, dim3(g1), dim3(kThreads), 0, s, p1);
+  if (e != cudaSuccess) return e;
+  const int g2 = p2.jk.BH * p2.jk.nblk + p2.nvt * p1.BHk;
+  return launch_pdl(prepare2_kernel<D>, dim3(g2), dim3(kThreads), 0, s, p2);
+}
+
+cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
+                           uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s) {
+  const int BHk = jk.BH, Nk = jk.N;
+  if (BHk <= 0 || Nk <= 0 || jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
+  const size_t wsm = (smooth_k_ws_bytes(BHk, Nk, d) + 255) / 256 * 256;
+  cudaError_t e = cudaMemsetAsync(ws, 0, prepare_ws_bytes(BHk, d), s);
+  if (e != cudaSuccess) return e;
+  Prep1Args p1{};
+  p1.jq = jq;
+  p1.K = jk.X;
+  p1.V = V;
+  p1.BHk = BHk;
+  p1.Nk = Nk;
+  p1.nkc = (Nk + kMeanRows * kThreads / (d / 8) - 1) / (kMeanRows * kThreads / (d / 8));
+  p1.nvc = (Nk + kTokPerChunk - 1) / kTokPerChunk;
+  p1.magic = ~0ull / static_cast<unsigned long long>(Nk);
+  p1.acc = static_cast<unsigned long long*>(ws);
+  p1.done = reinterpret_cast<unsigned int*>(p1.acc + static_cast<size_t>(BHk) * d);
+  p1.mu = const_cast<float*>(jk.chan);
+  p1.amax = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + wsm);
+  Prep2Args p2{};
+  p2.jk = jk;
+  p2.V = V;
+  p2.Nk = Nk;
+  p2.nvt = static_cast<int>((ldv + 127) / 128);
+  p2.amax = p1.amax;
+  p2.v8t = v8t;
+  p2.ldv = ldv;
+  p2.v_scales = v_scales;
+  switch (d) {
+    case 32: return prepare_t<32>(p1, p2, s);
+    case 64: return prepare_t<64>(p1, p2, s);
+    default: return prepare_t<128>(p1, p2, s);
+  }
 }
 
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran) {

@@ -18,7 +18,7 @@ class Problem:
     def __init__(self, B, Hq, Hkv, Nq, Nk, d, *, causal=False, q_gran=qb.GRAN_BLOCK,
                  k_gran=qb.GRAN_BLOCK, q_pos0=None, kv_codes=False, out_dtype=qb.DT_F32,
                  bias_head_stride=0, want_lse=False, k_carrier=True, pv_mode=qb.PV_E4M3,
-                 device="cuda"):
+                 fused_prepass=True, device="cuda"):
         self.B, self.Hq, self.Hkv, self.Nq, self.Nk, self.d = B, Hq, Hkv, Nq, Nk, d
         self.kv_codes = kv_codes
         self.shape = qb.make_shape(B, Hq, Hkv, Nq, Nk, d)
@@ -44,6 +44,10 @@ class Problem:
         self.lse = torch.empty((B, Hq, Nq), dtype=f32, device=dev) if want_lse else None
         ws = max(qb.workspace_size(self.shape, self.params), 256)
         self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
+        # qattn_prepare covers bf16 K/V with block granules (two launches
+        # instead of four); other granules take the three separate calls
+        self.fused_prepass = (fused_prepass and not kv_codes and Nk > 0 and
+                              q_gran == qb.GRAN_BLOCK and k_gran == qb.GRAN_BLOCK)
 
     def quantize(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
                  V_scale=None, stream=None):
@@ -55,6 +59,11 @@ class Problem:
             qb.quantize_v(V_codes, qb.DT_I8, V_scale, self.shape, self.v8t, self.ldv,
                           self.v_scales, self.workspace, stream)
             self._k_codes = K_codes
+        elif self.fused_prepass:  # the same outputs in two launches
+            qb.prepare(Q, K, V, self.shape, self.params, self.q_codes, self.q_scales,
+                       self.k_codes, self.k_scales, self.k_mean, self.v8t, self.ldv,
+                       self.v_scales, self.workspace, stream, k_carrier=self.k_carrier)
+            self._k_codes = self.k_codes
         else:
             qb.smooth_k(K, self.shape, self.k_mean, self.workspace, stream)
             qb.quantize_qk(Q, K, qb.DT_BF16, self.k_mean, None, self.shape, self.params,
@@ -112,6 +121,8 @@ class Problem:
         """Kernels of this library that one ``run`` launches (memsets excluded)."""
         two_pass = (self.params.q_gran != qb.GRAN_BLOCK or
                     (not self.kv_codes and self.params.k_gran != qb.GRAN_BLOCK))
+        if self.fused_prepass:
+            return 2 + 1 + int(self.k_carrier is None)  # qattn_prepare, [K carriers], attention
         n = 1 + int(two_pass)                        # Q and K codes (one grid)
         if self.kv_codes:
             n += 1 + int(self.k_carrier is not None)  # K scales set to 1, K carriers
