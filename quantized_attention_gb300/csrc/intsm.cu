@@ -22,7 +22,6 @@
 // converted once to fp16 rows that ldmatrix reads (V transposed); S stays in
 // registers and the P codes go straight into the A fragments of the PV
 // product.
-#include <climits>
 #include <cmath>
 #include <cuda_runtime.h>
 

@@ -178,7 +178,6 @@ class OverlappedSteps:
         self.ev_comp = [torch.cuda.Event() for _ in range(2)]
         self.ev_out = [torch.cuda.Event() for _ in range(2)]
         self.steps = 0
-        self.last = None  # set index of the most recent step
 
     def step(self, before=None):
         """Issue one step (asynchronously); ``before(stream)`` runs on the
@@ -205,7 +204,6 @@ class OverlappedSteps:
             self.host_out[b].copy_(self.dev_out[b], non_blocking=True)
         self.ev_out[b].record(self.s_out)
         self.steps += 1
-        self.last = b
         return self.host_out[b]
 
     def sync(self):
