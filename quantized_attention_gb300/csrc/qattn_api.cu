@@ -252,6 +252,11 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   jq.BH = B * Hq;
   qattn::RowsJob jk{};
   if (i8) {
+    // every K scale is 1: the Q quantizer's launch writes them
+    jq.ones = k_scales;
+    jq.n_ones = params->k_gran == QATTN_GRAN_TENSOR ? 1
+                : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
+                                                    : shape->B * shape->Hkv * nkb;
     cudaError_t e = qattn::launch_quantize_rows(jq, 2, jk, 0, d, s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
     if (k_carrier && shape->Nk > 0) {
@@ -259,10 +264,7 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
                                      static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * d), s);
       if (e != cudaSuccess) return QATTN_ERR_CUDA;
     }
-    const int64_t n = params->k_gran == QATTN_GRAN_TENSOR ? 1
-                      : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
-                                                          : shape->B * shape->Hkv * nkb;
-    return from_cuda(qattn::launch_fill_ones(k_scales, n, s));
+    return QATTN_OK;
   }
   if (shape->Nk > 0) {
     jk.X = static_cast<const uint16_t*>(K);

@@ -75,6 +75,8 @@ struct RowsJob {
   float* ws_amax;  // B*H*nblk block maxima (tensor / head granules only)
   uint16_t* carrier;  // nullable: the codes again as exact fp16, same layout
   int nblk, BH;    // 128-token blocks per head; B*H (0: no job)
+  float* ones;     // nullable (job 0 only): n_ones floats set to 1 by the
+  long long n_ones;  // launch (the K scales of an int8 cache)
 };
 // Quantizes j0 (mode m0) and j1 (mode m1) in the same launches.  Supported:
 // (m0, m1) = (0, 0), (0, 1), or (2, -) with j1.BH = 0.
@@ -87,7 +89,6 @@ size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
 cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
 size_t prepare_ws_bytes(long long BH, long long d);
-cudaError_t launch_fill_ones(float* p, long long n, cudaStream_t s);
 
 cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,
                               uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws_amax,

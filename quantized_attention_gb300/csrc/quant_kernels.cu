@@ -420,20 +420,18 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsJob j0, 
   pdl_trigger();
   pdl_wait();
   __shared__ float red[kThreads / 32];
+  if (pass == 1 && j0.n_ones > 0) {  // spread over every CTA of the launch
+    const long long nthr = static_cast<long long>(gridDim.x) * gridDim.y * kThreads;
+    for (long long i = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * kThreads + threadIdx.x;
+         i < j0.n_ones; i += nthr)
+      j0.ones[i] = 1.0f;
+  }
   const int x = blockIdx.x, blk = blockIdx.y;
   if (x < j0.BH) {
     if (blk < j0.nblk) quant_rows_body<D, M0>(j0, x, blk, pass, red);
   } else if (blk < j1.nblk) {
     quant_rows_body<D, M1>(j1, x - j0.BH, blk, pass, red);
   }
-}
-
-__global__ void fill_ones_kernel(float* p, long long n) {
-  pdl_trigger();
-  pdl_wait();
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    p[i] = 1.0f;
 }
 
 // ------------------------------------------------------------------ a3
@@ -834,12 +832,6 @@ cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, i
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
-}
-
-cudaError_t launch_fill_ones(float* p, long long n, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  return launch_pdl(fill_ones_kernel, dim3(grid_for(static_cast<size_t>(n), 256)), dim3(256), 0, s,
-                    p, n);
 }
 
 template <int D, bool I8>

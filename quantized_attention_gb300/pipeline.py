@@ -125,7 +125,7 @@ class Problem:
             return 2 + 1 + int(self.k_carrier is None)  # qattn_prepare, [K carriers], attention
         n = 1 + int(two_pass)                        # Q and K codes (one grid)
         if self.kv_codes:
-            n += 1 + int(self.k_carrier is not None)  # K scales set to 1, K carriers
+            n += int(self.k_carrier is not None)     # K carriers (K scales: the Q launch)
         else:
             n += 1                                   # channel mean
         n += 2                                       # V amax, V e4m3 transpose
@@ -134,9 +134,9 @@ class Problem:
 
     def decode_launches(self, append: bool = False) -> int:
         """Kernels one [append +] quantize_q + decode launches: [the cache
-        append,] Q codes (two passes for a tensor/head granule), K scales set
-        to 1, then the decode's two."""
-        return int(append) + 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 1 + 2
+        append,] Q codes with the K scales set to 1 (two passes for a
+        tensor/head granule), then the decode's two."""
+        return int(append) + 1 + int(self.params.q_gran != qb.GRAN_BLOCK) + 2
 
     def run(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
             V_scale=None, bias=None, stream=None, out=None):
