@@ -88,6 +88,18 @@ typedef enum {
                          the hard one": the int8 PV that flushes P < 1/254 to 0) */
 } qattn_pv_mode;
 
+/* Which kernel qattn_fwd runs (qattn_params.fwd_kernel).  Both compute the same
+ * recipe; they differ only in the order of the fp32 accumulations. */
+typedef enum {
+  QATTN_FWD_AUTO = 0,    /* the warp-level window kernel for Nq, Nk <= 64 (d in {32, 64},
+                            no causal mask, pv_mode E4M3), else the persistent kernel    */
+  QATTN_FWD_TC = 1,      /* the persistent tensor-core (tcgen05) kernel                  */
+  QATTN_FWD_SHORT = 2    /* the warp-level kernels for short non-causal key sequences:
+                            d in {32, 64}, 1 <= Nk <= 256, pv_mode E4M3, no causal mask
+                            (else QATTN_ERR_UNSUPPORTED); no workspace, reads the int8 K
+                            codes (k_carrier unused)                                    */
+} qattn_fwd_kernel;
+
 typedef struct {
   int32_t causal;           /* 1: key k is visible to query i iff k <= q_pos0 + i   */
   int32_t q_gran;           /* qattn_gran of the Q codes                           */
@@ -99,6 +111,7 @@ typedef struct {
   int64_t bias_head_stride; /* elements between heads' bias matrices; 0 = shared   */
   int64_t kv_capacity;      /* qattn_decode: rows per (batch, KV head) in the cache
                                arrays (>= Nk, the rows in use); 0 = Nk               */
+  int32_t fwd_kernel;       /* qattn_fwd_kernel; 0 = automatic                      */
 } qattn_params;
 
 /* Library version (major * 10000 + minor * 100 + patch). */

@@ -16,6 +16,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 _lib = None
 
 OK = 0
+FWD_AUTO, FWD_TC, FWD_SHORT = 0, 1, 2
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = 1, 2, 3, 4, 5
 GRAN_TENSOR, GRAN_HEAD, GRAN_BLOCK = 0, 1, 2
 DT_BF16, DT_F32, DT_I8, DT_E4M3 = 0, 1, 2, 3
@@ -46,7 +47,7 @@ class Params(ctypes.Structure):
                 ("k_gran", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("q_pos0", ctypes.c_int64), ("sm_scale", ctypes.c_float),
                 ("pv_mode", ctypes.c_int32), ("bias_head_stride", ctypes.c_int64),
-                ("kv_capacity", ctypes.c_int64)]
+                ("kv_capacity", ctypes.c_int64), ("fwd_kernel", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -127,10 +128,10 @@ def make_shape(B, Hq, Hkv, Nq, Nk, d) -> Shape:
 
 def make_params(causal=False, q_gran=GRAN_BLOCK, k_gran=GRAN_BLOCK, out_dtype=DT_F32,
                 q_pos0=None, sm_scale=0.0, bias_head_stride=0, pv_mode=PV_E4M3,
-                kv_capacity=0) -> Params:
+                kv_capacity=0, fwd_kernel=0) -> Params:
     return Params(int(bool(causal)), q_gran, k_gran, out_dtype,
                   POS0_BOTTOM_RIGHT if q_pos0 is None else int(q_pos0), float(sm_scale),
-                  int(pv_mode), int(bias_head_stride), int(kv_capacity))
+                  int(pv_mode), int(bias_head_stride), int(kv_capacity), int(fwd_kernel))
 
 
 def version() -> int:

@@ -97,6 +97,7 @@ qattn_status check_params(const qattn_params* p) {
   if (p->causal != 0 && p->causal != 1) return QATTN_ERR_INVALID_ARG;
   if (p->pv_mode != QATTN_PV_E4M3 && p->pv_mode != QATTN_PV_INT8) return QATTN_ERR_INVALID_ARG;
   if (p->bias_head_stride < 0 || p->kv_capacity < 0) return QATTN_ERR_INVALID_ARG;
+  if (p->fwd_kernel < QATTN_FWD_AUTO || p->fwd_kernel > QATTN_FWD_SHORT) return QATTN_ERR_INVALID_ARG;
   if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return QATTN_ERR_INVALID_ARG;
   return QATTN_OK;
 }
@@ -381,7 +382,17 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
     if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return QATTN_ERR_INVALID_ARG;
   }
-  if (!k_carrier) {  // the K codes are converted into the workspace
+  // the warp-level kernels for short non-causal key sequences, or the persistent
+  // one; chosen automatically for windows (Nq, Nk <= 64), where the persistent
+  // kernel's 128-row tiles would be mostly empty
+  const bool short_ok = (shape->d == 32 || shape->d == 64) && !params->causal &&
+                        params->pv_mode == QATTN_PV_E4M3 && shape->Nk >= 1 &&
+                        shape->Nk <= qattn::kShortMaxNk;
+  const bool window = short_ok && shape->Nq <= qattn::kWindowMax && shape->Nk <= qattn::kWindowMax;
+  const bool use_short = params->fwd_kernel == QATTN_FWD_SHORT ||
+                         (params->fwd_kernel == QATTN_FWD_AUTO && window);
+  if (use_short && !short_ok) return QATTN_ERR_UNSUPPORTED;
+  if (!use_short && !k_carrier) {  // the K codes are converted into the workspace
     const size_t need = ws_fwd(shape);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   }
@@ -411,6 +422,7 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   a.out_bf16 = params->out_dtype == QATTN_BF16;
   a.lse = lse;
   a.err = err;
+  if (use_short) return from_cuda(qattn::launch_attn_short(a, q_codes, k_codes, v8t, ldv, s));
   if (shape->Nk == 0) {
     // No keys: every row is fully masked.  The kernel's empty-tile path
     // writes the zeros; give it valid (unused) maps.

@@ -57,6 +57,14 @@ struct AttnArgs {
   unsigned int* err;
 };
 
+// ---- attn_short.cu: the recipe on the warp-level tensor cores for short
+// non-causal key sequences (d in {32, 64}, Nk <= kShortMaxNk)
+constexpr int kShortMaxNk = 256;
+constexpr int kWindowMax = 64;  // Nq, Nk of the window kernel
+bool attn_short_eligible(const AttnArgs& a);
+cudaError_t launch_attn_short(const AttnArgs& a, const int8_t* q_codes, const int8_t* k_codes,
+                              const uint8_t* v8t, long long ldv, cudaStream_t s);
+
 // ---- quant_kernels.cu
 cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
                             cudaStream_t s);

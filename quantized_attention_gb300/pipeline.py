@@ -18,13 +18,14 @@ class Problem:
     def __init__(self, B, Hq, Hkv, Nq, Nk, d, *, causal=False, q_gran=qb.GRAN_BLOCK,
                  k_gran=qb.GRAN_BLOCK, q_pos0=None, kv_codes=False, out_dtype=qb.DT_F32,
                  bias_head_stride=0, want_lse=False, k_carrier=True, pv_mode=qb.PV_E4M3,
-                 fused_prepass=True, device="cuda"):
+                 fused_prepass=True, fwd_kernel=qb.FWD_AUTO, device="cuda"):
         self.B, self.Hq, self.Hkv, self.Nq, self.Nk, self.d = B, Hq, Hkv, Nq, Nk, d
         self.kv_codes = kv_codes
         self.shape = qb.make_shape(B, Hq, Hkv, Nq, Nk, d)
         self.params = qb.make_params(causal=causal, q_gran=q_gran, k_gran=k_gran,
                                      out_dtype=out_dtype, q_pos0=q_pos0,
-                                     bias_head_stride=bias_head_stride, pv_mode=pv_mode)
+                                     bias_head_stride=bias_head_stride, pv_mode=pv_mode,
+                                     fwd_kernel=fwd_kernel)
         self.ldv = qb.v_ld(Nk)
         dev = torch.device(device)
         i8, f32 = torch.int8, torch.float32

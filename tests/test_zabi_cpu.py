@@ -59,9 +59,21 @@ def test_invalid_arguments_rejected_on_host(L):
                        ctypes.byref(s), ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
     assert L.qattn_fwd(fake, fake, fake, vp((1 << 20) + 2), fake, fake, 256, fake, None,
                        ctypes.byref(s), ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
-    # no K carrier and no workspace
+    # the persistent kernel without a K carrier needs a workspace
+    p_tc = qb.make_params(fwd_kernel=qb.FWD_TC)
     assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
-                       ctypes.byref(p), fake, None, None, 0, None) == 5
+                       ctypes.byref(p_tc), fake, None, None, 0, None) == 5
+    # the short-sequence kernel on a shape it does not cover, and an unknown kernel choice
+    s_c = qb.make_shape(1, 4, 2, 256, 256, 128)
+    p_short = qb.make_params(fwd_kernel=qb.FWD_SHORT)
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s_c),
+                       ctypes.byref(p_short), fake, None, None, 0, None) == 2
+    p_causal = qb.make_params(causal=True, fwd_kernel=qb.FWD_SHORT)
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p_causal), fake, None, None, 0, None) == 2
+    p_bad = qb.make_params(fwd_kernel=7)
+    assert L.qattn_fwd(fake, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
+                       ctypes.byref(p_bad), fake, None, None, 0, None) == 1
     # unsupported head dim
     s96 = qb.make_shape(1, 4, 2, 256, 256, 96)
     assert L.qattn_smooth_k(fake, ctypes.byref(s96), fake, fake, 1 << 30, None) == 2
