@@ -674,6 +674,174 @@ __global__ void __launch_bounds__(kThreads) prepare2_kernel(const Prep2Args p) {
                             *reinterpret_cast<VConvSmem<D>*>(sm));
 }
 
+// ------------------------------------------------------------------ a1-a3, short heads
+// Heads of at most 128 tokens and d <= 64 (one block granule each, e.g. Swin
+// windows; the V8^T tiles of d = 128 would not fit the static shared memory): one
+// warp runs a head's whole pre-pass in one launch -- a KV head's channel mean
+// (exact fixed-point sums), its K codes (and carriers), its V channel maxima and
+// transposed e4m3 codes; a Q head's codes -- re-reading the head's few KB from
+// L1 between passes.  The arithmetic is that of the bodies above, step by step.
+constexpr int kSmallHead = 128;  // tokens per head at most
+constexpr int kSmallWarps = 4;
+
+struct SmallPrepArgs {
+  const uint16_t* Q;
+  const uint16_t* K;
+  const uint16_t* V;
+  int BHq, BHk, Nq, Nk;
+  unsigned long long magic;
+  int8_t* q_codes;
+  float* q_scales;
+  int8_t* k_codes;
+  float* k_scales;
+  uint16_t* k_carrier;
+  float* k_mean;
+  uint8_t* v8t;
+  long long ldv;
+  float* v_scales;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// The 8 codes of x (8 channels) at inv, and (optionally) their fp16 carriers.
+__device__ __forceinline__ void codes8(const float (&x)[8], float inv, int8_t* dst, uint16_t* carrier) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    int q = __float2int_rn(__fmul_rn(x[e], inv));
+    q = max(-127, min(127, q));
+    w[e / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e % 4));
+  }
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  if (carrier != nullptr) {
+    uint4 h;
+    codes4_to_f16x2(w[0], h.x, h.y);
+    codes4_to_f16x2(w[1], h.z, h.w);
+    *reinterpret_cast<uint4*>(carrier) = h;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const SmallPrepArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int VPR = D / 8;    // 16-byte vectors per row
+  constexpr int RG = 32 / VPR;  // row groups per warp
+  __shared__ __align__(16) uint8_t tiles[kSmallWarps][D * kSmallHead];  // V8^T of a warp's head
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kSmallWarps + warp;
+  const int v = lane % VPR, rg = lane / VPR;
+  if (item < p.BHq) {  // ---- a Q head: block amax, codes, scale
+    const int bh = item;
+    const uint16_t* src = p.Q + static_cast<size_t>(bh) * p.Nq * D;
+    float am = 0.f;
+    for (int r = rg; r < p.Nq; r += RG) {
+      float x[8];
+      unpack_bf16x8(*(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + v), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e]));
+    }
+    const float g = warp_max(am);
+    const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
+    for (int r = rg; r < p.Nq; r += RG) {
+      float x[8];
+      unpack_bf16x8(*(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + v), x);
+      codes8(x, inv, p.q_codes + (static_cast<size_t>(bh) * p.Nq + r) * D + v * 8, nullptr);
+    }
+    if (lane == 0) p.q_scales[bh] = __fdiv_rn(g, 127.0f);
+    return;
+  }
+  const int bh = item - p.BHq;
+  if (bh >= p.BHk) return;
+  // ---- a KV head.  The channel mean: exact sums of round(K * 2^24).
+  const uint16_t* ks = p.K + static_cast<size_t>(bh) * p.Nk * D;
+  const uint16_t* vs = p.V + static_cast<size_t>(bh) * p.Nk * D;
+  long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r = rg; r < p.Nk; r += RG) {
+    const uint4 raw[1] = {*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v)};
+    long long s8[8];
+    fix24_column_sums<1>(raw, s8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] += s8[e];
+  }
+#pragma unroll
+  for (int o = VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
+  }
+  float mu[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mu[e] = mean_of_fix24(sum[e], static_cast<uint32_t>(p.Nk), p.magic);
+  if (rg == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p.k_mean[static_cast<size_t>(bh) * D + v * 8 + e] = mu[e];
+  }
+  // K - mean: block amax, codes (+ carriers), scale
+  float am = 0.f;
+  for (int r = rg; r < p.Nk; r += RG) {
+    float x[8];
+    unpack_bf16x8(*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(x[e], mu[e])));
+  }
+  const float g = warp_max(am);
+  const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
+  for (int r = rg; r < p.Nk; r += RG) {
+    float x[8];
+    unpack_bf16x8(*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
+    const size_t off = (static_cast<size_t>(bh) * p.Nk + r) * D + v * 8;
+    codes8(x, inv, p.k_codes + off, p.k_carrier ? p.k_carrier + off : nullptr);
+  }
+  if (lane == 0) p.k_scales[bh] = __fdiv_rn(g, 127.0f);
+  // V: channel maxima, scales, e4m3 codes into the warp's [D][128] tile
+  float vm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int r = rg; r < p.Nk; r += RG) {
+    float x[8];
+    unpack_bf16x8(*(reinterpret_cast<const uint4*>(vs + static_cast<size_t>(r) * D) + v), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], fabsf(x[e]));
+  }
+#pragma unroll
+  for (int o = VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], __shfl_xor_sync(0xffffffffu, vm[e], o));
+  }
+  float sc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sc[e] = (vm[e] > 0.f) ? __fdiv_rn(448.0f, vm[e]) : 0.f;
+    if (rg == 0) p.v_scales[static_cast<size_t>(bh) * D + v * 8 + e] = __fdiv_rn(vm[e], 448.0f);
+  }
+  uint8_t* tile = tiles[warp];
+  for (int i = lane; i < D * kSmallHead / 16; i += 32)  // keys past Nk are 0
+    reinterpret_cast<uint4*>(tile)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncwarp();
+  for (int r = rg; r < p.Nk; r += RG) {
+    float x[8];
+    unpack_bf16x8(*(reinterpret_cast<const uint4*>(vs + static_cast<size_t>(r) * D) + v), x);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const uint32_t b2 = cvt_e4m3x2(__fmul_rn(x[e], sc[e]), __fmul_rn(x[e + 1], sc[e + 1]));
+      tile[(v * 8 + e) * kSmallHead + r] = static_cast<uint8_t>(b2 & 0xFFu);
+      tile[(v * 8 + e + 1) * kSmallHead + r] = static_cast<uint8_t>(b2 >> 8);
+    }
+  }
+  __syncwarp();
+  const int nchunk = static_cast<int>(p.ldv / 16);  // 16-byte chunks of a V8^T row
+  for (int i = lane; i < D * nchunk; i += 32) {
+    const int c = i / nchunk, k = i % nchunk;
+    const uint4 w = (16 * k < kSmallHead) ? *reinterpret_cast<const uint4*>(tile + c * kSmallHead + 16 * k)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(p.v8t + (static_cast<size_t>(bh) * D + c) * p.ldv + 16 * k) = w;
+  }
+}
+
 // ------------------------------------------------------------------ carriers
 // int8 codes -> fp16 values (exact: |code| <= 127).
 __global__ void codes_to_f16_kernel(const int8_t* src, uint16_t* __restrict__ dst,
@@ -768,6 +936,29 @@ cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t*
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s) {
   const int BHk = jk.BH, Nk = jk.N;
   if (BHk <= 0 || Nk <= 0 || jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
+  if (d <= 64 && jq.N <= kSmallHead && Nk <= kSmallHead) {  // short heads: one warp each, one launch
+    SmallPrepArgs p{};
+    p.Q = jq.X;
+    p.K = jk.X;
+    p.V = V;
+    p.BHq = jq.BH;
+    p.BHk = BHk;
+    p.Nq = jq.N;
+    p.Nk = Nk;
+    p.magic = ~0ull / static_cast<unsigned long long>(Nk);
+    p.q_codes = jq.codes;
+    p.q_scales = jq.scales;
+    p.k_codes = jk.codes;
+    p.k_scales = jk.scales;
+    p.k_carrier = jk.carrier;
+    p.k_mean = const_cast<float*>(jk.chan);
+    p.v8t = v8t;
+    p.ldv = ldv;
+    p.v_scales = v_scales;
+    const dim3 grid((jq.BH + BHk + kSmallWarps - 1) / kSmallWarps);
+    if (d == 32) return launch_pdl(prepare_small_kernel<32>, grid, dim3(kSmallWarps * 32), 0, s, p);
+    return launch_pdl(prepare_small_kernel<64>, grid, dim3(kSmallWarps * 32), 0, s, p);
+  }
   const size_t wsm = (smooth_k_ws_bytes(BHk, Nk, d) + 255) / 256 * 256;
   cudaError_t e = cudaMemsetAsync(ws, 0, prepare_ws_bytes(BHk, d), s);
   if (e != cudaSuccess) return e;

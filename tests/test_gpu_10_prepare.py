@@ -21,8 +21,10 @@ def _lib():
 CASES = [
     I.small("llm8k", Hq=8, Hkv=2, Nq=1000, Nk=1000),      # GQA, d 128, ragged blocks
     I.small("llm8k", Hq=4, Hkv=4, Nq=130, Nk=2100, d=64),  # Nq != Nk, many mean chunks
-    I.small("swin", B=3, Hq=3, Hkv=3, has_bias=False),     # d 32, N 49: one short chunk
+    I.small("swin", B=3, Hq=3, Hkv=3, has_bias=False),     # d 32, N 49: short heads
     I.small("vit", B=2, Hq=2, Hkv=1, Nq=197, Nk=197),      # tensor-granule workload at block granules
+    I.small("swin", B=5, Hq=4, Hkv=2, Nq=128, Nk=100, d=64),  # short heads (one warp each), GQA, d 64
+    I.small("swin", B=2, Hq=2, Hkv=2, Nq=7, Nk=1),         # short heads: one key
 ]
 
 
