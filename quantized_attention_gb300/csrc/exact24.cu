@@ -58,11 +58,6 @@ __device__ __forceinline__ uint32_t pack_f2h2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
-  return static_cast<uint32_t>(__half_as_ushort(lo)) |
-         (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-}
-
 // D(16x8 f32) += A(16x16 f16) * B(16x8 f16).  a0/a2: row g, k = 2t, 2t+1 /
 // 2t+8, 2t+9; a1/a3: row g + 8; b0/b1: column g, k = 2t, 2t+1 / 2t+8, 2t+9;
 // d0, d1: row g, columns 2t, 2t+1; d2, d3: row g + 8.

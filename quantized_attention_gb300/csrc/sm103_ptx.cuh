@@ -48,19 +48,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for the phase with the given parity to complete.  Returns false if
 // the CTA-wide abort flag is raised or the wait exceeds kWaitTimeoutCycles; in
 // the timeout case the abort flag is raised and the device error word is set.
@@ -172,17 +159,6 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// kind::f8f6f4 with the A operand (M x K, 4 e4m3 per 32-bit column, row i in
-// lane i) read from tensor memory instead of shared memory.
-__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrives (once) on the mbarrier when every tcgen05 operation this thread
@@ -306,20 +282,6 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ---------------------------------------------------------------- registers
-// Per-thread register budget of the calling warpgroup (all four warps must
-// execute the same instruction).  inc waits until the CTA's pool holds enough
-// registers, so the budgets of all warpgroups must sum to at most the
-// registers the CTA was launched with.
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ---------------------------------------------------------------- smem, sync
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -335,11 +297,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                "r"(d)
                : "memory");
 }
-// Barrier `id` (1..15) over `n` threads (a multiple of 32).
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // Four int8 codes (one word, byte e = code e) -> four exact fp16 values as two
 // f16x2 words {code0, code1}, {code2, code3}.  Each biased byte u = code + 128
 // becomes the fp16 1024 + u (bit pattern 0x6400 | u, exact since u < 2^10),
