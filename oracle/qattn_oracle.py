@@ -12,7 +12,12 @@ Sources (page title, section):
   "K's outliers, and the subtraction softmax does not notice",
   "fp8 is not faster, it is shaped correctly".
 * [QFLASH]     "QFlash: Bridging Quantization and Memory Efficiency in Vision
-  Transformer Attention" -- section 4, eq. (1)-(3), Algorithm 1, section 2.1.
+  Transformer Attention" -- section 4, eq. (1)-(3), Algorithm 1, section 2.1;
+  sections 4.3-4.6 for the integer-only attention (attn_intsoftmax).
+* [STRATA]     "prompt_attn_i8v3_kernel" pull request -- the 24-bit exact split
+  mode (attn_exact24).
+* The ZINC post's decode section -- the int8 KV cache and its running-mean
+  header (kv_append).
 
 Precision: the pages fix fp32 for the online softmax statistics and for every
 value that decides a quantized code (K - mu, x * 127/amax, P * 448); those are
@@ -37,13 +42,16 @@ Readings where the pages are silent (each one is listed in the design notes):
 * GQA: query head h reads KV head h // (Hq / Hkv).
 * An additive bias [Nq, Nk] in natural-log units is added after scaling.
 
-Functions whose result has no independent pin are marked "parity unpinned";
-every other function is pinned by the tests under tests/test_oracle_*.py.
+Functions whose result has no independent pin are marked "parity unpinned"
+(scale_release: QFlash's ScaleRelease, whose definition is not in the pages);
+every other function is pinned by the CPU tests tests/test_oracle_pins.py,
+tests/test_oracle_mutations.py, tests/test_mean_rounding_claim.py,
+tests/test_prob_mass.py, tests/test_kv_append.py, tests/test_exact24.py and
+tests/test_intsoftmax.py.
 """
 from __future__ import annotations
 
 import math
-from typing import Optional
 
 import numpy as np
 

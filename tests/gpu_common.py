@@ -5,9 +5,7 @@ import os
 import numpy as np
 import torch
 
-from oracle import qattn_oracle as O
 from quantized_attention_gb300 import binding as qb
-from quantized_attention_gb300 import inputs as I
 from quantized_attention_gb300.pipeline import device_inputs, problem_for
 
 

@@ -1,7 +1,6 @@
 """Pins of the oracle's 24-bit exact split mode (Strata PR, "What it does":
 both operands of QK^T and PV split into three exact 8-bit parts, X = h*65536 +
 l*256 + m; "Measured": ~2e-6 max relative error against FP64).  CPU only."""
-import importlib.util
 import os
 import types
 

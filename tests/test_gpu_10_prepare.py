@@ -1,7 +1,6 @@
 """qattn_prepare (the pre-pass in two launches) writes, byte for byte, what
 qattn_smooth_k + qattn_quantize_qk + qattn_quantize_v write: the K mean, Q/K
 codes and scales, K's fp16 carriers, V's transposed e4m3 codes and scales."""
-import numpy as np
 import pytest
 import torch
 

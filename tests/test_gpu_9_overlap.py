@@ -2,7 +2,6 @@
 consecutive steps in flight together on three streams) gives, step by step,
 exactly the outputs of the serial path on the same inputs, with several input
 sets used in turn so that a step reading another step's buffers would show."""
-import numpy as np
 import pytest
 import torch
 
