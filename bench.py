@@ -533,6 +533,20 @@ def gpu_arm(args):
                                f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
                 "traffic": _attn_traffic(args.workload),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
+    if wl.name in ("vit", "swin") and not (args.intsoftmax or args.exact24):
+        # short rows (197 / 49 keys): the operands' bytes bound these shapes
+        v_ld = qb.v_ld(wl.Nk)
+        alg_bytes = (wl.B * wl.Hq * wl.Nq * wl.d + wl.B * wl.Hkv * wl.Nk * wl.d  # Q, K codes
+                     + wl.B * wl.Hkv * wl.d * v_ld                              # V8^T
+                     + wl.B * wl.Hq * wl.Nq * wl.d * 2                          # bf16 O
+                     + (wl.Nq * wl.Nk * 4 if bias is not None else 0))         # fp32 bias
+        gbs = alg_bytes / (attn_avg_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "attn_fwd_kernel (the one launch of qattn_fwd)",
+                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"],
+                    "peak_basis": f"{peaks['source']} HBM copy rate",
+                    "algorithmic_bytes": alg_bytes,
+                    "tensor_frac": achieved / pmix, "traffic": None}
     if args.intsoftmax:  # the integer softmax dominates: an ALU roofline
         # algorithmic integer operations per score: S - m, ShiftExp2's five
         # (quotient, remainder, halving, + X0, shift), requantization's three

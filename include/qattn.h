@@ -188,20 +188,22 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
                               float* v_scales, void* workspace, size_t workspace_bytes,
                               qattn_stream_t stream);
 
-/* a1-a3 in two launches, for bf16 Q, K and V with block granules: the same
- * outputs, bit for bit, as qattn_smooth_k, then qattn_quantize_qk (k_mean
- * given, k_dtype QATTN_BF16), then qattn_quantize_v (QATTN_BF16).  Launch 1
- * quantizes Q and reduces K's channel sums and V's channel maxima (three
- * independent jobs in one grid); launch 2 quantizes K - mean (with the fp16
- * carriers when k_carrier is not NULL) and writes V's transposed e4m3 codes.
- * This pre-pass is how the pages' recipe runs before the attention kernel;
- * fusing it is this library's own step (fewer launches, one read of Q).
+/* a1-a3 in one or two launches, for bf16 Q, K and V with block granules: the
+ * same outputs, bit for bit, as qattn_smooth_k, then qattn_quantize_qk
+ * (k_mean given, k_dtype QATTN_BF16), then qattn_quantize_v (QATTN_BF16).
+ * Launch 1 quantizes Q and reduces K's channel sums and V's channel maxima
+ * (three independent jobs in one grid); launch 2 quantizes K - mean (with the
+ * fp16 carriers when k_carrier is not NULL) and writes V's transposed e4m3
+ * codes.  Heads of at most 128 tokens with d <= 64 (e.g. Swin windows): one
+ * launch, one warp per head.  This pre-pass is how the pages' recipe runs
+ * before the attention kernel; fusing it is this library's own step (fewer
+ * launches, one read of Q).
  *   Q            bf16 [B][Hq][Nq][d];  K, V  bf16 [B][Hkv][Nk][d]
  *   k_mean (out) fp32 [B][Hkv][d]; the other outputs as for the three calls
  *   params       q_gran = k_gran = QATTN_GRAN_BLOCK, else QATTN_ERR_UNSUPPORTED
  *                (use the three calls); Nk >= 1, else QATTN_ERR_UNSUPPORTED
  *   ldv          >= qattn_v_ld(Nk), multiple of 16
- *   workspace    at least qattn_workspace_size() bytes (zeroed here).
+ *   workspace    at least qattn_workspace_size() bytes.
  */
 qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                            const qattn_shape* shape, const qattn_params* params,

@@ -91,9 +91,10 @@ struct RowsJob {
 cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, int m1, int d,
                                  cudaStream_t s);
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
-// The pre-pass for bf16 Q, K, V with block granules in two launches: jq (Q,
-// mode 0), jk (K minus jk.chan = the mean it writes, mode 1), V's e4m3
-// transpose.  ws: prepare_ws_bytes(), zeroed here.
+// The pre-pass for bf16 Q, K, V with block granules: jq (Q, mode 0), jk (K
+// minus jk.chan = the mean it writes, mode 1), V's e4m3 transpose.  One launch
+// for heads of at most 128 tokens and d <= 64, else two (ws zeroed here).
+// ws: prepare_ws_bytes().
 cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
 size_t prepare_ws_bytes(long long BH, long long d);

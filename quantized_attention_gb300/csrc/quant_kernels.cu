@@ -725,121 +725,201 @@ __device__ __forceinline__ void codes8(const float (&x)[8], float inv, int8_t* d
   }
 }
 
+// Per-warp pieces of a short head's pre-pass.  Lane (rg, v) handles rows rg,
+// rg + RG, ... and the 8 channels of 16-byte column v.
+template <int D>
+struct HeadLane {
+  static constexpr int VPR = D / 8;    // 16-byte vectors per row
+  static constexpr int RG = 32 / VPR;  // row groups per warp
+  static constexpr int UNR = 8;        // rows a lane loads before it uses them
+  int v, rg;
+  __device__ explicit HeadLane(int lane) : v(lane % VPR), rg(lane / VPR) {}
+  // Rows r0, r0 + RG, ... (UNR of them) of the lane's column; zeros past N.
+  __device__ void load_rows(const uint16_t* head, int N, int r0, uint4 (&raw)[UNR]) const {
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * RG;
+      raw[u] = (r < N) ? *(reinterpret_cast<const uint4*>(head + static_cast<size_t>(r) * D) + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+};
+
+// The channel mean of a head's N rows (exact fixed-point sums), every lane of a
+// column holding its 8 channels' means.
+template <int D>
+__device__ __forceinline__ void head_mean(const HeadLane<D>& L, const uint16_t* head, int N,
+                                          unsigned long long magic, float (&mu)[8]) {
+  constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
+  long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
+    uint4 raw[UNR];
+    L.load_rows(head, N, r0, raw);  // rows past N are zeros: they add nothing
+    long long s8[8];
+    fix24_column_sums<UNR>(raw, s8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] += s8[e];
+  }
+#pragma unroll
+  for (int o = HeadLane<D>::VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mu[e] = mean_of_fix24(sum[e], static_cast<uint32_t>(N), magic);
+}
+
+// max |x - mu| (MINUS) or max |x| over a head's rows, over the whole warp.
+template <int D, bool MINUS>
+__device__ __forceinline__ float head_amax(const HeadLane<D>& L, const uint16_t* head, int N,
+                                           const float (&mu)[8]) {
+  constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
+  float am = 0.f;
+  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
+    uint4 raw[UNR];
+    L.load_rows(head, N, r0, raw);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      if (r0 + u * RG >= N) break;
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(MINUS ? __fsub_rn(x[e], mu[e]) : x[e]));
+    }
+  }
+  return warp_max(am);
+}
+
+// The head's codes rint((x [- mu]) * inv) (and carriers) at codes + row * D.
+template <int D, bool MINUS>
+__device__ __forceinline__ void head_codes(const HeadLane<D>& L, const uint16_t* head, int N,
+                                           const float (&mu)[8], float inv, int8_t* codes,
+                                           uint16_t* carrier) {
+  constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
+  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
+    uint4 raw[UNR];
+    L.load_rows(head, N, r0, raw);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * RG;
+      if (r >= N) break;
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+      if (MINUS) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
+      }
+      const size_t off = static_cast<size_t>(r) * D + L.v * 8;
+      codes8(x, inv, codes + off, carrier ? carrier + off : nullptr);
+    }
+  }
+}
+
+// Per-channel max |V| over a head's rows, every lane of a column holding its 8.
+template <int D>
+__device__ __forceinline__ void head_vamax(const HeadLane<D>& L, const uint16_t* head, int N,
+                                           float (&vm)[8]) {
+  constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) vm[e] = 0.f;
+  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
+    uint4 raw[UNR];
+    L.load_rows(head, N, r0, raw);  // zero rows leave a maximum of |x| unchanged
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], fabsf(x[e]));
+    }
+  }
+#pragma unroll
+  for (int o = HeadLane<D>::VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], __shfl_xor_sync(0xffffffffu, vm[e], o));
+  }
+}
+
+// The head's V8^T rows [D][ldv] (keys past N are 0): e4m3(fp32(x * sc)) per
+// channel, through the warp's [D][TL] byte tile.
+template <int D, int TL>
+__device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* head, int N,
+                                         const float (&sc)[8], uint8_t* tile, uint8_t* v8t_head,
+                                         long long ldv, int lane) {
+  for (int i = lane; i < D * TL / 16; i += 32) reinterpret_cast<uint4*>(tile)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncwarp();
+  constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
+  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
+    uint4 raw[UNR];
+    L.load_rows(head, N, r0, raw);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * RG;
+      if (r >= N) break;
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t b2 = cvt_e4m3x2(__fmul_rn(x[e], sc[e]), __fmul_rn(x[e + 1], sc[e + 1]));
+        tile[(L.v * 8 + e) * TL + r] = static_cast<uint8_t>(b2 & 0xFFu);
+        tile[(L.v * 8 + e + 1) * TL + r] = static_cast<uint8_t>(b2 >> 8);
+      }
+    }
+  }
+  __syncwarp();
+  const int nchunk = static_cast<int>(ldv / 16);  // 16-byte chunks of a V8^T row
+  for (int i = lane; i < D * nchunk; i += 32) {
+    const int c = i / nchunk, k = i % nchunk;
+    const uint4 w = (16 * k < TL) ? *reinterpret_cast<const uint4*>(tile + c * TL + 16 * k)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(v8t_head + static_cast<size_t>(c) * ldv + 16 * k) = w;
+  }
+}
+
+// Block granules, heads of at most 128 tokens: everything in one launch.
 template <int D>
 __global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const SmallPrepArgs p) {
   pdl_trigger();
   pdl_wait();
-  constexpr int VPR = D / 8;    // 16-byte vectors per row
-  constexpr int RG = 32 / VPR;  // row groups per warp
   __shared__ __align__(16) uint8_t tiles[kSmallWarps][D * kSmallHead];  // V8^T of a warp's head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * kSmallWarps + warp;
-  const int v = lane % VPR, rg = lane / VPR;
+  const HeadLane<D> L(lane);
+  const float none[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (item < p.BHq) {  // ---- a Q head: block amax, codes, scale
     const int bh = item;
     const uint16_t* src = p.Q + static_cast<size_t>(bh) * p.Nq * D;
-    float am = 0.f;
-    for (int r = rg; r < p.Nq; r += RG) {
-      float x[8];
-      unpack_bf16x8(*(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + v), x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e]));
-    }
-    const float g = warp_max(am);
+    const float g = head_amax<D, false>(L, src, p.Nq, none);
     const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
-    for (int r = rg; r < p.Nq; r += RG) {
-      float x[8];
-      unpack_bf16x8(*(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + v), x);
-      codes8(x, inv, p.q_codes + (static_cast<size_t>(bh) * p.Nq + r) * D + v * 8, nullptr);
-    }
+    head_codes<D, false>(L, src, p.Nq, none, inv, p.q_codes + static_cast<size_t>(bh) * p.Nq * D, nullptr);
     if (lane == 0) p.q_scales[bh] = __fdiv_rn(g, 127.0f);
     return;
   }
   const int bh = item - p.BHq;
   if (bh >= p.BHk) return;
-  // ---- a KV head.  The channel mean: exact sums of round(K * 2^24).
+  // ---- a KV head: channel mean, K - mean codes, V maxima and e4m3 codes
   const uint16_t* ks = p.K + static_cast<size_t>(bh) * p.Nk * D;
   const uint16_t* vs = p.V + static_cast<size_t>(bh) * p.Nk * D;
-  long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int r = rg; r < p.Nk; r += RG) {
-    const uint4 raw[1] = {*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v)};
-    long long s8[8];
-    fix24_column_sums<1>(raw, s8);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sum[e] += s8[e];
-  }
-#pragma unroll
-  for (int o = VPR; o < 32; o <<= 1) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
-  }
   float mu[8];
+  head_mean<D>(L, ks, p.Nk, p.magic, mu);
+  if (L.rg == 0) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) mu[e] = mean_of_fix24(sum[e], static_cast<uint32_t>(p.Nk), p.magic);
-  if (rg == 0) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) p.k_mean[static_cast<size_t>(bh) * D + v * 8 + e] = mu[e];
+    for (int e = 0; e < 8; ++e) p.k_mean[static_cast<size_t>(bh) * D + L.v * 8 + e] = mu[e];
   }
-  // K - mean: block amax, codes (+ carriers), scale
-  float am = 0.f;
-  for (int r = rg; r < p.Nk; r += RG) {
-    float x[8];
-    unpack_bf16x8(*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(x[e], mu[e])));
-  }
-  const float g = warp_max(am);
+  const float g = head_amax<D, true>(L, ks, p.Nk, mu);
   const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
-  for (int r = rg; r < p.Nk; r += RG) {
-    float x[8];
-    unpack_bf16x8(*(reinterpret_cast<const uint4*>(ks + static_cast<size_t>(r) * D) + v), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
-    const size_t off = (static_cast<size_t>(bh) * p.Nk + r) * D + v * 8;
-    codes8(x, inv, p.k_codes + off, p.k_carrier ? p.k_carrier + off : nullptr);
-  }
+  const size_t hoff = static_cast<size_t>(bh) * p.Nk * D;
+  head_codes<D, true>(L, ks, p.Nk, mu, inv, p.k_codes + hoff, p.k_carrier ? p.k_carrier + hoff : nullptr);
   if (lane == 0) p.k_scales[bh] = __fdiv_rn(g, 127.0f);
-  // V: channel maxima, scales, e4m3 codes into the warp's [D][128] tile
-  float vm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int r = rg; r < p.Nk; r += RG) {
-    float x[8];
-    unpack_bf16x8(*(reinterpret_cast<const uint4*>(vs + static_cast<size_t>(r) * D) + v), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], fabsf(x[e]));
-  }
-#pragma unroll
-  for (int o = VPR; o < 32; o <<= 1) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], __shfl_xor_sync(0xffffffffu, vm[e], o));
-  }
-  float sc[8];
+  float vm[8], sc[8];
+  head_vamax<D>(L, vs, p.Nk, vm);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     sc[e] = (vm[e] > 0.f) ? __fdiv_rn(448.0f, vm[e]) : 0.f;
-    if (rg == 0) p.v_scales[static_cast<size_t>(bh) * D + v * 8 + e] = __fdiv_rn(vm[e], 448.0f);
+    if (L.rg == 0) p.v_scales[static_cast<size_t>(bh) * D + L.v * 8 + e] = __fdiv_rn(vm[e], 448.0f);
   }
-  uint8_t* tile = tiles[warp];
-  for (int i = lane; i < D * kSmallHead / 16; i += 32)  // keys past Nk are 0
-    reinterpret_cast<uint4*>(tile)[i] = make_uint4(0u, 0u, 0u, 0u);
-  __syncwarp();
-  for (int r = rg; r < p.Nk; r += RG) {
-    float x[8];
-    unpack_bf16x8(*(reinterpret_cast<const uint4*>(vs + static_cast<size_t>(r) * D) + v), x);
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const uint32_t b2 = cvt_e4m3x2(__fmul_rn(x[e], sc[e]), __fmul_rn(x[e + 1], sc[e + 1]));
-      tile[(v * 8 + e) * kSmallHead + r] = static_cast<uint8_t>(b2 & 0xFFu);
-      tile[(v * 8 + e + 1) * kSmallHead + r] = static_cast<uint8_t>(b2 >> 8);
-    }
-  }
-  __syncwarp();
-  const int nchunk = static_cast<int>(p.ldv / 16);  // 16-byte chunks of a V8^T row
-  for (int i = lane; i < D * nchunk; i += 32) {
-    const int c = i / nchunk, k = i % nchunk;
-    const uint4 w = (16 * k < kSmallHead) ? *reinterpret_cast<const uint4*>(tile + c * kSmallHead + 16 * k)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(p.v8t + (static_cast<size_t>(bh) * D + c) * p.ldv + 16 * k) = w;
-  }
+  head_v8t<D, kSmallHead>(L, vs, p.Nk, sc, tiles[warp], p.v8t + static_cast<size_t>(bh) * D * p.ldv, p.ldv,
+                          lane);
 }
 
 // ------------------------------------------------------------------ carriers
@@ -918,6 +998,7 @@ cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long*
   return smooth_k_t<128>(K, BH, Nk, ws, mu, s);
 }
 
+// Scratch: K channel sums and done counters, V channel maxima.
 size_t prepare_ws_bytes(long long BH, long long d) {
   auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
   return a256(smooth_k_ws_bytes(BH, 0, d)) + a256(static_cast<size_t>(BH * d) * sizeof(unsigned int));
@@ -935,7 +1016,8 @@ static cudaError_t prepare_t(const Prep1Args& p1, const Prep2Args& p2, cudaStrea
 cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s) {
   const int BHk = jk.BH, Nk = jk.N;
-  if (BHk <= 0 || Nk <= 0 || jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
+  if (BHk <= 0 || Nk <= 0) return cudaErrorInvalidValue;
+  if (jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
   if (d <= 64 && jq.N <= kSmallHead && Nk <= kSmallHead) {  // short heads: one warp each, one launch
     SmallPrepArgs p{};
     p.Q = jq.X;

@@ -45,8 +45,8 @@ class Problem:
         self.lse = torch.empty((B, Hq, Nq), dtype=f32, device=dev) if want_lse else None
         ws = max(qb.workspace_size(self.shape, self.params), 256)
         self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
-        # qattn_prepare covers bf16 K/V with block granules (two launches
-        # instead of four); other granules take the three separate calls
+        # qattn_prepare covers bf16 K/V with block granules (one or two
+        # launches instead of four); other granules take the three calls
         self.fused_prepass = (fused_prepass and not kv_codes and Nk > 0 and
                               q_gran == qb.GRAN_BLOCK and k_gran == qb.GRAN_BLOCK)
 
