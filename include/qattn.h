@@ -383,6 +383,16 @@ qattn_status qattn_debug_qk_scores(const int8_t* q_codes, const int8_t* k_codes,
                                    const qattn_shape* shape, int32_t* S, void* workspace,
                                    size_t workspace_bytes, qattn_stream_t stream);
 
+/* Which kernel qattn_fwd runs for a shape and params (a qattn_fwd_kernel value:
+ * QATTN_FWD_TC or QATTN_FWD_SHORT), or -1 if the call would be rejected
+ * (invalid arguments, or QATTN_FWD_SHORT asked for a shape it does not
+ * cover).  Host only, no device work. */
+int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params);
+
+/* How many kernels qattn_prepare launches for a shape and params (1 or 2; 0
+ * for an empty problem), or -1 if it would reject them.  Host only. */
+int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params);
+
 /* Synchronises `stream`, then returns and clears the device error word of
  * the current device (QATTN_ERR_TIMEOUT if a kernel gave up on a wait,
  * QATTN_ERR_INVALID_ARG if a kernel found device-held scales outside its

@@ -28,6 +28,7 @@ EXPORTED = (
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
     "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
+    "qattn_fwd_kernel_choice", "qattn_prepare_launches",
 )
 
 
@@ -84,6 +85,10 @@ def lib() -> ctypes.CDLL:
     L.qattn_fwd_exact24.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_fwd_intsoftmax.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp]
     L.qattn_get_error.argtypes = [vp]
+    L.qattn_fwd_kernel_choice.argtypes = [PS, PP]
+    L.qattn_fwd_kernel_choice.restype = ctypes.c_int
+    L.qattn_prepare_launches.argtypes = [PS, PP]
+    L.qattn_prepare_launches.restype = ctypes.c_int
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
@@ -281,6 +286,16 @@ def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):
                                        _p(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream)),
            "qattn_debug_qk_scores")
+
+
+def fwd_kernel_choice(shape: Shape, params: Params) -> int:
+    """The kernel qattn_fwd runs (FWD_TC or FWD_SHORT), or -1 if it would reject the call."""
+    return lib().qattn_fwd_kernel_choice(ctypes.byref(shape), ctypes.byref(params))
+
+
+def prepare_launches(shape: Shape, params: Params) -> int:
+    """Kernels qattn_prepare launches (1 or 2), or -1 if it would reject the call."""
+    return lib().qattn_prepare_launches(ctypes.byref(shape), ctypes.byref(params))
 
 
 def get_error(stream=None) -> int:

@@ -102,6 +102,21 @@ qattn_status check_params(const qattn_params* p) {
   return QATTN_OK;
 }
 
+// The kernel qattn_fwd runs: the warp-level kernels for short non-causal key
+// sequences, chosen automatically for windows (Nq, Nk <= 64, where the
+// persistent kernel's 128-row tiles would be mostly empty) or when asked for;
+// else the persistent one.  -1 when the requested kernel does not cover the
+// shape.  Shape and params already validated.
+int fwd_choice(const qattn_shape* shape, const qattn_params* params) {
+  const bool short_ok = (shape->d == 32 || shape->d == 64) && !params->causal &&
+                        params->pv_mode == QATTN_PV_E4M3 && shape->Nk >= 1 &&
+                        shape->Nk <= qattn::kShortMaxNk;
+  const bool window = short_ok && shape->Nq <= qattn::kWindowMax && shape->Nk <= qattn::kWindowMax;
+  if (params->fwd_kernel == QATTN_FWD_SHORT) return short_ok ? QATTN_FWD_SHORT : -1;
+  if (params->fwd_kernel == QATTN_FWD_AUTO && window) return QATTN_FWD_SHORT;
+  return QATTN_FWD_TC;
+}
+
 int64_t pos0_of(const qattn_shape* s, const qattn_params* p) {
   return p->q_pos0 == QATTN_POS0_BOTTOM_RIGHT ? s->Nk - s->Nq : p->q_pos0;
 }
@@ -382,16 +397,9 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
     if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return QATTN_ERR_INVALID_ARG;
   }
-  // the warp-level kernels for short non-causal key sequences, or the persistent
-  // one; chosen automatically for windows (Nq, Nk <= 64), where the persistent
-  // kernel's 128-row tiles would be mostly empty
-  const bool short_ok = (shape->d == 32 || shape->d == 64) && !params->causal &&
-                        params->pv_mode == QATTN_PV_E4M3 && shape->Nk >= 1 &&
-                        shape->Nk <= qattn::kShortMaxNk;
-  const bool window = short_ok && shape->Nq <= qattn::kWindowMax && shape->Nk <= qattn::kWindowMax;
-  const bool use_short = params->fwd_kernel == QATTN_FWD_SHORT ||
-                         (params->fwd_kernel == QATTN_FWD_AUTO && window);
-  if (use_short && !short_ok) return QATTN_ERR_UNSUPPORTED;
+  const int choice = fwd_choice(shape, params);
+  if (choice < 0) return QATTN_ERR_UNSUPPORTED;
+  const bool use_short = choice == QATTN_FWD_SHORT;
   if (!use_short && !k_carrier) {  // the K codes are converted into the workspace
     const size_t need = ws_fwd(shape);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
@@ -641,6 +649,19 @@ qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, in
       static_cast<int>(B * Hkv), static_cast<int>(d), static_cast<int>(T), static_cast<int>(pos),
       static_cast<long long>(capacity), k_chan_scale, v_chan_scale, k_mean, v_code_amax, k_codes,
       v_codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params) {
+  if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
+  return fwd_choice(shape, params);
+}
+
+int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params) {
+  if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
+  if (params->q_gran != QATTN_GRAN_BLOCK || params->k_gran != QATTN_GRAN_BLOCK || shape->Nk < 1) return -1;
+  if (empty_problem(shape)) return 0;
+  return qattn::prepare_launch_count(static_cast<int>(shape->d), static_cast<int>(shape->Nq),
+                                     static_cast<int>(shape->Nk));
 }
 
 qattn_status qattn_get_error(qattn_stream_t stream) {

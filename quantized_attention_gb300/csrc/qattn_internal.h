@@ -98,6 +98,7 @@ size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
 cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
 size_t prepare_ws_bytes(long long BH, long long d);
+int prepare_launch_count(int d, int Nq, int Nk);  // 1 for short heads, else 2
 
 cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,
                               uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws_amax,

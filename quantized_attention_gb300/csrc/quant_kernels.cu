@@ -1013,12 +1013,16 @@ static cudaError_t prepare_t(const Prep1Args& p1, const Prep2Args& p2, cudaStrea
   return launch_pdl(prepare2_kernel<D>, dim3(g2), dim3(kThreads), 0, s, p2);
 }
 
+int prepare_launch_count(int d, int Nq, int Nk) {
+  return (d <= 64 && Nq <= kSmallHead && Nk <= kSmallHead) ? 1 : 2;
+}
+
 cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s) {
   const int BHk = jk.BH, Nk = jk.N;
   if (BHk <= 0 || Nk <= 0) return cudaErrorInvalidValue;
   if (jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
-  if (d <= 64 && jq.N <= kSmallHead && Nk <= kSmallHead) {  // short heads: one warp each, one launch
+  if (prepare_launch_count(d, jq.N, Nk) == 1) {  // short heads: one warp each, one launch
     SmallPrepArgs p{};
     p.Q = jq.X;
     p.K = jk.X;

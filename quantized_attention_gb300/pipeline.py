@@ -120,19 +120,15 @@ class Problem:
 
     def short_fwd(self) -> bool:
         """Whether qattn_fwd runs a warp-level short-sequence kernel (the
-        library's choice for windows, Nq and Nk <= 64, or the one asked for)."""
-        p = self.params
-        ok = (self.d in (32, 64) and not p.causal and p.pv_mode == qb.PV_E4M3
-              and 1 <= self.Nk <= 256)
-        window = ok and self.Nq <= 64 and self.Nk <= 64
-        return p.fwd_kernel == qb.FWD_SHORT or (p.fwd_kernel == qb.FWD_AUTO and window)
+        library's own choice, asked of it)."""
+        return qb.fwd_kernel_choice(self.shape, self.params) == qb.FWD_SHORT
 
     def kernel_launches(self) -> int:
         """Kernels of this library that one ``run`` launches (memsets excluded)."""
         # [K carriers converted in qattn_fwd's workspace,] the attention kernel
         fwd = 1 + int(self.k_carrier is None and not self.short_fwd())
-        if self.fused_prepass:  # qattn_prepare: one launch for short heads, else two
-            return (1 if self.d <= 64 and self.Nq <= 128 and self.Nk <= 128 else 2) + fwd
+        if self.fused_prepass:
+            return qb.prepare_launches(self.shape, self.params) + fwd
         two_pass = (self.params.q_gran != qb.GRAN_BLOCK or
                     (not self.kv_codes and self.params.k_gran != qb.GRAN_BLOCK))
         n = 1 + int(two_pass)                        # Q and K codes (one grid)

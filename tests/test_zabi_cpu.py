@@ -128,3 +128,32 @@ def test_decode_and_append_arguments_rejected_on_host(L):
         p = qb.make_params(causal=True, kv_capacity=cap)
         assert L.qattn_decode(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(s),
                               ctypes.byref(p), fake, None, fake, 1 << 30, None) == st
+
+
+def test_kernel_choices_follow_the_documented_rules(L):
+    """qattn_fwd_kernel_choice / qattn_prepare_launches (host only) against the
+    rules include/qattn.h states for qattn_fwd_kernel and qattn_prepare."""
+    from quantized_attention_gb300 import binding as qb
+    shapes = [(49, 49), (64, 64), (65, 64), (64, 65), (1, 1), (197, 197), (128, 128),
+              (129, 100), (256, 256), (300, 300)]
+    for d in (32, 64, 128):
+        for nq, nk in shapes:
+            s = qb.make_shape(2, 4, 2, nq, nk, d)
+            for causal in (False, True):
+                for pv in (qb.PV_E4M3, qb.PV_INT8):
+                    short_ok = d in (32, 64) and not causal and pv == qb.PV_E4M3 and 1 <= nk <= 256
+                    window = short_ok and nq <= 64 and nk <= 64
+                    for kern in (qb.FWD_AUTO, qb.FWD_TC, qb.FWD_SHORT):
+                        p = qb.make_params(causal=causal, pv_mode=pv, fwd_kernel=kern)
+                        if kern == qb.FWD_SHORT:
+                            want = qb.FWD_SHORT if short_ok else -1
+                        elif kern == qb.FWD_AUTO and window:
+                            want = qb.FWD_SHORT
+                        else:
+                            want = qb.FWD_TC
+                        assert qb.fwd_kernel_choice(s, p) == want, (d, nq, nk, causal, pv, kern)
+            p = qb.make_params()
+            assert qb.prepare_launches(s, p) == (1 if d <= 64 and nq <= 128 and nk <= 128 else 2)
+            assert qb.prepare_launches(s, qb.make_params(q_gran=qb.GRAN_TENSOR)) == -1
+    assert qb.fwd_kernel_choice(qb.make_shape(1, 4, 2, 64, 64, 96), qb.make_params()) == -1
+    assert qb.prepare_launches(qb.make_shape(1, 4, 2, 64, 0, 64), qb.make_params()) == -1
