@@ -1,13 +1,22 @@
 """Benchmark of the quantized attention prefill path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-K channel mean, Q/K int8 quantization, V e4m3 quantization and the fused
-attention kernel (qattn_smooth_k, qattn_quantize_qk, qattn_quantize_v,
-qattn_fwd).  Default workload: LLM prefill, B=1, 32 query heads / 8 KV heads,
-8192 tokens, d=128, causal (the 8K causal prefill shape the throughput target
-is stated on).
+K channel mean, Q/K int8 quantization, V e4m3 quantization (qattn_prepare,
+one or two launches; the three separate calls for tensor/head granules) and
+the fused attention kernel (qattn_fwd).  Default workload: LLM prefill, B=1,
+32 query heads / 8 KV heads, 8192 tokens, d=128, causal (the 8K causal
+prefill shape the throughput target is stated on).  Other workloads: tiny,
+vit, swin, chunk32k (prefill on an int8 KV cache) and decode32k (a step
+appends one token to the int8 cache, quantizes its Q and decodes); modes
+--exact24 (the 24-bit exact split mode on the int8 cache) and --intsoftmax
+(QFlash's integer-only attention on per-tensor int8 codes).
+
+The line's value is device-resident throughput; "e2e" is the same step
+through the public path with host buffers, the copies in and out overlapped
+across consecutive steps (pipeline.OverlappedSteps; decode: serial).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--exact24 | --intsoftmax] [--no-cpu-baseline]
     python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints one JSON line on rank 0.
