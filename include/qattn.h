@@ -195,8 +195,8 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
  * (three independent jobs in one grid); launch 2 quantizes K - mean (with the
  * fp16 carriers when k_carrier is not NULL) and writes V's transposed e4m3
  * codes.  Heads of at most 128 tokens with d <= 64 (e.g. Swin windows): one
- * launch, one warp per head.  This pre-pass is how the pages' recipe runs
- * before the attention kernel; fusing it is this library's own step (fewer
+ * launch, one warp per head.  The ZINC post's recipe runs these three steps
+ * before the attention kernel; fusing them is this library's own step (fewer
  * launches, one read of Q).
  *   Q            bf16 [B][Hq][Nq][d];  K, V  bf16 [B][Hkv][Nk][d]
  *   k_mean (out) fp32 [B][Hkv][d]; the other outputs as for the three calls

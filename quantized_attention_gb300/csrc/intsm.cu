@@ -4,8 +4,8 @@
 // (X = Q X0 + R, 2^(s~ R) ~= s~ R / 2 + 1, so P = ((R >> 1) + X0) >> -Q at
 // scale s~, eq. (5)-(8)); P requantized to int8 by a fixed-point multiplier
 // (eq. (9)-(10)); row sums (eq. (11)); the accumulators rescaled by the
-// max-offset factor alpha with ScaleRelease (read here as floor(x * alpha / X0):
-// its definition, the paper's Appendix B.1, is not in the pages) and O += P.V
+// max-offset factor alpha with ScaleRelease (read here as floor(x * alpha / X0);
+// the paper defers its definition to an appendix not cited here) and O += P.V
 // in int32; out = floor(O / l) as int8 codes of V's scale.
 //
 // Both products run on the warp-level fp16 tensor cores (mma.m16n8k16, fp32
