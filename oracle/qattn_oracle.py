@@ -117,10 +117,13 @@ def smooth_k(K: np.ndarray) -> np.ndarray:
     """mu[b, h, c] = mean over keys of K[b, h, :, c], as fp32.
 
     Fixed point: fix(x) = round_half_even(x * 2^24) as int64, summed exactly,
-    then mu = fp32(fp64(sum) * 2^-24 / Nk).
+    then mu = fp32(fp64(sum) * 2^-24 / Nk).  With no keys (Nk = 0) the mean
+    has no value and nothing is subtracted from anything: mu = 0 (a reading).
     """
     K = np.asarray(K, dtype=F32)
     Nk = K.shape[2]
+    if Nk == 0:
+        return np.zeros((K.shape[0], K.shape[1], K.shape[3]), dtype=F32)
     fix = np.rint(K.astype(F64) * 2.0 ** FIX_BITS).astype(np.int64)
     s = fix.sum(axis=2, dtype=np.int64)
     assert np.abs(s).max(initial=0) < 2 ** 53, "channel sum leaves the exact range"
