@@ -252,6 +252,8 @@ qattn_status qattn_quantize_v_noalloc(const void* V, qattn_dtype v_dtype,
  *   m' = max(m, max t);  alpha = 2^(m - m');  P = 2^(t - m') <= 1
  *   l = alpha * l + sum P;  O = alpha * O + e4m3(448 P) . V8
  *   out = O * v_scale / (448 l)   (0 for a row with no visible key)
+ * Nk = 0: every row is fully masked; the call writes out = 0 and lse = -inf
+ * with no attention kernel and reads no K, V or workspace argument.
  * ("QFlash", section 2.1 and Algorithm 1 for the blockwise loop; ZINC post for
  * P <= 1, the static 448 and e4m3.)  The QK^T product runs on the tensor cores
  * as exact small integers held in fp16 (kind::f16, fp32 accumulation: every
@@ -313,6 +315,7 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
  *                out_dtype, kv_capacity (granules, pv_mode and bias unused)
  * Limits: d in {64, 128}, B * Hq <= 65535.  Workspace: at least
  * qattn_workspace_size() (three fp16 planes of Q's parts and the group scales).
+ * Nk = 0: out = 0 and lse = -inf, as for qattn_fwd.
  */
 qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float* k_chan_scale,
                                const int8_t* v_codes, const float* v_chan_scale,

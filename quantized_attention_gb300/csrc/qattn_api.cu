@@ -125,6 +125,15 @@ qattn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QATTN_OK : QAT
 
 bool empty_problem(const qattn_shape* s) { return s->B == 0 || s->Hq == 0 || s->Nq == 0; }
 
+// Nk = 0: every row is fully masked, so out = 0 and lse = -inf, with no
+// attention kernel.  Shape (non-empty) and params already validated.
+qattn_status no_key_rows(const qattn_shape* shape, const qattn_params* params, void* O, float* lse,
+                         cudaStream_t s) {
+  const size_t rows = static_cast<size_t>(shape->B * shape->Hq * shape->Nq);
+  const size_t esize = params->out_dtype == QATTN_BF16 ? 2 : 4;
+  return from_cuda(qattn::launch_no_key_rows(O, rows * static_cast<size_t>(shape->d) * esize, lse, rows, s));
+}
+
 // Workspace regions of each entry point.
 size_t ws_smooth(const qattn_shape* s) { return align256(qattn::smooth_k_ws_bytes(s->B * s->Hkv, s->Nk, s->d)); }
 size_t ws_quant_qk(const qattn_shape* s, const qattn_params* p) {
@@ -400,11 +409,12 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   const int choice = fwd_choice(shape, params);
   if (choice < 0) return QATTN_ERR_UNSUPPORTED;
   const bool use_short = choice == QATTN_FWD_SHORT;
-  if (!use_short && !k_carrier) {  // the K codes are converted into the workspace
+  if (!use_short && !k_carrier && shape->Nk > 0) {  // the K codes are converted into the workspace
     const size_t need = ws_fwd(shape);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (shape->Nk == 0) return no_key_rows(shape, params, O, lse, s);
   unsigned int* err = error_word();
   if (!err) return QATTN_ERR_CUDA;
   AttnArgs a{};
@@ -431,29 +441,21 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   a.lse = lse;
   a.err = err;
   if (use_short) return from_cuda(qattn::launch_attn_short(a, q_codes, k_codes, v8t, ldv, s));
-  if (shape->Nk == 0) {
-    // No keys: every row is fully masked.  The kernel's empty-tile path
-    // writes the zeros; give it valid (unused) maps.
-    a.Nk = 0;
-  }
   const uint16_t* kc16 = k_carrier;
   if (!kc16) {  // convert the K codes into the workspace (checked above)
     uint16_t* w16 = static_cast<uint16_t*>(workspace);
-    if (shape->Nk > 0) {
-      const cudaError_t e = qattn::launch_codes_to_f16(
-          k_codes, w16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
-      if (e != cudaSuccess) return QATTN_ERR_CUDA;
-    }
+    const cudaError_t e = qattn::launch_codes_to_f16(
+        k_codes, w16, static_cast<size_t>(shape->B * shape->Hkv * shape->Nk * shape->d), s);
+    if (e != cudaSuccess) return QATTN_ERR_CUDA;
     kc16 = w16;
   }
   CUtensorMap tq, tk, tv;
-  const int64_t nk_map = shape->Nk > 0 ? shape->Nk : 1;
   if (!encode_q_codes(&tq, q_codes, shape->B * shape->Hq, shape->Nq, shape->d) ||
-      !encode_carrier(&tk, kc16, shape->B * shape->Hkv, nk_map, shape->d) ||
-      !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, shape->Nk > 0 ? static_cast<const void*>(v8t) : workspace,
-                 static_cast<uint64_t>(nk_map), static_cast<uint64_t>(shape->d),
-                 static_cast<uint64_t>(shape->B * shape->Hkv), static_cast<uint64_t>(shape->Nk > 0 ? ldv : 16), 128,
-                 static_cast<uint32_t>(shape->d), CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_carrier(&tk, kc16, shape->B * shape->Hkv, shape->Nk, shape->d) ||
+      !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v8t, static_cast<uint64_t>(shape->Nk),
+                 static_cast<uint64_t>(shape->d), static_cast<uint64_t>(shape->B * shape->Hkv),
+                 static_cast<uint64_t>(ldv), 128, static_cast<uint32_t>(shape->d),
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return QATTN_ERR_CUDA;
   return from_cuda(qattn::launch_attn_fwd(tq, tk, tv, a, s));
 }
@@ -575,6 +577,7 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
     return QATTN_ERR_INVALID_ARG;
   const int64_t pos0 = pos0_of(shape, params);
   if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
+  if (shape->Nk == 0) return no_key_rows(shape, params, O, lse, reinterpret_cast<cudaStream_t>(stream));
   const size_t need = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Nq, shape->d);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   qattn::Exact24Args a{};

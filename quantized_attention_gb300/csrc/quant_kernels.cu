@@ -1146,4 +1146,20 @@ cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cuda
   return launch_pdl(codes_to_f16_kernel, dim3(grid_for(n16, 256)), dim3(256), 0, s, src, dst, n16);
 }
 
+// ------------------------------------------------------------------ rows with no keys
+__global__ void fill_u32_kernel(uint32_t* __restrict__ dst, size_t n, uint32_t v) {
+  pdl_trigger();
+  pdl_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[i] = v;
+}
+
+cudaError_t launch_no_key_rows(void* out, size_t out_bytes, float* lse, size_t rows, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(out, 0, out_bytes, s);
+  if (e != cudaSuccess || lse == nullptr || rows == 0) return e;
+  return launch_pdl(fill_u32_kernel, dim3(grid_for(rows, 256)), dim3(256), 0, s,
+                    reinterpret_cast<uint32_t*>(lse), rows, 0xFF800000u);  // -inf
+}
+
 }  // namespace qattn

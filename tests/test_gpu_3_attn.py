@@ -133,3 +133,28 @@ def test_int8_pv_ablation_matches_oracle(wl):
     # and it is not the e4m3 recipe
     e4 = O.run_workload(inp, prep, heads=heads, rows=rows)["O"]
     assert np.abs(gpu_out_rows(P, heads, rows) - e4).max() > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("out_dtype", [qb.DT_F32, qb.DT_BF16])
+def test_no_keys(causal, out_dtype):
+    """Nk = 0: every row is fully masked.  The oracle gives out = 0 and
+    lse = -inf; the call writes exactly that over poisoned outputs and reads
+    no K, V or workspace buffer."""
+    import torch
+    wl = I.small("tiny", Hq=2, Hkv=1, Nq=100, Nk=0, causal=causal)
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    ref = O.run_workload(inp, prep)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    odt = torch.bfloat16 if out_dtype == qb.DT_BF16 else torch.float32
+    out = torch.full((wl.B, wl.Hq, wl.Nq, wl.d), float("nan"), dtype=odt, device="cuda")
+    lse = torch.full((wl.B, wl.Hq, wl.Nq), 7.0, dtype=torch.float32, device="cuda")
+    qb.fwd(dev(prep["q_codes"]), dev(prep["q_scales"]), None, None, None, qb.v_ld(0), None, None,
+           qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, 0, wl.d),
+           qb.make_params(causal=causal, q_gran=wl.q_gran, k_gran=wl.k_gran, out_dtype=out_dtype),
+           out, lse, None)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    assert np.array_equal(out.float().cpu().numpy().reshape(ref["O"].shape), ref["O"])
+    assert np.array_equal(lse.cpu().numpy().reshape(ref["lse"].shape), ref["lse"])

@@ -82,3 +82,25 @@ def test_exact24_full_chunk_shape_sampled():
                              causal=wl.causal, q_pos0=wl.q_pos0, heads=heads, rows=rows)
     sub = np.stack([got[0, h][rows] for (_, h) in heads])
     assert np.abs(sub - want).max() <= TOL * np.abs(want).max()
+
+
+def test_exact24_no_keys():
+    """An empty cache (Nk = 0): the oracle gives out = 0 and lse = -inf for
+    every row; the call writes exactly that over poisoned outputs."""
+    wl = I.small("chunk32k", Hq=4, Hkv=2, Nq=70, Nk=0, q_pos0=0)
+    inp = I.make_inputs(wl)
+    want, want_lse = O.attn_exact24(inp.Q, inp.K_codes, inp.K_scale, inp.V_codes, inp.V_scale,
+                                    causal=wl.causal, q_pos0=wl.q_pos0)
+    dev = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dt)
+    shape = qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, 0, wl.d)
+    params = qb.make_params(causal=wl.causal, q_pos0=wl.q_pos0)
+    O_ = torch.full((wl.B, wl.Hq, wl.Nq, wl.d), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((wl.B, wl.Hq, wl.Nq), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(qb.workspace_size(shape, params), 256), dtype=torch.uint8, device="cuda")
+    qb.fwd_exact24(dev(inp.Q, torch.bfloat16), dev(inp.K_codes, torch.int8),
+                   dev(inp.K_scale, torch.float32), dev(inp.V_codes, torch.int8),
+                   dev(inp.V_scale, torch.float32), shape, params, O_, lse, ws)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    assert np.array_equal(O_.cpu().numpy().reshape(want.shape), want)
+    assert np.array_equal(lse.cpu().numpy().reshape(want_lse.shape), want_lse)

@@ -105,6 +105,16 @@ def test_invalid_arguments_rejected_on_host(L):
     s0 = qb.make_shape(0, 4, 2, 256, 256, 64)
     assert L.qattn_fwd(None, None, None, None, None, None, 0, None, None, ctypes.byref(s0),
                        ctypes.byref(p), None, None, None, 0, None) == 0
+    for empty in (qb.make_shape(1, 0, 2, 256, 256, 64), qb.make_shape(1, 4, 2, 0, 256, 64)):
+        assert L.qattn_fwd(None, None, None, None, None, None, 0, None, None, ctypes.byref(empty),
+                           ctypes.byref(p), None, None, None, 0, None) == 0
+    # no keys: the outputs are still required; the short kernel does not take it
+    s_nk0 = qb.make_shape(1, 4, 2, 32, 0, 64)
+    assert L.qattn_fwd(fake, fake, None, None, None, None, 16, None, None, ctypes.byref(s_nk0),
+                       ctypes.byref(p), None, None, None, 0, None) == 1
+    assert L.qattn_fwd(fake, fake, None, None, None, None, 16, None, None, ctypes.byref(s_nk0),
+                       ctypes.byref(p_short), fake, None, None, 0, None) == 2
+    assert qb.fwd_kernel_choice(s_nk0, p) == qb.FWD_TC
 
 
 def test_decode_and_append_arguments_rejected_on_host(L):
