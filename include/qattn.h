@@ -162,6 +162,8 @@ qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* 
  *                written to k_codes, or the I8 K given) as exact fp16 values,
  *                the operand form of the tensor-core product; hand it to
  *                qattn_fwd to spare it a conversion pass.
+ * Nk = 0: only Q is quantized; K, k_codes, k_scales and k_carrier may be NULL
+ * and nothing is written for K.
  */
 qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
                                const float* k_mean, const float* k_chan_scale,

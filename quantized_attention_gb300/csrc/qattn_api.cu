@@ -248,7 +248,8 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   if (k_dtype != QATTN_BF16 && k_dtype != QATTN_I8) return QATTN_ERR_INVALID_ARG;
   if (empty_problem(shape)) return QATTN_OK;
   const bool i8 = (k_dtype == QATTN_I8);
-  if (!Q || !aligned16(Q) || !q_codes || !aligned16(q_codes) || !q_scales || !k_scales) return QATTN_ERR_INVALID_ARG;
+  if (!Q || !aligned16(Q) || !q_codes || !aligned16(q_codes) || !q_scales || (shape->Nk > 0 && !k_scales))
+    return QATTN_ERR_INVALID_ARG;
   if (i8 && (!k_chan_scale || !aligned16(k_chan_scale))) return QATTN_ERR_INVALID_ARG;
   if (!i8 && shape->Nk > 0 && (!K || !aligned16(K) || !k_codes || !aligned16(k_codes))) return QATTN_ERR_INVALID_ARG;
   if (k_mean && (i8 || !aligned16(k_mean))) return QATTN_ERR_INVALID_ARG;
@@ -279,9 +280,10 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   if (i8) {
     // every K scale is 1: the Q quantizer's launch writes them
     jq.ones = k_scales;
-    jq.n_ones = params->k_gran == QATTN_GRAN_TENSOR ? 1
-                : params->k_gran == QATTN_GRAN_HEAD ? shape->B * shape->Hkv
-                                                    : shape->B * shape->Hkv * nkb;
+    jq.n_ones = shape->Nk == 0                        ? 0
+                : params->k_gran == QATTN_GRAN_TENSOR ? 1
+                : params->k_gran == QATTN_GRAN_HEAD   ? shape->B * shape->Hkv
+                                                      : shape->B * shape->Hkv * nkb;
     cudaError_t e = qattn::launch_quantize_rows(jq, 2, jk, 0, d, s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
     if (k_carrier && shape->Nk > 0) {

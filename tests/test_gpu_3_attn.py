@@ -158,3 +158,33 @@ def test_no_keys(causal, out_dtype):
     assert qb.get_error() == 0
     assert np.array_equal(out.float().cpu().numpy().reshape(ref["O"].shape), ref["O"])
     assert np.array_equal(lse.cpu().numpy().reshape(ref["lse"].shape), ref["lse"])
+
+
+NO_KEY_CASES = [
+    I.small("tiny", Nq=77, Nk=0),                                 # bf16 K/V, block granules
+    I.small("vit", B=2, Nq=50, Nk=0),                             # per-tensor granules
+    I.small("chunk32k", Hq=4, Hkv=2, Nq=64, Nk=0, q_pos0=0),      # an empty int8 cache
+]
+
+
+@pytest.mark.parametrize("wl", NO_KEY_CASES, ids=[_ids(w) for w in NO_KEY_CASES])
+def test_no_keys_through_the_pipeline(wl):
+    """Nk = 0 through the public path (quantize, then attend): Q's codes and
+    scales as the oracle's, every row fully masked (out = 0, lse = -inf)."""
+    import torch
+    from quantized_attention_gb300.pipeline import device_inputs, problem_for
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    ref = O.run_workload(inp, prep)
+    P = problem_for(wl, want_lse=True)
+    P.O.fill_(float("nan"))
+    P.lse.fill_(7.0)
+    dev = device_inputs(inp)
+    bias = dev.pop("bias", None)
+    P.run(**dev, bias=bias)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    assert np.array_equal(P.q_codes.cpu().numpy().reshape(prep["q_codes"].shape), prep["q_codes"])
+    assert np.array_equal(P.q_scales.cpu().numpy().ravel(), prep["q_scales"].ravel())
+    assert np.array_equal(P.O.float().cpu().numpy().reshape(ref["O"].shape), ref["O"])
+    assert np.array_equal(P.lse.cpu().numpy().reshape(ref["lse"].shape), ref["lse"])
