@@ -344,8 +344,8 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
  *   k_codes, v_codes  int8 [B][Hkv][Nk][d]; k_scale fp32[1] (device)
  *   O_codes  (out) int8 [B][Hq][Nq][d]
  *   params: sm_scale (0 -> fp32(1/sqrt(d))); causal must be 0
- * Limits: d in {32, 64, 128}, B * Hq <= 65535, Nk <= 131072 (int32 O), no
- * mask, O_codes 16-byte aligned.  No workspace.  The scales are read on the
+ * Limits: d in {32, 64, 128}, B * Hq <= 65535, 1 <= Nk <= 131072 (int32 O),
+ * no mask, O_codes 16-byte aligned.  No workspace.  The scales are read on the
  * device: if s~ is not a positive finite number or 1/s~ > 2^30 the kernel
  * writes nothing and qattn_get_error() returns QATTN_ERR_INVALID_ARG.
  */

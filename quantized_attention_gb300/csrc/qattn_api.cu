@@ -626,10 +626,12 @@ qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
     return QATTN_ERR_INVALID_ARG;
   const float sm = params->sm_scale > 0.f ? params->sm_scale
                                           : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
+  unsigned int* err = error_word();
+  if (!err) return QATTN_ERR_CUDA;
   return from_cuda(qattn::launch_intsoftmax(
       static_cast<int>(shape->B), static_cast<int>(shape->Hq), static_cast<int>(shape->Hkv),
       static_cast<int>(shape->Nq), static_cast<int>(shape->Nk), static_cast<int>(shape->d), sm, q_codes,
-      q_scale, k_codes, k_scale, v_codes, O_codes, error_word(), reinterpret_cast<cudaStream_t>(stream)));
+      q_scale, k_codes, k_scale, v_codes, O_codes, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, int64_t Hkv,

@@ -167,3 +167,36 @@ def test_kernel_choices_follow_the_documented_rules(L):
             assert qb.prepare_launches(s, qb.make_params(q_gran=qb.GRAN_TENSOR)) == -1
     assert qb.fwd_kernel_choice(qb.make_shape(1, 4, 2, 64, 64, 96), qb.make_params()) == -1
     assert qb.prepare_launches(qb.make_shape(1, 4, 2, 64, 0, 64), qb.make_params()) == -1
+
+
+def test_extra_modes_arguments_rejected_on_host(L):
+    """qattn_fwd_intsoftmax and qattn_fwd_exact24 reject what their header
+    limits exclude before any device work."""
+    from quantized_attention_gb300 import binding as qb
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    p = qb.make_params()
+
+    def ism(shape, params=p, O=fake, k_scale=fake):
+        return L.qattn_fwd_intsoftmax(fake, fake, fake, k_scale, fake, ctypes.byref(shape),
+                                      ctypes.byref(params), O, None)
+
+    ok = qb.make_shape(1, 3, 3, 197, 197, 64)
+    assert ism(ok, params=qb.make_params(causal=True)) == 2            # no mask
+    assert ism(qb.make_shape(1, 3, 3, 197, 0, 64)) == 2                # no keys
+    assert ism(qb.make_shape(1, 3, 3, 197, (1 << 17) + 1, 64)) == 2    # int32 O bound
+    assert ism(qb.make_shape(1, 3, 3, 197, 197, 96)) == 2              # head dim
+    assert ism(ok, O=vp((1 << 20) + 8)) == 1                           # O alignment
+    assert ism(ok, k_scale=None) == 1
+    assert ism(qb.make_shape(0, 3, 3, 197, 197, 64), O=None) == 0      # empty: nothing to do
+
+    def e24(shape, params=p, Q=fake, ws=fake, ws_bytes=1 << 30):
+        return L.qattn_fwd_exact24(Q, fake, fake, fake, fake, ctypes.byref(shape),
+                                   ctypes.byref(params), fake, None, ws, ws_bytes, None)
+
+    cache = qb.make_shape(1, 4, 2, 64, 1000, 128)
+    assert e24(qb.make_shape(1, 4, 2, 64, 1000, 32)) == 2              # d in {64, 128}
+    assert e24(cache, params=qb.make_params(kv_capacity=999)) == 1     # capacity below Nk
+    assert e24(cache, Q=vp((1 << 20) + 2)) == 1                        # Q alignment
+    assert e24(cache, ws=None, ws_bytes=0) == 5                        # workspace
+    assert e24(cache, ws_bytes=16) == 5
