@@ -290,7 +290,8 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
  *   v_code_amax  fp32 [B][Hkv][d]: max |code| of each V channel over the
  *                cache (the cache header keeps it as tokens arrive)
  *   O, lse       as for qattn_fwd; params as for qattn_fwd (pv_mode 0, no bias)
- * Limits: 1 <= (Hq / Hkv) * Nq <= 16, d in {64, 128}.  Workspace: at least
+ * Limits: 1 <= (Hq / Hkv) * Nq <= 16, d in {64, 128}, Nk >= 1 (a cache with
+ * no rows in use is QATTN_ERR_UNSUPPORTED), pv_mode E4M3.  Workspace: at least
  * qattn_workspace_size() for this shape.
  */
 qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,

@@ -138,6 +138,14 @@ def test_decode_and_append_arguments_rejected_on_host(L):
         p = qb.make_params(causal=True, kv_capacity=cap)
         assert L.qattn_decode(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(s),
                               ctypes.byref(p), fake, None, fake, 1 << 30, None) == st
+    # an empty cache, the int8-P ablation, more than 16 rows per KV head, d = 32
+    p = qb.make_params(causal=True)
+    for shp, pp in ((qb.make_shape(1, 8, 2, 1, 0, 128), p),
+                    (s, qb.make_params(causal=True, pv_mode=qb.PV_INT8)),
+                    (qb.make_shape(1, 8, 2, 5, 1000, 128), p),
+                    (qb.make_shape(1, 8, 2, 1, 1000, 32), p)):
+        assert L.qattn_decode(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(shp),
+                              ctypes.byref(pp), fake, None, fake, 1 << 30, None) == 2
 
 
 def test_kernel_choices_follow_the_documented_rules(L):
