@@ -108,6 +108,10 @@ def _p(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _nbytes(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def _stream(stream: Optional[torch.cuda.Stream] = None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -159,7 +163,7 @@ def smooth_k(K, shape, k_mean, workspace, stream=None):
     _dense(K, torch.bfloat16, "K")
     _dense(k_mean, torch.float32, "k_mean")
     _check(lib().qattn_smooth_k(_p(K), ctypes.byref(shape), _p(k_mean), _p(workspace),
-                                workspace.numel() * workspace.element_size(), _stream(stream)),
+                                _nbytes(workspace), _stream(stream)),
            "qattn_smooth_k")
 
 
@@ -172,7 +176,7 @@ def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_s
     _check(lib().qattn_quantize_qk(_p(Q), _p(K), k_dtype, _p(k_mean), _p(k_chan_scale),
                                    ctypes.byref(shape), ctypes.byref(params), _p(q_codes),
                                    _p(q_scales), _p(k_codes), _p(k_scales), _p(k_carrier),
-                                   _p(workspace), workspace.numel() * workspace.element_size(),
+                                   _p(workspace), _nbytes(workspace),
                                    _stream(stream)),
            "qattn_quantize_qk")
 
@@ -187,7 +191,7 @@ def prepare(Q, K, V, shape, params, q_codes, q_scales, k_codes, k_scales, k_mean
     _check(lib().qattn_prepare(_p(Q), _p(K), _p(V), ctypes.byref(shape), ctypes.byref(params),
                                _p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales),
                                _p(k_carrier), _p(k_mean), _p(v8t), ldv, _p(v_scales),
-                               _p(workspace), workspace.numel() * workspace.element_size(),
+                               _p(workspace), _nbytes(workspace),
                                _stream(stream)),
            "qattn_prepare")
 
@@ -196,7 +200,7 @@ def quantize_v(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, workspace, s
     _dense(V, torch.int8 if v_dtype == DT_I8 else torch.bfloat16, "V")
     _check(lib().qattn_quantize_v(_p(V), v_dtype, _p(v_chan_scale), ctypes.byref(shape), _p(v8t),
                                   ldv, _p(v_scales), _p(workspace),
-                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+                                  _nbytes(workspace), _stream(stream)),
            "qattn_quantize_v")
 
 
@@ -213,7 +217,7 @@ def fwd(q_codes, q_scales, k_codes, k_scales, v8t, ldv, v_scales, bias, shape, p
         workspace, stream=None, k_carrier=None):
     if k_carrier is not None:
         _dense(k_carrier, torch.float16, "k_carrier")
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ws_bytes = _nbytes(workspace)
     _check(lib().qattn_fwd(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_carrier), _p(k_scales),
                            _p(v8t), ldv, _p(v_scales), _p(bias), ctypes.byref(shape),
                            ctypes.byref(params), _p(O), _p(lse), _p(workspace), ws_bytes,
@@ -229,7 +233,7 @@ def decode(q_codes, q_scales, k_codes, k_scales, v_codes, v_chan_scale, v_code_a
     _check(lib().qattn_decode(_p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales), _p(v_codes),
                               _p(v_chan_scale), _p(v_code_amax), ctypes.byref(shape),
                               ctypes.byref(params), _p(O), _p(lse), _p(workspace),
-                              workspace.numel() * workspace.element_size(), _stream(stream)),
+                              _nbytes(workspace), _stream(stream)),
            "qattn_decode")
 
 
@@ -242,7 +246,7 @@ def fwd_exact24(Q, k_codes, k_chan_scale, v_codes, v_chan_scale, shape, params, 
     _check(lib().qattn_fwd_exact24(_p(Q), _p(k_codes), _p(k_chan_scale), _p(v_codes),
                                    _p(v_chan_scale), ctypes.byref(shape), ctypes.byref(params),
                                    _p(O), _p(lse), _p(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+                                   _nbytes(workspace), _stream(stream)),
            "qattn_fwd_exact24")
 
 
@@ -283,7 +287,7 @@ def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):
     _dense(k_codes, torch.int8, "k_codes")
     _dense(S, torch.int32, "S")
     _check(lib().qattn_debug_qk_scores(_p(q_codes), _p(k_codes), ctypes.byref(shape), _p(S),
-                                       _p(workspace), workspace.numel() * workspace.element_size(),
+                                       _p(workspace), _nbytes(workspace),
                                        _stream(stream)),
            "qattn_debug_qk_scores")
 
