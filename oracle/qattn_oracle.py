@@ -28,7 +28,7 @@ Readings where the pages are silent (each one is listed in the design notes):
 
 * The channel mean is taken per (batch, KV head) over all Nk keys, as an
   int64 fixed-point sum of round(K * 2^24), so that any summation order gives
-  the same bits.
+  the same bits; with no keys it is 0 (every row is then fully masked).
 * The int8 quantizer multiplies by the fp32 reciprocal 127/amax instead of
   dividing by amax/127; ties round to even; codes lie in [-127, 127].
 * Q/K scale granules: one per tensor, per (batch, head), or per (batch, head,
