@@ -405,6 +405,18 @@ int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params)
  * domain). */
 qattn_status qattn_get_error(qattn_stream_t stream);
 
+/* Failure-path check (debug; no counterpart on the pages): one thread runs
+ * the kernels' bounded pipeline wait on an mbarrier that nothing arrives at,
+ * so the wait runs out after its time limit (about 2 s at the boost clock)
+ * and takes the same exit as in the attention kernels: the abort flag is
+ * raised, the timeout bit is set in the device error word, the kernel
+ * returns.  The next qattn_get_error() then returns QATTN_ERR_TIMEOUT and
+ * clears the word; the context stays usable.
+ *   result  (out) device int32[2], 8-byte aligned: {1 if the wait reported
+ *           success else 0, the abort flag} -- {0, 1} after a timeout.
+ * QATTN_ERR_INVALID_ARG (nothing launched) for a NULL or misaligned result. */
+qattn_status qattn_debug_wait_timeout(int32_t* result, qattn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

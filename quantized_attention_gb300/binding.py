@@ -28,7 +28,7 @@ EXPORTED = (
     "qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
     "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
-    "qattn_fwd_kernel_choice", "qattn_prepare_launches",
+    "qattn_fwd_kernel_choice", "qattn_prepare_launches", "qattn_debug_wait_timeout",
 )
 
 
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
     L.qattn_fwd_exact24.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_fwd_intsoftmax.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp]
     L.qattn_get_error.argtypes = [vp]
+    L.qattn_debug_wait_timeout.argtypes = [vp, vp]
     L.qattn_fwd_kernel_choice.argtypes = [PS, PP]
     L.qattn_fwd_kernel_choice.restype = ctypes.c_int
     L.qattn_prepare_launches.argtypes = [PS, PP]
@@ -92,7 +93,7 @@ def lib() -> ctypes.CDLL:
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
-                 "qattn_prepare"):
+                 "qattn_prepare", "qattn_debug_wait_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -300,6 +301,15 @@ def fwd_kernel_choice(shape: Shape, params: Params) -> int:
 def prepare_launches(shape: Shape, params: Params) -> int:
     """Kernels qattn_prepare launches (1 or 2), or -1 if it would reject the call."""
     return lib().qattn_prepare_launches(ctypes.byref(shape), ctypes.byref(params))
+
+
+def debug_wait_timeout(result, stream=None):
+    """Runs the kernels' bounded wait on a barrier nothing completes; result is
+    a device int32[2] that receives {wait succeeded, abort flag}."""
+    _dense(result, torch.int32, "result")
+    if result.numel() < 2:
+        raise ValueError("result: needs 2 int32 elements")
+    _check(lib().qattn_debug_wait_timeout(_p(result), _stream(stream)), "qattn_debug_wait_timeout")
 
 
 def get_error(stream=None) -> int:

@@ -13,6 +13,7 @@
 
 #include "qattn.h"
 #include "qattn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -182,6 +183,22 @@ bool encode_carrier(CUtensorMap* map, const void* ptr, int64_t planes, int64_t r
 bool decode_shape_ok(const qattn_shape* s) {
   return s->Hkv > 0 && s->Nq >= 1 && (s->Hq / s->Hkv) * s->Nq <= qattn::kMaxDecodeRows &&
          (s->d == 64 || s->d == 128);
+}
+
+// The pipeline kernels' bounded mbarrier wait, run on a barrier that nothing
+// arrives at: after its time limit it raises the abort flag, sets the timeout
+// bit of the error word and returns false.  One thread; writes {1 if the wait
+// reported success else 0, the abort flag} to result.
+__global__ void wait_timeout_kernel(unsigned int* err, int* result) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  abort_flag = 0;
+  const uint32_t b = qattn::smem_u32(&bar);
+  qattn::mbar_init(b, 1);
+  qattn::fence_mbar_init();
+  const bool ok = qattn::mbar_wait(b, 0, &abort_flag, err, qattn::kErrTimeout);
+  result[0] = ok ? 1 : 0;
+  result[1] = abort_flag;
 }
 
 }  // namespace
@@ -669,6 +686,14 @@ int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params)
   if (empty_problem(shape)) return 0;
   return qattn::prepare_launch_count(static_cast<int>(shape->d), static_cast<int>(shape->Nq),
                                      static_cast<int>(shape->Nk));
+}
+
+qattn_status qattn_debug_wait_timeout(int32_t* result, qattn_stream_t stream) {
+  if (!result || (reinterpret_cast<uintptr_t>(result) & 7u)) return QATTN_ERR_INVALID_ARG;
+  unsigned int* err = error_word();
+  if (!err) return QATTN_ERR_CUDA;
+  wait_timeout_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, result);
+  return from_cuda(cudaGetLastError());
 }
 
 qattn_status qattn_get_error(qattn_stream_t stream) {

@@ -51,6 +51,9 @@ def test_invalid_arguments_rejected_on_host(L):
     s = qb.make_shape(1, 4, 2, 256, 256, 64)
     p = qb.make_params()
     fake = vp(1 << 20)  # aligned, never dereferenced: validation fails first
+    # the failure-path check wants an 8-byte aligned result
+    assert L.qattn_debug_wait_timeout(None, None) == 1
+    assert L.qattn_debug_wait_timeout(vp((1 << 20) + 4), None) == 1
     # null outputs
     assert L.qattn_fwd(None, fake, fake, None, fake, fake, 256, fake, None, ctypes.byref(s),
                        ctypes.byref(p), fake, None, fake, 1 << 30, None) == 1
