@@ -90,16 +90,90 @@ def _attn_traffic(wl_name):
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------
 
+# Active clock-event reason bits of NVML (nvml.h), by the names nvidia-smi
+# prints for them.
+_NVML_REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+                 (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+
+class _NvmlClocks:
+    """Read-only NVML queries through ctypes (the library ships with the
+    driver): the SM clock, its maximum and the active clock-event reasons of
+    one device.  Raises OSError when NVML or the device is unavailable."""
+    SM = 1  # NVML_CLOCK_SM
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.L = L
+        self.h = ctypes.c_void_p()
+        if L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            L.nvmlShutdown()
+            raise OSError("no NVML device handle")
+        try:
+            self.reasons_fn = L.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = L.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        if L.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(self.SM), ctypes.byref(mx)) != 0:
+            L.nvmlShutdown()
+            raise OSError("no maximum SM clock")
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        """(SM MHz, reason bits), or None if a query failed."""
+        ct = self.ct
+        c, r = ct.c_uint(0), ct.c_ulonglong(0)
+        if self.L.nvmlDeviceGetClockInfo(self.h, ct.c_int(self.SM), ct.byref(c)) != 0:
+            return None
+        if self.reasons_fn(self.h, ct.byref(r)) != 0:
+            return None
+        return float(c.value), int(r.value)
+
+    def close(self):
+        self.L.nvmlShutdown()
+
+
 class ClockSampler:
+    """Samples the SM clock and the clock-event reasons while the timed steps
+    run: NVML polled every 2 ms from a thread (so even a timed region of a few
+    milliseconds is sampled), else nvidia-smi every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
         self.gpu = gpu_index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
+        self.samples = []
+        self.lines = []
+
+    def _poll(self):
+        while not self._stop.is_set():
+            v = self.nvml.sample()
+            if v is not None:
+                self.samples.append(v)
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
+        try:
+            self.nvml = _NvmlClocks(self.gpu)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self._stop = threading.Event()
+            v = self.nvml.sample()  # one sample as the region opens
+            if v is not None:
+                self.samples.append(v)
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -110,7 +184,14 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self.nvml is not None:
+            v = self.nvml.sample()  # one sample as the region closes
+            if v is not None:
+                self.samples.append(v)
+            self._stop.set()
+            self._thread.join(timeout=5)
+            self.nvml.close()
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -121,24 +202,39 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if self.samples:
+            return summarize_nvml_samples(self.samples, self.nvml.max_mhz if self.nvml else None)
+        return summarize_smi_lines(self.lines)
+
+
+def summarize_nvml_samples(samples, max_mhz):
+    """Median SM clock, maximum and the union of the active slowdown reasons
+    of (MHz, NVML reason bits) samples."""
+    reasons = sorted({name for _, bits in samples for bit, name in _NVML_REASONS if bits & bit})
+    return {"sm_mhz": statistics.median(m for m, _ in samples), "sm_max_mhz": max_mhz,
+            "reasons": reasons, "samples": len(samples), "source": "nvml, every 2 ms"}
+
+
+def summarize_smi_lines(lines):
+    """The same summary from nvidia-smi's CSV lines (FIELDS order)."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm), "source": "nvidia-smi, every 200 ms"}
 
 
 # ----------------------------------------------------------------------------

@@ -1,0 +1,64 @@
+"""The bench's clock record: NVML reason bits and nvidia-smi lines map to the
+same slowdown names, and the sampler polls a (fake) NVML device from a thread
+so that a timed region of a few milliseconds still gets samples."""
+import os
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_nvml_reason_bits():
+    s = bench.summarize_nvml_samples([(2070.0, 0x0), (2000.0, 0x4), (1980.0, 0x1)], 2070.0)
+    assert s["sm_mhz"] == 2000.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]  # 0x1 (idle) is not a slowdown
+    s = bench.summarize_nvml_samples([(1500.0, 0x8 | 0x40), (1400.0, 0x20 | 0x80)], 2070.0)
+    assert s["reasons"] == ["hw_power_brake_slowdown", "hw_slowdown", "hw_thermal_slowdown",
+                            "sw_thermal_slowdown"]
+
+
+def test_smi_lines():
+    lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "garbage"]
+    s = bench.summarize_smi_lines(lines)
+    assert s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 2
+    assert s["reasons"] == ["sw_power_cap"]
+    assert bench.summarize_smi_lines([])["reasons"] == ["unsampled"]
+
+
+class _FakeNvml:
+    max_mhz = 2070.0
+
+    def __init__(self, index):
+        self.n = 0
+        self.closed = False
+
+    def sample(self):
+        self.n += 1
+        return (2070.0 if self.n % 2 else 2055.0), 0x0
+
+    def close(self):
+        self.closed = True
+
+
+def test_sampler_polls_during_a_short_region(monkeypatch):
+    monkeypatch.setattr(bench, "_NvmlClocks", _FakeNvml)
+    with bench.ClockSampler(0) as clk:
+        time.sleep(0.02)
+    s = clk.summary()
+    assert s["samples"] >= 3 and s["reasons"] == [] and s["sm_max_mhz"] == 2070.0
+    assert clk.nvml.closed
+
+
+def test_sampler_falls_back_without_nvml(monkeypatch):
+    def _fail(index):
+        raise OSError("no NVML here")
+    monkeypatch.setattr(bench, "_NvmlClocks", _fail)
+    monkeypatch.setattr(bench.subprocess, "Popen", _fail)
+    with bench.ClockSampler(0) as clk:
+        pass
+    assert clk.summary()["reasons"] == ["unsampled"]
