@@ -38,6 +38,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention effective TOPS and % of measured GB300 dense int8/fp8 tensor peak"
 UNIT = "TOPS"
+# Seconds of oracle work the reference arm spends on its warm-up and timed
+# steps together, whatever --steps and --warmup are.
+REF_BUDGET_S = 120.0
+# Seconds of oracle work (one warm-up and one timed step) behind the GPU
+# line's cpu_baseline.
+CPU_BASELINE_S = 16.0
 
 
 def _peaks():
@@ -278,45 +284,91 @@ def sample_problem(wl_name):
     return sub, inp, O.prepare(inp)
 
 
-def run_oracle_sample(sample, pool, n_tiles):
-    """Times the oracle on n_tiles (query head, 128-row tile) items of the
-    sample, heaviest causal tiles first; returns (ops, seconds)."""
-    wl = sample[0]
-    nqt = (wl.Nq + 127) // 128
-    items = []
-    for t in range(n_tiles):
-        h = t % wl.Hq
-        qt = nqt - 1 - (t // wl.Hq) % nqt
-        items.append((h, qt * 128, min(wl.Nq, qt * 128 + 128)))
+def oracle_items(wl, rows, n_items):
+    """Up to n_items (query head, row_lo, row_hi) spans covering `rows` query
+    rows of the sample, heaviest first: under a causal mask the last rows of
+    each query head see the most keys.  Spans never repeat a row."""
+    rows = max(1, min(rows, wl.Hq * wl.Nq))
+    n_items = max(1, min(n_items, rows))
+    per = -(-rows // n_items)
+    items, left = [], rows
+    for t in range(n_items):
+        h, k = t % wl.Hq, t // wl.Hq
+        hi = wl.Nq - k * per
+        lo = max(0, hi - min(per, left))
+        if hi <= 0 or lo >= hi:
+            break
+        items.append((h, lo, hi))
+        left -= hi - lo
+        if left <= 0:
+            break
+    return items
+
+
+def run_oracle_items(pool, items):
+    """Times the oracle on the items in the pool; returns (ops, seconds)."""
     t0 = time.perf_counter()
     ops = sum(pool.map(_oracle_sample_worker, items))
     return ops, time.perf_counter() - t0
 
 
-def make_pool(sample):
-    """A spawn-started pool over every host core, each worker holding the sample."""
-    import multiprocessing as mp
-    cores = len(os.sched_getaffinity(0))
-    return mp.get_context("spawn").Pool(cores, initializer=_init_worker, initargs=(sample,)), cores
-
-
-def time_cpu_baseline(wl_name, warmup=1, steps=1):
+def time_cpu_budgeted(wl_name, warmup, steps, budget_s):
+    """The reference arm: warmup + steps oracle steps in about budget_s
+    seconds whatever their number.  Two calibration passes (the heaviest 1 and
+    8 rows on each core) give the per-call cost and the per-row cost; every
+    step then runs the same sample of heaviest rows, sized so that all steps
+    fit the budget (at least one row per core), at most every row of the
+    sample."""
     sample = sample_problem(wl_name)
+    wl = sample[0]
     pool, cores = make_pool(sample)
     try:
-        n_tiles = 2 * cores
+        run_oracle_items(pool, oracle_items(wl, cores, cores))  # workers' first call
+        # time per pass with r rows per core: a + b r (a: per-call cost)
+        _, t1 = run_oracle_items(pool, oracle_items(wl, cores, cores))
+        _, t8 = run_oracle_items(pool, oracle_items(wl, 8 * cores, cores))
+        b = max((t8 - t1) / 7.0, 1e-6)
+        a = max(t1 - b, 0.0)
+        n = max(1, warmup + steps)
+        r = int((budget_s / n - a) / b)
+        rows = max(1, min(r * cores, wl.Hq * wl.Nq))
+        # one span per core while spans are short; more, dealt out dynamically,
+        # once long spans would differ in weight under a causal mask
+        items = oracle_items(wl, rows, cores if r < 64 else 4 * cores)
         for _ in range(warmup):
-            run_oracle_sample(sample, pool, cores)
+            run_oracle_items(pool, items)
         ops, secs = 0, 0.0
         for _ in range(steps):
-            o, s = run_oracle_sample(sample, pool, n_tiles)
+            o, s = run_oracle_items(pool, items)
             ops += o
             secs += s
     finally:
         pool.close()
-    desc = (f"{n_tiles} (query head, 128-row tile) items per step of {wl_name} "
-            f"(batch 0, KV head 0), heaviest tiles first")
+    n_rows = sum(hi - lo for _, lo, hi in items)
+    desc = (f"{n_rows} query rows per step of {wl_name} (batch 0, KV head 0: "
+            f"{len(items)} spans, heaviest rows first), sized so {warmup}+{steps} steps "
+            f"fit about {budget_s:.0f} s")
     return ops, secs, cores, desc
+
+
+def make_pool(sample):
+    """A spawn-started pool over every host core, each worker holding the
+    sample and running its NumPy/BLAS on one thread (so `cores` is the number
+    of threads in use, with no oversubscription)."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    os.environ.update({k: "1" for k in keys})
+    try:
+        pool = mp.get_context("spawn").Pool(cores, initializer=_init_worker, initargs=(sample,))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return pool, cores
 
 
 def time_cpu_mode_baseline(mode, wl_name, budget_s=10.0):
@@ -361,7 +413,8 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    ops, secs, cores, desc = time_cpu_baseline(args.workload, args.warmup, args.steps)
+    ops, secs, cores, desc = time_cpu_budgeted(args.workload, args.warmup, args.steps,
+                                               REF_BUDGET_S)
     value = ops / secs / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
@@ -693,7 +746,7 @@ def gpu_arm(args):
             c_ops, c_s, cores, desc = time_cpu_mode_baseline(
                 "intsoftmax" if args.intsoftmax else "exact24", args.workload)
         else:
-            c_ops, c_s, cores, desc = time_cpu_baseline(args.workload)
+            c_ops, c_s, cores, desc = time_cpu_budgeted(args.workload, 1, 1, CPU_BASELINE_S)
         cpu = {"value": c_ops / c_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}; {c_s:.1f} s"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -1,6 +1,8 @@
-"""The bench's clock record: NVML reason bits and nvidia-smi lines map to the
-same slowdown names, and the sampler polls a (fake) NVML device from a thread
-so that a timed region of a few milliseconds still gets samples."""
+"""Host logic of the bench.  The clock record: NVML reason bits and nvidia-smi
+lines map to the same slowdown names, and the sampler polls a (fake) NVML
+device from a thread so that a timed region of a few milliseconds still gets
+samples.  The oracle's timed sample: disjoint row spans, and a run of many
+steps that stays within its time budget."""
 import os
 import sys
 import time
@@ -62,3 +64,25 @@ def test_sampler_falls_back_without_nvml(monkeypatch):
     with bench.ClockSampler(0) as clk:
         pass
     assert clk.summary()["reasons"] == ["unsampled"]
+
+
+def test_reference_sample_spans_are_disjoint_rows():
+    from quantized_attention_gb300 import inputs as I
+    for name in ("llm8k", "chunk32k", "vit", "swin", "tiny"):
+        wl = I.WORKLOADS[name]
+        sub = wl.replace(B=1, Hq=wl.Hq // wl.Hkv, Hkv=1)
+        for rows, n in ((4096, 32), (64, 16), (20, 16), (1, 8), (10 ** 6, 64)):
+            items = bench.oracle_items(sub, rows, n)
+            seen = set()
+            for h, lo, hi in items:
+                assert 0 <= h < sub.Hq and 0 <= lo < hi <= sub.Nq
+                span = {(h, r) for r in range(lo, hi)}
+                assert not (span & seen)
+                seen |= span
+            assert len(seen) == min(rows, sub.Hq * sub.Nq) and len(items) <= n
+
+
+def test_reference_arm_stays_within_its_budget():
+    ops, secs, cores, desc = bench.time_cpu_budgeted("tiny", 2, 40, 4.0)
+    assert ops > 0 and cores >= 1
+    assert secs < 12.0, (secs, desc)  # timed steps within a few times the budget
