@@ -40,7 +40,7 @@ METRIC = "attention effective TOPS and % of measured GB300 dense int8/fp8 tensor
 UNIT = "TOPS"
 # Seconds of oracle work the reference arm spends on its warm-up and timed
 # steps together, whatever --steps and --warmup are.
-REF_BUDGET_S = 120.0
+REF_BUDGET_S = 100.0
 # Seconds of oracle work (one warm-up and one timed step) behind the GPU
 # line's cpu_baseline.
 CPU_BASELINE_S = 16.0
