@@ -29,6 +29,19 @@ MUTATIONS = [
     ("t = (t + bias2[:, k0:k1]", "t = (t - bias2[:, k0:k1]", "test_blockwise_loop_equals_dense_softmax"),
     ("(Kx - np.asarray(k_mean, dtype=F32)", "(Kx + np.asarray(k_mean, dtype=F32)", "test_smoothing_shrinks_outlier_channels_via_prepare"),
     ("F32(P_SCALE) / amax, F32(0)).astype(F32)\n    s_v", "F32(240) / amax, F32(0)).astype(F32)\n    s_v", "test_v_bf16_path"),
+    # the static P scale: 240, or 127 with e4m3 rounding, instead of 448
+    ("P448 = (P * ftype(P_SCALE)).astype(ftype)\n            Pq = e4m3_round(P448) / P_SCALE",
+     "P448 = (P * ftype(240.0)).astype(ftype)\n            Pq = e4m3_round(P448) / 240.0",
+     "test_static_p_scale_worked_cases"),
+    ("P448 = (P * ftype(P_SCALE)).astype(ftype)\n            Pq = e4m3_round(P448) / P_SCALE",
+     "P448 = (P * ftype(127.0)).astype(ftype)\n            Pq = e4m3_round(P448) / 127.0",
+     "test_static_p_scale_worked_cases"),
+    # flip allowance: a window too narrow to see the midpoints, half a step
+    # per flip instead of a whole one, no rescale of the allowance by alpha
+    ("window = 2.0 ** -20 * (4.0 + span) * Ps", "window = 2.0 ** -40 * (4.0 + span) * Ps",
+     "test_flip_bound_covers_every_flip"),
+    ("(amb * step / scale) @ absV", "(amb * step / scale / 2) @ absV", "test_flip_bound_covers_every_flip"),
+    ("Bacc = alpha.astype(F64)[:, None] * Bacc +", "Bacc = Bacc +", "test_flip_bound_covers_every_flip"),
 ]
 
 
@@ -58,7 +71,7 @@ def test_smoothing_shrinks_outlier_channels_via_prepare(O=None):
     assert amax.max() / np.median(amax) <= 4.1
 
 
-@pytest.mark.parametrize("old,new,pin", MUTATIONS, ids=[m[2] + ":" + m[0][:24] for m in MUTATIONS])
+@pytest.mark.parametrize("old,new,pin", MUTATIONS, ids=[f"{i}-{m[2]}" for i, m in enumerate(MUTATIONS)])
 def test_planted_mistake_is_caught(old, new, pin):
     mutant = _load_mutant(old, new)
     if pin == "test_smoothing_shrinks_outlier_channels_via_prepare":
@@ -73,6 +86,12 @@ def test_planted_mistake_is_caught(old, new, pin):
             if pin == "test_blockwise_loop_equals_dense_softmax":
                 for case in P.test_blockwise_loop_equals_dense_softmax.pytestmark[0].args[1]:
                     fn(case)
+            elif pin == "test_flip_bound_covers_every_flip":
+                mp = pytest.MonkeyPatch()
+                try:
+                    fn(mp)
+                finally:
+                    mp.undo()
             else:
                 fn()
     finally:

@@ -350,6 +350,129 @@ def test_flip_bound_is_small_and_nonnegative():
     assert r["bound"].max() < 1e-2 * np.abs(r["O"]).max()
 
 
+def _golden_p_scale():
+    rows = []
+    with open(os.path.join(GOLDEN, "p_scale_cases.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                x, _, want = line.split()[:3]
+                rows.append((float(x), float(want)))
+    return rows
+
+
+def test_static_p_scale_worked_cases():
+    """ZINC-ATTN "fp8 is not faster": P = exp2(t - m) <= 1 is scaled by the
+    static 448 before the e4m3 rounding.  One row sees two keys, t = 0 (P = 1)
+    and t = x (P = 2^x), and V is one-hot per key, so the output channels are
+    e4m3(448) / 448 / l and e4m3(448 P) / 448 / l with l = 1 + P: the hand
+    worked codes of tests/golden/p_scale_cases.txt fix the static scale (a
+    scale of 240, or 127 with e4m3 rounding, gives other codes)."""
+    V8 = np.eye(2)
+    s_v = np.ones(2)
+    for x, want in _golden_p_scale():
+        S = np.array([[0.0, x]])
+        r = O.online_softmax_pv(S, np.ones((1, 1), np.float32), V8, s_v,
+                                visible=np.ones((1, 2), bool))
+        l = 1.0 + 2.0 ** x
+        assert abs(r["O"][0, 0] * l - 1.0) <= 1e-6, (x, r["O"][0])
+        assert abs(r["O"][0, 1] * l - want / 448.0) <= 1e-6 * want / 448.0, (x, r["O"][0, 1] * l * 448)
+
+
+# --------------------------------------------------------------------------
+# flip allowance: the output change when a P code near an e4m3 rounding
+# midpoint is rounded the other way
+# --------------------------------------------------------------------------
+
+#: e4m3 rounding midpoints (halfway between neighbouring grid values) in four
+#: binades and in the subnormal range, and exact grid values
+_MIDPOINTS = (272.0, 304.0, 336.0, 400.0, 432.0, 136.0, 200.0, 248.0, 4.25, 4.75, 0.0029296875)
+_GRID = (320.0, 128.0, 4.5, 22.0, 448.0)
+
+
+def _flip_row(planted=True):
+    """One query row over two key blocks.  Block 0: key 0 at t = 0 (P = 1),
+    then keys whose 448 P sits on an e4m3 midpoint (if planted) and keys on
+    exact grid values.  Block 1: the row max grows to t = 1 (block 0 is
+    rescaled by 1/2), and the same pattern relative to the new max.  V holds
+    random e4m3 grid values, four channels with their own scales."""
+    Nk = 256
+    t = np.full(Nk, -30.0)
+    vis = np.zeros(Nk, bool)
+    planted_keys = []
+    for base, m in ((0, 0.0), (128, 1.0)):
+        t[base], vis[base] = m, True
+        vals = (_MIDPOINTS if planted else ()) + _GRID[:-1]
+        for i, v in enumerate(vals):
+            k = base + 1 + i
+            t[k], vis[k] = m + math.log2(v / 448.0), True
+            if planted and i < len(_MIDPOINTS):
+                planted_keys.append(k)
+    rng = np.random.default_rng(21)
+    grid = np.array(sorted({float(O.e4m3_round(g)) for g in np.linspace(-448, 448, 4001)}))
+    V8 = rng.choice(grid, size=(Nk, 4))
+    s_v = np.array([0.5, 1.0, 2.0, 0.25])
+    return t[None, :], vis[None, :], V8, s_v, planted_keys
+
+
+def _run_flipped(S, vis, V8, s_v, flips, monkeypatch):
+    """The oracle's output with the P codes of the given keys rounded to the
+    other neighbour of their midpoint (the grid value on the far side)."""
+    orig = O.e4m3_round
+    calls = {"j": 0}
+
+    def flipped(x):
+        y = np.array(orig(x), dtype=np.float64)
+        j = calls["j"]
+        calls["j"] += 1
+        for k in flips:
+            if k // O.BLOCK == j:
+                kk = k % O.BLOCK
+                y[0, kk] = orig(2.0 * float(np.asarray(x, np.float64)[0, kk]) - y[0, kk])
+        return y
+
+    monkeypatch.setattr(O, "e4m3_round", flipped)
+    try:
+        return O.online_softmax_pv(S, np.ones((1, 2), np.float32), V8, s_v, visible=vis)["O"]
+    finally:
+        monkeypatch.setattr(O, "e4m3_round", orig)
+
+
+def test_flip_bound_covers_every_flip(monkeypatch):
+    """The allowance is the largest output change that rounding ambiguous P
+    codes the other way can cause: it must find exactly the planted midpoint
+    codes, equal the sum of the single flips' changes (a flip moves one code
+    by one grid step), and bound every combination of flips."""
+    S, vis, V8, s_v, planted = _flip_row()
+    base = O.online_softmax_pv(S, np.ones((1, 2), np.float32), V8, s_v, visible=vis,
+                               want_bound=True)
+    assert base["n_ambiguous"] == len(planted)
+    bound = base["bound"][0]
+    total = np.zeros_like(bound)
+    for k in planted:
+        d = np.abs(_run_flipped(S, vis, V8, s_v, [k], monkeypatch)[0] - base["O"][0])
+        assert (d > 0).any(), k  # the flip changes the output
+        assert np.all(d <= bound * (1 + 1e-9)), (k, d, bound)
+        total += d
+    np.testing.assert_allclose(total, bound, rtol=1e-9)
+    rng = np.random.default_rng(5)
+    subsets = [planted] + [list(rng.choice(planted, size=int(rng.integers(2, len(planted))),
+                                           replace=False)) for _ in range(24)]
+    for sub in subsets:
+        d = np.abs(_run_flipped(S, vis, V8, s_v, sub, monkeypatch)[0] - base["O"][0])
+        assert np.all(d <= bound * (1 + 1e-9)), (sub, d, bound)
+
+
+def test_flip_bound_zero_without_ambiguous_codes():
+    """P codes far from every midpoint (exact grid values) leave no allowance."""
+    S, vis, V8, s_v, planted = _flip_row(planted=False)
+    assert planted == []
+    r = O.online_softmax_pv(S, np.ones((1, 2), np.float32), V8, s_v, visible=vis,
+                            want_bound=True)
+    assert r["n_ambiguous"] == 0
+    assert np.array_equal(r["bound"], np.zeros_like(r["bound"]))
+
+
 def test_cache_inputs_fold_channel_scale_into_q():
     """int8 K codes with per-channel scales: S * sq equals Q . K_real up to the
     Q quantization error, i.e. the fold puts the K scale on the Q side."""
