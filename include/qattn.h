@@ -224,8 +224,10 @@ qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t*
  *            held by every GPU that loads the library until the process exits.
  *   Limit:   B * Hkv * d <= 524288, else QATTN_ERR_UNSUPPORTED.
  *   Set-up:  the first call on a device looks up that array's device address
- *            (cudaGetSymbolAddress) with the device current; make that first
- *            call before any stream capture.
+ *            (cudaGetSymbolAddress) with the device current, and again the
+ *            first call in a new CUDA context of that device (after
+ *            cudaDeviceReset); make such a first call before any stream
+ *            capture.
  *   Sharing: every call uses the same array, which keeps the last call's
  *            contents; each call zeroes the slots it uses first.  Calls that
  *            overlap on the GPU (e.g. on two streams at once) race on the

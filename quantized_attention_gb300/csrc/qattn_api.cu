@@ -15,6 +15,36 @@
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
+namespace qattn {
+
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return false;
+  return get_id(c, id) == CUDA_SUCCESS;
+}
+
+}  // namespace qattn
+
 namespace {
 
 using qattn::AttnArgs;
@@ -24,7 +54,10 @@ __device__ unsigned int g_qattn_error_word;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// The error word's device address per device, and the context it belongs to
+// (0: unknown, resolved again on every call).
 unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_err_ctx[kMaxDevices] = {0};
 
 // Tags of qattn_decode calls: a per-call count XOR a random per-process salt
 // marks the chunk records and the unit counter a call writes in its workspace,
@@ -40,15 +73,22 @@ uint32_t next_decode_tag() {
   }
 }
 
+// Device address of the error word in the current device's current context:
+// cached per device and context (a new context after cudaDeviceReset resolves
+// it again); nullptr on failure.
 unsigned int* error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = 0;
+  const bool known = qattn::current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_qattn_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<unsigned int*>(p);
-  }
+  if (known && g_err_ptr[dev] && g_err_ctx[dev] == ctx) return g_err_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_qattn_error_word) != cudaSuccess || p == nullptr) return nullptr;
+  // the symbol lookup makes the device's primary context current if none was
+  const bool now_known = known || qattn::current_context_id(&ctx);
+  g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  g_err_ctx[dev] = now_known ? ctx : 0;
   return g_err_ptr[dev];
 }
 

@@ -35,6 +35,13 @@ inline int num_sms() {
   return n;
 }
 
+// Unique id (cuCtxGetId) of the CUDA context current on the calling thread;
+// false when no context is current or the driver cannot say.  The library
+// caches device addresses of its own __device__ symbols per device and per
+// context, so that a context destroyed by cudaDeviceReset (and replaced by a
+// new one) never leaves a stale address behind.
+bool current_context_id(unsigned long long* id);
+
 // Bits of the device error word.
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrDomain = 2u;  // device-held scales outside a kernel's domain

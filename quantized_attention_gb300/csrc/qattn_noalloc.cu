@@ -22,24 +22,30 @@ constexpr long long kNoAllocMaxChannels = 1ll << 19;
 
 // One 32-bit amax slot per (batch, KV head, channel).  In host code this
 // name is only a stand-in: its device address comes from
-// cudaGetSymbolAddress, once per device.
+// cudaGetSymbolAddress, once per device and CUDA context.
 static __device__ __align__(256) unsigned int g_v_amax_scratch[kNoAllocMaxChannels];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // 0: unknown, resolve every call
 
-// Device address of the scratch array on the current device, resolved on the
-// first call per device; nullptr on failure.
+// Device address of the scratch array on the current device, resolved with
+// that device current on the first call in each context (so after a
+// cudaDeviceReset the new context gets its own address); nullptr on failure.
 unsigned int* scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = 0;
+  const bool known = qattn::current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_v_amax_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_ptr[dev] = static_cast<unsigned int*>(p);
-  }
+  if (known && g_scratch_ptr[dev] && g_scratch_ctx[dev] == ctx) return g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_v_amax_scratch) != cudaSuccess || p == nullptr) return nullptr;
+  // the symbol lookup makes the device's primary context current if none was
+  const bool now_known = known || qattn::current_context_id(&ctx);
+  g_scratch_ptr[dev] = static_cast<unsigned int*>(p);
+  g_scratch_ctx[dev] = now_known ? ctx : 0;
   return g_scratch_ptr[dev];
 }
 
