@@ -60,12 +60,42 @@ def _peaks():
 
 
 def mixed_peak(peaks, sustained=True):
-    """Peak of the attention contraction: half the algorithmic ops (QK^T) run
-    at the fp16 rate (= the measured bf16 rate), half (PV) at the e4m3 rate
-    (= the fp16 rate times the nominal 4.5/2.25 ratio); harmonic combination."""
+    """Peak of the attention contraction from the cuBLAS bf16 figure: half the
+    algorithmic ops (QK^T) run at the fp16 rate (= the measured bf16 rate),
+    half (PV) at the e4m3 rate (= the fp16 rate times the nominal 4.5/2.25
+    ratio); harmonic combination."""
     p16 = peaks["bf16_sustained"] if sustained else peaks["bf16"]
     p8 = 2.0 * p16
     return 1.0 / (0.5 / p16 + 0.5 / p8)
+
+
+def tensor_roofline(achieved, peaks, unit_peaks):
+    """The attention kernel's tensor roofline against the stricter of two
+    measured peaks: the tcgen05 kind::f16 and kind::f8f6f4 loops run in this
+    process on this GPU (quantized_attention_gb300.peaks), and the cuBLAS
+    bf16 burst figure with the nominal e4m3/f16 ratio.  Both are reported."""
+    cub_burst = mixed_peak(peaks, sustained=False)
+    cub_sus = mixed_peak(peaks, sustained=True)
+    r = {"bound": "tensor", "achieved": achieved, "unit": "TFLOP/s",
+         "peak_cublas_burst": cub_burst, "frac_cublas_burst": achieved / cub_burst,
+         "peak_cublas_sustained": cub_sus, "frac_cublas_sustained": achieved / cub_sus}
+    if unit_peaks is not None:
+        m = unit_peaks["mixed"]
+        r.update({"peak_tcgen05_loops": m, "frac_tcgen05_loops": achieved / m,
+                  "tcgen05_f16": unit_peaks["f16"], "tcgen05_f8": unit_peaks["f8"]})
+    if unit_peaks is not None and unit_peaks["mixed"] >= cub_burst:
+        r["peak"] = unit_peaks["mixed"]
+        r["peak_basis"] = (f"measured in this run: tcgen05 kind::f16 {unit_peaks['f16']:.1f} and "
+                           f"kind::f8f6f4 {unit_peaks['f8']:.1f} TFLOP/s loops (QK^T half, PV half, "
+                           f"harmonic), the stricter of it and the cuBLAS bf16 burst figure "
+                           f"({peaks['source']}) with the nominal e4m3/f16 ratio")
+    else:
+        r["peak"] = cub_burst
+        r["peak_basis"] = (f"{peaks['source']} cuBLAS bf16 burst {peaks['bf16']:.1f} for QK^T, "
+                           f"2x that (nominal e4m3/f16 ratio) for PV, harmonic; the stricter of "
+                           f"it and the tcgen05 loops measured in this run")
+    r["frac"] = achieved / r["peak"]
+    return r
 
 
 def _attn_traffic(wl_name):
@@ -444,6 +474,80 @@ def _config(wl_name):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def prefill_roofline(wl, attn_ms, ops, has_bias, peaks, unit_peaks, v_ld):
+    """Roofline of qattn_fwd's kernel on a prefill workload: tensor-bound for
+    long rows; for ViT / Swin (197 / 49 keys) the operands' bytes bound it
+    (HBM), with the tensor fraction beside."""
+    achieved = ops / (attn_ms * 1e-3) / 1e12
+    tr = tensor_roofline(achieved, peaks, unit_peaks)
+    tr["kernel"] = "attn_fwd_kernel (the one launch of qattn_fwd)"
+    if wl.name.split("@")[0] not in ("vit", "swin"):
+        return tr
+    alg_bytes = (wl.B * wl.Hq * wl.Nq * wl.d + wl.B * wl.Hkv * wl.Nk * wl.d  # Q, K codes
+                 + wl.B * wl.Hkv * wl.d * v_ld                              # V8^T
+                 + wl.B * wl.Hq * wl.Nq * wl.d * 2                          # bf16 O
+                 + (wl.Nq * wl.Nk * 4 if has_bias else 0))                 # fp32 bias
+    gbs = alg_bytes / (attn_ms * 1e-3) / 1e9
+    return {"bound": "hbm",
+            "kernel": ("attn_window_kernel (qattn_fwd's warp-level kernel for short windows)"
+                       if wl.name.startswith("swin") else tr["kernel"]),
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"],
+            "peak_basis": f"{peaks['source']} HBM copy rate",
+            "algorithmic_bytes": alg_bytes,
+            "tensor_frac": tr["frac"], "traffic": None}
+
+
+def measure_unit_peaks():
+    """tcgen05 / mma.sync / MUFU loop rates on this GPU, or (error, None)."""
+    try:
+        from quantized_attention_gb300 import peaks as PK
+        rates = PK.measure()
+        return rates, PK.attention_peak(rates)
+    except Exception as e:  # reported in the line; the cuBLAS figure then stands alone
+        return {"error": f"{type(e).__name__}: {e}"}, None
+
+
+def time_prefill_workload(name, steps, warmup, flush, stream, local, peaks, unit_peaks):
+    """Device time of the prefill step (pre-pass + qattn_fwd) on one more
+    workload, with the same L2 flush and clock sampling as the main line."""
+    import torch
+    from quantized_attention_gb300 import binding as qb
+    from quantized_attention_gb300 import inputs as I
+    from quantized_attention_gb300.pipeline import device_inputs, problem_for
+
+    wl = I.WORKLOADS[name]
+    inp = I.make_inputs(wl)
+    dev = device_inputs(inp)
+    bias = dev.pop("bias", None)
+    P = problem_for(wl, out_dtype=qb.DT_BF16, k_carrier=True)
+    for _ in range(warmup):
+        P.quantize(**dev, stream=stream)
+        P.attend(bias, stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            P.quantize(**dev, stream=stream)
+            ev[i][1].record(stream)
+            P.attend(bias, stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if qb.get_error() != 0:
+        raise RuntimeError(f"device error word set during the {name} steps")
+    step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / steps
+    attn_ms = sum(b.elapsed_time(c) for _, b, c in ev) / steps
+    ops = 4 * wl.d * wl.unmasked_pairs()
+    return {"config": _config(name)["workload"], "steps": steps, "warmup": warmup,
+            "ms_per_step": step_ms, "value": ops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+            "attn_kernel_ms": attn_ms,
+            "roofline": prefill_roofline(wl, attn_ms, ops, bias is not None, peaks, unit_peaks,
+                                         qb.v_ld(wl.Nk)),
+            "gpu_launches": P.kernel_launches() * steps, "clocks": clk.summary()}
+
+
 def max_over_ranks(ms: float, world: int) -> float:
     """The slowest rank's time (every rank gets it), then a barrier; the
     identity for one process."""
@@ -478,6 +582,7 @@ def gpu_arm(args):
     from quantized_attention_gb300 import inputs as I
     from quantized_attention_gb300.pipeline import device_inputs, problem_for
 
+    unit_rates, unit_peaks = measure_unit_peaks()
     wl = I.WORKLOADS[args.workload]
     inp = I.make_inputs(wl)
     dev = device_inputs(inp)
@@ -682,29 +787,12 @@ def gpu_arm(args):
     if rank != 0:
         return 0
     peaks = _peaks()
-    pmix = mixed_peak(peaks, sustained=True)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    achieved = ops / (attn_avg_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel (the one launch of qattn_fwd)",
-                "achieved": achieved, "peak": pmix, "unit": "TFLOP/s", "frac": achieved / pmix,
-                "peak_basis": (f"{peaks['source']}: QK^T at the sustained bf16 rate "
-                               f"{peaks['bf16_sustained']:.1f}, PV at 2x that (nominal e4m3/f16 ratio)"),
-                "traffic": _attn_traffic(args.workload),
-                "traffic_unit": "bytes per launch (ncu dram read + write)"}
-    if wl.name in ("vit", "swin") and not (args.intsoftmax or args.exact24):
-        # short rows (197 / 49 keys): the operands' bytes bound these shapes
-        v_ld = qb.v_ld(wl.Nk)
-        alg_bytes = (wl.B * wl.Hq * wl.Nq * wl.d + wl.B * wl.Hkv * wl.Nk * wl.d  # Q, K codes
-                     + wl.B * wl.Hkv * wl.d * v_ld                              # V8^T
-                     + wl.B * wl.Hq * wl.Nq * wl.d * 2                          # bf16 O
-                     + (wl.Nq * wl.Nk * 4 if bias is not None else 0))         # fp32 bias
-        gbs = alg_bytes / (attn_avg_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "attn_fwd_kernel (the one launch of qattn_fwd)",
-                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"],
-                    "peak_basis": f"{peaks['source']} HBM copy rate",
-                    "algorithmic_bytes": alg_bytes,
-                    "tensor_frac": achieved / pmix, "traffic": None}
+    roofline = prefill_roofline(wl, attn_avg_ms, ops, bias is not None, peaks, unit_peaks,
+                                qb.v_ld(wl.Nk))
+    if roofline["bound"] == "tensor":
+        roofline["traffic"] = _attn_traffic(args.workload)
+        roofline["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     if args.intsoftmax:  # the integer softmax dominates: an ALU roofline
         # algorithmic integer operations per score: S - m, ShiftExp2's five
         # (quotient, remainder, halving, + X0, shift), requantization's three
@@ -723,12 +811,18 @@ def gpu_arm(args):
                     "traffic": None}
     if args.exact24:  # three exact fp16 tensor-core products per attention product
         mma_tflops = 3 * ops / (attn_avg_ms * 1e-3) / 1e12
-        pb = peaks["bf16_sustained"]
+        pb = peaks["bf16"]
+        if unit_peaks is not None:
+            pb = max(pb, unit_peaks["f16"])
         roofline = {"bound": "tensor", "kernel": "exact24_attn_kernel + q_split_kernel (qattn_fwd_exact24)",
                     "achieved": mma_tflops, "peak": pb, "unit": "TFLOP/s", "frac": mma_tflops / pb,
-                    "peak_basis": f"{peaks['source']} sustained bf16 (fp16 MMA runs at the bf16 rate); "
-                                  "achieved counts the 3 fp16 products per attention product",
+                    "peak_basis": "the stricter of the cuBLAS bf16 burst figure and the tcgen05 "
+                                  "kind::f16 loop (fp16 MMA runs at the bf16 rate); achieved counts "
+                                  "the 3 fp16 products per attention product",
                     "traffic": None}
+        if "mma_sync_f16" in unit_rates:
+            roofline["mma_sync_f16_loop"] = unit_rates["mma_sync_f16"]["rate"]
+            roofline["frac_mma_sync_f16_loop"] = mma_tflops / unit_rates["mma_sync_f16"]["rate"]
     if decode and not args.exact24:  # memory-bound: the cache's bytes over the decode call's time
         gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
         ref_us = _stream_ref_us(dev["K_codes"], dev["V_codes"], flush, stream)
@@ -762,7 +856,6 @@ def gpu_arm(args):
                            "step": "attention on resident per-tensor int8 codes",
                            "granularity": "tensor", "kv_input": "int8 codes",
                            "output": "int8 codes"} if args.intsoftmax else {})},
-            "frac_of_mixed_peak": value / pmix,
             "attn_kernel_ms": attn_avg_ms,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -777,12 +870,27 @@ def gpu_arm(args):
             "gpu_launches": (1 if args.intsoftmax else 2 if args.exact24
                              else P.decode_launches(append=True) if decode
                              else P.kernel_launches()) * args.steps,
-            "clocks": clk.summary()}
+            "clocks": clk.summary(),
+            "unit_peaks": {k: ({"rate": v["rate"], "unit": v["unit"], "sm_mhz": v["sm_mhz"],
+                                "per_sm_per_clk": v["per_sm_per_clk"]} if isinstance(v, dict) else v)
+                           for k, v in unit_rates.items()}}
+    if not (args.exact24 or args.intsoftmax or decode or args.no_workloads):
+        # the other prefill workloads, device-timed with fewer steps each
+        subs = {}
+        for name in SUB_WORKLOADS:
+            if name == args.workload:
+                continue
+            subs[name] = time_prefill_workload(name, min(args.steps, 20), args.warmup, flush,
+                                               stream, local, peaks, unit_peaks)
+        line["workloads"] = subs
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
 
+
+# prefill workloads timed beside the main one (sub-records of the line)
+SUB_WORKLOADS = ("llm8k", "chunk32k", "vit", "swin", "tiny")
 
 # GB300 unit counts for the ALU roofline of the integer-only mode
 NUM_SMS = 152
@@ -819,6 +927,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llm8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other prefill workloads' sub-records")
     ap.add_argument("--intsoftmax", action="store_true",
                     help="time QFlash's integer-only attention (qattn_fwd_intsoftmax) on int8 codes")
     ap.add_argument("--exact24", action="store_true",

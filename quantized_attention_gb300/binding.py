@@ -29,6 +29,7 @@ EXPORTED = (
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
     "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
     "qattn_fwd_kernel_choice", "qattn_prepare_launches", "qattn_debug_wait_timeout",
+    "qattn_peak_loop",
 )
 
 
@@ -90,6 +91,9 @@ def lib() -> ctypes.CDLL:
     L.qattn_fwd_kernel_choice.restype = ctypes.c_int
     L.qattn_prepare_launches.argtypes = [PS, PP]
     L.qattn_prepare_launches.restype = ctypes.c_int
+    ci = ctypes.c_int
+    L.qattn_peak_loop.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp]
+    L.qattn_peak_loop.restype = ci
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libqattn.so")
-SOURCES = ["qattn_api.cu", "quant_kernels.cu", "attn_fwd.cu", "qattn_noalloc.cu", "decode.cu", "exact24.cu", "intsm.cu", "attn_short.cu"]
+SOURCES = ["qattn_api.cu", "quant_kernels.cu", "attn_fwd.cu", "qattn_noalloc.cu", "decode.cu", "exact24.cu",
+           "intsm.cu", "attn_short.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

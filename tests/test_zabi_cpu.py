@@ -19,9 +19,14 @@ def L():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "qattn.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(qattn_[a-z0-9_]+)\s*\(", src)))
+    """Every function declared by the headers under include/."""
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(qattn_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_every_declared_function_is_exported(L):
