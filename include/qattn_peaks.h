@@ -13,6 +13,10 @@
  *   QATTN_PEAK_MMA_F16   mma.sync m16n8k16 f16 -> f32
  *   QATTN_PEAK_MMA_E4M3  mma.sync m16n8k32 e4m3 -> f32
  *   QATTN_PEAK_EX2       ex2.approx.ftz.f32 on the MUFU unit (one per score)
+ *   QATTN_PEAK_TC_ATTN_MIX  the fused attention's MMA sequence per key block
+ *                        and query tile: 8 kind::f16 MMAs (N = 128, K = 16)
+ *                        into one accumulator, then 4 kind::f8f6f4 MMAs
+ *                        (N = 128, K = 32) into another
  * Operands are resident in shared memory (tcgen05: one CTA per SM, one
  * issuing thread, 4 MMAs per round over 128-byte K slices, 128B swizzle) or
  * in registers (mma.sync: 8 independent accumulator chains per warp; ex2: 8
@@ -31,7 +35,8 @@ enum {
   QATTN_PEAK_MMA_S8 = 2,
   QATTN_PEAK_MMA_F16 = 3,
   QATTN_PEAK_MMA_E4M3 = 4,
-  QATTN_PEAK_EX2 = 5
+  QATTN_PEAK_EX2 = 5,
+  QATTN_PEAK_TC_ATTN_MIX = 6
 };
 
 /* Error bit set in *err when a tcgen05 loop's completion wait ran out
@@ -41,11 +46,12 @@ enum {
 /* Launches one loop asynchronously on `stream` (a cudaStream_t):
  *   kind    one of the QATTN_PEAK_* values
  *   n       tcgen05 kinds: the MMA's N (64, 128 or 256); ignored otherwise
- *   iters   loop rounds per CTA (tcgen05: 4 MMAs; mma.sync: 8 per warp;
- *           ex2: 8 per thread)
+ *   iters   loop rounds per CTA (tcgen05: 4 MMAs; the attention mix: 8 + 4;
+ *           mma.sync: 8 per warp; ex2: 8 per thread)
  *   blocks  CTAs (tcgen05: one per SM, 128 threads; others: 256 threads)
- *   clocks  device buffer of 2 * blocks uint64: each CTA's SM clock at the
- *           start and at the end of its loop
+ *   clocks  device buffer of 4 * blocks uint64: per CTA the SM clock
+ *           (clock64) at the start and the end of its loop, then the global
+ *           timer (nanoseconds) at the same two points
  *   err     device uint32 error word (see kQattnPeakErrTimeout)
  *   sink    device uint32 the loops may increment (keeps them live)
  * Device buffers are owned by the caller; the operation count of a launch

@@ -235,16 +235,19 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
 //          (their bias is never read)
 //   brow   BIAS: the row's bias for this block
 //   c      the block's score scale (> 0 without BIAS, so -inf * c = -inf)
+//   smax   without BIAS and with no masked key: the largest score of the
+//          block (the TMEM read computed it); else NaN, and the maximum is
+//          taken here
 // Updates the running max m and sum l (l in units of 448 P), returns alpha
 // and the e4m3 codes of 448 P packed four per word (key 4q + e in byte e).
 // One body serves masked and unmasked blocks: a second, masked copy of this
 // fully unrolled code would double the loop's instruction footprint.
 template <bool BIAS, bool PQ>
 __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int nvis,
-                                              const float* brow, float& m, float& l,
+                                              const float* brow, float smax, float& m, float& l,
                                               uint32_t (&pw)[kBN / 4], uint32_t (&pw2)[kBN / 4]) {
-  float mx;
-  {
+  float mx = smax;
+  if (BIAS || smax != smax) {
     if (BIAS) {  // only visible keys' bias is read: the row may end inside the block
 #pragma unroll
       for (int k = 0; k < kBN; ++k) {
@@ -572,9 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint32_t s[kBN];
+        float pmax[kBN / 32];  // the largest score of each 32-key group
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q)
-          tmem_ld32(tS + lane_base + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[q * 32]));
+          tmem_ld32_max(tS + lane_base + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[q * 32]),
+                        pmax[q]);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten by the next QK
@@ -595,7 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t pw[kBN / 4], pw2[kBN / 4];
         const float* bk = BIAS ? brow + kbase : nullptr;
-        const float alpha = softmax_step<BIAS, PQ>(s, c, nvis, bk, m, l, pw, pw2);
+        // the TMEM read's maxima serve unmasked blocks; masked keys are -inf
+        // only after the read, so those blocks take the maximum themselves
+        const float smax = (BIAS || need_mask) ? __int_as_float(0x7fc00000)
+                                               : fmax3(pmax[0], pmax[1], fmaxf(pmax[2], pmax[3]));
+        const float alpha = softmax_step<BIAS, PQ>(s, c, nvis, bk, smax, m, l, pw, pw2);
         if (j > 0) {  // PV(t, j-1) must be done with P_t and O_t
           ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);
           ++pvc;

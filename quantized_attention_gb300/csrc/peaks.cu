@@ -20,6 +20,23 @@ constexpr int kTcSmem = 160 * 1024;  // more than half an SM: one CTA per SM
 constexpr int kATileBytes = 128 * 128;  // A: 128 rows x 128 bytes, 128B swizzle
 constexpr int kBTileBytes = 256 * 128;  // B: up to 256 rows x 128 bytes
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Start and end of a CTA's loop: SM clock cycles and global nanoseconds, so
+// the clock the loop ran at is cycles / nanoseconds.
+__device__ __forceinline__ void stamp(unsigned long long* clocks, unsigned long long c0,
+                                      unsigned long long c1, unsigned long long n0,
+                                      unsigned long long n1) {
+  clocks[4 * blockIdx.x] = c0;
+  clocks[4 * blockIdx.x + 1] = c1;
+  clocks[4 * blockIdx.x + 2] = n0;
+  clocks[4 * blockIdx.x + 3] = n1;
+}
+
 // Deterministic pseudo-random 32-bit words (a multiplicative hash).
 __device__ __forceinline__ uint32_t hash32(uint32_t x) {
   x ^= x >> 16;
@@ -44,8 +61,8 @@ __device__ void fill_operands(uint8_t* smem, int bytes, bool f8) {
 
 // tcgen05 loop: iters rounds of 4 MMAs (M = 128, N = n, one 128-byte K slice
 // each: K = 16 for kind::f16, K = 32 for kind::f8f6f4) into one TMEM
-// accumulator, issued by one thread.  clocks[2 * cta] = SM clock at the first
-// issue and after the last MMA completed.
+// accumulator, issued by one thread; the stamps bracket the first issue and
+// the completion of the last MMA.
 template <bool F8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_loop_kernel(int n, int iters, unsigned long long* clocks, unsigned int* err) {
@@ -81,7 +98,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ad[s] = smem_desc(sA + s * 32, 1024, kSwizzle128B);
       bd[s] = smem_desc(sB + s * 32, 1024, kSwizzle128B);
     }
-    const unsigned long long t0 = cycles();
+    const unsigned long long g0 = global_ns(), t0 = cycles();
     for (int i = 0; i < iters; ++i) {
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
@@ -91,9 +108,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mma_commit(smem_u32(bar));
     const bool ok = mbar_wait(smem_u32(bar), 0, abort_flag, err, kQattnPeakErrTimeout);
-    const unsigned long long t1 = cycles();
-    clocks[2 * blockIdx.x] = t0;
-    clocks[2 * blockIdx.x + 1] = ok ? t1 : t0;
+    const unsigned long long t1 = cycles(), g1 = global_ns();
+    stamp(clocks, t0, ok ? t1 : t0, g0, ok ? g1 : g0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// The fused attention's MMA sequence per key block and query tile: 8
+// kind::f16 MMAs (M = 128, N = 128, K = 16; S = Q K^T over 128 channels) into
+// one accumulator, then 4 kind::f8f6f4 MMAs (N = 128, K = 32; O += P V over
+// 128 keys) into a second; operands are the same 128-byte-row tiles (finite
+// as fp16 and as e4m3).
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_mixed_loop_kernel(int iters, unsigned long long* clocks, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + kATileBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kATileBytes + kBTileBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kATileBytes + kBTileBytes + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kATileBytes + kBTileBytes + 12);
+  const int warp = threadIdx.x >> 5;
+  {
+    uint32_t* w = reinterpret_cast<uint32_t*>(smem);
+    for (int i = threadIdx.x; i < (kATileBytes + kBTileBytes) / 4; i += blockDim.x)
+      w[i] = hash32(i * 2654435761u + blockIdx.x) & 0xBFBFBFBFu;  // finite in both formats
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(bar), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = make_idesc(128, 128, 0, 0);
+    uint64_t ad[4], bd[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      ad[s] = smem_desc(sA + s * 32, 1024, kSwizzle128B);
+      bd[s] = smem_desc(sB + s * 32, 1024, kSwizzle128B);
+    }
+    const unsigned long long g0 = global_ns(), t0 = cycles();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) mma_f16(tmem, ad[s & 3], bd[s & 3], idesc, (i | s) ? 1u : 0u);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) mma_f8(tmem + 128, ad[s], bd[s], idesc, (i | s) ? 1u : 0u);
+    }
+    mma_commit(smem_u32(bar));
+    const bool ok = mbar_wait(smem_u32(bar), 0, abort_flag, err, kQattnPeakErrTimeout);
+    const unsigned long long t1 = cycles(), g1 = global_ns();
+    stamp(clocks, t0, ok ? t1 : t0, g0, ok ? g1 : g0);
   }
   tc_fence_before();
   __syncthreads();
@@ -120,7 +199,7 @@ __global__ void __launch_bounds__(256)
   for (int c = 0; c < 8; ++c)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[c][e] = 0u;
-  const unsigned long long t0 = cycles();
+  const unsigned long long g0 = global_ns(), t0 = cycles();
   for (int i = 0; i < iters; ++i) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -146,17 +225,14 @@ __global__ void __launch_bounds__(256)
     }
   }
   __syncthreads();
-  const unsigned long long t1 = cycles();
+  const unsigned long long t1 = cycles(), g1 = global_ns();
   uint32_t x = 0;
 #pragma unroll
   for (int c = 0; c < 8; ++c)
 #pragma unroll
     for (int e = 0; e < 4; ++e) x ^= acc[c][e];
   if (x == 0x9E3779B9u) atomicAdd(sink, 1u);  // keeps the chains live
-  if (threadIdx.x == 0) {
-    clocks[2 * blockIdx.x] = t0;
-    clocks[2 * blockIdx.x + 1] = t1;
-  }
+  if (threadIdx.x == 0) stamp(clocks, t0, t1, g0, g1);
 }
 
 // MUFU ex2 loop: 8 independent chains per thread, x <- -2^x stays in [-1, -0.5].
@@ -165,21 +241,18 @@ __global__ void __launch_bounds__(256)
   float x[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) x[c] = -0.5f - 0.0625f * c - 1e-6f * threadIdx.x;
-  const unsigned long long t0 = cycles();
+  const unsigned long long g0 = global_ns(), t0 = cycles();
   for (int i = 0; i < iters; ++i) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) x[c] = -ex2_approx(x[c]);
   }
   __syncthreads();
-  const unsigned long long t1 = cycles();
+  const unsigned long long t1 = cycles(), g1 = global_ns();
   float s = 0.f;
 #pragma unroll
   for (int c = 0; c < 8; ++c) s += x[c];
   if (s == 1.0f) atomicAdd(sink, 1u);
-  if (threadIdx.x == 0) {
-    clocks[2 * blockIdx.x] = t0;
-    clocks[2 * blockIdx.x + 1] = t1;
-  }
+  if (threadIdx.x == 0) stamp(clocks, t0, t1, g0, g1);
 }
 
 }  // namespace
@@ -201,6 +274,13 @@ extern "C" int qattn_peak_loop(int kind, int n, int iters, int blocks,
           cudaSuccess)
         return 3;
       k<<<blocks, kTcThreads, kTcSmem, s>>>(n, iters, clocks, err);
+      break;
+    }
+    case QATTN_PEAK_TC_ATTN_MIX: {
+      if (cudaFuncSetAttribute(tc_mixed_loop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcSmem) != cudaSuccess)
+        return 3;
+      tc_mixed_loop_kernel<<<blocks, kTcThreads, kTcSmem, s>>>(iters, clocks, err);
       break;
     }
     case QATTN_PEAK_MMA_S8: warp_mma_loop_kernel<0><<<blocks, 256, 0, s>>>(iters, clocks, sink); break;

@@ -14,18 +14,23 @@ import torch
 
 from . import binding as qb
 
-TC_F16, TC_F8, MMA_S8, MMA_F16, MMA_E4M3, EX2 = range(6)
+TC_F16, TC_F8, MMA_S8, MMA_F16, MMA_E4M3, EX2, TC_ATTN_MIX = range(7)
 
-# name: (kind, n, operations per loop round and CTA, CTAs per SM, unit)
+# name: (kind, n, operations per loop round and CTA, CTAs per SM, unit); the
+# light loops first, so that the power-limited clock of the tcgen05 loops
+# does not carry over into them
 LOOPS = {
-    "tcgen05_f16_n256": (TC_F16, 256, 4 * 2 * 128 * 256 * 16, 1, "TFLOP/s"),
-    "tcgen05_f16_n128": (TC_F16, 128, 4 * 2 * 128 * 128 * 16, 1, "TFLOP/s"),
-    "tcgen05_f8_n256": (TC_F8, 256, 4 * 2 * 128 * 256 * 32, 1, "TFLOP/s"),
-    "tcgen05_f8_n128": (TC_F8, 128, 4 * 2 * 128 * 128 * 32, 1, "TFLOP/s"),
+    "mufu_ex2": (EX2, 0, 256 * 8, 4, "Tex2/s"),
     "mma_sync_s8": (MMA_S8, 0, 8 * 8 * 2 * 16 * 8 * 32, 4, "TOP/s"),
     "mma_sync_f16": (MMA_F16, 0, 8 * 8 * 2 * 16 * 8 * 16, 4, "TFLOP/s"),
     "mma_sync_e4m3": (MMA_E4M3, 0, 8 * 8 * 2 * 16 * 8 * 32, 4, "TFLOP/s"),
-    "mufu_ex2": (EX2, 0, 256 * 8, 4, "Tex2/s"),
+    "tcgen05_f16_n128": (TC_F16, 128, 4 * 2 * 128 * 128 * 16, 1, "TFLOP/s"),
+    "tcgen05_f16_n256": (TC_F16, 256, 4 * 2 * 128 * 256 * 16, 1, "TFLOP/s"),
+    "tcgen05_f8_n128": (TC_F8, 128, 4 * 2 * 128 * 128 * 32, 1, "TFLOP/s"),
+    "tcgen05_f8_n256": (TC_F8, 256, 4 * 2 * 128 * 256 * 32, 1, "TFLOP/s"),
+    # the fused attention's per-block sequence: 8 f16 (QK^T) + 4 f8 (PV) MMAs
+    "tcgen05_attn_mix": (TC_ATTN_MIX, 128, 8 * 2 * 128 * 128 * 16 + 4 * 2 * 128 * 128 * 32, 1,
+                         "TFLOP/s"),
 }
 
 
@@ -45,7 +50,7 @@ def measure(target_ms: float = 5.0, names=None) -> dict:
     for name in (names or LOOPS):
         kind, n, ops_round, per_sm, unit = LOOPS[name]
         blocks = sms * per_sm
-        clocks = torch.zeros(2 * blocks, dtype=torch.int64, device="cuda")
+        clocks = torch.zeros(4 * blocks, dtype=torch.int64, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         sink = torch.zeros(1, dtype=torch.int32, device="cuda")
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -64,12 +69,15 @@ def measure(target_ms: float = 5.0, names=None) -> dict:
         ms = timed(iters)
         if int(err.item()) != 0:
             raise RuntimeError(f"{name}: a completion wait ran out")
-        c = clocks.view(blocks, 2).cpu()
+        c = clocks.view(blocks, 4).cpu()
         cyc = (c[:, 1] - c[:, 0]).double()
-        mhz = float(cyc.median()) / (ms * 1e3)
+        ns = (c[:, 3] - c[:, 2]).double().clamp(min=1.0)
+        mhz = float((cyc / ns).median()) * 1e3  # the clock the loops ran at
         ops = float(ops_round) * iters * blocks
-        out[name] = {"rate": ops / (ms * 1e-3) / 1e12, "unit": unit, "ms": ms,
-                     "sm_mhz": mhz, "per_sm_per_clk": ops / blocks * per_sm / float(cyc.median())}
+        rate = ops / (ms * 1e-3)
+        out[name] = {"rate": rate / 1e12, "unit": unit, "ms": ms, "sm_mhz": mhz,
+                     "per_sm_per_clk": rate / sms / (mhz * 1e6),
+                     "cta_span_of_elapsed": float(ns.median()) / (ms * 1e6)}
     return out
 
 
