@@ -411,16 +411,18 @@ def time_cpu_mode_baseline(mode, wl_name, budget_s=10.0):
     wl = I.WORKLOADS[wl_name]
     inp = I.make_inputs(wl)
     ops, n, t0 = 0, 0, time.perf_counter()
-    if mode == "intsoftmax":
-        qc, sq = _tensor_codes_np(inp.Q)
-        kc, sk = _tensor_codes_np(inp.K)
-        vc, _ = _tensor_codes_np(inp.V)
+    if mode == "intsoftmax":  # per-tensor codes of Q, K, V, then the integer attention
+        qc, sq = O.quantize_sym(inp.Q, O.GRAN_TENSOR)
+        kc, sk = O.quantize_sym(inp.K, O.GRAN_TENSOR)
+        vc, _ = O.quantize_sym(inp.V, O.GRAN_TENSOR)
+        sq, sk = F32(np.asarray(sq).reshape(-1)[0]), F32(np.asarray(sk).reshape(-1)[0])
         heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
         while n < len(heads) and time.perf_counter() - t0 < budget_s:
             O.attn_intsoftmax(qc, sq, kc, sk, vc, heads=[heads[n]])
             ops += 4 * wl.d * wl.Nq * wl.Nk
             n += 1
-        desc = f"{n} whole (image, head) attentions of {wl_name}, int64 NumPy, one process"
+        desc = (f"per-tensor codes of the whole tensors, then {n} whole (image, head) attentions "
+                f"of {wl_name}, int64 NumPy, one process")
     else:  # exact24: 128-row query blocks of head 0 against the whole cache
         nblk = (wl.Nq + 127) // 128
         while n < nblk and time.perf_counter() - t0 < budget_s:
@@ -433,10 +435,7 @@ def time_cpu_mode_baseline(mode, wl_name, budget_s=10.0):
     return ops, time.perf_counter() - t0, 1, desc
 
 
-def _tensor_codes_np(x):
-    """Per-tensor int8 codes: scale fp32(max |x| / 127), codes rint(x / scale)."""
-    sc = np.float32(np.abs(x).max() / np.float32(127.0))
-    return np.clip(np.rint(x / sc), -127, 127).astype(np.int8), sc
+F32 = np.float32
 
 
 def reference_arm(args):
@@ -582,7 +581,8 @@ def gpu_arm(args):
     from quantized_attention_gb300 import inputs as I
     from quantized_attention_gb300.pipeline import device_inputs, problem_for
 
-    unit_rates, unit_peaks = measure_unit_peaks()
+    unit_rates, unit_peaks = (measure_unit_peaks() if not args.no_unit_peaks
+                              else ({"skipped": "--no-unit-peaks"}, None))
     wl = I.WORKLOADS[args.workload]
     inp = I.make_inputs(wl)
     dev = device_inputs(inp)
@@ -609,22 +609,11 @@ def gpu_arm(args):
         e24_ws = torch.empty(max(qb.workspace_size(e24_shape, e24_params), 256), dtype=torch.uint8,
                              device="cuda")
 
-    if args.intsoftmax:  # QFlash integer-only attention on per-tensor int8 codes
+    if args.intsoftmax:  # QFlash: per-tensor int8 codes of bf16 Q, K, V, integer-only attention
         if wl.kv_codes or wl.causal:
             raise SystemExit("--intsoftmax needs an unmasked bf16 workload (vit, tiny)")
-        def tensor_codes(x):
-            codes, sc = _tensor_codes_np(x)
-            return (torch.from_numpy(codes).to("cuda"),
-                    torch.tensor([sc], dtype=torch.float32, device="cuda"))
-        ism_q, ism_sq = tensor_codes(inp.Q)
-        ism_k, ism_sk = tensor_codes(inp.K)
-        ism_v, _ = tensor_codes(inp.V)
-        ism_out = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d), dtype=torch.int8, device="cuda")
-        ism_shape = qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
-        ism_params = qb.make_params()
-
-    def run_intsoftmax():
-        qb.fwd_intsoftmax(ism_q, ism_sq, ism_k, ism_sk, ism_v, ism_shape, ism_params, ism_out, stream)
+        from quantized_attention_gb300.pipeline import QFlashProblem
+        ism = QFlashProblem(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
 
     def run_exact24():
         qb.fwd_exact24(dev["Q"], dev["K_codes"], dev["K_scale"], dev["V_codes"], dev["V_scale"],
@@ -632,8 +621,9 @@ def gpu_arm(args):
 
     def step():
         if args.intsoftmax:
+            ism.quantize(dev["Q"], dev["K"], dev["V"], stream)
             ev_a.record(stream)
-            run_intsoftmax()
+            ism.attend(stream)
             ev_b.record(stream)
             return
         if args.exact24:
@@ -684,10 +674,9 @@ def gpu_arm(args):
     value = whole_job_value(ops, world, ms_per_step)
 
     # ---- end to end through the public API, host buffers, copies timed
-    if args.intsoftmax:  # the int8 codes in, the int8 output codes back
-        dev = {"q": ism_q, "k": ism_k, "v": ism_v}
-        host = {k: v.cpu().pin_memory() for k, v in dev.items()}
-        out_dev = ism_out
+    if args.intsoftmax:  # bf16 Q, K, V in, the int8 output codes back
+        host = {k: v.cpu().pin_memory() for k, v in dev.items() if k in ("Q", "K", "V")}
+        out_dev = ism.O
     else:
         host = {k: v.cpu().pin_memory() for k, v in dev.items()
                 if (not decode and not args.exact24) or k in ("Q", "K_new", "V_new")}
@@ -700,7 +689,7 @@ def gpu_arm(args):
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
         if args.intsoftmax:
-            run_intsoftmax()
+            ism.run(dev["Q"], dev["K"], dev["V"], stream)
         elif args.exact24:
             run_exact24()
         elif decode:
@@ -727,8 +716,7 @@ def gpu_arm(args):
 
         if args.intsoftmax:
             def compute(d_in, d_out, s):
-                qb.fwd_intsoftmax(d_in["q"], ism_sq, d_in["k"], ism_sk, d_in["v"], ism_shape,
-                                  ism_params, d_out, s)
+                ism.run(d_in["Q"], d_in["K"], d_in["V"], s, out=d_out)
         elif args.exact24:  # the cache is resident; each step brings its queries
             def compute(d_in, d_out, s):
                 qb.fwd_exact24(d_in["Q"], dev["K_codes"], dev["K_scale"], dev["V_codes"],
@@ -853,8 +841,9 @@ def gpu_arm(args):
                        **({"mode": "24-bit exact split (qattn_fwd_exact24)",
                            "step": "split Q, attention with exact fp16 products"} if args.exact24 else {}),
                        **({"mode": "integer-only softmax (qattn_fwd_intsoftmax)",
-                           "step": "attention on resident per-tensor int8 codes",
-                           "granularity": "tensor", "kv_input": "int8 codes",
+                           "step": "per-tensor int8 codes of bf16 Q, K, V (qattn_quantize_qk), "
+                                   "integer-only attention",
+                           "granularity": "tensor", "kv_input": "bf16",
                            "output": "int8 codes"} if args.intsoftmax else {})},
             "attn_kernel_ms": attn_avg_ms,
             "roofline": roofline, "cpu_baseline": cpu,
@@ -867,7 +856,7 @@ def gpu_arm(args):
                     **({"copy_only_ms_per_step": copy_ms,
                         "copy_bound_value": world * ops / (copy_ms * 1e-3) / 1e12}
                        if copy_ms else {})},
-            "gpu_launches": (1 if args.intsoftmax else 2 if args.exact24
+            "gpu_launches": (ism.kernel_launches() if args.intsoftmax else 2 if args.exact24
                              else P.decode_launches(append=True) if decode
                              else P.kernel_launches()) * args.steps,
             "clocks": clk.summary(),
@@ -929,8 +918,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other prefill workloads' sub-records")
+    ap.add_argument("--no-unit-peaks", action="store_true",
+                    help="skip the tcgen05 / mma.sync / MUFU rate loops (profiling runs)")
     ap.add_argument("--intsoftmax", action="store_true",
-                    help="time QFlash's integer-only attention (qattn_fwd_intsoftmax) on int8 codes")
+                    help="time QFlash's integer-only attention (qattn_fwd_intsoftmax) with "
+                         "per-tensor int8 codes of bf16 Q, K, V")
     ap.add_argument("--exact24", action="store_true",
                     help="time the 24-bit exact split mode (qattn_fwd_exact24) on an int8-cache workload")
     args = ap.parse_args()

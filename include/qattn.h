@@ -383,6 +383,22 @@ qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, in
                              float* k_mean, float* v_code_amax, int8_t* k_codes,
                              int8_t* v_codes, qattn_stream_t stream);
 
+/* The int8 KV cache header's V part for a cache filled outside the library:
+ * v_code_amax[b][h][c] = max over rows t < Nk of |v_codes[b][h][t][c]| (0 for
+ * Nk = 0).  This is the per-channel maximum that qattn_kv_append keeps up to
+ * date as it appends tokens and that qattn_decode turns into V's e4m3 scale
+ * (ZINC post, "What actually changed for decode": the cache stores int8 codes
+ * and the header carries what the kernels need about them).
+ *   v_codes      int8 [B][Hkv][capacity][d], device, 16-byte aligned; rows
+ *                0..Nk-1 are read (NULL allowed when Nk = 0)
+ *   v_code_amax  (out) fp32 [B][Hkv][d], device, 4-byte aligned
+ * Limits: d in {32, 64, 128}, 0 <= Nk <= capacity <= 2^24, B * Hkv <= 65535.
+ * Asynchronous on the stream; no workspace.
+ */
+qattn_status qattn_kv_header_init(const int8_t* v_codes, int64_t B, int64_t Hkv, int64_t Nk,
+                                  int64_t d, int64_t capacity, float* v_code_amax,
+                                  qattn_stream_t stream);
+
 /* a4 alone (debug) -- the int32 score tiles S = q_codes . k_codes^T
  * ("QFlash", eq. (3)), through the same tensor-core path as qattn_fwd.
  *   S (out) int32 [B][Hq][Nq][Nk]

@@ -589,6 +589,16 @@ def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax
     return mu, amax, kc, vc
 
 
+def kv_header(v_codes, Nk):
+    """The cache header's V part for a cache filled elsewhere: per (batch, KV
+    head, channel) the largest |code| over rows 0..Nk-1 (0 for Nk = 0) -- the
+    quantity kv_append keeps as tokens arrive."""
+    v = np.asarray(v_codes)[:, :, :Nk, :].astype(np.int64)
+    if Nk == 0:
+        return np.zeros((v.shape[0], v.shape[1], v.shape[3]), np.float32)
+    return np.abs(v).max(axis=2).astype(np.float32)
+
+
 EXACT24_GROUP = 64   # q scaled per (head, 64-channel group)
 EXACT24_CHUNK = 64   # P scaled per (row, 64-key chunk); also the online-softmax block
 

@@ -29,7 +29,7 @@ EXPORTED = (
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
     "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
     "qattn_fwd_kernel_choice", "qattn_prepare_launches", "qattn_debug_wait_timeout",
-    "qattn_peak_loop",
+    "qattn_peak_loop", "qattn_kv_header_init",
 )
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
     L.qattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_kv_append.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+    L.qattn_kv_header_init.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp]
     L.qattn_fwd_exact24.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_fwd_intsoftmax.argtypes = [vp, vp, vp, vp, vp, PS, PP, vp, vp]
     L.qattn_get_error.argtypes = [vp]
@@ -97,7 +98,7 @@ def lib() -> ctypes.CDLL:
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
-                 "qattn_prepare", "qattn_debug_wait_timeout"):
+                 "qattn_prepare", "qattn_debug_wait_timeout", "qattn_kv_header_init"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -175,7 +176,8 @@ def smooth_k(K, shape, k_mean, workspace, stream=None):
 def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_scales,
                 k_codes, k_scales, workspace, stream=None, k_carrier=None):
     _dense(Q, torch.bfloat16, "Q")
-    _dense(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")
+    if K is not None:  # no keys (shape.Nk = 0): Q alone
+        _dense(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")
     if k_carrier is not None:
         _dense(k_carrier, torch.float16, "k_carrier")
     _check(lib().qattn_quantize_qk(_p(Q), _p(K), k_dtype, _p(k_mean), _p(k_chan_scale),
@@ -285,6 +287,18 @@ def kv_append(K_new, V_new, pos, k_chan_scale, v_chan_scale, k_mean, v_code_amax
                                  _p(k_chan_scale), _p(v_chan_scale), _p(k_mean), _p(v_code_amax),
                                  _p(k_codes), _p(v_codes), _stream(stream)),
            "qattn_kv_append")
+
+
+def kv_header_init(v_codes, Nk, v_code_amax, stream=None):
+    """The cache header's per-channel max |V code| over rows 0..Nk-1 (see
+    qattn_kv_header_init in include/qattn.h).  v_codes: int8 [B, Hkv,
+    capacity, d]; v_code_amax: fp32 [B, Hkv, d] (written)."""
+    _dense(v_codes, torch.int8, "v_codes")
+    _dense(v_code_amax, torch.float32, "v_code_amax")
+    B, H, cap, d = v_codes.shape
+    _check(lib().qattn_kv_header_init(_p(v_codes), B, H, int(Nk), d, cap, _p(v_code_amax),
+                                      _stream(stream)),
+           "qattn_kv_header_init")
 
 
 def debug_qk_scores(q_codes, k_codes, shape, S, workspace, stream=None):

@@ -715,6 +715,19 @@ qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, in
       v_codes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qattn_status qattn_kv_header_init(const int8_t* v_codes, int64_t B, int64_t Hkv, int64_t Nk,
+                                  int64_t d, int64_t capacity, float* v_code_amax,
+                                  qattn_stream_t stream) {
+  if (B <= 0 || Hkv <= 0 || Nk < 0 || capacity < Nk || capacity > (int64_t{1} << 24) ||
+      B * Hkv > 65535 || !valid_d(d))
+    return QATTN_ERR_INVALID_ARG;
+  if (!v_code_amax || (reinterpret_cast<uintptr_t>(v_code_amax) & 3u)) return QATTN_ERR_INVALID_ARG;
+  if (Nk > 0 && (!v_codes || !aligned16(v_codes))) return QATTN_ERR_INVALID_ARG;
+  return from_cuda(qattn::launch_v_code_amax(v_codes, static_cast<int>(B * Hkv), static_cast<int>(Nk),
+                                             static_cast<long long>(capacity), static_cast<int>(d),
+                                             v_code_amax, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params) {
   if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
   return fwd_choice(shape, params);

@@ -113,6 +113,11 @@ cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int B
 
 cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t s);
 
+// max |code| per channel of int8 V codes [BH][rows][d], rows 0 .. Nk-1
+// (out: [BH][d] fp32, zeroed first)
+cudaError_t launch_v_code_amax(const int8_t* v_codes, int BH, int Nk, long long rows, int d,
+                               float* out, cudaStream_t s);
+
 // Rows that see no key (Nk = 0): out = 0 (out_bytes of it), lse = -inf for
 // `rows` rows when lse is not null.
 cudaError_t launch_no_key_rows(void* out, size_t out_bytes, float* lse, size_t rows, cudaStream_t s);

@@ -444,7 +444,7 @@ struct VAmaxSmem {
 };
 
 template <int D, bool I8>
-__device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
+__device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk, long long rows,
                                              unsigned int* __restrict__ amax_bits, int chunk, int bh,
                                              VAmaxSmem<D, I8>& sm) {
   constexpr int EPV = I8 ? 16 : 8;
@@ -454,7 +454,8 @@ __device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
   float* red = sm.red;
   const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
   const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
-  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
+  // rows: rows between consecutive (batch, head) slices (Nk when dense)
+  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * rows * row_bytes;
   uint4 raw[NIT];
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
@@ -492,11 +493,12 @@ __device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
 
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
+                                                         long long rows,
                                                          unsigned int* __restrict__ amax_bits) {
   pdl_trigger();
   pdl_wait();
   __shared__ VAmaxSmem<D, I8> sm;
-  v_amax_chunk<D, I8>(V, Nk, amax_bits, blockIdx.x, blockIdx.y, sm);
+  v_amax_chunk<D, I8>(V, Nk, rows, amax_bits, blockIdx.x, blockIdx.y, sm);
 }
 
 // Quantize a 128-key slice of one (batch, KV head) to e4m3 and write it
@@ -653,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare1_kernel(const Prep1Args p
     return;
   }
   x -= nk;
-  v_amax_chunk<D, false>(p.V, p.Nk, p.amax, x % p.nvc, x / p.nvc,
+  v_amax_chunk<D, false>(p.V, p.Nk, p.Nk, p.amax, x % p.nvc, x / p.nvc,
                          *reinterpret_cast<VAmaxSmem<D, false>*>(sm));
 }
 
@@ -1116,7 +1118,8 @@ static cudaError_t quantize_v_impl(const void* V, const float* chan, int BH, int
                                    uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws,
                                    cudaStream_t s) {
   const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  cudaError_t e = launch_pdl(v_amax_kernel<D, I8>, dim3(nchunks, BH), dim3(kThreads), 0, s, V, Nk, ws);
+  cudaError_t e = launch_pdl(v_amax_kernel<D, I8>, dim3(nchunks, BH), dim3(kThreads), 0, s, V, Nk,
+                             static_cast<long long>(Nk), ws);
   if (e != cudaSuccess) return e;
   const int nt = static_cast<int>((ldv + 127) / 128);
   return launch_pdl(v_convert_kernel<D, I8>, dim3(nt, BH), dim3(kThreads), 0, s, V, Nk,
@@ -1138,6 +1141,26 @@ cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int B
     default: QATTN_QV(128)
   }
 #undef QATTN_QV
+}
+
+// The int8 cache header's per-channel max |V code| over rows 0 .. Nk-1 of
+// each (batch, KV head) slice of `rows` cached rows: the amax kernel of the
+// int8 V path, writing the maxima straight into `out` (non-negative floats
+// order like their bit patterns, so the kernel's integer atomic max applies).
+cudaError_t launch_v_code_amax(const int8_t* v_codes, int BH, int Nk, long long rows, int d,
+                               float* out, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(BH) * d * sizeof(float), s);
+  if (e != cudaSuccess || Nk == 0 || BH == 0) return e;
+  const dim3 grid((Nk + kTokPerChunk - 1) / kTokPerChunk, BH);
+  unsigned int* bits = reinterpret_cast<unsigned int*>(out);
+  switch (d) {
+    case 32: return launch_pdl(v_amax_kernel<32, true>, grid, dim3(kThreads), 0, s,
+                               static_cast<const void*>(v_codes), Nk, rows, bits);
+    case 64: return launch_pdl(v_amax_kernel<64, true>, grid, dim3(kThreads), 0, s,
+                               static_cast<const void*>(v_codes), Nk, rows, bits);
+    default: return launch_pdl(v_amax_kernel<128, true>, grid, dim3(kThreads), 0, s,
+                               static_cast<const void*>(v_codes), Nk, rows, bits);
+  }
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t s) {

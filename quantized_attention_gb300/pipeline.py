@@ -86,8 +86,8 @@ class Problem:
         rows in use, and for qattn_kv_append the channel scales and the
         running channel mean of K (zeros if not given)."""
         self._cache_k, self._cache_v, self._cache_vs = K_codes, V_codes, V_scale
-        used = V_codes[:, :, : self.shape.Nk]
-        self._cache_vamax = used.to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+        self._cache_vamax = torch.empty(V_scale.shape, dtype=torch.float32, device=V_codes.device)
+        qb.kv_header_init(V_codes, self.shape.Nk, self._cache_vamax)
         self._cache_ks = K_scale
         self._cache_kmean = (K_mean.clone().contiguous() if K_mean is not None
                              else torch.zeros_like(V_scale))
@@ -217,6 +217,53 @@ class OverlappedSteps:
         """Wait for every step issued so far."""
         for s in (self.s_in, self.s_comp, self.s_out):
             s.synchronize()
+
+
+class QFlashProblem:
+    """QFlash's integer-only attention for one shape: per-tensor int8 codes of
+    bf16 Q, K and V ("QFlash", section 4, eq. (1)-(2), made by
+    qattn_quantize_qk's per-tensor Q path: V as a query tensor with no keys),
+    then qattn_fwd_intsoftmax.  The output is int8 codes of V's scale."""
+
+    def __init__(self, B, Hq, Hkv, Nq, Nk, d, *, sm_scale=0.0, device="cuda"):
+        dev = torch.device(device)
+        self.shape = qb.make_shape(B, Hq, Hkv, Nq, Nk, d)
+        self.params = qb.make_params(sm_scale=sm_scale)
+        tensor = qb.make_params(q_gran=qb.GRAN_TENSOR, k_gran=qb.GRAN_TENSOR)
+        self._qk = (qb.make_shape(B, Hq, Hkv, Nq, Nk, d), tensor)
+        self._v = (qb.make_shape(B, Hkv, Hkv, Nk, 0, d), tensor)
+        i8, f32 = torch.int8, torch.float32
+        self.q_codes = torch.empty((B, Hq, Nq, d), dtype=i8, device=dev)
+        self.k_codes = torch.empty((B, Hkv, Nk, d), dtype=i8, device=dev)
+        self.v_codes = torch.empty((B, Hkv, Nk, d), dtype=i8, device=dev)
+        self.q_scale = torch.empty(1, dtype=f32, device=dev)
+        self.k_scale = torch.empty(1, dtype=f32, device=dev)
+        self.v_scale = torch.empty(1, dtype=f32, device=dev)
+        self.O = torch.empty((B, Hq, Nq, d), dtype=i8, device=dev)
+        ws = max(qb.workspace_size(*self._qk), qb.workspace_size(*self._v), 256)
+        self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
+
+    def quantize(self, Q, K, V, stream=None):
+        qb.quantize_qk(Q, K, qb.DT_BF16, None, None, *self._qk, self.q_codes, self.q_scale,
+                       self.k_codes, self.k_scale, self.workspace, stream)
+        qb.quantize_qk(V, None, qb.DT_BF16, None, None, *self._v, self.v_codes, self.v_scale,
+                       None, None, self.workspace, stream)
+
+    def attend(self, stream=None, out=None):
+        O = self.O if out is None else out
+        qb.fwd_intsoftmax(self.q_codes, self.q_scale, self.k_codes, self.k_scale, self.v_codes,
+                          self.shape, self.params, O, stream)
+        return O
+
+    def run(self, Q, K, V, stream=None, out=None):
+        self.quantize(Q, K, V, stream)
+        return self.attend(stream, out)
+
+    @staticmethod
+    def kernel_launches() -> int:
+        """Kernels one run launches: two passes per per-tensor quantize call
+        (amax, codes), then the attention kernel."""
+        return 2 + 2 + 1
 
 
 def problem_for(wl, **kw) -> Problem:

@@ -45,7 +45,8 @@ def run_decode(wl, inp, out_dtype=qb.DT_F32):
     P = problem_for(wl, out_dtype=out_dtype, want_lse=True)
     dev = device_inputs(inp)
     P.quantize(**dev)
-    amax = dev["V_codes"].to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+    amax = torch.empty(dev["V_scale"].shape, dtype=torch.float32, device="cuda")
+    qb.kv_header_init(dev["V_codes"], wl.Nk, amax)
     ws = torch.empty(max(qb.workspace_size(P.shape, P.params), 256), dtype=torch.uint8,
                      device="cuda")
     qb.decode(P.q_codes, P.q_scales, dev["K_codes"], P.k_scales, dev["V_codes"],
@@ -124,7 +125,8 @@ def test_decode_ignores_workspace_contents():
     P = problem_for(wl, want_lse=True)
     dev = device_inputs(inp)
     P.quantize(**dev)
-    amax = dev["V_codes"].to(torch.int32).abs().amax(dim=2).to(torch.float32).contiguous()
+    amax = torch.empty(dev["V_scale"].shape, dtype=torch.float32, device="cuda")
+    qb.kv_header_init(dev["V_codes"], wl.Nk, amax)
     n = max(qb.workspace_size(P.shape, P.params), 256)
 
     def run(ws):

@@ -118,3 +118,24 @@ def test_decode_steps_on_an_appended_cache():
         want = O.run_workload(inp, prep, heads=heads, rows=np.arange(1), want_bound=True)
         got = P.O.cpu().numpy().reshape(wl.Hq, 1, wl.d).astype(np.float64)
         check_output(got, want["O"], want["bound"], f"step {s}")
+
+
+@pytest.mark.parametrize("d,cap,Nk", [(128, 300, 300), (128, 300, 129), (64, 70, 1), (32, 257, 200),
+                                      (64, 16, 0)])
+def test_header_init_matches_oracle(d, cap, Nk):
+    """qattn_kv_header_init: the max |V code| per channel over the rows in use of
+    a cache filled outside the library, bit-exact with the oracle's definition
+    (rows beyond Nk hold larger codes that must not count)."""
+    rng = np.random.default_rng(d + cap + Nk)
+    B, H = 2, 3
+    codes = rng.integers(-100, 101, size=(B, H, cap, d)).astype(np.int8)
+    codes[:, :, Nk:, :] = 127          # unused rows: never read
+    codes[0, 1, :, 5] = 0              # an all-zero channel
+    if Nk > 3:
+        codes[1, 2, Nk - 1, 7] = -127  # the extreme code in the last row in use
+    dev = torch.from_numpy(codes).cuda()
+    out = torch.full((B, H, d), -1.0, dtype=torch.float32, device="cuda")
+    qb.kv_header_init(dev, Nk, out)
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    assert np.array_equal(out.cpu().numpy(), O.kv_header(codes, Nk))

@@ -67,6 +67,30 @@ def test_intsoftmax_bit_exact(wl):
     _check(got, want)
 
 
+@pytest.mark.parametrize("wl", [CASES[0], CASES[2], CASES[3]], ids=["deit", "swin", "gqa"])
+def test_library_codes_then_intsoftmax_bit_exact(wl):
+    """The whole QFlash path from bf16 activations: the library's per-tensor
+    int8 codes of Q, K and V (QFlash, section 4, eq. (1)-(2)) equal the
+    oracle's quantizer bit for bit, and the integer-only attention on them
+    equals the oracle's on the oracle's codes."""
+    from quantized_attention_gb300.pipeline import QFlashProblem, device_inputs
+    inp = I.make_inputs(wl)
+    dev = device_inputs(inp)
+    P = QFlashProblem(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
+    P.run(dev["Q"], dev["K"], dev["V"])
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    want = {}
+    for name, x, codes, scale in (("Q", inp.Q, P.q_codes, P.q_scale), ("K", inp.K, P.k_codes, P.k_scale),
+                                  ("V", inp.V, P.v_codes, P.v_scale)):
+        c, s = O.quantize_sym(x, O.GRAN_TENSOR)
+        assert np.array_equal(codes.cpu().numpy(), c), name
+        assert np.float32(scale.item()) == np.float32(np.asarray(s).reshape(-1)[0]), name
+        want[name] = (c, np.float32(np.asarray(s).reshape(-1)[0]))
+    ref = O.attn_intsoftmax(want["Q"][0], want["Q"][1], want["K"][0], want["K"][1], want["V"][0])
+    _check(P.O.cpu().numpy().astype(np.int64), ref)
+
+
 def test_intsoftmax_coarse_scales_bit_exact():
     """s~ > 2: X0 = 1 and the requantization shift is negative (every P >= 1
     saturates); the rescale runs with alpha in {0, 1}."""

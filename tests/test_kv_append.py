@@ -108,3 +108,20 @@ def test_chunked_appends_equal_single_steps(chunks):
         pos += T
     for a, b in zip(ref, state):
         assert np.array_equal(a, b)
+
+
+def test_header_of_codes_equals_the_appended_header():
+    """kv_header (the V max |code| of a cache filled elsewhere) equals the header
+    kv_append builds while it writes those codes one token at a time, for any
+    number of rows in use; an empty cache has a zero header."""
+    rng = np.random.default_rng(9)
+    B, H, d, cap, T = 2, 3, 16, 40, 29
+    sk = np.full((B, H, d), 0.05, np.float32)
+    sv = rng.uniform(0.01, 0.05, size=(B, H, d)).astype(np.float32)
+    K = _tokens(rng, B, H, T, d)
+    V = _tokens(rng, B, H, T, d, scale=2.0)
+    state = _empty(B, H, cap, d)
+    for t in range(T):
+        state = O.kv_append(K[:, :, t:t + 1], V[:, :, t:t + 1], t, sk, sv, *state)
+        assert np.array_equal(O.kv_header(state[3], t + 1), state[1])
+    assert not O.kv_header(state[3], 0).any()
