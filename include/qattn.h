@@ -24,9 +24,16 @@
  *     library allocates no device memory of its own except one error word per
  *     device.  Scratch memory is the caller's `workspace` of at least
  *     qattn_workspace_size() bytes; its contents need not be initialised.
- *   - Tensors are dense and row-major.  Q-like tensors are [B][Hq][Nq][d],
- *     K/V-like tensors [B][Hkv][Nk][d].  bf16 tensors are passed as uint16_t
- *     bit patterns.  Every tensor pointer must be 16-byte aligned.
+ *   - Tensors are row-major.  Q-like tensors are [B][Hq][Nq][d], K/V-like
+ *     tensors [B][Hkv][Nk][d].  bf16 tensors are passed as uint16_t bit
+ *     patterns.  Every tensor pointer must be 16-byte aligned.  Outputs are
+ *     dense.  The pre-pass calls (qattn_smooth_k, qattn_quantize_qk,
+ *     qattn_quantize_v, qattn_prepare) also read inputs at any strides: an
+ *     input's `*_strides` array gives its 4 strides in elements, in [B][H][N][d]
+ *     order; the last must be 1 and the others non-negative multiples of 16
+ *     bytes (so every row starts on a 16-byte boundary).  NULL = dense.  A
+ *     packed projection output (e.g. [B][N][3][H][d] viewed as Q, K and V)
+ *     is read in place, with no copy.
  *   - Supported head dims: d in {32, 64, 128}.  Hq must be a multiple of Hkv;
  *     query head h reads KV head h / (Hq / Hkv).  Limits (else
  *     QATTN_ERR_UNSUPPORTED): Nq, Nk <= 65535 * 128 and B * Hq <= 65535.
@@ -131,15 +138,16 @@ int64_t qattn_v_ld(int64_t Nk);
 /* a1 -- K channel mean ("int8 Flash Attention on RDNA4", section "K's outliers,
  * and the subtraction softmax does not notice": one reduction over the K
  * block, reused by every query tile).
- *   K       bf16 [B][Hkv][Nk][d]
+ *   K          bf16 [B][Hkv][Nk][d]; k_strides as in the conventions (NULL = dense)
  *   k_mean  fp32 [B][Hkv][d] (out):
  *           mu = fp32( fp64( sum_t round_half_even(K * 2^24) ) * 2^-24 / Nk )
  *           The int64 fixed-point sum makes the result independent of the
  *           summation order.  Exact while Nk * max|K| < 2^29 (the sum stays
  *           below 2^53); Nk = 0 gives mu = 0.
  */
-qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* k_mean,
-                            void* workspace, size_t workspace_bytes, qattn_stream_t stream);
+qattn_status qattn_smooth_k(const uint16_t* K, const int64_t* k_strides, const qattn_shape* shape,
+                            float* k_mean, void* workspace, size_t workspace_bytes,
+                            qattn_stream_t stream);
 
 /* a2 -- Q/K to int8 codes ("QFlash", section 4, eq. (1)-(2)).
  * For each scale granule:  amax = max |x|;  inv = fp32(127 / amax) (0 if amax
@@ -147,7 +155,9 @@ qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* 
  * scale = fp32(amax / 127).
  *   Q            bf16 [B][Hq][Nq][d]                          x = fp32(Q)
  *   K, k_dtype   QATTN_BF16: bf16 [B][Hkv][Nk][d];             x = fp32(fp32(K) - k_mean)
- *                QATTN_I8:   int8 codes of an int8 KV cache, used as they are.
+ *                QATTN_I8:   int8 codes of an int8 KV cache, used as they are
+ *                            (dense only: QATTN_ERR_UNSUPPORTED otherwise).
+ *   q_strides, k_strides  as in the conventions (NULL = dense)
  *   k_mean       fp32 [B][Hkv][d] (BF16 K; NULL = no mean subtraction)
  *   k_chan_scale fp32 [B][Hkv][d] per-channel scale of int8 K codes (I8 K only).
  *                It is folded into Q before Q is quantized,
@@ -165,7 +175,8 @@ qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* 
  * Nk = 0: only Q is quantized; K, k_codes, k_scales and k_carrier may be NULL
  * and nothing is written for K.
  */
-qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
+qattn_status qattn_quantize_qk(const uint16_t* Q, const int64_t* q_strides, const void* K,
+                               const int64_t* k_strides, qattn_dtype k_dtype,
                                const float* k_mean, const float* k_chan_scale,
                                const qattn_shape* shape, const qattn_params* params,
                                int8_t* q_codes, float* q_scales, int8_t* k_codes,
@@ -178,6 +189,7 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
  *   V, v_dtype   QATTN_BF16: bf16 [B][Hkv][Nk][d];  x = fp32(V)
  *                QATTN_I8:   int8 codes [B][Hkv][Nk][d] with v_chan_scale
  *                            fp32 [B][Hkv][d];       x = fp32(code)
+ *   v_strides    as in the conventions (NULL = dense)
  *   amax_c = max_t |x|;  v8 = e4m3_rn_satfinite(fp32(x * fp32(448 / amax_c)))
  *   v_scales (out) fp32 [B][Hkv][d]: amax_c / 448 (BF16), or
  *                  fp32(fp32(v_chan_scale * amax_c) / 448) (I8)
@@ -185,8 +197,9 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
  *                  fastest); bytes for keys Nk..ldv-1 are written as 0.
  *   ldv            row stride in bytes, >= qattn_v_ld(Nk), multiple of 16.
  */
-qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,
-                              const qattn_shape* shape, uint8_t* v8t, int64_t ldv,
+qattn_status qattn_quantize_v(const void* V, const int64_t* v_strides, qattn_dtype v_dtype,
+                              const float* v_chan_scale, const qattn_shape* shape,
+                              uint8_t* v8t, int64_t ldv,
                               float* v_scales, void* workspace, size_t workspace_bytes,
                               qattn_stream_t stream);
 
@@ -201,13 +214,15 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
  * before the attention kernel; fusing them is this library's own step (fewer
  * launches, one read of Q).
  *   Q            bf16 [B][Hq][Nq][d];  K, V  bf16 [B][Hkv][Nk][d]
+ *   q_strides, k_strides, v_strides  as in the conventions (NULL = dense)
  *   k_mean (out) fp32 [B][Hkv][d]; the other outputs as for the three calls
  *   params       q_gran = k_gran = QATTN_GRAN_BLOCK, else QATTN_ERR_UNSUPPORTED
  *                (use the three calls); Nk >= 1, else QATTN_ERR_UNSUPPORTED
  *   ldv          >= qattn_v_ld(Nk), multiple of 16
  *   workspace    at least qattn_workspace_size() bytes.
  */
-qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const uint16_t* K,
+                           const int64_t* k_strides, const uint16_t* V, const int64_t* v_strides,
                            const qattn_shape* shape, const qattn_params* params,
                            int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
                            uint16_t* k_carrier, float* k_mean, uint8_t* v8t, int64_t ldv,

@@ -73,11 +73,12 @@ def lib() -> ctypes.CDLL:
     L.qattn_workspace_size.argtypes = [PS, PP]
     L.qattn_v_ld.restype = i64
     L.qattn_v_ld.argtypes = [i64]
-    L.qattn_smooth_k.argtypes = [vp, PS, vp, vp, sz, vp]
-    L.qattn_quantize_qk.argtypes = [vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp,
-                                    sz, vp]
-    L.qattn_quantize_v.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
-    L.qattn_prepare.argtypes = [vp, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, sz, vp]
+    L.qattn_smooth_k.argtypes = [vp, vp, PS, vp, vp, sz, vp]
+    L.qattn_quantize_qk.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, PS, PP, vp, vp, vp, vp,
+                                    vp, vp, sz, vp]
+    L.qattn_quantize_v.argtypes = [vp, vp, ctypes.c_int, vp, PS, vp, i64, vp, vp, sz, vp]
+    L.qattn_prepare.argtypes = [vp, vp, vp, vp, vp, vp, PS, PP, vp, vp, vp, vp, vp, vp, vp, i64, vp,
+                                vp, sz, vp]
     L.qattn_quantize_v_noalloc.argtypes = [vp, ctypes.c_int, vp, PS, vp, i64, vp, vp]
     L.qattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, PS, PP, vp, vp, vp, sz, vp]
     L.qattn_debug_qk_scores.argtypes = [vp, vp, PS, vp, vp, sz, vp]
@@ -137,6 +138,23 @@ def _dense(t: torch.Tensor, dtype, name: str):
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
+def _input(t: Optional[torch.Tensor], dtype, name: str):
+    """An input the pre-pass reads at any strides: returns its strides as a
+    ctypes int64[4] (None when dense).  The last stride must be 1 and the
+    others multiples of 16 bytes (the library checks and rejects otherwise)."""
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, N, d]")
+    if t.is_contiguous():
+        return None
+    return (ctypes.c_int64 * 4)(*t.stride())
+
+
 def make_shape(B, Hq, Hkv, Nq, Nk, d) -> Shape:
     return Shape(B, Hq, Hkv, Nq, Nk, d)
 
@@ -166,21 +184,20 @@ def n_scales(gran: int, B: int, H: int, N: int) -> int:
 
 
 def smooth_k(K, shape, k_mean, workspace, stream=None):
-    _dense(K, torch.bfloat16, "K")
+    ks = _input(K, torch.bfloat16, "K")
     _dense(k_mean, torch.float32, "k_mean")
-    _check(lib().qattn_smooth_k(_p(K), ctypes.byref(shape), _p(k_mean), _p(workspace),
+    _check(lib().qattn_smooth_k(_p(K), ks, ctypes.byref(shape), _p(k_mean), _p(workspace),
                                 _nbytes(workspace), _stream(stream)),
            "qattn_smooth_k")
 
 
 def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_scales,
                 k_codes, k_scales, workspace, stream=None, k_carrier=None):
-    _dense(Q, torch.bfloat16, "Q")
-    if K is not None:  # no keys (shape.Nk = 0): Q alone
-        _dense(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")
+    qs = _input(Q, torch.bfloat16, "Q")
+    ks = _input(K, torch.int8 if k_dtype == DT_I8 else torch.bfloat16, "K")  # None: no keys
     if k_carrier is not None:
         _dense(k_carrier, torch.float16, "k_carrier")
-    _check(lib().qattn_quantize_qk(_p(Q), _p(K), k_dtype, _p(k_mean), _p(k_chan_scale),
+    _check(lib().qattn_quantize_qk(_p(Q), qs, _p(K), ks, k_dtype, _p(k_mean), _p(k_chan_scale),
                                    ctypes.byref(shape), ctypes.byref(params), _p(q_codes),
                                    _p(q_scales), _p(k_codes), _p(k_scales), _p(k_carrier),
                                    _p(workspace), _nbytes(workspace),
@@ -191,11 +208,11 @@ def quantize_qk(Q, K, k_dtype, k_mean, k_chan_scale, shape, params, q_codes, q_s
 def prepare(Q, K, V, shape, params, q_codes, q_scales, k_codes, k_scales, k_mean, v8t, ldv,
             v_scales, workspace, stream=None, k_carrier=None):
     """qattn_prepare: K mean, Q/K codes and V's e4m3 codes in two launches."""
-    for t, name in ((Q, "Q"), (K, "K"), (V, "V")):
-        _dense(t, torch.bfloat16, name)
+    st = [_input(t, torch.bfloat16, name) for t, name in ((Q, "Q"), (K, "K"), (V, "V"))]
     if k_carrier is not None:
         _dense(k_carrier, torch.float16, "k_carrier")
-    _check(lib().qattn_prepare(_p(Q), _p(K), _p(V), ctypes.byref(shape), ctypes.byref(params),
+    _check(lib().qattn_prepare(_p(Q), st[0], _p(K), st[1], _p(V), st[2], ctypes.byref(shape),
+                               ctypes.byref(params),
                                _p(q_codes), _p(q_scales), _p(k_codes), _p(k_scales),
                                _p(k_carrier), _p(k_mean), _p(v8t), ldv, _p(v_scales),
                                _p(workspace), _nbytes(workspace),
@@ -204,8 +221,8 @@ def prepare(Q, K, V, shape, params, q_codes, q_scales, k_codes, k_scales, k_mean
 
 
 def quantize_v(V, v_dtype, v_chan_scale, shape, v8t, ldv, v_scales, workspace, stream=None):
-    _dense(V, torch.int8 if v_dtype == DT_I8 else torch.bfloat16, "V")
-    _check(lib().qattn_quantize_v(_p(V), v_dtype, _p(v_chan_scale), ctypes.byref(shape), _p(v8t),
+    vs = _input(V, torch.int8 if v_dtype == DT_I8 else torch.bfloat16, "V")
+    _check(lib().qattn_quantize_v(_p(V), vs, v_dtype, _p(v_chan_scale), ctypes.byref(shape), _p(v8t),
                                   ldv, _p(v_scales), _p(workspace),
                                   _nbytes(workspace), _stream(stream)),
            "qattn_quantize_v")

@@ -116,6 +116,26 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool valid_d(int64_t d) { return d == 32 || d == 64 || d == 128; }
 
+// An input tensor [B][H][N][d] with element strides st (NULL: dense): the last
+// stride must be 1 and the others non-negative multiples of 16 bytes (every
+// row starts on a 16-byte boundary, as the vector loads need).
+bool make_src(const void* p, const int64_t* st, int64_t H, int64_t N, int64_t d, int elem,
+              qattn::Src* out) {
+  if (!st) {
+    *out = qattn::dense_src(p, static_cast<int>(H), N, static_cast<int>(d));
+    return true;
+  }
+  if (st[3] != 1) return false;
+  for (int i = 0; i < 3; ++i)
+    if (st[i] < 0 || (st[i] * elem) % 16 != 0) return false;
+  *out = qattn::Src{p, st[0], st[1], st[2], static_cast<int>(H)};
+  return true;
+}
+
+bool is_dense(const int64_t* st, int64_t H, int64_t N, int64_t d) {
+  return !st || (st[3] == 1 && st[2] == d && st[1] == N * d && st[0] == H * N * d);
+}
+
 // Shape checks shared by all entry points.  Returns QATTN_OK, or an error.
 qattn_status check_shape(const qattn_shape* s) {
   if (!s) return QATTN_ERR_INVALID_ARG;
@@ -279,21 +299,25 @@ size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params
   return m;
 }
 
-qattn_status qattn_smooth_k(const uint16_t* K, const qattn_shape* shape, float* k_mean,
-                            void* workspace, size_t workspace_bytes, qattn_stream_t stream) {
+qattn_status qattn_smooth_k(const uint16_t* K, const int64_t* k_strides, const qattn_shape* shape,
+                            float* k_mean, void* workspace, size_t workspace_bytes,
+                            qattn_stream_t stream) {
   qattn_status st = check_shape(shape);
   if (st != QATTN_OK) return st;
   if (shape->B == 0 || shape->Hkv == 0) return QATTN_OK;
   if (!k_mean || !aligned16(k_mean) || (shape->Nk > 0 && (!K || !aligned16(K)))) return QATTN_ERR_INVALID_ARG;
+  qattn::Src ks;
+  if (!make_src(K, k_strides, shape->Hkv, shape->Nk, shape->d, 2, &ks)) return QATTN_ERR_INVALID_ARG;
   const size_t need = ws_smooth(shape);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
-  return from_cuda(qattn::launch_smooth_k(K, static_cast<int>(shape->B * shape->Hkv),
+  return from_cuda(qattn::launch_smooth_k(ks, static_cast<int>(shape->B * shape->Hkv),
                                           static_cast<int>(shape->Nk), static_cast<int>(shape->d),
                                           static_cast<long long*>(workspace), k_mean,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
-qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_dtype,
+qattn_status qattn_quantize_qk(const uint16_t* Q, const int64_t* q_strides, const void* K,
+                               const int64_t* k_strides, qattn_dtype k_dtype,
                                const float* k_mean, const float* k_chan_scale,
                                const qattn_shape* shape, const qattn_params* params,
                                int8_t* q_codes, float* q_scales, int8_t* k_codes,
@@ -311,6 +335,11 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   if (!i8 && shape->Nk > 0 && (!K || !aligned16(K) || !k_codes || !aligned16(k_codes))) return QATTN_ERR_INVALID_ARG;
   if (k_mean && (i8 || !aligned16(k_mean))) return QATTN_ERR_INVALID_ARG;
   if (k_carrier && !aligned16(k_carrier)) return QATTN_ERR_INVALID_ARG;
+  qattn::Src qs, ks;
+  if (!make_src(Q, q_strides, shape->Hq, shape->Nq, shape->d, 2, &qs)) return QATTN_ERR_INVALID_ARG;
+  if (!make_src(K, k_strides, shape->Hkv, shape->Nk, shape->d, i8 ? 1 : 2, &ks)) return QATTN_ERR_INVALID_ARG;
+  // int8 cache codes go to qattn_fwd as they are: dense only
+  if (i8 && !is_dense(k_strides, shape->Hkv, shape->Nk, shape->d)) return QATTN_ERR_UNSUPPORTED;
   const size_t wq = align256(qattn::quantize_rows_ws_bytes(shape->B, shape->Hq, shape->Nq, params->q_gran));
   const size_t need = ws_quant_qk(shape, params);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
@@ -322,6 +351,9 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   const int64_t nqb = (shape->Nq + 127) / 128, nkb = (shape->Nk + 127) / 128;
   qattn::RowsJob jq{};
   jq.X = Q;
+  jq.sB = qs.sB;
+  jq.sH = qs.sH;
+  jq.sN = qs.sN;
   jq.H = Hq;
   jq.N = static_cast<int>(shape->Nq);
   jq.chan = i8 ? k_chan_scale : nullptr;
@@ -352,6 +384,9 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   }
   if (shape->Nk > 0) {
     jk.X = static_cast<const uint16_t*>(K);
+    jk.sB = ks.sB;
+    jk.sH = ks.sH;
+    jk.sN = ks.sN;
     jk.H = Hkv;
     jk.N = static_cast<int>(shape->Nk);
     jk.chan = k_mean;
@@ -368,7 +403,8 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const void* K, qattn_dtype k_d
   return from_cuda(qattn::launch_quantize_rows(jq, 0, jk, k_mean ? 1 : 0, d, s));
 }
 
-qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const uint16_t* K,
+                           const int64_t* k_strides, const uint16_t* V, const int64_t* v_strides,
                            const qattn_shape* shape, const qattn_params* params,
                            int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
                            uint16_t* k_carrier, float* k_mean, uint8_t* v8t, int64_t ldv,
@@ -390,10 +426,18 @@ qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t*
   if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
   const size_t need = ws_prepare(shape);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
+  qattn::Src qs, ks, vs;
+  if (!make_src(Q, q_strides, shape->Hq, shape->Nq, shape->d, 2, &qs) ||
+      !make_src(K, k_strides, shape->Hkv, shape->Nk, shape->d, 2, &ks) ||
+      !make_src(V, v_strides, shape->Hkv, shape->Nk, shape->d, 2, &vs))
+    return QATTN_ERR_INVALID_ARG;
   const int B = static_cast<int>(shape->B), Hq = static_cast<int>(shape->Hq);
   const int Hkv = static_cast<int>(shape->Hkv), d = static_cast<int>(shape->d);
   qattn::RowsJob jq{};
   jq.X = Q;
+  jq.sB = qs.sB;
+  jq.sH = qs.sH;
+  jq.sN = qs.sN;
   jq.H = Hq;
   jq.N = static_cast<int>(shape->Nq);
   jq.Hchan = 1;
@@ -405,6 +449,9 @@ qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t*
   jq.BH = B * Hq;
   qattn::RowsJob jk{};
   jk.X = K;
+  jk.sB = ks.sB;
+  jk.sH = ks.sH;
+  jk.sN = ks.sN;
   jk.H = Hkv;
   jk.N = static_cast<int>(shape->Nk);
   jk.chan = k_mean;
@@ -416,11 +463,12 @@ qattn_status qattn_prepare(const uint16_t* Q, const uint16_t* K, const uint16_t*
   jk.carrier = k_carrier;
   jk.nblk = static_cast<int>((shape->Nk + 127) / 128);
   jk.BH = B * Hkv;
-  return from_cuda(qattn::launch_prepare(jq, jk, V, d, v8t, ldv, v_scales, workspace,
+  return from_cuda(qattn::launch_prepare(jq, jk, vs, d, v8t, ldv, v_scales, workspace,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
-qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v_chan_scale,
+qattn_status qattn_quantize_v(const void* V, const int64_t* v_strides, qattn_dtype v_dtype,
+                              const float* v_chan_scale,
                               const qattn_shape* shape, uint8_t* v8t, int64_t ldv,
                               float* v_scales, void* workspace, size_t workspace_bytes,
                               qattn_stream_t stream) {
@@ -435,7 +483,9 @@ qattn_status qattn_quantize_v(const void* V, qattn_dtype v_dtype, const float* v
   if (ldv < qattn_v_ld(shape->Nk) || (ldv % 16) != 0) return QATTN_ERR_INVALID_ARG;
   const size_t need = ws_quant_v(shape);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
-  return from_cuda(qattn::launch_quantize_v(V, i8 ? 1 : 0, v_chan_scale,
+  qattn::Src vs;
+  if (!make_src(V, v_strides, shape->Hkv, shape->Nk, shape->d, i8 ? 1 : 2, &vs)) return QATTN_ERR_INVALID_ARG;
+  return from_cuda(qattn::launch_quantize_v(vs, i8 ? 1 : 0, v_chan_scale,
                                             static_cast<int>(shape->B * shape->Hkv),
                                             static_cast<int>(shape->Nk), static_cast<int>(shape->d),
                                             v8t, ldv, v_scales, static_cast<unsigned int*>(workspace),

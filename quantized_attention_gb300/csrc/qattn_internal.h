@@ -73,7 +73,19 @@ cudaError_t launch_attn_short(const AttnArgs& a, const int8_t* q_codes, const in
                               const uint8_t* v8t, long long ldv, cudaStream_t s);
 
 // ---- quant_kernels.cu
-cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
+// An input tensor [B][H][N][d] (bf16 or int8) at any strides, in elements: row
+// t of (batch, head) bh = b H + h starts at p + b sB + h sH + t sN and its d
+// elements are contiguous.  Dense: sB = H N d, sH = N d, sN = d.
+struct Src {
+  const void* p;
+  long long sB, sH, sN;
+  int H;
+};
+inline Src dense_src(const void* p, int H, long long N, int d) {
+  return Src{p, static_cast<long long>(H) * N * d, N * d, static_cast<long long>(d), H};
+}
+
+cudaError_t launch_smooth_k(const Src& K, int BH, int Nk, int d, long long* ws, float* mu,
                             cudaStream_t s);
 size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d);
 
@@ -82,6 +94,7 @@ size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d);
 //   2: x = X * chan[b][h / group][:] (chan has Hchan heads, group = H / Hchan)
 struct RowsJob {
   const uint16_t* X;
+  long long sB, sH, sN;  // X's strides in elements (see Src)
   int H, N;
   const float* chan;
   int Hchan, group, gran;
@@ -102,12 +115,12 @@ size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran);
 // minus jk.chan = the mean it writes, mode 1), V's e4m3 transpose.  One launch
 // for heads of at most 128 tokens and d <= 64, else two (ws zeroed here).
 // ws: prepare_ws_bytes().
-cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
+cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const Src& V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
 size_t prepare_ws_bytes(long long BH, long long d);
 int prepare_launch_count(int d, int Nq, int Nk);  // 1 for short heads, else 2
 
-cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,
+cudaError_t launch_quantize_v(const Src& V, int is_i8, const float* chan, int BH, int Nk, int d,
                               uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws_amax,
                               cudaStream_t s);
 

@@ -78,7 +78,8 @@ extern "C" qattn_status qattn_quantize_v_noalloc(const void* V, qattn_dtype v_dt
   if (!scratch) return QATTN_ERR_CUDA;
   // launch_quantize_v zeroes the first B*Hkv*d slots before using them.
   const cudaError_t e = qattn::launch_quantize_v(
-      V, i8 ? 1 : 0, v_chan_scale, static_cast<int>(shape->B * shape->Hkv),
+      qattn::dense_src(V, static_cast<int>(shape->Hkv), shape->Nk, static_cast<int>(shape->d)),
+      i8 ? 1 : 0, v_chan_scale, static_cast<int>(shape->B * shape->Hkv),
       static_cast<int>(shape->Nk), static_cast<int>(shape->d), v8t, ldv, v_scales, scratch,
       reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : QATTN_ERR_CUDA;

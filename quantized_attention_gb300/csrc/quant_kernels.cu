@@ -199,13 +199,19 @@ __device__ __forceinline__ float mean_of_fix24(long long S, uint32_t N, unsigned
   return __uint_as_float(bits | (S < 0 ? 0x80000000u : 0u));
 }
 
+// First element of (batch, head) bh's slice of an input tensor.
+template <typename T>
+__device__ __forceinline__ const T* src_head(const Src& x, int bh) {
+  const int b = bh / x.H, h = bh - b * x.H;
+  return static_cast<const T*>(x.p) + static_cast<long long>(b) * x.sB + static_cast<long long>(h) * x.sH;
+}
+
 constexpr int kMeanRows = 8;  // rows per thread in the mean kernels
 
 // Channel mean for short heads: one warp per (batch, head), all Nk rows
 // (Nk <= 8 * 32 / (D / 8)); lanes = (row group, 16-byte column).
 template <int D>
-__global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const uint16_t* __restrict__ K,
-                                                              int BH, int Nk,
+__global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const Src K, int BH, int Nk,
                                                               unsigned long long magic,
                                                               float* __restrict__ mu) {
   pdl_trigger();
@@ -216,12 +222,12 @@ __global__ void __launch_bounds__(kThreads) k_mean_warp_kernel(const uint16_t* _
   if (bh >= BH) return;
   const int lane = threadIdx.x & 31;
   const int v = lane % VPR, rg = lane / VPR;
-  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
+  const uint16_t* base = src_head<uint16_t>(K, bh);
   uint4 raw[kMeanRows];
 #pragma unroll
   for (int it = 0; it < kMeanRows; ++it) {
     const int t = rg + it * RG;
-    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * D) + v)
+    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(t) * K.sN) + v)
                        : make_uint4(0u, 0u, 0u, 0u);
   }
   long long sum[8];
@@ -254,7 +260,7 @@ struct KMeanSmem {
 };
 
 template <int D, bool MULTI>
-__device__ __forceinline__ void k_mean_chunk(const uint16_t* __restrict__ K, int Nk, int nchunks,
+__device__ __forceinline__ void k_mean_chunk(const Src& K, int Nk, int nchunks,
                                              unsigned long long magic,
                                              unsigned long long* __restrict__ acc,
                                              unsigned int* __restrict__ done, float* __restrict__ mu,
@@ -265,12 +271,12 @@ __device__ __forceinline__ void k_mean_chunk(const uint16_t* __restrict__ K, int
   auto& red = sm.red;
   unsigned int& last = sm.last;
   const int v = threadIdx.x % VPR, rg = threadIdx.x / VPR;
-  const uint16_t* base = K + static_cast<size_t>(bh) * Nk * D;
+  const uint16_t* base = src_head<uint16_t>(K, bh);
   uint4 raw[kMeanRows];
 #pragma unroll
   for (int it = 0; it < kMeanRows; ++it) {
     const int t = chunk * kChunk + rg + it * RG;
-    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * D) + v)
+    raw[it] = (t < Nk) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(t) * K.sN) + v)
                        : make_uint4(0u, 0u, 0u, 0u);
   }
   long long sum[8];
@@ -301,7 +307,7 @@ __device__ __forceinline__ void k_mean_chunk(const uint16_t* __restrict__ K, int
 }
 
 template <int D, bool MULTI>
-__global__ void __launch_bounds__(kThreads) k_mean_kernel(const uint16_t* __restrict__ K, int Nk,
+__global__ void __launch_bounds__(kThreads) k_mean_kernel(const Src K, int Nk,
                                                          int nchunks, unsigned long long magic,
                                                          unsigned long long* __restrict__ acc,
                                                          unsigned int* __restrict__ done,
@@ -337,7 +343,8 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
   const int b = bh / j.H, h = bh % j.H;
   const int t0 = blk * 128;
   const int rows = min(128, j.N - t0);
-  const uint16_t* src = j.X + (static_cast<size_t>(bh) * j.N + t0) * D;
+  const uint16_t* src = j.X + static_cast<long long>(b) * j.sB + static_cast<long long>(h) * j.sH +
+                        static_cast<long long>(t0) * j.sN;
   // Every vector a thread handles is the same 8 channels (kThreads % VPR == 0).
   static_assert(kThreads % VPR == 0, "fixed channel group per thread");
   float ch[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -352,7 +359,7 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
   for (int i = 0; i < NV; ++i) {
     const int v = threadIdx.x + i * kThreads;
     const int r = v / VPR, cv = v % VPR;
-    raw[i] = (r < rows) ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D) + cv)
+    raw[i] = (r < rows) ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * j.sN) + cv)
                         : make_uint4(0u, 0u, 0u, 0u);
   }
   float amax = 0.f;
@@ -444,7 +451,7 @@ struct VAmaxSmem {
 };
 
 template <int D, bool I8>
-__device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk, long long rows,
+__device__ __forceinline__ void v_amax_chunk(const Src& V, int Nk,
                                              unsigned int* __restrict__ amax_bits, int chunk, int bh,
                                              VAmaxSmem<D, I8>& sm) {
   constexpr int EPV = I8 ? 16 : 8;
@@ -453,9 +460,10 @@ __device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
   constexpr int NIT = (kTokPerChunk + RPI - 1) / RPI;
   float* red = sm.red;
   const int v = threadIdx.x % VPR, r0 = threadIdx.x / VPR;
-  const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
-  // rows: rows between consecutive (batch, head) slices (Nk when dense)
-  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * rows * row_bytes;
+  constexpr int kElem = I8 ? 1 : 2;  // bytes per element
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(src_head<uint8_t>(
+      Src{V.p, V.sB * kElem, V.sH * kElem, V.sN * kElem, V.H}, bh));
+  const long long row_bytes = V.sN * kElem;
   uint4 raw[NIT];
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
@@ -492,13 +500,12 @@ __device__ __forceinline__ void v_amax_chunk(const void* __restrict__ V, int Nk,
 }
 
 template <int D, bool I8>
-__global__ void __launch_bounds__(kThreads) v_amax_kernel(const void* __restrict__ V, int Nk,
-                                                         long long rows,
+__global__ void __launch_bounds__(kThreads) v_amax_kernel(const Src V, int Nk,
                                                          unsigned int* __restrict__ amax_bits) {
   pdl_trigger();
   pdl_wait();
   __shared__ VAmaxSmem<D, I8> sm;
-  v_amax_chunk<D, I8>(V, Nk, rows, amax_bits, blockIdx.x, blockIdx.y, sm);
+  v_amax_chunk<D, I8>(V, Nk, amax_bits, blockIdx.x, blockIdx.y, sm);
 }
 
 // Quantize a 128-key slice of one (batch, KV head) to e4m3 and write it
@@ -516,7 +523,7 @@ struct VConvSmem {
 };
 
 template <int D, bool I8>
-__device__ __forceinline__ void v_convert_slice(const void* __restrict__ V, int Nk,
+__device__ __forceinline__ void v_convert_slice(const Src& V, int Nk,
                                                 const unsigned int* amax_bits,
                                                 const float* __restrict__ chan,
                                                 uint8_t* __restrict__ v8t, long long ldv,
@@ -530,8 +537,10 @@ __device__ __forceinline__ void v_convert_slice(const void* __restrict__ V, int 
   float* inv_s = sm.inv_s;
   const int t0 = tblk * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row_bytes = static_cast<size_t>(D) * (I8 ? 1 : 2);
-  const uint8_t* base = static_cast<const uint8_t*>(V) + static_cast<size_t>(bh) * Nk * row_bytes;
+  constexpr int kElem = I8 ? 1 : 2;  // bytes per element
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(src_head<uint8_t>(
+      Src{V.p, V.sB * kElem, V.sH * kElem, V.sN * kElem, V.H}, bh));
+  const long long row_bytes = V.sN * kElem;
   uint4 raw[NS][4][2];
 #pragma unroll
   for (int u = 0; u < NS; ++u) {
@@ -594,7 +603,7 @@ __device__ __forceinline__ void v_convert_slice(const void* __restrict__ V, int 
 
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads) v_convert_kernel(
-    const void* __restrict__ V, int Nk, const unsigned int* amax_bits,
+    const Src V, int Nk, const unsigned int* amax_bits,
     const float* __restrict__ chan, uint8_t* __restrict__ v8t, long long ldv,
     float* __restrict__ v_scales) {
   pdl_trigger();
@@ -611,8 +620,8 @@ __global__ void __launch_bounds__(kThreads) v_convert_kernel(
 // one of the bodies the separate kernels run, so the outputs are the same.
 struct Prep1Args {
   RowsJob jq;
-  const uint16_t* K;
-  const uint16_t* V;
+  Src K;
+  Src V;
   int BHk, Nk, nkc, nvc;
   unsigned long long magic;
   unsigned long long* acc;
@@ -623,7 +632,7 @@ struct Prep1Args {
 
 struct Prep2Args {
   RowsJob jk;
-  const uint16_t* V;
+  Src V;
   int Nk, nvt;
   const unsigned int* amax;
   uint8_t* v8t;
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare1_kernel(const Prep1Args p
     return;
   }
   x -= nk;
-  v_amax_chunk<D, false>(p.V, p.Nk, p.Nk, p.amax, x % p.nvc, x / p.nvc,
+  v_amax_chunk<D, false>(p.V, p.Nk, p.amax, x % p.nvc, x / p.nvc,
                          *reinterpret_cast<VAmaxSmem<D, false>*>(sm));
 }
 
@@ -687,9 +696,7 @@ constexpr int kSmallHead = 128;  // tokens per head at most
 constexpr int kSmallWarps = 4;
 
 struct SmallPrepArgs {
-  const uint16_t* Q;
-  const uint16_t* K;
-  const uint16_t* V;
+  Src Q, K, V;
   int BHq, BHk, Nq, Nk;
   unsigned long long magic;
   int8_t* q_codes;
@@ -737,11 +744,13 @@ struct HeadLane {
   int v, rg;
   __device__ explicit HeadLane(int lane) : v(lane % VPR), rg(lane / VPR) {}
   // Rows r0, r0 + RG, ... (UNR of them) of the lane's column; zeros past N.
-  __device__ void load_rows(const uint16_t* head, int N, int r0, uint4 (&raw)[UNR]) const {
+  // rows of a head at a row stride of sN elements
+  __device__ void load_rows(const uint16_t* head, long long sN, int N, int r0,
+                            uint4 (&raw)[UNR]) const {
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int r = r0 + u * RG;
-      raw[u] = (r < N) ? *(reinterpret_cast<const uint4*>(head + static_cast<size_t>(r) * D) + v)
+      raw[u] = (r < N) ? *(reinterpret_cast<const uint4*>(head + static_cast<long long>(r) * sN) + v)
                        : make_uint4(0u, 0u, 0u, 0u);
     }
   }
@@ -750,13 +759,13 @@ struct HeadLane {
 // The channel mean of a head's N rows (exact fixed-point sums), every lane of a
 // column holding its 8 channels' means.
 template <int D>
-__device__ __forceinline__ void head_mean(const HeadLane<D>& L, const uint16_t* head, int N,
+__device__ __forceinline__ void head_mean(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                           unsigned long long magic, float (&mu)[8]) {
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
   long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
     uint4 raw[UNR];
-    L.load_rows(head, N, r0, raw);  // rows past N are zeros: they add nothing
+    L.load_rows(head, sN, N, r0, raw);  // rows past N are zeros: they add nothing
     long long s8[8];
     fix24_column_sums<UNR>(raw, s8);
 #pragma unroll
@@ -773,13 +782,13 @@ __device__ __forceinline__ void head_mean(const HeadLane<D>& L, const uint16_t* 
 
 // max |x - mu| (MINUS) or max |x| over a head's rows, over the whole warp.
 template <int D, bool MINUS>
-__device__ __forceinline__ float head_amax(const HeadLane<D>& L, const uint16_t* head, int N,
+__device__ __forceinline__ float head_amax(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                            const float (&mu)[8]) {
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
   float am = 0.f;
   for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
     uint4 raw[UNR];
-    L.load_rows(head, N, r0, raw);
+    L.load_rows(head, sN, N, r0, raw);
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       if (r0 + u * RG >= N) break;
@@ -794,13 +803,13 @@ __device__ __forceinline__ float head_amax(const HeadLane<D>& L, const uint16_t*
 
 // The head's codes rint((x [- mu]) * inv) (and carriers) at codes + row * D.
 template <int D, bool MINUS>
-__device__ __forceinline__ void head_codes(const HeadLane<D>& L, const uint16_t* head, int N,
+__device__ __forceinline__ void head_codes(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                            const float (&mu)[8], float inv, int8_t* codes,
                                            uint16_t* carrier) {
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
   for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
     uint4 raw[UNR];
-    L.load_rows(head, N, r0, raw);
+    L.load_rows(head, sN, N, r0, raw);
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int r = r0 + u * RG;
@@ -819,14 +828,14 @@ __device__ __forceinline__ void head_codes(const HeadLane<D>& L, const uint16_t*
 
 // Per-channel max |V| over a head's rows, every lane of a column holding its 8.
 template <int D>
-__device__ __forceinline__ void head_vamax(const HeadLane<D>& L, const uint16_t* head, int N,
+__device__ __forceinline__ void head_vamax(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                            float (&vm)[8]) {
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
 #pragma unroll
   for (int e = 0; e < 8; ++e) vm[e] = 0.f;
   for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
     uint4 raw[UNR];
-    L.load_rows(head, N, r0, raw);  // zero rows leave a maximum of |x| unchanged
+    L.load_rows(head, sN, N, r0, raw);  // zero rows leave a maximum of |x| unchanged
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       float x[8];
@@ -845,7 +854,7 @@ __device__ __forceinline__ void head_vamax(const HeadLane<D>& L, const uint16_t*
 // The head's V8^T rows [D][ldv] (keys past N are 0): e4m3(fp32(x * sc)) per
 // channel, through the warp's [D][TL] byte tile.
 template <int D, int TL>
-__device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* head, int N,
+__device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                          const float (&sc)[8], uint8_t* tile, uint8_t* v8t_head,
                                          long long ldv, int lane) {
   for (int i = lane; i < D * TL / 16; i += 32) reinterpret_cast<uint4*>(tile)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -853,7 +862,7 @@ __device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* h
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
   for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
     uint4 raw[UNR];
-    L.load_rows(head, N, r0, raw);
+    L.load_rows(head, sN, N, r0, raw);
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int r = r0 + u * RG;
@@ -890,37 +899,39 @@ __global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const S
   const float none[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (item < p.BHq) {  // ---- a Q head: block amax, codes, scale
     const int bh = item;
-    const uint16_t* src = p.Q + static_cast<size_t>(bh) * p.Nq * D;
-    const float g = head_amax<D, false>(L, src, p.Nq, none);
+    const uint16_t* src = src_head<uint16_t>(p.Q, bh);
+    const float g = head_amax<D, false>(L, src, p.Q.sN, p.Nq, none);
     const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
-    head_codes<D, false>(L, src, p.Nq, none, inv, p.q_codes + static_cast<size_t>(bh) * p.Nq * D, nullptr);
+    head_codes<D, false>(L, src, p.Q.sN, p.Nq, none, inv, p.q_codes + static_cast<size_t>(bh) * p.Nq * D,
+                         nullptr);
     if (lane == 0) p.q_scales[bh] = __fdiv_rn(g, 127.0f);
     return;
   }
   const int bh = item - p.BHq;
   if (bh >= p.BHk) return;
   // ---- a KV head: channel mean, K - mean codes, V maxima and e4m3 codes
-  const uint16_t* ks = p.K + static_cast<size_t>(bh) * p.Nk * D;
-  const uint16_t* vs = p.V + static_cast<size_t>(bh) * p.Nk * D;
+  const uint16_t* ks = src_head<uint16_t>(p.K, bh);
+  const uint16_t* vs = src_head<uint16_t>(p.V, bh);
   float mu[8];
-  head_mean<D>(L, ks, p.Nk, p.magic, mu);
+  head_mean<D>(L, ks, p.K.sN, p.Nk, p.magic, mu);
   if (L.rg == 0) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) p.k_mean[static_cast<size_t>(bh) * D + L.v * 8 + e] = mu[e];
   }
-  const float g = head_amax<D, true>(L, ks, p.Nk, mu);
+  const float g = head_amax<D, true>(L, ks, p.K.sN, p.Nk, mu);
   const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
   const size_t hoff = static_cast<size_t>(bh) * p.Nk * D;
-  head_codes<D, true>(L, ks, p.Nk, mu, inv, p.k_codes + hoff, p.k_carrier ? p.k_carrier + hoff : nullptr);
+  head_codes<D, true>(L, ks, p.K.sN, p.Nk, mu, inv, p.k_codes + hoff,
+                      p.k_carrier ? p.k_carrier + hoff : nullptr);
   if (lane == 0) p.k_scales[bh] = __fdiv_rn(g, 127.0f);
   float vm[8], sc[8];
-  head_vamax<D>(L, vs, p.Nk, vm);
+  head_vamax<D>(L, vs, p.V.sN, p.Nk, vm);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     sc[e] = (vm[e] > 0.f) ? __fdiv_rn(448.0f, vm[e]) : 0.f;
     if (L.rg == 0) p.v_scales[static_cast<size_t>(bh) * D + L.v * 8 + e] = __fdiv_rn(vm[e], 448.0f);
   }
-  head_v8t<D, kSmallHead>(L, vs, p.Nk, sc, tiles[warp], p.v8t + static_cast<size_t>(bh) * D * p.ldv, p.ldv,
+  head_v8t<D, kSmallHead>(L, vs, p.V.sN, p.Nk, sc, tiles[warp], p.v8t + static_cast<size_t>(bh) * D * p.ldv, p.ldv,
                           lane);
 }
 
@@ -967,7 +978,7 @@ size_t smooth_k_ws_bytes(long long BH, long long Nk, long long d) {
 }
 
 template <int D>
-static cudaError_t smooth_k_t(const uint16_t* K, int BH, int Nk, long long* ws, float* mu,
+static cudaError_t smooth_k_t(const Src& K, int BH, int Nk, long long* ws, float* mu,
                               cudaStream_t s) {
   constexpr int kWarpRows = kMeanRows * 32 / (D / 8);
   constexpr int kChunk = kMeanRows * kThreads / (D / 8);
@@ -992,7 +1003,7 @@ static cudaError_t smooth_k_t(const uint16_t* K, int BH, int Nk, long long* ws, 
                     done, mu);
 }
 
-cudaError_t launch_smooth_k(const uint16_t* K, int BH, int Nk, int d, long long* ws, float* mu,
+cudaError_t launch_smooth_k(const Src& K, int BH, int Nk, int d, long long* ws, float* mu,
                             cudaStream_t s) {
   if (Nk == 0) return cudaMemsetAsync(mu, 0, static_cast<size_t>(BH) * d * sizeof(float), s);
   if (d == 32) return smooth_k_t<32>(K, BH, Nk, ws, mu, s);
@@ -1019,15 +1030,15 @@ int prepare_launch_count(int d, int Nq, int Nk) {
   return (d <= 64 && Nq <= kSmallHead && Nk <= kSmallHead) ? 1 : 2;
 }
 
-cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t* V, int d,
+cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const Src& V, int d,
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s) {
   const int BHk = jk.BH, Nk = jk.N;
   if (BHk <= 0 || Nk <= 0) return cudaErrorInvalidValue;
   if (jq.gran != 2 || jk.gran != 2) return cudaErrorInvalidValue;
   if (prepare_launch_count(d, jq.N, Nk) == 1) {  // short heads: one warp each, one launch
     SmallPrepArgs p{};
-    p.Q = jq.X;
-    p.K = jk.X;
+    p.Q = Src{jq.X, jq.sB, jq.sH, jq.sN, jq.H};
+    p.K = Src{jk.X, jk.sB, jk.sH, jk.sN, jk.H};
     p.V = V;
     p.BHq = jq.BH;
     p.BHk = BHk;
@@ -1052,7 +1063,7 @@ cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const uint16_t*
   if (e != cudaSuccess) return e;
   Prep1Args p1{};
   p1.jq = jq;
-  p1.K = jk.X;
+  p1.K = Src{jk.X, jk.sB, jk.sH, jk.sN, jk.H};
   p1.V = V;
   p1.BHk = BHk;
   p1.Nk = Nk;
@@ -1114,19 +1125,18 @@ cudaError_t launch_quantize_rows(const RowsJob& j0, int m0, const RowsJob& j1, i
 }
 
 template <int D, bool I8>
-static cudaError_t quantize_v_impl(const void* V, const float* chan, int BH, int Nk,
+static cudaError_t quantize_v_impl(const Src& V, const float* chan, int BH, int Nk,
                                    uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws,
                                    cudaStream_t s) {
   const int nchunks = (Nk + kTokPerChunk - 1) / kTokPerChunk;
-  cudaError_t e = launch_pdl(v_amax_kernel<D, I8>, dim3(nchunks, BH), dim3(kThreads), 0, s, V, Nk,
-                             static_cast<long long>(Nk), ws);
+  cudaError_t e = launch_pdl(v_amax_kernel<D, I8>, dim3(nchunks, BH), dim3(kThreads), 0, s, V, Nk, ws);
   if (e != cudaSuccess) return e;
   const int nt = static_cast<int>((ldv + 127) / 128);
   return launch_pdl(v_convert_kernel<D, I8>, dim3(nt, BH), dim3(kThreads), 0, s, V, Nk,
                     static_cast<const unsigned int*>(ws), chan, v8t, ldv, v_scales);
 }
 
-cudaError_t launch_quantize_v(const void* V, int is_i8, const float* chan, int BH, int Nk, int d,
+cudaError_t launch_quantize_v(const Src& V, int is_i8, const float* chan, int BH, int Nk, int d,
                               uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws_amax,
                               cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(ws_amax, 0, static_cast<size_t>(BH) * d * sizeof(unsigned), s);
@@ -1153,13 +1163,11 @@ cudaError_t launch_v_code_amax(const int8_t* v_codes, int BH, int Nk, long long 
   if (e != cudaSuccess || Nk == 0 || BH == 0) return e;
   const dim3 grid((Nk + kTokPerChunk - 1) / kTokPerChunk, BH);
   unsigned int* bits = reinterpret_cast<unsigned int*>(out);
+  const Src v = dense_src(v_codes, 1, rows, d);  // (batch, head) slices of `rows` rows
   switch (d) {
-    case 32: return launch_pdl(v_amax_kernel<32, true>, grid, dim3(kThreads), 0, s,
-                               static_cast<const void*>(v_codes), Nk, rows, bits);
-    case 64: return launch_pdl(v_amax_kernel<64, true>, grid, dim3(kThreads), 0, s,
-                               static_cast<const void*>(v_codes), Nk, rows, bits);
-    default: return launch_pdl(v_amax_kernel<128, true>, grid, dim3(kThreads), 0, s,
-                               static_cast<const void*>(v_codes), Nk, rows, bits);
+    case 32: return launch_pdl(v_amax_kernel<32, true>, grid, dim3(kThreads), 0, s, v, Nk, bits);
+    case 64: return launch_pdl(v_amax_kernel<64, true>, grid, dim3(kThreads), 0, s, v, Nk, bits);
+    default: return launch_pdl(v_amax_kernel<128, true>, grid, dim3(kThreads), 0, s, v, Nk, bits);
   }
 }
 

@@ -84,12 +84,12 @@ def test_invalid_arguments_rejected_on_host(L):
                        ctypes.byref(p_bad), fake, None, None, 0, None) == 1
     # unsupported head dim
     s96 = qb.make_shape(1, 4, 2, 256, 256, 96)
-    assert L.qattn_smooth_k(fake, ctypes.byref(s96), fake, fake, 1 << 30, None) == 2
+    assert L.qattn_smooth_k(fake, None, ctypes.byref(s96), fake, fake, 1 << 30, None) == 2
     # Hq not a multiple of Hkv
     s_bad = qb.make_shape(1, 5, 2, 256, 256, 64)
-    assert L.qattn_smooth_k(fake, ctypes.byref(s_bad), fake, fake, 1 << 30, None) == 1
+    assert L.qattn_smooth_k(fake, None, ctypes.byref(s_bad), fake, fake, 1 << 30, None) == 1
     # ldv too small
-    assert L.qattn_quantize_v(fake, 0, None, ctypes.byref(s), fake, 128, fake, fake, 1 << 30,
+    assert L.qattn_quantize_v(fake, None, 0, None, ctypes.byref(s), fake, 128, fake, fake, 1 << 30,
                               None) == 1
     # int8 P ablation with a bias: unsupported
     p_i8 = qb.make_params(pv_mode=qb.PV_INT8)
@@ -101,14 +101,27 @@ def test_invalid_arguments_rejected_on_host(L):
                        ctypes.byref(p_pv), fake, None, fake, 1 << 30, None) == 1
     # bad enum
     p_bad = qb.make_params(q_gran=7)
-    assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p_bad),
-                               fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
-    # misaligned K carrier
-    assert L.qattn_quantize_qk(fake, fake, 0, None, None, ctypes.byref(s), ctypes.byref(p),
-                               fake, fake, fake, fake, vp((1 << 20) + 8), fake, 1 << 30,
+    assert L.qattn_quantize_qk(fake, None, fake, None, 0, None, None, ctypes.byref(s),
+                               ctypes.byref(p_bad), fake, fake, fake, fake, None, fake, 1 << 30,
                                None) == 1
+    # misaligned K carrier
+    assert L.qattn_quantize_qk(fake, None, fake, None, 0, None, None, ctypes.byref(s),
+                               ctypes.byref(p), fake, fake, fake, fake, vp((1 << 20) + 8), fake,
+                               1 << 30, None) == 1
     # workspace too small
-    assert L.qattn_smooth_k(fake, ctypes.byref(s), fake, fake, 16, None) == 5
+    assert L.qattn_smooth_k(fake, None, ctypes.byref(s), fake, fake, 16, None) == 5
+    # input strides: the last must be 1, the others multiples of 16 bytes;
+    # int8 cache K codes are dense only
+    i64x4 = ctypes.c_int64 * 4
+    for bad in (i64x4(256 * 64, 256 * 64, 64, 2), i64x4(256 * 64, 256 * 64, 60, 1),
+                i64x4(-64, 256 * 64, 64, 1)):
+        assert L.qattn_smooth_k(fake, bad, ctypes.byref(s), fake, fake, 1 << 30, None) == 1
+        assert L.qattn_quantize_v(fake, bad, 0, None, ctypes.byref(s), fake, 256, fake, fake,
+                                  1 << 30, None) == 1
+    packed = i64x4(256 * 3 * 2 * 64, 64, 3 * 2 * 64, 1)  # [B][N][3][H][d] viewed as [B][H][N][d]
+    assert L.qattn_quantize_qk(fake, packed, fake, packed, 2, None, fake, ctypes.byref(s),
+                               ctypes.byref(p), fake, fake, None, fake, None, fake, 1 << 30,
+                               None) == 2
     # empty problem: ok, nothing launched
     s0 = qb.make_shape(0, 4, 2, 256, 256, 64)
     assert L.qattn_fwd(None, None, None, None, None, None, 0, None, None, ctypes.byref(s0),
