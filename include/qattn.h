@@ -46,6 +46,11 @@
  *   - Kernels never wait forever: a pipeline wait that exceeds its time limit
  *     makes the kernel record QATTN_ERR_TIMEOUT in the device error word and
  *     return early; qattn_get_error() reports it.
+ *   - Launch log: with the environment variable QATTN_LOG set (to anything
+ *     but "" or "0"; read once, at the library's first call), every call that launches
+ *     work prints one line to stderr, "[qattn] <entry point> <shape>: <the
+ *     kernels it launches>", and qattn_fwd_kernel_choice prints its answer.
+ *     Unset, the library prints nothing.
  */
 #ifndef QATTN_H_
 #define QATTN_H_

@@ -3,6 +3,8 @@
 // No entry point allocates device memory; every failure becomes a status.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -112,6 +114,32 @@ EncodeTiledFn encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// QATTN_LOG set to anything but "" or "0": every call that reaches its launch
+// (and the host-only kernel-choice queries) prints one line on stderr naming
+// the kernels it runs and the problem shape.  Read once per process.
+bool log_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("QATTN_LOG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+#define QATTN_LOG_LINE(...)                         \
+  do {                                              \
+    if (log_on()) {                                 \
+      std::fprintf(stderr, "[qattn] " __VA_ARGS__); \
+      std::fputc('\n', stderr);                     \
+    }                                               \
+  } while (0)
+
+const char* shape_str(const qattn_shape* s, char* buf, size_t n) {
+  std::snprintf(buf, n, "B=%lld Hq=%lld Hkv=%lld Nq=%lld Nk=%lld d=%lld", static_cast<long long>(s->B),
+                static_cast<long long>(s->Hq), static_cast<long long>(s->Hkv),
+                static_cast<long long>(s->Nq), static_cast<long long>(s->Nk),
+                static_cast<long long>(s->d));
+  return buf;
+}
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool valid_d(int64_t d) { return d == 32 || d == 64 || d == 128; }
@@ -310,6 +338,9 @@ qattn_status qattn_smooth_k(const uint16_t* K, const int64_t* k_strides, const q
   if (!make_src(K, k_strides, shape->Hkv, shape->Nk, shape->d, 2, &ks)) return QATTN_ERR_INVALID_ARG;
   const size_t need = ws_smooth(shape);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return QATTN_ERR_WORKSPACE;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_smooth_k %s strided=%d: k_mean kernel (exact fixed-point channel sums)",
+                 shape_str(shape, sb, sizeof sb), k_strides != nullptr);
   return from_cuda(qattn::launch_smooth_k(ks, static_cast<int>(shape->B * shape->Hkv),
                                           static_cast<int>(shape->Nk), static_cast<int>(shape->d),
                                           static_cast<long long*>(workspace), k_mean,
@@ -373,6 +404,9 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const int64_t* q_strides, cons
                 : params->k_gran == QATTN_GRAN_TENSOR ? 1
                 : params->k_gran == QATTN_GRAN_HEAD   ? shape->B * shape->Hkv
                                                       : shape->B * shape->Hkv * nkb;
+    char sb[128];
+    QATTN_LOG_LINE("qattn_quantize_qk %s int8 cache: quant_rows_kernel (Q with K's channel scales)%s",
+                   shape_str(shape, sb, sizeof sb), k_carrier ? " + codes_to_f16_kernel" : "");
     cudaError_t e = qattn::launch_quantize_rows(jq, 2, jk, 0, d, s);
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
     if (k_carrier && shape->Nk > 0) {
@@ -400,6 +434,11 @@ qattn_status qattn_quantize_qk(const uint16_t* Q, const int64_t* q_strides, cons
     jk.nblk = static_cast<int>(nkb);
     jk.BH = B * Hkv;
   }
+  char sb[128];
+  QATTN_LOG_LINE("qattn_quantize_qk %s granules q=%d k=%d mean=%d strided=%d: quant_rows_kernel, %d pass(es)",
+                 shape_str(shape, sb, sizeof sb), params->q_gran, params->k_gran, k_mean != nullptr,
+                 q_strides != nullptr || k_strides != nullptr,
+                 (params->q_gran != QATTN_GRAN_BLOCK || (shape->Nk > 0 && params->k_gran != QATTN_GRAN_BLOCK)) ? 2 : 1);
   return from_cuda(qattn::launch_quantize_rows(jq, 0, jk, k_mean ? 1 : 0, d, s));
 }
 
@@ -463,6 +502,11 @@ qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const ui
   jk.carrier = k_carrier;
   jk.nblk = static_cast<int>((shape->Nk + 127) / 128);
   jk.BH = B * Hkv;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_prepare %s: %s", shape_str(shape, sb, sizeof sb),
+                 qattn::prepare_launch_count(d, jq.N, jk.N) == 1
+                     ? "prepare_small_kernel (one warp per head, one launch)"
+                     : "prepare1_kernel + prepare2_kernel (two launches)");
   return from_cuda(qattn::launch_prepare(jq, jk, vs, d, v8t, ldv, v_scales, workspace,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -485,6 +529,9 @@ qattn_status qattn_quantize_v(const void* V, const int64_t* v_strides, qattn_dty
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   qattn::Src vs;
   if (!make_src(V, v_strides, shape->Hkv, shape->Nk, shape->d, i8 ? 1 : 2, &vs)) return QATTN_ERR_INVALID_ARG;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_quantize_v %s %s strided=%d: v_amax_kernel + v_convert_kernel",
+                 shape_str(shape, sb, sizeof sb), i8 ? "int8 codes" : "bf16", v_strides != nullptr);
   return from_cuda(qattn::launch_quantize_v(vs, i8 ? 1 : 0, v_chan_scale,
                                             static_cast<int>(shape->B * shape->Hkv),
                                             static_cast<int>(shape->Nk), static_cast<int>(shape->d),
@@ -549,6 +596,16 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
   a.out_bf16 = params->out_dtype == QATTN_BF16;
   a.lse = lse;
   a.err = err;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_fwd %s causal=%d pos0=%lld bias=%d pv=%s out=%s: %s%s", shape_str(shape, sb, sizeof sb),
+                 params->causal, static_cast<long long>(pos0), bias != nullptr,
+                 a.pv_int8 ? "int8" : "e4m3", a.out_bf16 ? "bf16" : "fp32",
+                 use_short ? (qattn::attn_short_eligible(a) && shape->Nq <= qattn::kWindowMax &&
+                                      shape->Nk <= qattn::kWindowMax
+                                  ? "warp-level kernel (attn_window_kernel or attn_short_kernel)"
+                                  : "warp-level kernel (attn_short_kernel)")
+                           : "persistent tcgen05 kernel (attn_fwd_kernel), one CTA per SM",
+                 use_short || k_carrier ? "" : " after codes_to_f16_kernel (K carriers in the workspace)");
   if (use_short) return from_cuda(qattn::launch_attn_short(a, q_codes, k_codes, v8t, ldv, s));
   const uint16_t* kc16 = k_carrier;
   if (!kc16) {  // convert the K codes into the workspace (checked above)
@@ -634,6 +691,9 @@ qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const in
       !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_codes, shape->d, shape->Nk, planes,
                  shape->d, static_cast<uint32_t>(shape->d), 128, swz, cap))
     return QATTN_ERR_CUDA;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_decode %s capacity=%lld: decode kernel over key chunks + chunk combine",
+                 shape_str(shape, sb, sizeof sb), static_cast<long long>(cap));
   return from_cuda(qattn::launch_decode(tk, tv, a, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -710,6 +770,8 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
   a.out_bf16 = params->out_dtype == QATTN_BF16;
   a.lse = lse;
   a.ws = workspace;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_fwd_exact24 %s: q_split_kernel + exact24_attn_kernel", shape_str(shape, sb, sizeof sb));
   return from_cuda(qattn::launch_exact24(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -735,6 +797,8 @@ qattn_status qattn_fwd_intsoftmax(const int8_t* q_codes, const float* q_scale,
                                           : static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape->d)));
   unsigned int* err = error_word();
   if (!err) return QATTN_ERR_CUDA;
+  char sb[128];
+  QATTN_LOG_LINE("qattn_fwd_intsoftmax %s: intsm_attn_kernel", shape_str(shape, sb, sizeof sb));
   return from_cuda(qattn::launch_intsoftmax(
       static_cast<int>(shape->B), static_cast<int>(shape->Hq), static_cast<int>(shape->Hkv),
       static_cast<int>(shape->Nq), static_cast<int>(shape->Nk), static_cast<int>(shape->d), sm, q_codes,
@@ -758,6 +822,9 @@ qattn_status qattn_kv_append(const void* K_new, const void* V_new, int64_t B, in
                         static_cast<const void*>(k_mean), static_cast<const void*>(v_code_amax)})
     if (reinterpret_cast<uintptr_t>(f) & 3u) return QATTN_ERR_INVALID_ARG;
   if (T == 0) return QATTN_OK;
+  QATTN_LOG_LINE("qattn_kv_append B=%lld Hkv=%lld T=%lld d=%lld pos=%lld capacity=%lld: kv_append_kernel",
+                 static_cast<long long>(B), static_cast<long long>(Hkv), static_cast<long long>(T),
+                 static_cast<long long>(d), static_cast<long long>(pos), static_cast<long long>(capacity));
   return from_cuda(qattn::launch_kv_append(
       static_cast<const uint16_t*>(K_new), static_cast<const uint16_t*>(V_new),
       static_cast<int>(B * Hkv), static_cast<int>(d), static_cast<int>(T), static_cast<int>(pos),
@@ -780,7 +847,11 @@ qattn_status qattn_kv_header_init(const int8_t* v_codes, int64_t B, int64_t Hkv,
 
 int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params) {
   if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
-  return fwd_choice(shape, params);
+  const int c = fwd_choice(shape, params);
+  char sb[128];
+  QATTN_LOG_LINE("qattn_fwd_kernel_choice %s causal=%d: %s", shape_str(shape, sb, sizeof sb),
+                 params->causal, c == QATTN_FWD_SHORT ? "warp-level" : c < 0 ? "rejected" : "persistent tcgen05");
+  return c;
 }
 
 int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params) {

@@ -229,3 +229,35 @@ def test_extra_modes_arguments_rejected_on_host(L):
     assert e24(cache, Q=vp((1 << 20) + 2)) == 1                        # Q alignment
     assert e24(cache, ws=None, ws_bytes=0) == 5                        # workspace
     assert e24(cache, ws_bytes=16) == 5
+
+
+_LOG_PROBE = """
+from quantized_attention_gb300 import binding as qb
+s = qb.make_shape(2, 4, 2, 300, 300, 128)
+print(qb.fwd_kernel_choice(s, qb.make_params(causal=True)))
+print(qb.fwd_kernel_choice(qb.make_shape(1, 4, 2, 49, 49, 64), qb.make_params()))
+"""
+
+
+@pytest.mark.parametrize("value", ["1", "", "0", None])
+def test_launch_log_follows_the_environment(L, value):
+    """QATTN_LOG set: one "[qattn]" line on stderr per call naming the entry
+    point, the shape and the kernel; unset, "" or "0": nothing on stderr."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("QATTN_LOG", None)
+    if value is not None:
+        env["QATTN_LOG"] = value
+    r = subprocess.run([sys.executable, "-c", _LOG_PROBE], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == ["1", "2"]
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[qattn]")]
+    if value == "1":
+        assert len(lines) == 2, r.stderr
+        assert "qattn_fwd_kernel_choice B=2 Hq=4 Hkv=2 Nq=300 Nk=300 d=128 causal=1" in lines[0]
+        assert lines[0].endswith("persistent tcgen05")
+        assert lines[1].endswith("warp-level")
+    else:
+        assert lines == [], r.stderr
