@@ -208,21 +208,29 @@ qattn_status qattn_quantize_v(const void* V, const int64_t* v_strides, qattn_dty
                               float* v_scales, void* workspace, size_t workspace_bytes,
                               qattn_stream_t stream);
 
-/* a1-a3 in one or two launches, for bf16 Q, K and V with block granules: the
- * same outputs, bit for bit, as qattn_smooth_k, then qattn_quantize_qk
- * (k_mean given, k_dtype QATTN_BF16), then qattn_quantize_v (QATTN_BF16).
- * Launch 1 quantizes Q and reduces K's channel sums and V's channel maxima
- * (three independent jobs in one grid); launch 2 quantizes K - mean (with the
- * fp16 carriers when k_carrier is not NULL) and writes V's transposed e4m3
- * codes.  Heads of at most 128 tokens with d <= 64 (e.g. Swin windows): one
- * launch, one warp per head.  The ZINC post's recipe runs these three steps
- * before the attention kernel; fusing them is this library's own step (fewer
- * launches, one read of Q).
+/* a1-a3 in one or two launches, for bf16 Q, K and V: the same outputs, bit
+ * for bit, as qattn_smooth_k, then qattn_quantize_qk (k_mean given, k_dtype
+ * QATTN_BF16), then qattn_quantize_v (QATTN_BF16).
+ * Block granules: launch 1 quantizes Q and reduces K's channel sums and V's
+ * channel maxima (three independent jobs in one grid); launch 2 quantizes
+ * K - mean (with the fp16 carriers when k_carrier is not NULL) and writes V's
+ * transposed e4m3 codes.  Heads of at most 128 tokens with d <= 64 (e.g. Swin
+ * windows): one launch, one warp per head.
+ * Tensor granules (q_gran = k_gran = QATTN_GRAN_TENSOR; d in {32, 64}, Nk <=
+ * 256, e.g. ViT's 197 tokens): launch 1, one warp per head, reduces max |Q|
+ * and, per KV head, the channel mean, max |K - mean| and V's channel maxima,
+ * and writes V's e4m3 codes; launch 2 writes the Q and K codes at the two
+ * tensor scales -- two launches where the three calls take five.
+ * The ZINC post's recipe runs these three steps before the attention kernel;
+ * fusing them is this library's own step (fewer launches, fewer reads).
  *   Q            bf16 [B][Hq][Nq][d];  K, V  bf16 [B][Hkv][Nk][d]
  *   q_strides, k_strides, v_strides  as in the conventions (NULL = dense)
  *   k_mean (out) fp32 [B][Hkv][d]; the other outputs as for the three calls
- *   params       q_gran = k_gran = QATTN_GRAN_BLOCK, else QATTN_ERR_UNSUPPORTED
- *                (use the three calls); Nk >= 1, else QATTN_ERR_UNSUPPORTED
+ *   params       q_gran = k_gran = QATTN_GRAN_BLOCK, or both
+ *                QATTN_GRAN_TENSOR within the limits above, else
+ *                QATTN_ERR_UNSUPPORTED (use the three calls);
+ *                Nk >= 1, else QATTN_ERR_UNSUPPORTED
+ *                (qattn_prepare_launches answers which, on the host)
  *   ldv          >= qattn_v_ld(Nk), multiple of 16
  *   workspace    at least qattn_workspace_size() bytes.
  */

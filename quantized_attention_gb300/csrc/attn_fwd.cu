@@ -3,18 +3,18 @@
 // Persistent kernel, one CTA per SM.  A work item is one (batch, head) and two
 // consecutive 128-row query tiles (t0, t1); items are handed out heaviest
 // first (causal) in a snake order over the CTAs.  Warp roles (12 warps):
-//   warp 0      lane 0 issues every TMA load: the item's two int8 Q tiles, a
+//   warp 0      lane 0 issues every TMA load: the item's slot (its decoded
+//               indices and scales, see ItemSlot), its two int8 Q tiles, a
 //               ring of K stages and a ring of V^T stages;
 //   warp 1      owns the 512 TMEM columns; lane 0 issues the MMAs of tile t0;
 //   warp 2      lane 0 issues the MMAs of tile t1;
-//   warp 3      idle;
+//   warp 3      widens each item's int8 Q codes to exact fp16 in shared
+//               memory (q_conv), running ahead of the softmax warps;
 //   warps 4-7   softmax of tile t0, warps 8-11 softmax of tile t1 (one query
-//               row per thread, row r = TMEM lane r).
+//               row per thread, row r = TMEM lane r), then the epilogue.
 // TMEM: S_t at columns [128 t, 128 t + 128), O_t at [256 + 128 t, ...).
-// Shared memory holds the e4m3 P_t tiles the PV MMAs read.
-//
-// Per item, each softmax warpgroup first widens its tile's int8 Q codes to
-// exact fp16 in shared memory (q_conv); K arrives as fp16 carriers.
+// Shared memory holds the e4m3 P_t tiles the PV MMAs read; the epilogue
+// stages O through them for TMA stores.  K arrives as fp16 carriers.
 // Per tile t and key block j:
 //   softmax(t, j) loads S_t(j) from TMEM and at once releases it (s_free), so
 //   the tile's MMA thread issues QK(t, j+1) -- S_t = Q_t . K_{j+1}^T,
@@ -77,7 +77,11 @@ struct Cfg {
   static constexpr int kQ8Bytes = kBM * D;
   static constexpr int kOffQ8 = kOffP + 2 * kPPlanes * kPBytes;
   static constexpr int kOffBar = kOffQ8 + (kQ8InPlace ? 0 : kQS * 2 * kQ8Bytes);
-  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
+  // Item slots (a ring of 2): the item's decoded indices, its Q scales per
+  // tile, K's first block scale and V's D channel scales (see ItemSlot).
+  static constexpr int kSlotBytes = 64 + 4 * D;
+  static constexpr int kOffSlot = kOffBar + 512;
+  static constexpr int kSmemBytes = kOffSlot + 2 * kSlotBytes + 1024;  // + alignment slack
   static_assert(kQTileBytes % 1024 == 0 && kKBytes % 1024 == 0 && kVBytes % 1024 == 0,
                 "tile alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -167,10 +171,13 @@ __device__ __forceinline__ void convert_q_tile(uint32_t tile, uint32_t codes, in
   }
 }
 
+__device__ __forceinline__ const float* scale_ptr(const float* s, int gran, int bh, int nblk, int blk) {
+  if (gran == 0) return s;
+  if (gran == 1) return s + bh;
+  return s + static_cast<size_t>(bh) * nblk + blk;
+}
 __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int nblk, int blk) {
-  if (gran == 0) return s[0];
-  if (gran == 1) return s[bh];
-  return s[static_cast<size_t>(bh) * nblk + blk];
+  return *scale_ptr(s, gran, bh, nblk, blk);
 }
 
 // Barrier slots.
@@ -186,8 +193,21 @@ enum {
   kBarPFull = 24,   // [2]  P_t written, O_t rescaled (128 threads)
   kBarPVDone = 26,  // [2]  PV(t, j) finished (MMA commit)
   kBarDrain = 28,   // [2]  every MMA of the QK / PV issuer done (teardown)
-  kBarQConv = 30,   // [2]  Q_t widened to fp16 (128 threads)
-  kNumBars = 32
+  kBarQConv = 30,      // [2][2]  Q stage s, tile t widened to fp16 (the Q-widening warp)
+  kBarSlotFull = 34,   // [2]  item slot written and its scales landed
+  kBarSlotEmpty = 36,  // [2]  item slot read by every softmax thread (256 threads)
+  kNumBars = 38
+};
+
+// Header of an item slot in shared memory; V's channel scales follow at byte
+// 64.  The TMA thread writes the header and copies the scales in (cp.async for
+// the three single floats, the bulk engine for V's), then arrives on the
+// slot's full barrier, so the softmax warps neither decode the item nor wait
+// for global loads of scales on their own critical path.
+struct ItemSlot {
+  int bq, bkv, h, q0, nb0, nb1;
+  float sq[2];  // the Q scale of each tile's first row block (0 if the tile is empty)
+  float sk0;    // the scale of K's first block
 };
 
 // One work item: (batch, head) x a pair of query tiles.
@@ -313,7 +333,8 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
 template <int D, bool BIAS, bool PQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a, int n_items) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnArgs a, int n_items) {
   using C = Cfg<D, PQ>;
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
@@ -332,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return C::kQ8InPlace ? sQ(qs, t) + C::kQTileBytes / 2
                          : base + C::kOffQ8 + (qs * 2 + t) * C::kQ8Bytes;
   };
+  auto slot_hdr = [&](int sl) {
+    return reinterpret_cast<ItemSlot*>(smem + C::kOffSlot + sl * C::kSlotBytes);
+  };
+  auto sSlot = [&](int sl) { return base + C::kOffSlot + sl * C::kSlotBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -341,13 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool softmax_side = (i >= kBarSFree && i < kBarSFree + 2) ||
-                                (i >= kBarPFull && i < kBarPFull + 2) ||
-                                (i >= kBarQConv && i < kBarQConv + 2);
+                                (i >= kBarPFull && i < kBarPFull + 2);
       // Q, K and V stages are freed by both tiles' issuers.
       const bool shared_stage = (i >= kBarQEmpty && i < kBarQEmpty + 2) ||
                                 (i >= kBarKEmpty && i < kBarKEmpty + 4) ||
                                 (i >= kBarVEmpty && i < kBarVEmpty + 4);
-      mbar_init(bar(i), softmax_side ? kBM : shared_stage ? 2 : 1);
+      const bool slot_empty = i >= kBarSlotEmpty && i < kBarSlotEmpty + 2;
+      mbar_init(bar(i), slot_empty ? 2 * kBM : softmax_side ? kBM : shared_stage ? 2 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -371,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int last_q[2] = {-1, -1}, last_k[4] = {-1, -1, -1, -1}, last_v[4] = {-1, -1, -1, -1};
+      int last_slot[2] = {-1, -1};
+      const int nqb = (a.Nq + kBM - 1) / kBM, nkb = (a.Nk + kBN - 1) / kBN;
       uint32_t kc = 0, vc = 0;
       int i = 0;
       bool ok = true;
@@ -398,6 +425,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w = item_index(k, cta, G, n_items);
         if (w < 0) continue;
         const Item it = decode_item(w, a, n_pairs);
+        {  // the item's slot: header, Q / K scales, V's channel scales
+          const int sl = i & 1;
+          if (i >= 2 && !(ok = mbar_wait(bar(kBarSlotEmpty + sl), ((i >> 1) - 1) & 1, abort_flag,
+                                         a.err, kErrTimeout)))
+            break;
+          ItemSlot* hs = slot_hdr(sl);
+          hs->bq = it.bq;
+          hs->bkv = it.bkv;
+          hs->h = it.h;
+          hs->q0 = it.q0;
+          hs->nb0 = it.nb[0];
+          hs->nb1 = it.nb[1];
+          for (int tt = 0; tt < 2; ++tt) {
+            if (it.nb[tt] > 0)
+              cp_async4(sSlot(sl) + offsetof(ItemSlot, sq) + 4 * tt,
+                        scale_ptr(a.q_scales, a.q_gran, it.bq, nqb, it.q0 / kBM + tt));
+            else
+              hs->sq[tt] = 0.f;
+          }
+          if (it.nb[0] > 0 || it.nb[1] > 0)
+            cp_async4(sSlot(sl) + offsetof(ItemSlot, sk0), scale_ptr(a.k_scales, a.k_gran, it.bkv, nkb, 0));
+          else
+            hs->sk0 = 0.f;
+          cp_async_mbar_arrive(bar(kBarSlotFull + sl));
+          mbar_arrive_expect_tx(bar(kBarSlotFull + sl), 4 * D);
+          bulk_g2s(sSlot(sl) + 64, a.v_scales + static_cast<size_t>(it.bkv) * D, 4 * D,
+                   bar(kBarSlotFull + sl));
+          last_slot[sl] = i;
+        }
         const int qs = i % C::kQS;
         if (i >= C::kQS &&
             !(ok = mbar_wait(bar(kBarQEmpty + qs), ((i / C::kQS) - 1) & 1, abort_flag, a.err,
@@ -426,8 +482,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < C::kNV; ++st)
         if (last_v[st] >= 0)
           mbar_wait(bar(kBarVFull + st), (last_v[st] / C::kNV) & 1, &never, a.err, kErrTimeout);
+      for (int sl = 0; sl < 2; ++sl)
+        if (last_slot[sl] >= 0)
+          mbar_wait(bar(kBarSlotFull + sl), (last_slot[sl] >> 1) & 1, &never, a.err, kErrTimeout);
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ Q widening
+    // Per item, as soon as its int8 Q codes land, the warp widens the rows of
+    // each tile with keys to visit (lane l: rows l, l + 32, l + 64, l + 96)
+    // and releases the tile's first QK (q_conv).  It runs ahead of the
+    // softmax warps, so the next item's first QK is issued under this item's
+    // last key block and epilogue.
+    int i = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * G < n_items; ++k) {
+      const int w = item_index(k, cta, G, n_items);
+      if (w < 0) continue;
+      const Item it = decode_item(w, a, n_pairs);
+      const int qs = i % C::kQS;
+      if (it.nb[0] > 0 || it.nb[1] > 0) {
+        ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      // One q_conv phase per item and stage; a tile without keys is not
+      // widened.  The barrier of stage s completes item i + kQS's phase only
+      // after both issuers freed the stage from item i (q_empty), that is
+      // after they waited for item i's phase: never two phases ahead.
+      for (int t = 0; t < 2; ++t) {
+        if (it.nb[t] > 0) {
+#pragma unroll 1
+          for (int rr = lane; rr < kBM; rr += 32) convert_q_tile<D>(sQ(qs, t), sQ8(qs, t), rr);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQConv + 2 * qs + t));
+      }
+      ++i;
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
   } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
@@ -445,7 +541,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = warp - 1;
       uint32_t kvc = 0;          // K (and V) blocks of earlier items
       uint32_t nqk = 0, npv = 0;  // QKs / PVs issued for this tile
-      uint32_t nqc = 0;          // Q tiles widened for this tile
       int i = 0;
       bool ok = true;
       for (int k = 0; ok && k * G < n_items; ++k) {
@@ -469,11 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (nqk > 0 &&
                   !(ok = mbar_wait(bar(kBarSFree + t), (nqk - 1) & 1, abort_flag, a.err, kErrTimeout)))
                 break;
-              if (b == 0) {  // the item's Q_t, widened by the tile's softmax warps
-                if (!(ok = mbar_wait(bar(kBarQConv + t), nqc & 1, abort_flag, a.err, kErrTimeout)))
-                  break;
-                ++nqc;
-              }
+              if (b == 0 &&  // the item's Q_t, widened by warp 3
+                  !(ok = mbar_wait(bar(kBarQConv + 2 * qs + t), (i / C::kQS) & 1, abort_flag, a.err,
+                                   kErrTimeout)))
+                break;
               tc_fence_after();
               issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st));
               mma_commit(bar(kBarSFull + t));
@@ -518,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
     const uint32_t prow = sP(t) + r * 128;
     const uint32_t sw = r & 7;
-    const int nqb = (a.Nq + kBM - 1) / kBM, nkb = (a.Nk + kBN - 1) / kBN;
+    const int nkb = (a.Nk + kBN - 1) / kBN;
     uint32_t sc = 0, pvc = 0;
     bool ok = true;
     int i = -1;  // items of this CTA so far
@@ -526,12 +620,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = item_index(k, cta, G, n_items);
       if (w < 0) continue;
       ++i;
-      const Item it = decode_item(w, a, n_pairs);
+      // the item as the TMA thread decoded it, with its scales (item slot)
+      const int sl = i & 1;
+      ok = mbar_wait(bar(kBarSlotFull + sl), (i >> 1) & 1, abort_flag, a.err, kErrTimeout);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const ItemSlot* hs = slot_hdr(sl);
+      Item it;
+      it.bq = hs->bq;
+      it.bkv = hs->bkv;
+      it.h = hs->h;
+      it.q0 = hs->q0;
+      it.nb[0] = hs->nb0;
+      it.nb[1] = hs->nb1;
       const int q0t = it.q0 + t * kBM;
       const int qi = q0t + r;
       const int nbt = it.nb[t];
-      const size_t row = static_cast<size_t>(it.bq) * a.Nq + qi;
       if (nbt == 0) {  // no visible key for any row of this tile: output 0
+        mbar_arrive(bar(kBarSlotEmpty + sl));
+        const size_t row = static_cast<size_t>(it.bq) * a.Nq + qi;
         if (qi < a.Nq) {
           for (int cidx = 0; cidx < D; ++cidx) {
             if (a.out_bf16)
@@ -543,20 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      // the item's scales first: their loads overlap the Q widening
-      const float sq = scale_of(a.q_scales, a.q_gran, it.bq, nqb, q0t / kBM);
-      float sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, 0);
-      {  // widen this tile's Q codes for the item's QK MMAs
-        const int qs = i % C::kQS;
-        ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        convert_q_tile<D>(sQ(qs, t), sQ8(qs, t), r);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(kBarQConv + t));
-      }
+      const float sq = hs->sq[t];
+      float sk_next = hs->sk0;
       const int lim = a.causal ? min(a.Nk - 1, a.pos0 + qi) : a.Nk - 1;  // last visible key
       const int tile_lim = a.causal ? a.pos0 + q0t : a.Nk;  // blocks ending <= this need no causal mask
       const float* brow = nullptr;
@@ -614,6 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
+        if (j == 0) {  // an earlier item's output store has read P_t's rows
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
 #pragma unroll
         for (int ch = 0; ch < kBN / 16; ++ch) {
           const uint32_t addr = prow + ((static_cast<uint32_t>(ch) ^ sw) << 4);
@@ -650,11 +751,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarPFull + t));
       }
       if (!ok) break;
-      // V scales of the first 32 channels, loaded while the last PV runs
-      const float4* sv4 = reinterpret_cast<const float4*>(a.v_scales + static_cast<size_t>(it.bkv) * D);
-      float4 svn[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) svn[q] = sv4[q];
       ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);  // last PV
       ++pvc;
       if (!__all_sync(0xffffffffu, ok)) {
@@ -663,29 +759,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // With the TMA store, the warp's 32 rows of O go out in 128-byte row
+      // chunks (64 bf16 or 32 fp32 columns) staged in the warp's 32 rows of
+      // P_t (free once the last PV is done; 128B swizzle as for P): one store
+      // per warp and chunk writes whole lines, where a thread-per-row store
+      // would touch 32 lines per instruction.  Rows past Nq are not written.
+      const bool issue = lane == 0 && q0t + wq * 32 < a.Nq;
+      const size_t row = static_cast<size_t>(it.bq) * a.Nq + qi;
+      const int yo = q0t + wq * 32;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        float svc[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          svc[4 * q] = svn[q].x;
-          svc[4 * q + 1] = svn[q].y;
-          svc[4 * q + 2] = svn[q].z;
-          svc[4 * q + 3] = svn[q].w;
-        }
-        if (cc + 1 < D / 32) {  // the next chunk's scales load under this chunk's TMEM read
-#pragma unroll
-          for (int q = 0; q < 8; ++q) svn[q] = sv4[8 * (cc + 1) + q];
-        }
         uint32_t o[32];
         tmem_ld32(tO + lane_base + cc * 32, o);
-        tmem_wait_ld();
-        if (qi < a.Nq) {
-          float v[32];
+        float svc[32];  // V's channel scales from the item slot (one broadcast read per 4)
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(o[q]) * (svc[q] * inv_l);
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v4 = lds128(sSlot(sl) + 64 + (cc * 32 + 4 * q) * 4);
+          svc[4 * q] = __uint_as_float(v4.x);
+          svc[4 * q + 1] = __uint_as_float(v4.y);
+          svc[4 * q + 2] = __uint_as_float(v4.z);
+          svc[4 * q + 3] = __uint_as_float(v4.w);
+        }
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(o[q]) * (svc[q] * inv_l);
+        if (!a.out_bf16 || D >= 64) {  // TMA stores (all but bf16 rows of 64 bytes)
+          const bool first_half = !a.out_bf16 || (cc & 1) == 0;  // a new 128-byte chunk starts
+          if (first_half && cc > 0) {  // the previous chunk's store has read the stage
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
           if (a.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + cc * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t wv[4];
@@ -694,18 +799,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
                 wv[e] = *reinterpret_cast<const uint32_t*>(&pr);
               }
-              dst[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              const uint32_t c16 = static_cast<uint32_t>((cc & 1) * 4 + q);
+              st_shared_v4(prow + ((c16 ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + row * D + cc * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(prow + ((static_cast<uint32_t>(q) ^ sw) << 4), __float_as_uint(v[4 * q]),
+                           __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                           __float_as_uint(v[4 * q + 3]));
+          }
+          if (!a.out_bf16 || (cc & 1) == 1) {  // the 128-byte chunk is complete: store it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (issue) {
+              tma_store_3d(&tmO, prow - (static_cast<uint32_t>(lane) << 7), a.out_bf16 ? (cc / 2) * 64 : cc * 32, yo, it.bq);
+              bulk_commit_group();
+            }
+          }
+        } else if (qi < a.Nq) {  // bf16 rows of 64 bytes (D = 32): direct stores
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+              wv[e] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            dst[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
       }
+      mbar_arrive(bar(kBarSlotEmpty + sl));  // the slot's last read by this thread
       if (a.lse && qi < a.Nq)
         a.lse[row] = (l > 0.f) ? (m + __log2f(l) - (PQ ? kLog2_127 : kLog2_448)) * kLn2 : kNegInf;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
     if (!ok) *abort_flag = 1;
   }
   tc_fence_before();
@@ -806,7 +936,7 @@ __global__ void __launch_bounds__(160, 1)
 
 template <int D, bool BIAS, bool PQ = false>
 cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const AttnArgs& a, cudaStream_t s) {
+                          const CUtensorMap& to, const AttnArgs& a, cudaStream_t s) {
   const int smem = Cfg<D, PQ>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BIAS, PQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -816,7 +946,7 @@ cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   if (n_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
   return launch_pdl(attn_fwd_kernel<D, BIAS, PQ>, dim3(grid), dim3(kThreads), smem, s, tq, tk, tv,
-                    a, static_cast<int>(n_items));
+                    to, a, static_cast<int>(n_items));
 }
 
 template <int D>
@@ -834,19 +964,19 @@ cudaError_t launch_dbg_t(const CUtensorMap& tq, const CUtensorMap& tk, int B, in
 }  // namespace
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& a, cudaStream_t s) {
+                            const CUtensorMap& to, const AttnArgs& a, cudaStream_t s) {
   if (a.pv_int8) {  // the int8 P ablation (no bias)
     switch (a.d) {
-      case 32: return launch_attn_t<32, false, true>(tq, tk, tv, a, s);
-      case 64: return launch_attn_t<64, false, true>(tq, tk, tv, a, s);
-      default: return launch_attn_t<128, false, true>(tq, tk, tv, a, s);
+      case 32: return launch_attn_t<32, false, true>(tq, tk, tv, to, a, s);
+      case 64: return launch_attn_t<64, false, true>(tq, tk, tv, to, a, s);
+      default: return launch_attn_t<128, false, true>(tq, tk, tv, to, a, s);
     }
   }
   const bool bias = a.bias != nullptr;
   switch (a.d) {
-    case 32: return bias ? launch_attn_t<32, true>(tq, tk, tv, a, s) : launch_attn_t<32, false>(tq, tk, tv, a, s);
-    case 64: return bias ? launch_attn_t<64, true>(tq, tk, tv, a, s) : launch_attn_t<64, false>(tq, tk, tv, a, s);
-    default: return bias ? launch_attn_t<128, true>(tq, tk, tv, a, s) : launch_attn_t<128, false>(tq, tk, tv, a, s);
+    case 32: return bias ? launch_attn_t<32, true>(tq, tk, tv, to, a, s) : launch_attn_t<32, false>(tq, tk, tv, to, a, s);
+    case 64: return bias ? launch_attn_t<64, true>(tq, tk, tv, to, a, s) : launch_attn_t<64, false>(tq, tk, tv, to, a, s);
+    default: return bias ? launch_attn_t<128, true>(tq, tk, tv, to, a, s) : launch_attn_t<128, false>(tq, tk, tv, to, a, s);
   }
 }
 

@@ -453,8 +453,8 @@ qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const ui
   if (st != QATTN_OK) return st;
   if ((st = check_params(params)) != QATTN_OK) return st;
   if (empty_problem(shape)) return QATTN_OK;
-  if (params->q_gran != QATTN_GRAN_BLOCK || params->k_gran != QATTN_GRAN_BLOCK || shape->Nk < 1)
-    return QATTN_ERR_UNSUPPORTED;
+  if (qattn_prepare_launches(shape, params) < 1) return QATTN_ERR_UNSUPPORTED;
+  const bool tensor = params->q_gran == QATTN_GRAN_TENSOR;
   for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K),
                         static_cast<const void*>(V), static_cast<const void*>(q_codes),
                         static_cast<const void*>(q_scales), static_cast<const void*>(k_codes),
@@ -481,7 +481,7 @@ qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const ui
   jq.N = static_cast<int>(shape->Nq);
   jq.Hchan = 1;
   jq.group = 1;
-  jq.gran = QATTN_GRAN_BLOCK;
+  jq.gran = params->q_gran;
   jq.codes = q_codes;
   jq.scales = q_scales;
   jq.nblk = static_cast<int>((shape->Nq + 127) / 128);
@@ -496,7 +496,7 @@ qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const ui
   jk.chan = k_mean;
   jk.Hchan = Hkv;
   jk.group = 1;
-  jk.gran = QATTN_GRAN_BLOCK;
+  jk.gran = params->k_gran;
   jk.codes = k_codes;
   jk.scales = k_scales;
   jk.carrier = k_carrier;
@@ -504,9 +504,13 @@ qattn_status qattn_prepare(const uint16_t* Q, const int64_t* q_strides, const ui
   jk.BH = B * Hkv;
   char sb[128];
   QATTN_LOG_LINE("qattn_prepare %s: %s", shape_str(shape, sb, sizeof sb),
-                 qattn::prepare_launch_count(d, jq.N, jk.N) == 1
+                 tensor ? "prepare_tensor1_kernel + prepare_tensor2_kernel (tensor granules, two launches)"
+                 : qattn::prepare_launch_count(d, jq.N, jk.N) == 1
                      ? "prepare_small_kernel (one warp per head, one launch)"
                      : "prepare1_kernel + prepare2_kernel (two launches)");
+  if (tensor)
+    return from_cuda(qattn::launch_prepare_tensor(jq, jk, vs, d, v8t, ldv, v_scales, workspace,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
   return from_cuda(qattn::launch_prepare(jq, jk, vs, d, v8t, ldv, v_scales, workspace,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -615,7 +619,8 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
     if (e != cudaSuccess) return QATTN_ERR_CUDA;
     kc16 = w16;
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
+  std::memset(&to, 0, sizeof to);
   if (!encode_q_codes(&tq, q_codes, shape->B * shape->Hq, shape->Nq, shape->d) ||
       !encode_carrier(&tk, kc16, shape->B * shape->Hkv, shape->Nk, shape->d) ||
       !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v8t, static_cast<uint64_t>(shape->Nk),
@@ -623,7 +628,15 @@ qattn_status qattn_fwd(const int8_t* q_codes, const float* q_scales, const int8_
                  static_cast<uint64_t>(ldv), 128, static_cast<uint32_t>(shape->d),
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return QATTN_ERR_CUDA;
-  return from_cuda(qattn::launch_attn_fwd(tq, tk, tv, a, s));
+  if (!a.out_bf16 || shape->d >= 64) {  // the output map: boxes of 128-byte rows x 32 rows
+    const size_t es = a.out_bf16 ? 2 : 4;
+    if (!encode_3d(&to, a.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   es, O, static_cast<uint64_t>(shape->d), static_cast<uint64_t>(shape->Nq),
+                   static_cast<uint64_t>(shape->B * shape->Hq), static_cast<uint64_t>(shape->d) * es,
+                   static_cast<uint32_t>(128 / es), 32, CU_TENSOR_MAP_SWIZZLE_128B))
+      return QATTN_ERR_CUDA;
+  }
+  return from_cuda(qattn::launch_attn_fwd(tq, tk, tv, to, a, s));
 }
 
 qattn_status qattn_decode(const int8_t* q_codes, const float* q_scales, const int8_t* k_codes,
@@ -856,10 +869,16 @@ int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params
 
 int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params) {
   if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
-  if (params->q_gran != QATTN_GRAN_BLOCK || params->k_gran != QATTN_GRAN_BLOCK || shape->Nk < 1) return -1;
+  if (shape->Nk < 1) return -1;
+  const int d = static_cast<int>(shape->d), Nq = static_cast<int>(shape->Nq),
+            Nk = static_cast<int>(shape->Nk);
+  if (params->q_gran == QATTN_GRAN_TENSOR && params->k_gran == QATTN_GRAN_TENSOR) {
+    if (!qattn::prepare_tensor_eligible(d, Nq, Nk)) return -1;
+    return empty_problem(shape) ? 0 : 2;
+  }
+  if (params->q_gran != QATTN_GRAN_BLOCK || params->k_gran != QATTN_GRAN_BLOCK) return -1;
   if (empty_problem(shape)) return 0;
-  return qattn::prepare_launch_count(static_cast<int>(shape->d), static_cast<int>(shape->Nq),
-                                     static_cast<int>(shape->Nk));
+  return qattn::prepare_launch_count(d, Nq, Nk);
 }
 
 qattn_status qattn_debug_wait_timeout(int32_t* result, qattn_stream_t stream) {

@@ -119,6 +119,13 @@ cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const Src& V, i
                            uint8_t* v8t, long long ldv, float* v_scales, void* ws, cudaStream_t s);
 size_t prepare_ws_bytes(long long BH, long long d);
 int prepare_launch_count(int d, int Nq, int Nk);  // 1 for short heads, else 2
+// The same pre-pass with tensor granules (jq.gran = jk.gran = 0): two launches,
+// one warp per head, for d in {32, 64} and 1 <= Nk <= 256.  ws: 8 bytes (the
+// two maxima, zeroed here).
+bool prepare_tensor_eligible(int d, int Nq, int Nk);
+cudaError_t launch_prepare_tensor(const RowsJob& jq, const RowsJob& jk, const Src& V, int d,
+                                  uint8_t* v8t, long long ldv, float* v_scales, void* ws,
+                                  cudaStream_t s);
 
 cudaError_t launch_quantize_v(const Src& V, int is_i8, const float* chan, int BH, int Nk, int d,
                               uint8_t* v8t, long long ldv, float* v_scales, unsigned int* ws_amax,
@@ -203,8 +210,11 @@ cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, flo
                               unsigned int* err, cudaStream_t s);
 
 // ---- attn_fwd.cu
+// tq: int8 Q codes; tk: fp16 K carriers; tv: e4m3 V^T; to: the output
+// [B*Hq][Nq][d] (bf16 or fp32) in boxes of 128-byte rows x 32 rows, 128B
+// swizzle (unused, and may be left zero, for bf16 with d = 32).
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& a, cudaStream_t s);
+                            const CUtensorMap& to, const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_qk_debug(const CUtensorMap& tq, const CUtensorMap& tk, int B, int Hq, int Hkv,
                             int Nq, int Nk, int d, int32_t* S, unsigned int* err,
                             cudaStream_t s);

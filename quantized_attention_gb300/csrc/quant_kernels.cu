@@ -935,6 +935,250 @@ __global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const S
                           lane);
 }
 
+// Tensor granules (one scale for all of Q, one for all of K - mean), KV heads
+// of at most 256 tokens with d <= 64 (e.g. ViT's 197 tokens): the pre-pass in
+// two launches instead of five, one CTA per head.  A CTA's 256 threads hold a
+// whole head in registers -- thread (g, v) the 8 channels of 16-byte column v
+// of rows g * UNR .. g * UNR + UNR - 1 (UNR consecutive rows) -- so each head
+// is read once per launch.  Launch 1: a Q head's max |x|; a K head's channel
+// mean and max |K - mean|; a V head's channel maxima, scales and transposed
+// e4m3 codes.  The two maxima merge into two words (Q, K) with atomicMax on
+// their bit patterns (non-negative floats order as unsigned integers; the
+// words start at 0).  Launch 2: the Q and K codes at the two tensor scales
+// (K's with the fp16 carriers).  Q heads of more than 256 rows are taken 256
+// rows at a time.  The arithmetic is that of the bodies above, step by step.
+constexpr int kTensorHead = 256;  // rows a CTA holds at once (and KV tokens at most)
+
+template <int D>
+struct TensorLane {
+  static constexpr int VPR = D / 8;                // 16-byte vectors per row
+  static constexpr int RG = kThreads / VPR;        // row groups (32 or 64)
+  static constexpr int UNR = kTensorHead / RG;     // consecutive rows per thread (8 or 4)
+  static constexpr int kWarps = kThreads / 32;
+  int v, g;
+  __device__ TensorLane() : v(threadIdx.x % VPR), g(threadIdx.x / VPR) {}
+  __device__ int row(int base, int u) const { return base + g * UNR + u; }
+  // the thread's rows of the 256-row chunk at `base` (zeros past N)
+  __device__ void load(const uint16_t* head, long long sN, int N, int base, uint4 (&raw)[UNR]) const {
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = row(base, u);
+      raw[u] = (r < N) ? __ldg(reinterpret_cast<const uint4*>(head + static_cast<long long>(r) * sN) + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+};
+
+struct TensorPrepArgs {
+  Src Q, K, V;
+  int BHq, BHk, Nq, Nk;
+  unsigned long long magic;
+  int8_t* q_codes;
+  float* q_scales;
+  int8_t* k_codes;
+  float* k_scales;
+  uint16_t* k_carrier;
+  float* k_mean;
+  uint8_t* v8t;
+  long long ldv;
+  float* v_scales;
+  unsigned int* amax;  // [2]: max |Q|, max |K - mean| (bit patterns)
+};
+
+template <int D>
+struct TensorSmem {
+  union {
+    long long sums[kThreads / 32][D];  // K: the warps' channel sums
+    float vmax[kThreads / 32][D];      // V: the warps' channel maxima
+  };
+  float chan[D];                       // K's mean or V's 448 / amax per channel
+  float red[kThreads / 32];
+  uint8_t tile[D * kTensorHead];       // V8^T of the head [D][256]
+};
+
+// max over the CTA of a per-thread value >= 0.
+__device__ __forceinline__ float cta_max(float v, float* red) { return block_max(v, red); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 3) prepare_tensor1_kernel(const TensorPrepArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  using TL = TensorLane<D>;
+  constexpr int UNR = TL::UNR, VPR = TL::VPR;
+  __shared__ __align__(16) TensorSmem<D> sm;
+  const TL L;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int item = blockIdx.x;
+  if (item < p.BHq) {  // ---- a Q head: its max |x|
+    const uint16_t* src = src_head<uint16_t>(p.Q, item);
+    float am = 0.f;
+    for (int base = 0; base < p.Nq; base += kTensorHead) {
+      uint4 raw[UNR];
+      L.load(src, p.Q.sN, p.Nq, base, raw);  // zero rows leave the maximum unchanged
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        float x[8];
+        unpack_bf16x8(raw[u], x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e]));
+      }
+    }
+    am = cta_max(am, sm.red);
+    if (threadIdx.x == 0) atomicMax(p.amax, __float_as_uint(am));
+    return;
+  }
+  item -= p.BHq;
+  if (item < p.BHk) {  // ---- a K head: channel mean, then max |K - mean|
+    const int bh = item;
+    uint4 raw[UNR];
+    L.load(src_head<uint16_t>(p.K, bh), p.K.sN, p.Nk, 0, raw);
+    long long sum[8];
+    fix24_column_sums<UNR>(raw, sum);  // rows past Nk are zeros: they add nothing
+#pragma unroll
+    for (int o = VPR; o < 32; o <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
+    }
+    if (lane < VPR) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm.sums[warp][lane * 8 + e] = sum[e];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+      long long tot = 0;
+#pragma unroll
+      for (int w = 0; w < TL::kWarps; ++w) tot += sm.sums[w][c];
+      const float mu = mean_of_fix24(tot, static_cast<uint32_t>(p.Nk), p.magic);
+      sm.chan[c] = mu;
+      p.k_mean[static_cast<size_t>(bh) * D + c] = mu;
+    }
+    __syncthreads();
+    float mu[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mu[e] = sm.chan[L.v * 8 + e];
+    L.load(src_head<uint16_t>(p.K, bh), p.K.sN, p.Nk, 0, raw);  // again, from L1
+    float am = 0.f;
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      if (L.row(0, u) < p.Nk) {
+        float x[8];
+        unpack_bf16x8(raw[u], x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(__fsub_rn(x[e], mu[e])));
+      }
+    }
+    am = cta_max(am, sm.red);
+    if (threadIdx.x == 0) atomicMax(p.amax + 1, __float_as_uint(am));
+    return;
+  }
+  item -= p.BHk;
+  if (item >= p.BHk) return;
+  // ---- a V head: channel maxima, scales, e4m3 codes through the [D][256] tile
+  const int bh = item;
+  uint4 raw[UNR];
+  L.load(src_head<uint16_t>(p.V, bh), p.V.sN, p.Nk, 0, raw);
+  float vm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {  // zero rows leave the maxima unchanged
+    float x[8];
+    unpack_bf16x8(raw[u], x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], fabsf(x[e]));
+  }
+#pragma unroll
+  for (int o = VPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], __shfl_xor_sync(0xffffffffu, vm[e], o));
+  }
+  if (lane < VPR) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm.vmax[warp][lane * 8 + e] = vm[e];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += kThreads) {
+    float m = 0.f;
+#pragma unroll
+    for (int w = 0; w < TL::kWarps; ++w) m = fmaxf(m, sm.vmax[w][c]);
+    sm.chan[c] = (m > 0.f) ? __fdiv_rn(448.0f, m) : 0.f;
+    p.v_scales[static_cast<size_t>(bh) * D + c] = __fdiv_rn(m, 448.0f);
+  }
+  __syncthreads();
+  float sc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sc[e] = sm.chan[L.v * 8 + e];
+  // the thread's UNR consecutive keys of each of its channels: UNR bytes of a
+  // tile row (zero rows give code 0, the padding the layout wants)
+#pragma unroll
+  for (int q = 0; q < UNR / 4; ++q) {  // keys 4q .. 4q + 3 of the thread's rows: one word per channel
+    uint32_t b[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int u = 4 * q; u < 4 * q + 4; ++u) {
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t b2 = cvt_e4m3x2(__fmul_rn(x[e], sc[e]), __fmul_rn(x[e + 1], sc[e + 1]));
+        b[e] |= (b2 & 0xFFu) << (8 * (u % 4));
+        b[e + 1] |= (b2 >> 8) << (8 * (u % 4));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<uint32_t*>(sm.tile + (L.v * 8 + e) * kTensorHead + L.g * UNR + 4 * q) = b[e];
+  }
+  __syncthreads();
+  const int nchunk = static_cast<int>(p.ldv / 16);  // 16-byte chunks of a V8^T row
+  uint8_t* dst = p.v8t + static_cast<size_t>(bh) * D * p.ldv;
+  for (int i = threadIdx.x; i < D * nchunk; i += kThreads) {
+    const int c = i / nchunk, k = i % nchunk;
+    const uint4 w = (16 * k < kTensorHead) ? *reinterpret_cast<const uint4*>(sm.tile + c * kTensorHead + 16 * k)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * p.ldv + 16 * k) = w;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) prepare_tensor2_kernel(const TensorPrepArgs p) {
+  pdl_trigger();
+  pdl_wait();  // the maxima and K's mean of launch 1
+  using TL = TensorLane<D>;
+  constexpr int UNR = TL::UNR;
+  const TL L;
+  const bool is_q = blockIdx.x < p.BHq;
+  const int bh = is_q ? blockIdx.x : blockIdx.x - p.BHq;
+  if (!is_q && bh >= p.BHk) return;
+  const Src& X = is_q ? p.Q : p.K;
+  const int N = is_q ? p.Nq : p.Nk;
+  float mu[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (!is_q) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mu[e] = p.k_mean[static_cast<size_t>(bh) * D + L.v * 8 + e];
+  }
+  const float g = __uint_as_float(p.amax[is_q ? 0 : 1]);
+  const float inv = (g > 0.f) ? __fdiv_rn(127.0f, g) : 0.f;
+  const uint16_t* src = src_head<uint16_t>(X, bh);
+  int8_t* codes = (is_q ? p.q_codes : p.k_codes) + static_cast<size_t>(bh) * N * D;
+  uint16_t* carrier = (!is_q && p.k_carrier) ? p.k_carrier + static_cast<size_t>(bh) * N * D : nullptr;
+  for (int base = 0; base < N; base += kTensorHead) {
+    uint4 raw[UNR];
+    L.load(src, X.sN, N, base, raw);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = L.row(base, u);
+      if (r >= N) break;
+      float x[8];
+      unpack_bf16x8(raw[u], x);
+      if (!is_q) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
+      }
+      const size_t off = static_cast<size_t>(r) * D + L.v * 8;
+      codes8(x, inv, codes + off, carrier ? carrier + off : nullptr);
+    }
+  }
+  if (bh == 0 && threadIdx.x == 0) (is_q ? p.q_scales : p.k_scales)[0] = __fdiv_rn(g, 127.0f);
+}
+
 // ------------------------------------------------------------------ carriers
 // int8 codes -> fp16 values (exact: |code| <= 127).
 __global__ void codes_to_f16_kernel(const int8_t* src, uint16_t* __restrict__ dst,
@@ -1088,6 +1332,48 @@ cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const Src& V, i
     case 64: return prepare_t<64>(p1, p2, s);
     default: return prepare_t<128>(p1, p2, s);
   }
+}
+
+bool prepare_tensor_eligible(int d, int Nq, int Nk) {
+  (void)Nq;
+  return (d == 32 || d == 64) && Nk >= 1 && Nk <= kTensorHead;
+}
+
+cudaError_t launch_prepare_tensor(const RowsJob& jq, const RowsJob& jk, const Src& V, int d,
+                                  uint8_t* v8t, long long ldv, float* v_scales, void* ws,
+                                  cudaStream_t s) {
+  if (!prepare_tensor_eligible(d, jq.N, jk.N) || jq.gran != 0 || jk.gran != 0)
+    return cudaErrorInvalidValue;
+  TensorPrepArgs p{};
+  p.Q = Src{jq.X, jq.sB, jq.sH, jq.sN, jq.H};
+  p.K = Src{jk.X, jk.sB, jk.sH, jk.sN, jk.H};
+  p.V = V;
+  p.BHq = jq.BH;
+  p.BHk = jk.BH;
+  p.Nq = jq.N;
+  p.Nk = jk.N;
+  p.magic = ~0ull / static_cast<unsigned long long>(jk.N);
+  p.q_codes = jq.codes;
+  p.q_scales = jq.scales;
+  p.k_codes = jk.codes;
+  p.k_scales = jk.scales;
+  p.k_carrier = jk.carrier;
+  p.k_mean = const_cast<float*>(jk.chan);
+  p.v8t = v8t;
+  p.ldv = ldv;
+  p.v_scales = v_scales;
+  p.amax = static_cast<unsigned int*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  const dim3 g1(jq.BH + 2 * jk.BH), g2(jq.BH + jk.BH);  // one CTA per Q, K, V head
+  if (d == 32) {
+    e = launch_pdl(prepare_tensor1_kernel<32>, g1, dim3(kThreads), 0, s, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(prepare_tensor2_kernel<32>, g2, dim3(kThreads), 0, s, p);
+  }
+  e = launch_pdl(prepare_tensor1_kernel<64>, g1, dim3(kThreads), 0, s, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(prepare_tensor2_kernel<64>, g2, dim3(kThreads), 0, s, p);
 }
 
 size_t quantize_rows_ws_bytes(long long B, long long H, long long N, int gran) {

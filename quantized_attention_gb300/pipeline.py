@@ -46,9 +46,10 @@ class Problem:
         ws = max(qb.workspace_size(self.shape, self.params), 256)
         self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
         # qattn_prepare covers bf16 K/V with block granules (one or two
-        # launches instead of four); other granules take the three calls
+        # launches instead of four) and with tensor granules for heads of at
+        # most 256 keys (two instead of five); other cases take the three calls
         self.fused_prepass = (fused_prepass and not kv_codes and Nk > 0 and
-                              q_gran == qb.GRAN_BLOCK and k_gran == qb.GRAN_BLOCK)
+                              qb.prepare_launches(self.shape, self.params) > 0)
 
     def quantize(self, Q, K=None, V=None, *, K_codes=None, K_scale=None, V_codes=None,
                  V_scale=None, stream=None):

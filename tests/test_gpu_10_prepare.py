@@ -1,6 +1,8 @@
-"""qattn_prepare (the pre-pass in two launches) writes, byte for byte, what
-qattn_smooth_k + qattn_quantize_qk + qattn_quantize_v write: the K mean, Q/K
-codes and scales, K's fp16 carriers, V's transposed e4m3 codes and scales."""
+"""qattn_prepare (the pre-pass in one or two launches) writes, byte for byte,
+what qattn_smooth_k + qattn_quantize_qk + qattn_quantize_v write: the K mean,
+Q/K codes and scales, K's fp16 carriers, V's transposed e4m3 codes and scales
+-- with block granules, and with tensor granules for heads of at most 256
+keys (d 32 or 64)."""
 import pytest
 import torch
 
@@ -34,10 +36,15 @@ def _ids(w):
 OUTS = ("q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v8t", "v_scales", "k_carrier")
 
 
-@pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
-@pytest.mark.parametrize("carrier", [True, False])
-def test_prepare_equals_three_calls(wl, carrier):
-    wl = wl.replace(q_gran=qb.GRAN_BLOCK, k_gran=qb.GRAN_BLOCK)
+TENSOR_CASES = [
+    I.small("vit", B=2, Hq=3, Hkv=3, Nq=197, Nk=197),          # the ViT head shape
+    I.small("vit", B=3, Hq=4, Hkv=2, Nq=300, Nk=256, d=32),    # GQA, the longest keys, Nq > 256
+    I.small("vit", B=2, Hq=2, Hkv=2, Nq=5, Nk=1),              # one key
+    I.small("vit", B=1, Hq=2, Hkv=1, Nq=129, Nk=129, d=64),    # ragged past one 128-row block
+]
+
+
+def _check_prepare(wl, carrier):
     dev = device_inputs(I.make_inputs(wl))
     dev.pop("bias", None)
     res = []
@@ -55,6 +62,21 @@ def test_prepare_equals_three_calls(wl, carrier):
     for n in res[0]:
         a, b = res[0][n].view(torch.uint8), res[1][n].view(torch.uint8)
         assert torch.equal(a, b), f"{n}: {int((a != b).sum())} bytes differ"
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[_ids(w) for w in CASES])
+@pytest.mark.parametrize("carrier", [True, False])
+def test_prepare_equals_three_calls(wl, carrier):
+    _check_prepare(wl.replace(q_gran=qb.GRAN_BLOCK, k_gran=qb.GRAN_BLOCK), carrier)
+
+
+@pytest.mark.parametrize("wl", TENSOR_CASES, ids=[_ids(w) for w in TENSOR_CASES])
+@pytest.mark.parametrize("carrier", [True, False])
+def test_prepare_tensor_granules_equals_three_calls(wl, carrier):
+    wl = wl.replace(q_gran=qb.GRAN_TENSOR, k_gran=qb.GRAN_TENSOR)
+    assert qb.prepare_launches(qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d),
+                               qb.make_params(q_gran=qb.GRAN_TENSOR, k_gran=qb.GRAN_TENSOR)) == 2
+    _check_prepare(wl, carrier)
 
 
 def test_prepare_rejects_other_granules():

@@ -1,8 +1,8 @@
 """The pre-pass reads its inputs at any strides: Q, K and V taken in place from
 a packed projection output [B, N, 3, H, d] (a non-contiguous view per tensor)
 give, byte for byte, the codes, scales, means and e4m3 V of the same tensors
-made dense -- through qattn_prepare (two-launch and short-head paths) and
-through the three separate calls (per-tensor granules)."""
+made dense -- through qattn_prepare (two-launch, short-head and tensor-granule
+paths) and through the three separate calls (per-tensor granules)."""
 import numpy as np
 import pytest
 import torch
@@ -24,6 +24,7 @@ CASES = [  # B, H, N, d, granularity, fused pre-pass
     (3, 2, 49, 32, qb.GRAN_BLOCK, True),      # qattn_prepare, one warp per head
     (2, 3, 197, 64, qb.GRAN_TENSOR, False),   # smooth_k, quantize_qk (two passes), quantize_v
     (1, 2, 260, 64, qb.GRAN_BLOCK, False),    # the three calls with block granules
+    (2, 3, 197, 64, qb.GRAN_TENSOR, True),    # qattn_prepare, tensor granules
 ]
 
 

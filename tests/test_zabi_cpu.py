@@ -194,6 +194,9 @@ def test_kernel_choices_follow_the_documented_rules(L):
             p = qb.make_params()
             assert qb.prepare_launches(s, p) == (1 if d <= 64 and nq <= 128 and nk <= 128 else 2)
             assert qb.prepare_launches(s, qb.make_params(q_gran=qb.GRAN_TENSOR)) == -1
+            tens = qb.make_params(q_gran=qb.GRAN_TENSOR, k_gran=qb.GRAN_TENSOR)
+            assert qb.prepare_launches(s, tens) == (2 if d <= 64 and nk <= 256 else -1)
+            assert qb.prepare_launches(s, qb.make_params(q_gran=qb.GRAN_HEAD, k_gran=qb.GRAN_HEAD)) == -1
     assert qb.fwd_kernel_choice(qb.make_shape(1, 4, 2, 64, 64, 96), qb.make_params()) == -1
     assert qb.prepare_launches(qb.make_shape(1, 4, 2, 64, 0, 64), qb.make_params()) == -1
 
