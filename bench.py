@@ -802,15 +802,13 @@ def gpu_arm(args):
         pb = peaks["bf16"]
         if unit_peaks is not None:
             pb = max(pb, unit_peaks["f16"])
-        roofline = {"bound": "tensor", "kernel": "exact24_attn_kernel + q_split_kernel (qattn_fwd_exact24)",
+        roofline = {"bound": "tensor",
+                    "kernel": "exact24_tc_kernel + q_split/k_rows_f16/v_t_f16 (qattn_fwd_exact24)",
                     "achieved": mma_tflops, "peak": pb, "unit": "TFLOP/s", "frac": mma_tflops / pb,
                     "peak_basis": "the stricter of the cuBLAS bf16 burst figure and the tcgen05 "
                                   "kind::f16 loop (fp16 MMA runs at the bf16 rate); achieved counts "
                                   "the 3 fp16 products per attention product",
                     "traffic": None}
-        if "mma_sync_f16" in unit_rates:
-            roofline["mma_sync_f16_loop"] = unit_rates["mma_sync_f16"]["rate"]
-            roofline["frac_mma_sync_f16_loop"] = mma_tflops / unit_rates["mma_sync_f16"]["rate"]
     if decode and not args.exact24:  # memory-bound: the cache's bytes over the decode call's time
         gbs = cache_bytes / (attn_avg_ms * 1e-3) / 1e9
         ref_us = _stream_ref_us(dev["K_codes"], dev["V_codes"], flush, stream)

@@ -252,6 +252,19 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const voi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+namespace qattn {
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                     uint64_t rows, uint64_t planes, uint64_t row_stride_bytes, uint32_t box_inner,
+                     uint32_t box_rows, CUtensorMapSwizzle swz, uint64_t plane_rows) {
+  return encode_3d(map, dt, 0, ptr, inner, rows, planes, row_stride_bytes, box_inner, box_rows, swz,
+                   plane_rows);
+}
+}  // namespace qattn
+
+namespace {
+
 // Map over the int8 Q codes [B*Hq][Nq][d]: one 128-row tile per load,
 // unswizzled (the kernels widen it to fp16 themselves).
 bool encode_q_codes(CUtensorMap* map, const void* ptr, int64_t planes, int64_t rows, int64_t d) {
@@ -322,7 +335,8 @@ size_t qattn_workspace_size(const qattn_shape* shape, const qattn_params* params
                                               shape->Nk, shape->d);
     if (dws > m) m = dws;
   }
-  const size_t e24 = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Nq, shape->d);
+  const size_t e24 = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Hkv, shape->Nq, shape->Nk,
+                                             shape->d);
   if (e24 > m) m = e24;
   return m;
 }
@@ -760,7 +774,8 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
   const int64_t pos0 = pos0_of(shape, params);
   if (params->causal && (pos0 <= -(int64_t{1} << 30) || pos0 >= (int64_t{1} << 30))) return QATTN_ERR_UNSUPPORTED;
   if (shape->Nk == 0) return no_key_rows(shape, params, O, lse, reinterpret_cast<cudaStream_t>(stream));
-  const size_t need = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Nq, shape->d);
+  const size_t need = qattn::exact24_ws_bytes(shape->B, shape->Hq, shape->Hkv, shape->Nq, shape->Nk,
+                                              shape->d);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QATTN_ERR_WORKSPACE;
   qattn::Exact24Args a{};
   a.B = static_cast<int>(shape->B);
@@ -784,7 +799,10 @@ qattn_status qattn_fwd_exact24(const void* Q, const int8_t* k_codes, const float
   a.lse = lse;
   a.ws = workspace;
   char sb[128];
-  QATTN_LOG_LINE("qattn_fwd_exact24 %s: q_split_kernel + exact24_attn_kernel", shape_str(shape, sb, sizeof sb));
+  a.err = error_word();
+  if (!a.err) return QATTN_ERR_CUDA;
+  QATTN_LOG_LINE("qattn_fwd_exact24 %s: q_split_kernel + k_rows_f16_kernel + v_t_f16_kernel + exact24_tc_kernel",
+                 shape_str(shape, sb, sizeof sb));
   return from_cuda(qattn::launch_exact24(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -199,8 +199,10 @@ struct Exact24Args {
   int out_bf16;
   float* lse;
   void* ws;                     // exact24_ws_bytes
+  unsigned int* err;            // device error word (a bounded wait that ran out)
 };
-size_t exact24_ws_bytes(long long B, long long Hq, long long Nq, long long d);
+size_t exact24_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
+                        long long d);
 cudaError_t launch_exact24(const Exact24Args& x, cudaStream_t s);
 
 // ---- intsm.cu
@@ -208,6 +210,13 @@ cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, flo
                               const int8_t* q_codes, const float* q_scale, const int8_t* k_codes,
                               const float* k_scale, const int8_t* v_codes, int8_t* out,
                               unsigned int* err, cudaStream_t s);
+
+// 3-D tiled TMA map over a dense [planes][rows][inner] tensor (qattn_api.cu):
+// row_stride_bytes between rows, plane_rows rows between planes (0 = rows);
+// false if the driver entry point is missing or rejects the map.
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                     uint64_t rows, uint64_t planes, uint64_t row_stride_bytes, uint32_t box_inner,
+                     uint32_t box_rows, CUtensorMapSwizzle swz, uint64_t plane_rows = 0);
 
 // ---- attn_fwd.cu
 // tq: int8 Q codes; tk: fp16 K carriers; tv: e4m3 V^T; to: the output
