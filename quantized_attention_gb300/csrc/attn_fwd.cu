@@ -6,8 +6,10 @@
 //   warp 0      lane 0 issues every TMA load: the item's slot (its decoded
 //               indices and scales, see ItemSlot), its two int8 Q tiles, a
 //               ring of K stages and a ring of V^T stages;
-//   warp 1      owns the 512 TMEM columns; lane 0 issues the MMAs of tile t0;
-//   warp 2      lane 0 issues the MMAs of tile t1;
+//   warp 1      owns the 512 TMEM columns and issues the MMAs of tile t0 (the
+//               whole warp runs the waits and forms the operand descriptors,
+//               lane 0 issues the MMAs and commits);
+//   warp 2      the same for tile t1;
 //   warp 3      widens each item's int8 Q codes to exact fp16 in shared
 //               memory (q_conv), running ahead of the softmax warps;
 //   warps 4-7   softmax of tile t0, warps 8-11 softmax of tile t1 (one query
@@ -110,6 +112,32 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t sq, uint32_t 
     const uint32_t off = (s / kStepsPerBlock) * C::kColBlockBytes + (s % kStepsPerBlock) * 32;
     mma_f16(tmem_s, smem_desc(sq + off, C::kSBO, C::kSwz), smem_desc(sk + off, C::kSBO, C::kSwz),
             idesc, s > 0 ? 1u : 0u);
+  }
+}
+
+// The same with the operands' descriptors given (start address advanced by
+// adding (offset >> 4) to the low word: addresses stay below 2^18).
+template <int D>
+__device__ __forceinline__ void issue_qk_d(uint32_t tmem_s, uint64_t dq, uint64_t dk) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = make_idesc(kBM, kBN, 0, 0);
+  constexpr int kStepsPerBlock = C::kRowBytes / 32;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    const uint32_t off = (s / kStepsPerBlock) * C::kColBlockBytes + (s % kStepsPerBlock) * 32;
+    mma_f16(tmem_s, dq + (off >> 4), dk + (off >> 4), idesc, s > 0 ? 1u : 0u);
+  }
+}
+template <int D, bool PQ>
+__device__ __forceinline__ void issue_pv_d(uint32_t tmem_o, uint64_t dp, uint64_t dv, bool acc) {
+  constexpr uint32_t idesc = make_idesc(kBM, D, 0, 0);
+#pragma unroll
+  for (int pl = 0; pl < (PQ ? 2 : 1); ++pl) {
+#pragma unroll
+    for (int s = 0; s < kBN / 32; ++s) {
+      mma_f8(tmem_o, dp + ((pl * kBM * kBN + s * 32) >> 4), dv + ((s * 32) >> 4), idesc,
+             (acc || pl > 0 || s > 0) ? 1u : 0u);
+    }
   }
 }
 
@@ -525,9 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) *abort_flag = 1;
   } else if (warp == 1 || warp == 2) {
-    if (lane == 0) {
+    {
       // ------------------------------------------------------------ MMA
-      // One issuing thread per query tile (warp 1: t0, warp 2: t1), so a tile
+      // One issuing warp per query tile (warp 1: t0, warp 2: t1), so a tile
       // whose softmax runs ahead is never held back by the other.  Per item
       // it issues, in the order its softmax frees the inputs,
       //   QK(0), QK(1), PV(0), QK(2), PV(1), ..., PV(nb_t - 1)
@@ -551,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = max(it.nb[0], it.nb[1]);
         const int nbt = it.nb[t];
         if (nbt == 0) {  // nothing for this tile: free the item's Q stage
-          if ((ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)))
+          if ((ok = mbar_wait(bar(kBarQFull + qs), (i / C::kQS) & 1, abort_flag, a.err, kErrTimeout)) && lane == 0)
             mma_commit(bar(kBarQEmpty + qs));
         }
         for (int b = 0; ok && b <= nb; ++b) {
@@ -569,12 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    kErrTimeout)))
                 break;
               tc_fence_after();
-              issue_qk<D>(tmem + 128 * t, sQ(qs, t), sK(st));
-              mma_commit(bar(kBarSFull + t));
+              const uint64_t dq = smem_desc(sQ(qs, t), C::kSBO, C::kSwz), dk = smem_desc(sK(st), C::kSBO, C::kSwz);
+              if (lane == 0) {
+                issue_qk_d<D>(tmem + 128 * t, dq, dk);
+                mma_commit(bar(kBarSFull + t));
+              }
               ++nqk;
             }
-            mma_commit(bar(kBarKEmpty + st));
-            if (b == nbt - 1) mma_commit(bar(kBarQEmpty + qs));  // the tile's last QK
+            if (lane == 0) mma_commit(bar(kBarKEmpty + st));
+            if (b == nbt - 1 && lane == 0) mma_commit(bar(kBarQEmpty + qs));  // the tile's last QK
           }
           if (b >= 1) {  // value block b - 1
             const uint32_t vv = kvc + b - 1;
@@ -585,11 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait(bar(kBarPFull + t), npv & 1, abort_flag, a.err, kErrTimeout)))
                 break;
               tc_fence_after();
-              issue_pv<D, PQ>(tmem + 256 + 128 * t, sP(t), sV(st), b > 1);
-              mma_commit(bar(kBarPVDone + t));
+              const uint64_t dp = smem_desc(sP(t), 1024, kSwizzle128B), dv = smem_desc(sV(st), 1024, kSwizzle128B);
+              if (lane == 0) {
+                issue_pv_d<D, PQ>(tmem + 256 + 128 * t, dp, dv, b > 1);
+                mma_commit(bar(kBarPVDone + t));
+              }
               ++npv;
             }
-            mma_commit(bar(kBarVEmpty + st));
+            if (lane == 0) mma_commit(bar(kBarVEmpty + st));
           }
         }
         kvc += nb;
@@ -597,10 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every MMA this thread issued finishes before TMEM is freed.
       const int drain = kBarDrain + t;
-      mma_commit(bar(drain));
+      if (lane == 0) mma_commit(bar(drain));
       volatile int never = 0;
       mbar_wait(bar(drain), 0, &never, a.err, kErrTimeout);
-      if (!ok) *abort_flag = 1;
+      if (!ok && lane == 0) *abort_flag = 1;
     }
     __syncwarp();
   } else if (warp >= 4) {
