@@ -104,3 +104,33 @@ def test_exact24_no_keys():
     assert qb.get_error() == 0
     assert np.array_equal(O_.cpu().numpy().reshape(want.shape), want)
     assert np.array_equal(lse.cpu().numpy().reshape(want_lse.shape), want_lse)
+
+
+def test_exact24_cache_capacity_and_bf16_out():
+    """The cache holds capacity > Nk rows (qattn_params.kv_capacity), the rows past Nk
+    filled with extreme codes the call must not read; the fp32 output matches the
+    oracle on the first Nk rows, and the bf16 output is the fp32 one rounded."""
+    wl = I.small("chunk32k", Hq=4, Hkv=2, Nq=130, Nk=300, q_pos0=170)
+    inp = I.make_inputs(wl)
+    cap = 448
+    dev = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dt)
+    Kc = np.full((wl.B, wl.Hkv, cap, wl.d), 127, dtype=np.int8)
+    Vc = np.full((wl.B, wl.Hkv, cap, wl.d), -128, dtype=np.int8)
+    Kc[:, :, :wl.Nk] = inp.K_codes
+    Vc[:, :, :wl.Nk] = inp.V_codes
+    shape = qb.make_shape(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nk, wl.d)
+    outs = {}
+    for out_dt, tdt in ((qb.DT_F32, torch.float32), (qb.DT_BF16, torch.bfloat16)):
+        params = qb.make_params(causal=wl.causal, q_pos0=wl.q_pos0, kv_capacity=cap, out_dtype=out_dt)
+        O_ = torch.full((wl.B, wl.Hq, wl.Nq, wl.d), float("nan"), dtype=tdt, device="cuda")
+        ws = torch.empty(max(qb.workspace_size(shape, params), 256), dtype=torch.uint8, device="cuda")
+        qb.fwd_exact24(dev(inp.Q, torch.bfloat16), dev(Kc, torch.int8), dev(inp.K_scale, torch.float32),
+                       dev(Vc, torch.int8), dev(inp.V_scale, torch.float32), shape, params, O_, None, ws)
+        torch.cuda.synchronize()
+        assert qb.get_error() == 0
+        outs[out_dt] = O_
+    want, _ = O.attn_exact24(inp.Q, inp.K_codes, inp.K_scale, inp.V_codes, inp.V_scale,
+                             causal=wl.causal, q_pos0=wl.q_pos0)
+    got = outs[qb.DT_F32].cpu().numpy().astype(np.float64).reshape(want.shape)
+    assert np.abs(got - want).max() <= TOL * np.abs(want).max()
+    assert torch.equal(outs[qb.DT_BF16], outs[qb.DT_F32].to(torch.bfloat16))
