@@ -358,6 +358,83 @@ __device__ __forceinline__ float softmax_step(uint32_t (&s)[kBN], float c, int n
   return alpha;
 }
 
+// softmax_step without BIAS or PQ for d <= 64, where a masked block (the
+// ragged end of a short key sequence, e.g. ViT's 69-key second block) is a
+// large share of the work.  Keys fall in four groups of 32: groups below
+// nvis / 32 hold only visible keys and take their maximum from pmax (the TMEM
+// read's maxima); the group holding the row's last visible key is masked
+// (-inf) and maximized here; later groups hold no visible key and are skipped
+// (P codes 0, nothing added to l).  Skipping is exact: their P would be 0 and
+// adding 0 changes no sum.  The same arithmetic as softmax_step otherwise.
+// (At d = 128 the per-group branches cost the block loop spills.)
+__device__ __forceinline__ float softmax_step_groups(uint32_t (&s)[kBN], float c, int nvis,
+                                                     const float (&pmax)[kBN / 32], bool masked,
+                                                     float& m, float& l, uint32_t (&pw)[kBN / 4]) {
+  constexpr int kG = kBN / 32;
+  static_assert(kG == 4, "four 32-key groups per block");
+  int ng = kG;  // groups with a visible key
+  float mx;
+  if (!masked) {
+    mx = fmax3(pmax[0], pmax[1], fmaxf(pmax[2], pmax[3]));
+  } else {
+    ng = (nvis + 31) >> 5;
+    const int nfull = nvis >> 5;
+    mx = kNegInf;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      if (g < nfull) {
+        mx = fmaxf(mx, pmax[g]);
+      } else if (g < ng) {  // the partial group
+        float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+        for (int k = 32 * g; k < 32 * g + 32; k += 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (k + e >= nvis) s[k + e] = 0xFF800000u;
+          mx0 = fmax3(mx0, __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(s[k + 2]), __uint_as_float(s[k + 3]));
+        }
+        mx = fmax3(mx, mx0, mx1);
+      }
+    }
+  }
+  const float m_blk = (mx == kNegInf) ? kNegInf : __fmul_rn(mx, c);
+  const float m_new = fmaxf(m, m_blk);
+  const bool dead = (m_new == kNegInf);
+  const float alpha = dead ? 1.f : ex2_approx(m - m_new);
+  const float kneg = dead ? 0.f : (kLog2_448 - m_new);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    if (g >= ng) {  // no visible key in the group
+#pragma unroll
+      for (int q = 8 * g; q < 8 * g + 8; ++q) pw[q] = 0u;
+      continue;
+    }
+#pragma unroll
+    for (int k = 32 * g; k < 32 * g + 32; k += 4) {
+      uint32_t half[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kk = k + 2 * e;
+        const float2 x = ffma2(make_float2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])),
+                               make_float2(c, c), make_float2(kneg, kneg));
+        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[(k / 2 + e) & 3] = fadd2(acc[(k / 2 + e) & 3], p);
+        half[e] = cvt_e4m3x2(p.x, p.y);
+      }
+      pw[k / 4] = half[0] | (half[1] << 16);
+    }
+  }
+  const float2 a01 = fadd2(acc[0], acc[1]);
+  const float2 a23 = fadd2(acc[2], acc[3]);
+  const float2 tot = fadd2(a01, a23);
+  l = fmaf(alpha, l, tot.x + tot.y);
+  m = m_new;
+  return alpha;
+}
+
 template <int D, bool BIAS, bool PQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -718,12 +795,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kbase = j * kBN;
         const bool need_mask = (kbase + kBN > a.Nk) || (kbase + kBN - 1 > tile_lim);
         const int nvis = need_mask ? max(0, min(kBN, lim - kbase + 1)) : kBN;
+        constexpr bool kGroups = (D <= 64) && !BIAS && !PQ;  // softmax_step_groups
         if (!BIAS) {
           // Masked keys become -inf scores.  A zero (or subnormal) c would
           // turn them into NaN; c = FLT_MIN leaves every visible t = S c at
           // or within 2^-105 of the exact S c, so no P, alpha or l changes.
           c = fmaxf(c, 0x1p-126f);
-          if (need_mask) {
+          if (!kGroups && need_mask) {
 #pragma unroll
             for (int k = 0; k < kBN; ++k)
               if (k >= nvis) s[k] = 0xFF800000u;
@@ -731,11 +809,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t pw[kBN / 4], pw2[kBN / 4];
         const float* bk = BIAS ? brow + kbase : nullptr;
-        // the TMEM read's maxima serve unmasked blocks; masked keys are -inf
-        // only after the read, so those blocks take the maximum themselves
-        const float smax = (BIAS || need_mask) ? __int_as_float(0x7fc00000)
-                                               : fmax3(pmax[0], pmax[1], fmaxf(pmax[2], pmax[3]));
-        const float alpha = softmax_step<BIAS, PQ>(s, c, nvis, bk, smax, m, l, pw, pw2);
+        float alpha;
+        if constexpr (kGroups) {
+          alpha = softmax_step_groups(s, c, nvis, pmax, need_mask, m, l, pw);
+        } else {
+          // the TMEM read's maxima serve unmasked blocks; masked keys are -inf
+          // only after the read, so those blocks take the maximum themselves
+          const float smax = (BIAS || need_mask) ? __int_as_float(0x7fc00000)
+                                                 : fmax3(pmax[0], pmax[1], fmaxf(pmax[2], pmax[3]));
+          alpha = softmax_step<BIAS, PQ>(s, c, nvis, bk, smax, m, l, pw, pw2);
+        }
         if (j > 0) {  // PV(t, j-1) must be done with P_t and O_t
           ok = mbar_wait(bar(kBarPVDone + t), pvc & 1, abort_flag, a.err, kErrTimeout);
           ++pvc;
