@@ -776,8 +776,23 @@ __device__ __forceinline__ void head_mean(const HeadLane<D>& L, const uint16_t* 
 #pragma unroll
     for (int e = 0; e < 8; ++e) sum[e] += __shfl_xor_sync(0xffffffffu, sum[e], o);
   }
+  // Every lane of a column now holds its 8 sums; the RG lanes of the column
+  // share the 8 divisions (lane rg takes channels e = rg, rg + RG, ...) and
+  // hand the means round: lane (e % RG) * VPR + v holds channel e's.
+  constexpr int VPR = HeadLane<D>::VPR;
+  static_assert(8 % RG == 0, "every lane of a column takes the same number of channels");
+  constexpr int PER = 8 / RG;  // divisions per lane
+  float own[PER];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) mu[e] = mean_of_fix24(sum[e], static_cast<uint32_t>(N), magic);
+  for (int i = 0; i < PER; ++i) {
+    const int e = L.rg + i * RG;  // < 8 for every lane when RG divides 8
+    long long se = sum[0];
+#pragma unroll
+    for (int ee = 1; ee < 8; ++ee) se = (ee == e) ? sum[ee] : se;  // selects, no divergence
+    own[i] = mean_of_fix24(se, static_cast<uint32_t>(N), magic);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mu[e] = __shfl_sync(0xffffffffu, own[e / RG], (e % RG) * VPR + L.v);
 }
 
 // max |x - mu| (MINUS) or max |x| over a head's rows, over the whole warp.
