@@ -114,7 +114,7 @@ def _attn_traffic(wl_name):
                 k, v = line.split("=", 1)
                 kv[k] = v
     h = hashlib.sha256()
-    for name in ("attn_fwd.cu", "sm103_ptx.cuh"):
+    for name in ("attn_fwd.cu", "sm103_ptx.cuh", "qattn_check.cuh"):
         with open(os.path.join(ROOT, "quantized_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     if kv.get("workload") != wl_name or kv.get("kernel_source_sha256") != h.hexdigest():

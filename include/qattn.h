@@ -70,7 +70,9 @@ typedef enum {
   QATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d = 96)      */
   QATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed            */
   QATTN_ERR_TIMEOUT = 4,      /* a kernel's pipeline wait ran out (device)    */
-  QATTN_ERR_WORKSPACE = 5     /* workspace missing or smaller than required   */
+  QATTN_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required   */
+  QATTN_ERR_BOUNDS = 6        /* checked build: a kernel skipped an access whose
+                                 index fell outside its buffer (device)        */
 } qattn_status;
 
 /* Scale granularity of Q and K codes ("QFlash", section 3.3: per tensor,
@@ -444,6 +446,20 @@ int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params
 /* How many kernels qattn_prepare launches for a shape and params (1 or 2; 0
  * for an empty problem), or -1 if it would reject them.  Host only. */
 int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params);
+
+/* The checked build (the library compiled with QATTN_CHECK=1, by
+ * build.build(checked=True) into _lib/check/): the kernels guard the device
+ * accesses whose indices they compute -- output rows and columns, scale
+ * indices, cache rows, TMA coordinates -- against their buffers' extents; a
+ * failing guard skips the access (nothing traps) and qattn_get_error()
+ * returns QATTN_ERR_BOUNDS.  A stand-in for a memory checker where none can
+ * run.  qattn_checked() is 1 in that build, 0 in the normal one (host only). */
+int qattn_checked(void);
+
+/* Runs one guard that fails for 16 of 32 threads and touches no memory: in
+ * the checked build the next qattn_get_error() returns QATTN_ERR_BOUNDS, in
+ * the normal build QATTN_OK -- a test of the reporting path. */
+qattn_status qattn_debug_bounds_probe(qattn_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of
  * the current device (QATTN_ERR_TIMEOUT if a kernel gave up on a wait,

@@ -12,12 +12,15 @@ from typing import Optional
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqattn.so")
+# QATTN_LIBRARY: the path of another build of the library to load instead
+# (e.g. the checked build, _lib/check/libqattn.so)
+_LIB_PATH = os.environ.get("QATTN_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "_lib", "libqattn.so")
 _lib = None
 
 OK = 0
 FWD_AUTO, FWD_TC, FWD_SHORT = 0, 1, 2
-ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = 1, 2, 3, 4, 5
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_BOUNDS = 1, 2, 3, 4, 5, 6
 GRAN_TENSOR, GRAN_HEAD, GRAN_BLOCK = 0, 1, 2
 DT_BF16, DT_F32, DT_I8, DT_E4M3 = 0, 1, 2, 3
 POS0_BOTTOM_RIGHT = -(2 ** 63)
@@ -29,7 +32,7 @@ EXPORTED = (
     "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc", "qattn_decode",
     "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax", "qattn_prepare",
     "qattn_fwd_kernel_choice", "qattn_prepare_launches", "qattn_debug_wait_timeout",
-    "qattn_peak_loop", "qattn_kv_header_init",
+    "qattn_peak_loop", "qattn_kv_header_init", "qattn_checked", "qattn_debug_bounds_probe",
 )
 
 
@@ -93,16 +96,31 @@ def lib() -> ctypes.CDLL:
     L.qattn_fwd_kernel_choice.restype = ctypes.c_int
     L.qattn_prepare_launches.argtypes = [PS, PP]
     L.qattn_prepare_launches.restype = ctypes.c_int
+    L.qattn_checked.argtypes = []
+    L.qattn_checked.restype = ctypes.c_int
+    L.qattn_debug_bounds_probe.argtypes = [vp]
     ci = ctypes.c_int
     L.qattn_peak_loop.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp]
     L.qattn_peak_loop.restype = ci
     for name in ("qattn_smooth_k", "qattn_quantize_qk", "qattn_quantize_v", "qattn_fwd",
                  "qattn_decode", "qattn_kv_append", "qattn_fwd_exact24", "qattn_fwd_intsoftmax",
                  "qattn_debug_qk_scores", "qattn_get_error", "qattn_quantize_v_noalloc",
-                 "qattn_prepare", "qattn_debug_wait_timeout", "qattn_kv_header_init"):
+                 "qattn_prepare", "qattn_debug_wait_timeout", "qattn_kv_header_init",
+                 "qattn_debug_bounds_probe"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
+
+
+def checked() -> bool:
+    """Whether the loaded library is the checked build (QATTN_CHECK=1)."""
+    return bool(lib().qattn_checked())
+
+
+def debug_bounds_probe(stream=None):
+    """One guard that fails for half a warp, touching no memory: the checked
+    build then reports ERR_BOUNDS from get_error(), the normal build OK."""
+    _check(lib().qattn_debug_bounds_probe(_stream(stream)), "qattn_debug_bounds_probe")
 
 
 def status_string(st: int) -> str:

@@ -31,6 +31,7 @@
 // the other's softmax runs, and QK(t, j+1) overlaps softmax(t, j).
 #include <cuda_bf16.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -203,6 +204,11 @@ __device__ __forceinline__ const float* scale_ptr(const float* s, int gran, int 
   if (gran == 0) return s;
   if (gran == 1) return s + bh;
   return s + static_cast<size_t>(bh) * nblk + blk;
+}
+// Checked build: whether (bh, blk) addresses one of the BH * nblk scales (the
+// granule's array: 1, BH or BH * nblk floats).
+__device__ __forceinline__ bool scale_in_range(int gran, int bh, int BH, int nblk, int blk) {
+  return gran == 0 || (gran == 1 ? bh < BH : (bh < BH && blk < nblk));
 }
 __device__ __forceinline__ float scale_of(const float* s, int gran, int bh, int nblk, int blk) {
   return *scale_ptr(s, gran, bh, nblk, blk);
@@ -511,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kc >= static_cast<uint32_t>(C::kNK) &&
             !mbar_wait(bar(kBarKEmpty + st), ((kc / C::kNK) - 1) & 1, abort_flag, a.err, kErrTimeout))
           return false;
+        (void)QATTN_IN_BOUNDS(j * kBN < a.Nk && bkv < a.B * a.Hkv);  // TMA coordinates
         mbar_arrive_expect_tx(bar(kBarKFull + st), C::kKBytes);
         tma_tile<D>(&tmK, sK(st), bar(kBarKFull + st), j * kBN, bkv);
         last_k[st] = static_cast<int>(kc++);
@@ -521,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (vc >= static_cast<uint32_t>(C::kNV) &&
             !mbar_wait(bar(kBarVEmpty + st), ((vc / C::kNV) - 1) & 1, abort_flag, a.err, kErrTimeout))
           return false;
+        (void)QATTN_IN_BOUNDS(j * kBN < a.Nk && bkv < a.B * a.Hkv);  // TMA coordinates
         mbar_arrive_expect_tx(bar(kBarVFull + st), C::kVBytes);
         tma_load_3d(sV(st), &tmV, bar(kBarVFull + st), j * kBN, 0, bkv);
         last_v[st] = static_cast<int>(vc++);
@@ -543,20 +551,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           hs->nb0 = it.nb[0];
           hs->nb1 = it.nb[1];
           for (int tt = 0; tt < 2; ++tt) {
-            if (it.nb[tt] > 0)
+            if (it.nb[tt] > 0 &&
+                QATTN_IN_BOUNDS(scale_in_range(a.q_gran, it.bq, a.B * a.Hq, nqb, it.q0 / kBM + tt)))
               cp_async4(sSlot(sl) + offsetof(ItemSlot, sq) + 4 * tt,
                         scale_ptr(a.q_scales, a.q_gran, it.bq, nqb, it.q0 / kBM + tt));
             else
               hs->sq[tt] = 0.f;
           }
-          if (it.nb[0] > 0 || it.nb[1] > 0)
+          if ((it.nb[0] > 0 || it.nb[1] > 0) &&
+              QATTN_IN_BOUNDS(scale_in_range(a.k_gran, it.bkv, a.B * a.Hkv, nkb, 0)))
             cp_async4(sSlot(sl) + offsetof(ItemSlot, sk0), scale_ptr(a.k_scales, a.k_gran, it.bkv, nkb, 0));
           else
             hs->sk0 = 0.f;
           cp_async_mbar_arrive(bar(kBarSlotFull + sl));
           mbar_arrive_expect_tx(bar(kBarSlotFull + sl), 4 * D);
-          bulk_g2s(sSlot(sl) + 64, a.v_scales + static_cast<size_t>(it.bkv) * D, 4 * D,
-                   bar(kBarSlotFull + sl));
+          if (QATTN_IN_BOUNDS(it.bkv < a.B * a.Hkv))  // (a skipped copy leaves the slot's wait to time out)
+            bulk_g2s(sSlot(sl) + 64, a.v_scales + static_cast<size_t>(it.bkv) * D, 4 * D,
+                     bar(kBarSlotFull + sl));
           last_slot[sl] = i;
         }
         const int qs = i % C::kQS;
@@ -564,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             !(ok = mbar_wait(bar(kBarQEmpty + qs), ((i / C::kQS) - 1) & 1, abort_flag, a.err,
                              kErrTimeout)))
           break;
+        (void)QATTN_IN_BOUNDS(it.bq < a.B * a.Hq && it.q0 < a.Nq);  // TMA coordinates
         mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * C::kQ8Bytes);  // int8 codes
         tma_load_3d(sQ8(qs, 0), &tmQ, bar(kBarQFull + qs), 0, it.q0, it.bq);
         tma_load_3d(sQ8(qs, 1), &tmQ, bar(kBarQFull + qs), 0, it.q0 + kBM, it.bq);
@@ -752,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nbt == 0) {  // no visible key for any row of this tile: output 0
         mbar_arrive(bar(kBarSlotEmpty + sl));
         const size_t row = static_cast<size_t>(it.bq) * a.Nq + qi;
-        if (qi < a.Nq) {
+        if (qi < a.Nq && QATTN_IN_BOUNDS(it.bq < a.B * a.Hq)) {
           for (int cidx = 0; cidx < D; ++cidx) {
             if (a.out_bf16)
               reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + cidx] = __float2bfloat16(0.f);
@@ -774,7 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = kNegInf, l = 0.f;
       for (int j = 0; j < nbt; ++j) {
         const float sk = sk_next;
-        if (j + 1 < nbt) sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j + 1);
+        if (j + 1 < nbt && QATTN_IN_BOUNDS(scale_in_range(a.k_gran, it.bkv, a.B * a.Hkv, nkb, j + 1)))
+          sk_next = scale_of(a.k_scales, a.k_gran, it.bkv, nkb, j + 1);
         ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag, a.err, kErrTimeout);
         ++sc;
         if (!__all_sync(0xffffffffu, ok)) {  // keep the warp converged for tcgen05.ld
@@ -929,12 +942,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!a.out_bf16 || (cc & 1) == 1) {  // the 128-byte chunk is complete: store it
             fence_proxy_async_smem();
             __syncwarp();
-            if (issue) {
+            if (issue && QATTN_IN_BOUNDS(it.bq < a.B * a.Hq && yo < a.Nq)) {
               tma_store_3d(&tmO, prow - (static_cast<uint32_t>(lane) << 7), a.out_bf16 ? (cc / 2) * 64 : cc * 32, yo, it.bq);
               bulk_commit_group();
             }
           }
-        } else if (qi < a.Nq) {  // bf16 rows of 64 bytes (D = 32): direct stores
+        } else if (qi < a.Nq && QATTN_IN_BOUNDS(it.bq < a.B * a.Hq)) {  // bf16 rows of 64 bytes (D = 32): direct stores
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + cc * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -949,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mbar_arrive(bar(kBarSlotEmpty + sl));  // the slot's last read by this thread
-      if (a.lse && qi < a.Nq)
+      if (a.lse && qi < a.Nq && QATTN_IN_BOUNDS(it.bq < a.B * a.Hq))
         a.lse[row] = (l > 0.f) ? (m + __log2f(l) - (PQ ? kLog2_127 : kLog2_448)) * kLn2 : kNegInf;
     }
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
@@ -1079,6 +1092,8 @@ cudaError_t launch_dbg_t(const CUtensorMap& tq, const CUtensorMap& tk, int B, in
 }
 
 }  // namespace
+
+unsigned int check_take_attn_fwd() { return check_take_local(); }
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const AttnArgs& a, cudaStream_t s) {

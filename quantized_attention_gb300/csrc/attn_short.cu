@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -226,6 +227,7 @@ __device__ __forceinline__ void epilogue(const AttnArgs& a, int bh, int bkv, int
       const float il = half ? il_hi : il_lo;
       const float v0 = o[n][2 * half] * (sv0 * il), v1 = o[n][2 * half + 1] * (sv1 * il);
       const size_t off = (static_cast<size_t>(bh) * a.Nq + row) * D + c;
+      if (!QATTN_IN_BOUNDS(bh < a.B * a.Hq && c + 1 < D)) continue;
       if (a.out_bf16) {
         *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
             __floats2bfloat162_rn(v0, v1);
@@ -449,6 +451,8 @@ cudaError_t launch_window_t(const ShortArgs& sa, cudaStream_t s) {
 }
 
 }  // namespace
+
+unsigned int check_take_short() { return check_take_local(); }
 
 bool attn_short_eligible(const AttnArgs& a) {
   return (a.d == 32 || a.d == 64) && !a.causal && !a.pv_int8 && a.Nk >= 1 && a.Nk <= kShortMaxNk &&

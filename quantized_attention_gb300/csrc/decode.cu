@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   float lt = 0.f;
 #pragma unroll
   for (int g2 = 0; g2 < CG; ++g2) lt += redl[g2];
-  if (threadIdx.x < D) {
+  if (threadIdx.x < D && QATTN_IN_BOUNDS(b < a.B && hkv * G + g < a.Hq && i < a.Nq)) {
     const int c = threadIdx.x;
     float s = 0.f;
 #pragma unroll
@@ -656,6 +657,8 @@ cudaError_t launch_decode_r(const CUtensorMap& tk, const CUtensorMap& tv, Decode
 // depend on the GPU: the unit counter (64-bit), chunk shares O
 // [B*Hkv][chunks][R][d], their l and m [B*Hkv][chunks][R], and the tagged
 // chunk maxima [B*Hkv][chunks][R] (64-bit).
+unsigned int check_take_decode() { return check_take_local(); }
+
 size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
                        long long d) {
   const long long R = (Hq / Hkv) * Nq;

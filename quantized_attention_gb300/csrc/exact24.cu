@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -117,6 +118,7 @@ __global__ void k_rows_f16_kernel(const int8_t* __restrict__ codes, long long ca
     const long long row = i / per_row;  // bkv * Nk + key
     const int c16 = static_cast<int>(i % per_row);
     const long long bkv = row / Nk, key = row % Nk;
+    if (!QATTN_IN_BOUNDS(key < cap)) continue;
     const uint4 x = __ldg(reinterpret_cast<const uint4*>(codes + (bkv * cap + key) * D) + c16);
     uint32_t h[8];
     codes4_to_f16x2(x.x, h[0], h[1]);
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(256) v_t_f16_kernel(const int8_t* __restrict__
   for (int i = threadIdx.x; i < 64 * D / 16; i += 256) {
     const int key = i / (D / 16), c16 = i % (D / 16);
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (k0 + key < Nk)
+    if (k0 + key < Nk && QATTN_IN_BOUNDS(k0 + key < cap))
       x = __ldg(reinterpret_cast<const uint4*>(codes + (static_cast<long long>(bkv) * cap + k0 + key) * D) + c16);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float l_other;
       if ((ok = exchange(nc, l, l_other))) l += l_other;
     }
-    if (ok && row < a.Nq) {
+    if (ok && row < a.Nq && QATTN_IN_BOUNDS(bh < static_cast<int>(gridDim.y))) {
       // ---- epilogue: O * s_v / l
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       const float* svc = a.v_chan_scale + static_cast<size_t>(bkv) * D + DH * hf;
@@ -628,6 +630,8 @@ cudaError_t launch_t(const Exact24Args& x, cudaStream_t s) {
 }
 
 }  // namespace
+
+unsigned int check_take_exact24() { return check_take_local(); }
 
 size_t exact24_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
                         long long d) {

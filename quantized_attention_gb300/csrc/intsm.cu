@@ -25,6 +25,7 @@
 #include <cmath>
 #include <cuda_runtime.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -448,6 +449,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, D <= 64 ? 2 : 1) intsm_attn_ke
       const int v0 = min(127, max(-127, floor_div_recip(o[n][2 * half], dl, fi)));
       const int v1 = min(127, max(-127, floor_div_recip(o[n][2 * half + 1], dl, fi)));
       const uint16_t pair = static_cast<uint16_t>((v0 & 0xff) | ((v1 & 0xff) << 8));
+      if (!QATTN_IN_BOUNDS(8 * n + 2 * t4 + 1 < D)) continue;
       *reinterpret_cast<uint16_t*>(a.out + (static_cast<size_t>(bh) * a.Nq + row) * D + 8 * n + 2 * t4) = pair;
     }
   }
@@ -467,6 +469,8 @@ cudaError_t launch_t(const IntsmArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+unsigned int check_take_intsm() { return check_take_local(); }
 
 cudaError_t launch_intsoftmax(int B, int Hq, int Hkv, int Nq, int Nk, int d, float sm_scale,
                               const int8_t* q_codes, const float* q_scale, const int8_t* k_codes,

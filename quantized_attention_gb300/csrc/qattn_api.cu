@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "qattn.h"
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -316,6 +317,7 @@ const char* qattn_status_string(qattn_status s) {
     case QATTN_ERR_CUDA: return "CUDA error";
     case QATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
     case QATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case QATTN_ERR_BOUNDS: return "a kernel index fell outside its buffer (checked build)";
   }
   return "unknown status";
 }
@@ -885,6 +887,12 @@ int qattn_fwd_kernel_choice(const qattn_shape* shape, const qattn_params* params
   return c;
 }
 
+int qattn_checked(void) { return qattn::kChecked ? 1 : 0; }
+
+qattn_status qattn_debug_bounds_probe(qattn_stream_t stream) {
+  return from_cuda(qattn::launch_bounds_probe(reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int qattn_prepare_launches(const qattn_shape* shape, const qattn_params* params) {
   if (check_shape(shape) != QATTN_OK || check_params(params) != QATTN_OK) return -1;
   if (shape->Nk < 1) return -1;
@@ -915,7 +923,11 @@ qattn_status qattn_get_error(qattn_stream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_qattn_error_word, &zero, sizeof(zero)) != cudaSuccess) return QATTN_ERR_CUDA;
   }
+  const unsigned int checks = qattn::check_take_attn_fwd() | qattn::check_take_quant() |
+                              qattn::check_take_decode() | qattn::check_take_short() |
+                              qattn::check_take_exact24() | qattn::check_take_intsm();
   if (v & qattn::kErrTimeout) return QATTN_ERR_TIMEOUT;
+  if (checks != 0) return QATTN_ERR_BOUNDS;
   return (v & qattn::kErrDomain) ? QATTN_ERR_INVALID_ARG : QATTN_OK;
 }
 

@@ -46,6 +46,18 @@ bool current_context_id(unsigned long long* id);
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrDomain = 2u;  // device-held scales outside a kernel's domain
 
+// The checked build's bounds-check words, one per kernel translation unit
+// (qattn_check.cuh): each call reads and clears its unit's word (always 0 in
+// the normal build).
+unsigned int check_take_attn_fwd();
+unsigned int check_take_quant();
+unsigned int check_take_decode();
+unsigned int check_take_short();
+unsigned int check_take_exact24();
+unsigned int check_take_intsm();
+// One guard that fails for 16 of 32 threads, touching no memory (quant_kernels.cu).
+cudaError_t launch_bounds_probe(cudaStream_t s);
+
 struct AttnArgs {
   int B, Hq, Hkv, Nq, Nk, d;
   int causal;

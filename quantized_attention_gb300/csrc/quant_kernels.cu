@@ -9,6 +9,7 @@
 // (__float2ll_rn, __float2int_rn) and the hardware RN/satfinite e4m3 convert.
 #include <cuda_fp16.h>
 
+#include "qattn_check.cuh"
 #include "qattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -402,6 +403,7 @@ __device__ __forceinline__ void quant_rows_body(const RowsJob& j, int bh, int bl
         w[e / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e % 4));
       }
       const size_t off = (static_cast<size_t>(bh) * j.N + t0 + r) * D + cv * 8;
+      if (!QATTN_IN_BOUNDS(bh < j.BH && t0 + r < j.N && cv * 8 < D)) continue;
       *reinterpret_cast<uint2*>(j.codes + off) = make_uint2(w[0], w[1]);
       if (j.carrier != nullptr) {
         uint4 h;
@@ -1148,7 +1150,8 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_tensor1_kernel(const Tens
     const int c = i / nchunk, k = i % nchunk;
     const uint4 w = (16 * k < kTensorHead) ? *reinterpret_cast<const uint4*>(sm.tile + c * kTensorHead + 16 * k)
                                            : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * p.ldv + 16 * k) = w;
+    if (QATTN_IN_BOUNDS(bh < p.BHk && 16 * k + 16 <= p.ldv))
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * p.ldv + 16 * k) = w;
   }
 }
 
@@ -1188,11 +1191,14 @@ __global__ void __launch_bounds__(kThreads) prepare_tensor2_kernel(const TensorP
         for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
       }
       const size_t off = static_cast<size_t>(r) * D + L.v * 8;
-      codes8(x, inv, codes + off, carrier ? carrier + off : nullptr);
+      if (QATTN_IN_BOUNDS(r < N && L.v * 8 < D)) codes8(x, inv, codes + off, carrier ? carrier + off : nullptr);
     }
   }
   if (bh == 0 && threadIdx.x == 0) (is_q ? p.q_scales : p.k_scales)[0] = __fdiv_rn(g, 127.0f);
 }
+
+// The checked build's reporting path: the guard fails for threads >= n.
+__global__ void bounds_probe_kernel(int n) { (void)QATTN_IN_BOUNDS(static_cast<int>(threadIdx.x) < n); }
 
 // ------------------------------------------------------------------ carriers
 // int8 codes -> fp16 values (exact: |code| <= 127).
@@ -1347,6 +1353,13 @@ cudaError_t launch_prepare(const RowsJob& jq, const RowsJob& jk, const Src& V, i
     case 64: return prepare_t<64>(p1, p2, s);
     default: return prepare_t<128>(p1, p2, s);
   }
+}
+
+unsigned int check_take_quant() { return check_take_local(); }
+
+cudaError_t launch_bounds_probe(cudaStream_t s) {
+  bounds_probe_kernel<<<1, 32, 0, s>>>(16);
+  return cudaGetLastError();
 }
 
 bool prepare_tensor_eligible(int d, int Nq, int Nk) {

@@ -12,7 +12,7 @@ from quantized_attention_gb300.pipeline import device_inputs, problem_for
 def ensure_library():
     from quantized_attention_gb300 import build
     if not os.path.exists(qb.library_path()):
-        build.build()
+        build.build(checked=os.path.abspath(qb.library_path()) == build.CHECK_LIB)
     qb.lib()
 
 

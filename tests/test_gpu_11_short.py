@@ -31,6 +31,7 @@ CASES = [
     I.small("swin", B=2, Hq=2, Hkv=1, Nq=200, Nk=17),           # Nq > Nk, bias, 1 step of keys
     I.small("swin", B=3, Hq=2, Hkv=1, Nq=33, Nk=50),            # window kernel: GQA, Nq != Nk
     I.small("vit", B=4, Hq=2, Hkv=2, Nq=64, Nk=64),             # window kernel: d 64, full window
+    I.small("vit", B=1, Hq=2, Hkv=1, Nq=255, Nk=255, d=32),     # one key short of the longest head
 ]
 
 

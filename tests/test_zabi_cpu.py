@@ -38,6 +38,21 @@ def test_every_declared_function_is_exported(L):
     assert sorted(binding.EXPORTED) == names
 
 
+def test_checked_build_exports_the_same_and_says_so(L):
+    """The bounds-checked build (QATTN_CHECK=1) is the same ABI; only
+    qattn_checked() tells the two apart."""
+    from quantized_attention_gb300 import binding, build
+    if not os.path.exists(build.CHECK_LIB):
+        build.build(checked=True)
+    C = ctypes.CDLL(build.CHECK_LIB)
+    for n in _declared():
+        assert hasattr(C, n), n
+    assert C.qattn_checked() == 1
+    assert L.qattn_checked() == (1 if os.path.abspath(binding.library_path()) == build.CHECK_LIB else 0)
+    C.qattn_status_string.restype = ctypes.c_char_p
+    assert b"checked build" in C.qattn_status_string(binding.ERR_BOUNDS)
+
+
 def test_host_only_queries(L):
     from quantized_attention_gb300 import binding as qb
     assert qb.version() == 100
