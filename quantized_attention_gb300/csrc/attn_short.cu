@@ -102,11 +102,14 @@ struct RowPair {
 // rows: S from the fp16 Q rows (q_addr) and K rows (k_addr, pitch 2D + 16),
 // the masked, scaled scores, the running max and alpha, O *= alpha, 448 P, its
 // e4m3 codes and O += P8 . V8 (v_addr: V^T rows, pitch 2 KB + 16), and l.
-template <int D, bool BIAS, int KB>
+// FRAG (with BIAS): the bias comes from bfrag, the lane's S-fragment-ordered
+// values bias * log2 e (-inf past nvis) in shared memory, one float4 per
+// 8-key n-tile at bfrag[32 n], instead of the rows.
+template <int D, bool BIAS, int KB, bool FRAG = false>
 __device__ __forceinline__ void block_step(uint32_t q_addr, uint32_t k_addr, uint32_t v_addr, int nvis,
                                            int kbase, float c_lo, float c_hi, const float* brow_lo,
                                            const float* brow_hi, int t4, RowPair& rp,
-                                           float (&o)[D / 8][4]) {
+                                           float (&o)[D / 8][4], const float4* bfrag = nullptr) {
   constexpr int KS = D / 16;
   constexpr int NTO = D / 8;
   constexpr int kQKPitch = 2 * D + 16;
@@ -136,11 +139,15 @@ __device__ __forceinline__ void block_step(uint32_t q_addr, uint32_t k_addr, uin
   float mx_lo = kNegInf, mx_hi = kNegInf;
 #pragma unroll
   for (int n = 0; n < KB / 8; ++n) {
+    float4 bf;
+    if (FRAG) bf = bfrag[32 * n];  // n-tile n's entry of the lane (the lanes' entries interleave)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int key = 8 * n + 2 * t4 + (e & 1);
       float v = S[n][e];
-      if (BIAS) {
+      if (FRAG) {
+        v = fmaf(v, (e < 2) ? c_lo : c_hi, e == 0 ? bf.x : e == 1 ? bf.y : e == 2 ? bf.z : bf.w);
+      } else if (BIAS) {
         v = (key < nvis) ? fmaf(v, (e < 2) ? c_lo : c_hi,
                                 __fmul_rn(((e < 2) ? brow_lo : brow_hi)[kbase + key], kLog2e))
                          : kNegInf;
@@ -385,6 +392,13 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
   const uint32_t q_addr = smem_u32(sq) + (16 * warp + mrow + (mat & 1) * 8) * SM::kQKPitch + (mat >> 1) * 16;
   const uint32_t k_addr = smem_u32(sk) + (mrow + (mat >> 1) * 8) * SM::kQKPitch + (mat & 1) * 16;
   const uint32_t v_addr = smem_u32(sv) + (mrow + (mat >> 1) * 8) * SM::kVPitch + (mat & 1) * 16;
+  // BIAS: the lane's 32 bias values of its rows and S-fragment keys, times
+  // log2 e, -inf past Nk (so fmaf(S, c, b) is the block step's masked t),
+  // refilled only when the head index changes (never, when the grid is a
+  // multiple of Hq: each CTA then sees one head index).  A lane reads back
+  // only what it wrote, so no barrier guards the array.
+  __shared__ float4 sbias[BIAS ? kWinThreads / 32 : 1][BIAS ? kWin / 8 : 1][32];
+  int h_frag = -1;
   WinRaw<D> raw;
   if (blockIdx.x < n_heads) win_load<D>(sa, blockIdx.x, raw);
   for (int w = blockIdx.x; w < n_heads; w += gridDim.x) {
@@ -405,18 +419,28 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
     const float sq_ = scale_of(a.q_scales, a.q_gran, w, 1, 0);
     const float sk_ = scale_of(a.k_scales, a.k_gran, bkv, 1, 0);
     const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq_, sk_), a.sm_scale), kLog2e);
-    const float* brow_lo = nullptr;
-    const float* brow_hi = nullptr;
-    if (BIAS) {
+    if (BIAS && h != h_frag) {
       const float* bh0 = a.bias + static_cast<size_t>(h) * a.bias_head_stride;
-      brow_lo = bh0 + static_cast<size_t>(min(r_lo, a.Nq - 1)) * a.Nk;
-      brow_hi = bh0 + static_cast<size_t>(min(r_hi, a.Nq - 1)) * a.Nk;
+      const float* brow_lo = bh0 + static_cast<size_t>(min(r_lo, a.Nq - 1)) * a.Nk;
+      const float* brow_hi = bh0 + static_cast<size_t>(min(r_hi, a.Nq - 1)) * a.Nk;
+#pragma unroll
+      for (int n = 0; n < kWin / 8; ++n) {
+        float b[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = 8 * n + 2 * t4 + (e & 1);
+          b[e] = (key < a.Nk) ? __fmul_rn(((e < 2) ? brow_lo : brow_hi)[key], kLog2e) : kNegInf;
+        }
+        sbias[warp][n][lane] = make_float4(b[0], b[1], b[2], b[3]);
+      }
+      h_frag = h;
     }
     RowPair rp;
     float o[D / 8][4];
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    block_step<D, BIAS, kWin>(q_addr, k_addr, v_addr, a.Nk, 0, c, c, brow_lo, brow_hi, t4, rp, o);
+    block_step<D, BIAS, kWin, BIAS>(q_addr, k_addr, v_addr, a.Nk, 0, c, c, nullptr, nullptr, t4, rp, o,
+                                    BIAS ? &sbias[warp][0][lane] : nullptr);
     epilogue<D>(a, w, bkv, r_lo, r_hi, t4, rp, o);
   }
 }
