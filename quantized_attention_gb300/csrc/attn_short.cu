@@ -104,8 +104,9 @@ struct RowPair {
 // e4m3 codes and O += P8 . V8 (v_addr: V^T rows, pitch 2 KB + 16), and l.
 // FRAG (with BIAS): the bias comes from bfrag, the lane's S-fragment-ordered
 // values bias * log2 e (-inf past nvis) in shared memory, one float4 per
-// 8-key n-tile at bfrag[32 n], instead of the rows.
-template <int D, bool BIAS, int KB, bool FRAG = false>
+// 8-key n-tile at bfrag[32 n], instead of the rows.  FIRST: the row's first
+// block (rp fresh, o zero), where O *= alpha and alpha l change nothing.
+template <int D, bool BIAS, int KB, bool FRAG = false, bool FIRST = false>
 __device__ __forceinline__ void block_step(uint32_t q_addr, uint32_t k_addr, uint32_t v_addr, int nvis,
                                            int kbase, float c_lo, float c_hi, const float* brow_lo,
                                            const float* brow_hi, int t4, RowPair& rp,
@@ -174,12 +175,14 @@ __device__ __forceinline__ void block_step(uint32_t q_addr, uint32_t k_addr, uin
   const float kn_hi = dead_hi ? 0.f : (kLog2_448 - mn_hi);
   rp.m_lo = mn_lo;
   rp.m_hi = mn_hi;
+  if (!FIRST) {
 #pragma unroll
-  for (int n = 0; n < NTO; ++n) {  // O = alpha O (alpha = 1 is exact)
-    o[n][0] *= al_lo;
-    o[n][1] *= al_lo;
-    o[n][2] *= al_hi;
-    o[n][3] *= al_hi;
+    for (int n = 0; n < NTO; ++n) {  // O = alpha O (alpha = 1 is exact)
+      o[n][0] *= al_lo;
+      o[n][1] *= al_lo;
+      o[n][2] *= al_hi;
+      o[n][3] *= al_hi;
+    }
   }
   float sum_lo = 0.f, sum_hi = 0.f;
 #pragma unroll
@@ -213,20 +216,23 @@ __device__ __forceinline__ void block_step(uint32_t q_addr, uint32_t k_addr, uin
     sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, sh);
     sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, sh);
   }
-  rp.l_lo = fmaf(al_lo, rp.l_lo, sum_lo);
-  rp.l_hi = fmaf(al_hi, rp.l_hi, sum_hi);
+  rp.l_lo = FIRST ? sum_lo : fmaf(al_lo, rp.l_lo, sum_lo);  // (alpha 0 l + sum = sum: l is 0)
+  rp.l_hi = FIRST ? sum_hi : fmaf(al_hi, rp.l_hi, sum_hi);
 }
 
 // out = O s_v / l (l in units of 448 P) and lse for a lane's rows r_lo, r_hi.
+// sv_pre: the lane's V channel scales (channels 8n + 2 t4, + 1), read ahead
+// by the caller; else read here.
 template <int D>
 __device__ __forceinline__ void epilogue(const AttnArgs& a, int bh, int bkv, int r_lo, int r_hi, int t4,
-                                         const RowPair& rp, const float (&o)[D / 8][4]) {
+                                         const RowPair& rp, const float (&o)[D / 8][4],
+                                         const float2* sv_pre = nullptr) {
   const float* svp = a.v_scales + static_cast<size_t>(bkv) * D;
   const float il_lo = (rp.l_lo > 0.f) ? 1.f / rp.l_lo : 0.f, il_hi = (rp.l_hi > 0.f) ? 1.f / rp.l_hi : 0.f;
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) {
     const int c = 8 * n + 2 * t4;
-    const float sv0 = svp[c], sv1 = svp[c + 1];
+    const float sv0 = sv_pre ? sv_pre[n].x : svp[c], sv1 = sv_pre ? sv_pre[n].y : svp[c + 1];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int row = half ? r_hi : r_lo;
@@ -355,9 +361,8 @@ struct WinRaw {
 };
 
 template <int D>
-__device__ __forceinline__ void win_load(const ShortArgs& sa, int w, WinRaw<D>& raw) {
+__device__ __forceinline__ void win_load(const ShortArgs& sa, int w, int bkv, WinRaw<D>& raw) {
   const AttnArgs& a = sa.a;
-  const int b = w / a.Hq, h = w % a.Hq, bkv = b * a.Hkv + h / (a.Hq / a.Hkv);
   const int8_t* qg = sa.q_codes + static_cast<size_t>(w) * a.Nq * D;
   const int8_t* kg = sa.k_codes + static_cast<size_t>(bkv) * a.Nk * D;
   const uint8_t* vg = sa.v8t + static_cast<size_t>(bkv) * D * sa.ldv;
@@ -375,7 +380,7 @@ __device__ __forceinline__ void win_load(const ShortArgs& sa, int w, WinRaw<D>& 
 }
 
 template <int D, bool BIAS>
-__global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArgs sa, int n_heads) {
+__global__ void __launch_bounds__(kWinThreads, D == 32 ? 5 : 4) attn_window_kernel(const ShortArgs sa, int n_heads) {
   using SM = WinSmem<D>;
   const AttnArgs& a = sa.a;
   __shared__ __align__(16) uint8_t smem[SM::kBytes];
@@ -399,10 +404,34 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
   // only what it wrote, so no barrier guards the array.
   __shared__ float4 sbias[BIAS ? kWinThreads / 32 : 1][BIAS ? kWin / 8 : 1][32];
   int h_frag = -1;
+  // The CTA's heads w = blockIdx.x + k G (G = gridDim.x), as (batch, head)
+  // pairs stepped without divisions: (b, h) of w + G = (b + G / Hq, h + G % Hq),
+  // carrying h >= Hq into b.
+  const int grp = a.Hq / a.Hkv;
+  const int db = static_cast<int>(gridDim.x) / a.Hq, dh = static_cast<int>(gridDim.x) % a.Hq;
+  int b = static_cast<int>(blockIdx.x) / a.Hq, h = static_cast<int>(blockIdx.x) % a.Hq;
+  auto kv_of = [&](int bb, int hh) { return bb * a.Hkv + hh / grp; };
+  auto step = [&](int& bb, int& hh) {
+    bb += db;
+    hh += dh;
+    if (hh >= a.Hq) {
+      hh -= a.Hq;
+      ++bb;
+    }
+  };
   WinRaw<D> raw;
-  if (blockIdx.x < n_heads) win_load<D>(sa, blockIdx.x, raw);
-  for (int w = blockIdx.x; w < n_heads; w += gridDim.x) {
+  if (blockIdx.x < n_heads) win_load<D>(sa, blockIdx.x, kv_of(b, h), raw);
+  for (int w = blockIdx.x; w < n_heads; w += gridDim.x, step(b, h)) {
     __syncthreads();  // the previous head's rows are read
+    // the head's scales, read before the conversion so their latency hides
+    // under it and the block step
+    const int bkv = kv_of(b, h);
+    const float sq_ = scale_of(a.q_scales, a.q_gran, w, 1, 0);
+    const float sk_ = scale_of(a.k_scales, a.k_gran, bkv, 1, 0);
+    float2 vsc[D / 8];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+      vsc[n] = *reinterpret_cast<const float2*>(a.v_scales + static_cast<size_t>(bkv) * D + 8 * n + 2 * t4);
 #pragma unroll
     for (int i = 0; i < SM::kPer; ++i) {
       const int v = threadIdx.x + i * kWinThreads;
@@ -412,12 +441,13 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
       const int c = v / (kWin / 16), k16 = v % (kWin / 16);
       store_e4m3x16_f16(sv + c * SM::kVPitch + 32 * k16, raw.v[i]);
     }
-    if (w + gridDim.x < n_heads) win_load<D>(sa, w + gridDim.x, raw);  // under this head's math
+    if (w + gridDim.x < n_heads) {  // under this head's math
+      int bn = b, hn = h;
+      step(bn, hn);
+      win_load<D>(sa, w + gridDim.x, kv_of(bn, hn), raw);
+    }
     __syncthreads();
     if (!active) continue;
-    const int b = w / a.Hq, h = w % a.Hq, bkv = b * a.Hkv + h / (a.Hq / a.Hkv);
-    const float sq_ = scale_of(a.q_scales, a.q_gran, w, 1, 0);
-    const float sk_ = scale_of(a.k_scales, a.k_gran, bkv, 1, 0);
     const float c = __fmul_rn(__fmul_rn(__fmul_rn(sq_, sk_), a.sm_scale), kLog2e);
     if (BIAS && h != h_frag) {
       const float* bh0 = a.bias + static_cast<size_t>(h) * a.bias_head_stride;
@@ -425,13 +455,13 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
       const float* brow_hi = bh0 + static_cast<size_t>(min(r_hi, a.Nq - 1)) * a.Nk;
 #pragma unroll
       for (int n = 0; n < kWin / 8; ++n) {
-        float b[4];
+        float bv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = 8 * n + 2 * t4 + (e & 1);
-          b[e] = (key < a.Nk) ? __fmul_rn(((e < 2) ? brow_lo : brow_hi)[key], kLog2e) : kNegInf;
+          bv[e] = (key < a.Nk) ? __fmul_rn(((e < 2) ? brow_lo : brow_hi)[key], kLog2e) : kNegInf;
         }
-        sbias[warp][n][lane] = make_float4(b[0], b[1], b[2], b[3]);
+        sbias[warp][n][lane] = make_float4(bv[0], bv[1], bv[2], bv[3]);
       }
       h_frag = h;
     }
@@ -439,9 +469,9 @@ __global__ void __launch_bounds__(kWinThreads) attn_window_kernel(const ShortArg
     float o[D / 8][4];
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    block_step<D, BIAS, kWin, BIAS>(q_addr, k_addr, v_addr, a.Nk, 0, c, c, nullptr, nullptr, t4, rp, o,
+    block_step<D, BIAS, kWin, BIAS, true>(q_addr, k_addr, v_addr, a.Nk, 0, c, c, nullptr, nullptr, t4, rp, o,
                                     BIAS ? &sbias[warp][0][lane] : nullptr);
-    epilogue<D>(a, w, bkv, r_lo, r_hi, t4, rp, o);
+    epilogue<D>(a, w, bkv, r_lo, r_hi, t4, rp, o, vsc);
   }
 }
 

@@ -758,6 +758,16 @@ struct HeadLane {
   }
 };
 
+// Brings a head's rows into L1 (prefetch.global.L1: no registers, no wait)
+// so a later pass over them finds them there: each lane touches the lines of
+// its own rows.
+template <int D>
+__device__ __forceinline__ void head_prefetch_l1(const HeadLane<D>& L, const uint16_t* head, long long sN,
+                                                 int N) {
+  for (int r = L.rg; r < N; r += HeadLane<D>::RG)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(head + static_cast<long long>(r) * sN + 8 * L.v));
+}
+
 // The channel mean of a head's N rows (exact fixed-point sums), every lane of a
 // column holding its 8 channels' means.
 template <int D>
@@ -869,7 +879,9 @@ __device__ __forceinline__ void head_vamax(const HeadLane<D>& L, const uint16_t*
 }
 
 // The head's V8^T rows [D][ldv] (keys past N are 0): e4m3(fp32(x * sc)) per
-// channel, through the warp's [D][TL] byte tile.
+// channel, through the warp's [D][TL] byte tile.  Here a lane takes UNR
+// consecutive rows (not rows RG apart), so its 8 codes of one channel are 8
+// consecutive bytes of the tile: one 8-byte store per channel.
 template <int D, int TL>
 __device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* head, long long sN, int N,
                                          const float (&sc)[8], uint8_t* tile, uint8_t* v8t_head,
@@ -877,22 +889,28 @@ __device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* h
   for (int i = lane; i < D * TL / 16; i += 32) reinterpret_cast<uint4*>(tile)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncwarp();
   constexpr int RG = HeadLane<D>::RG, UNR = HeadLane<D>::UNR;
-  for (int r0 = L.rg; r0 < N; r0 += UNR * RG) {
-    uint4 raw[UNR];
-    L.load_rows(head, sN, N, r0, raw);
+  static_assert(UNR == 8, "two words of codes per channel");
+  for (int base = 0; base < N; base += UNR * RG) {
+    const int r0 = base + L.rg * UNR;
+    if (r0 >= N) continue;  // (rows past N stay the tile's zeros)
+    uint32_t w[8][2] = {};  // channel e: the codes of rows r0 .. r0 + 3, r0 + 4 .. r0 + 7
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      const int r = r0 + u * RG;
-      if (r >= N) break;
+      const int r = r0 + u;
+      const uint4 raw = (r < N) ? *(reinterpret_cast<const uint4*>(head + static_cast<long long>(r) * sN) + L.v)
+                                : make_uint4(0u, 0u, 0u, 0u);  // 0 codes
       float x[8];
-      unpack_bf16x8(raw[u], x);
+      unpack_bf16x8(raw, x);
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
         const uint32_t b2 = cvt_e4m3x2(__fmul_rn(x[e], sc[e]), __fmul_rn(x[e + 1], sc[e + 1]));
-        tile[(L.v * 8 + e) * TL + r] = static_cast<uint8_t>(b2 & 0xFFu);
-        tile[(L.v * 8 + e + 1) * TL + r] = static_cast<uint8_t>(b2 >> 8);
+        w[e][u / 4] |= (b2 & 0xFFu) << (8 * (u % 4));
+        w[e + 1][u / 4] |= (b2 >> 8) << (8 * (u % 4));
       }
     }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<uint2*>(tile + (L.v * 8 + e) * TL + r0) = make_uint2(w[e][0], w[e][1]);
   }
   __syncwarp();
   const int nchunk = static_cast<int>(ldv / 16);  // 16-byte chunks of a V8^T row
@@ -929,6 +947,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const S
   // ---- a KV head: channel mean, K - mean codes, V maxima and e4m3 codes
   const uint16_t* ks = src_head<uint16_t>(p.K, bh);
   const uint16_t* vs = src_head<uint16_t>(p.V, bh);
+  head_prefetch_l1<D>(L, vs, p.V.sN, p.Nk);  // V's reads overlap K's passes
   float mu[8];
   head_mean<D>(L, ks, p.K.sN, p.Nk, p.magic, mu);
   if (L.rg == 0) {
