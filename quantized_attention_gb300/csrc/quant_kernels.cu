@@ -922,9 +922,10 @@ __device__ __forceinline__ void head_v8t(const HeadLane<D>& L, const uint16_t* h
   }
 }
 
-// Block granules, heads of at most 128 tokens: everything in one launch.
+// Block granules, heads of at most 128 tokens: everything in one launch.  Six
+// CTAs per SM (80 registers, a few spilled) run faster than four at 126.
 template <int D>
-__global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const SmallPrepArgs p) {
+__global__ void __launch_bounds__(kSmallWarps * 32, 6) prepare_small_kernel(const SmallPrepArgs p) {
   pdl_trigger();
   pdl_wait();
   __shared__ __align__(16) uint8_t tiles[kSmallWarps][D * kSmallHead];  // V8^T of a warp's head
@@ -962,10 +963,23 @@ __global__ void __launch_bounds__(kSmallWarps * 32) prepare_small_kernel(const S
   if (lane == 0) p.k_scales[bh] = __fdiv_rn(g, 127.0f);
   float vm[8], sc[8];
   head_vamax<D>(L, vs, p.V.sN, p.Nk, vm);
+  {
+    // The RG lanes of a column share the column's 16 divisions (lane rg takes
+    // channels e = rg, rg + RG, ...) and hand the factors 448 / max round, as
+    // head_mean does with its means.
+    constexpr int RG = HeadLane<D>::RG, VPR = HeadLane<D>::VPR, PER = 8 / RG;
+    float own[PER];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    sc[e] = (vm[e] > 0.f) ? __fdiv_rn(448.0f, vm[e]) : 0.f;
-    if (L.rg == 0) p.v_scales[static_cast<size_t>(bh) * D + L.v * 8 + e] = __fdiv_rn(vm[e], 448.0f);
+    for (int i = 0; i < PER; ++i) {
+      const int e = L.rg + i * RG;
+      float ve = vm[0];
+#pragma unroll
+      for (int ee = 1; ee < 8; ++ee) ve = (ee == e) ? vm[ee] : ve;  // selects, no divergence
+      own[i] = (ve > 0.f) ? __fdiv_rn(448.0f, ve) : 0.f;
+      p.v_scales[static_cast<size_t>(bh) * D + L.v * 8 + e] = __fdiv_rn(ve, 448.0f);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sc[e] = __shfl_sync(0xffffffffu, own[e / RG], (e % RG) * VPR + L.v);
   }
   head_v8t<D, kSmallHead>(L, vs, p.V.sN, p.Nk, sc, tiles[warp], p.v8t + static_cast<size_t>(bh) * D * p.ldv, p.ldv,
                           lane);
