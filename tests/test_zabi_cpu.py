@@ -53,6 +53,21 @@ def test_checked_build_exports_the_same_and_says_so(L):
     assert b"checked build" in C.qattn_status_string(binding.ERR_BOUNDS)
 
 
+def test_library_override_loads_the_checked_build(L):
+    """QATTN_LIBRARY points the binding at another build of the library."""
+    import subprocess
+    import sys
+    from quantized_attention_gb300 import build
+    if not os.path.exists(build.CHECK_LIB):
+        build.build(checked=True)
+    code = ("from quantized_attention_gb300 import binding as qb; import os; "
+            "assert os.path.samefile(qb.library_path(), os.environ['QATTN_LIBRARY']); "
+            "assert qb.checked(); print('ok')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       env=dict(os.environ, QATTN_LIBRARY=build.CHECK_LIB), timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
 def test_host_only_queries(L):
     from quantized_attention_gb300 import binding as qb
     assert qb.version() == 100
