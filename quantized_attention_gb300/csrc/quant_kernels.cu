@@ -930,7 +930,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 6) prepare_small_kernel(cons
   pdl_wait();
   __shared__ __align__(16) uint8_t tiles[kSmallWarps][D * kSmallHead];  // V8^T of a warp's head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x * kSmallWarps + warp;
+  // the heavier KV heads take the first warps, the Q heads fill the tail
+  int item = blockIdx.x * kSmallWarps + warp;
+  item = (item < p.BHk) ? item + p.BHq : item - p.BHk;
   const HeadLane<D> L(lane);
   const float none[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (item < p.BHq) {  // ---- a Q head: block amax, codes, scale
@@ -1058,7 +1060,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_tensor1_kernel(const Tens
   __shared__ __align__(16) TensorSmem<D> sm;
   const TL L;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the heavier K and V heads take the first CTAs, the Q heads (a max and
+  // nothing else) fill the tail
   int item = blockIdx.x;
+  item = (item < 2 * p.BHk) ? item + p.BHq : item - 2 * p.BHk;
   if (item < p.BHq) {  // ---- a Q head: its max |x|
     const uint16_t* src = src_head<uint16_t>(p.Q, item);
     float am = 0.f;
