@@ -653,12 +653,12 @@ cudaError_t launch_decode_r(const CUtensorMap& tk, const CUtensorMap& tv, Decode
 
 }  // namespace
 
+unsigned int check_take_decode() { return check_take_local(); }
+
 // Workspace, sized for the most chunks (one block each) so the layout does not
 // depend on the GPU: the unit counter (64-bit), chunk shares O
 // [B*Hkv][chunks][R][d], their l and m [B*Hkv][chunks][R], and the tagged
 // chunk maxima [B*Hkv][chunks][R] (64-bit).
-unsigned int check_take_decode() { return check_take_local(); }
-
 size_t decode_ws_bytes(long long B, long long Hq, long long Hkv, long long Nq, long long Nk,
                        long long d) {
   const long long R = (Hq / Hkv) * Nq;
