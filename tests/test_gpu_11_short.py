@@ -3,6 +3,8 @@ QATTN_FWD_SHORT; the automatic choice for the ViT/DeiT and Swin shapes)
 against the oracle, and against the persistent tensor-core kernel on the same
 quantized operands: the two compute the same recipe and differ only in the
 order of fp32 accumulations."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -65,6 +67,31 @@ def test_short_kernel_parity(wl):
     assert np.abs(got - tc).max() <= 2e-6 * scale, _ids(wl)
     ls, lt = gpu_lse_rows(Ps, heads, rows), gpu_lse_rows(Pt, heads, rows)
     np.testing.assert_allclose(ls, lt, rtol=0, atol=2e-5)
+
+
+@pytest.mark.parametrize("kernel", [qb.FWD_AUTO, qb.FWD_SHORT, qb.FWD_TC], ids=["window", "short", "tc"])
+def test_per_head_bias(kernel):
+    """A bias per head ([Hq][Nq][Nk], bias_head_stride = Nq Nk; the window
+    kernel keeps a head index's bias fragments and refills them when the index
+    changes): every head against the oracle run with that head's bias."""
+    wl = I.small("swin", B=3, Hq=3, Hkv=3)  # N 49, d 32
+    inp = I.make_inputs(wl)
+    prep = O.prepare(inp)
+    rng = np.random.default_rng(20241)
+    bias3 = rng.standard_normal((wl.Hq, wl.Nq, wl.Nk)).astype(np.float32)
+    P = problem_for(wl, out_dtype=qb.DT_F32, want_lse=True, fwd_kernel=kernel,
+                    bias_head_stride=wl.Nq * wl.Nk)
+    dev = device_inputs(inp)
+    dev.pop("bias", None)
+    P.run(**dev, bias=torch.from_numpy(bias3).to("cuda"))
+    torch.cuda.synchronize()
+    assert qb.get_error() == 0
+    rows = np.arange(wl.Nq)
+    for h in range(wl.Hq):
+        heads = [(b, h) for b in range(wl.B)]
+        ref = O.run_workload(dataclasses.replace(inp, bias=bias3[h]), prep, heads=heads, rows=rows,
+                             want_bound=True)
+        check_output(gpu_out_rows(P, heads, rows), ref["O"], ref["bound"], f"head {h}")
 
 
 def test_short_kernel_is_the_automatic_choice():
