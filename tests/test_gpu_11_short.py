@@ -69,12 +69,18 @@ def test_short_kernel_parity(wl):
     np.testing.assert_allclose(ls, lt, rtol=0, atol=2e-5)
 
 
-@pytest.mark.parametrize("kernel", [qb.FWD_AUTO, qb.FWD_SHORT, qb.FWD_TC], ids=["window", "short", "tc"])
-def test_per_head_bias(kernel):
+BIAS_CASES = [
+    I.small("swin", B=3, Hq=3, Hkv=3),                                  # N 49, d 32: the window kernel
+    I.small("tiny", B=2, Hq=2, Hkv=1, Nq=130, Nk=200, has_bias=True),   # d 64, ragged blocks, GQA
+]
+
+
+@pytest.mark.parametrize("wl", BIAS_CASES, ids=[_ids(w) for w in BIAS_CASES])
+@pytest.mark.parametrize("kernel", [qb.FWD_AUTO, qb.FWD_SHORT, qb.FWD_TC], ids=["auto", "short", "tc"])
+def test_per_head_bias(wl, kernel):
     """A bias per head ([Hq][Nq][Nk], bias_head_stride = Nq Nk; the window
     kernel keeps a head index's bias fragments and refills them when the index
     changes): every head against the oracle run with that head's bias."""
-    wl = I.small("swin", B=3, Hq=3, Hkv=3)  # N 49, d 32
     inp = I.make_inputs(wl)
     prep = O.prepare(inp)
     rng = np.random.default_rng(20241)
