@@ -25,6 +25,7 @@ CASES = [
     I.small("llm8k", Hq=1, Hkv=1, Nq=1, Nk=1, d=64),                # single token
     I.small("llm8k", Hq=2, Hkv=1, Nq=1, Nk=777),                    # one query (decode-shaped row)
     I.small("llm8k", Hq=2, Hkv=1, Nq=255, Nk=255),                  # one row short of two tiles
+    I.small("llm8k", B=2, Hq=8, Hkv=1, Nq=200, Nk=200),             # eight query heads per KV head
     I.small("tiny", causal=False, Nq=3, Nk=1000),                   # few rows, many keys
     I.small("chunk32k", Hq=4, Hkv=2, Nq=256, Nk=1024, q_pos0=768),
     I.small("chunk32k", Hq=2, Hkv=2, Nq=100, Nk=301, q_pos0=201, d=32),
